@@ -1,0 +1,620 @@
+#!/usr/bin/env python3
+"""Throughput of the MXFP4 A4W4 / FP8 PTPC A8W8 hot path on one GB300 per rank.
+
+Default workload (one "step"): the 5-layer o_proj decode chain -- M = 64 tokens
+(concurrency 8 x (1 verified + 7 drafted) tokens), N = 7168, K = 8192, five
+seeded weights already converted to MXFP4 and resident in HBM; per layer the
+bf16 activations are quantized to MXFP4 on the fly (dynamic, per 32-group)
+and fed to the block-scaled A4W4 GEMM, bf16 out.  Inputs are synthetic
+(see synth/), no trained weights.  The step runs as one CUDA graph; L2 is
+flushed (256 MiB write) between timed steps, outside the timed interval.
+
+Other workloads (--workload): oproj_m8 (one layer, M = 8), oproj_prefill
+(M = 8192, standalone quantization + full-tile GEMM), mlp_fp8_m64 /
+mlp_fp8_m8192 (FP8 PTPC gate_up + down), sweep (mixed-precision draft layer
+over M; one line per M).
+
+Prints ONE JSON line on rank 0 (plus one per M for the sweep).  N > 1: one
+process per GPU (torchrun), every rank runs its own replica of the workload
+(weak scaling, no data-path collective), time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MXFP4 A4W4 / FP8 A8W8 GEMM TFLOPS & HBM GB/s vs GB300 roofline by M"
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------- accounting
+def a4w4_gemm_bytes(M, N, K):
+    """Algorithmic bytes of one A4W4 GEMM launch on pre-quantized operands:
+    weight codes + scales, activation codes + scales, bf16 output."""
+    return N * K // 2 + N * K // 32 + M * K // 2 + M * K // 32 + 2 * M * N
+
+
+def a4w4_fused_bytes(M, N, K):
+    """The same GEMM fed bf16 activations: 2MK replaces the activation codes."""
+    return N * K // 2 + N * K // 32 + 2 * M * K + 2 * M * N
+
+
+def ptpc_gemm_bytes(M, N, K):
+    return N * K + 4 * N + M * K + 4 * M + 2 * M * N
+
+
+def mx_quant_bytes(M, K):
+    return 2 * M * K + M * K // 2 + M * K // 32
+
+
+def fp8_quant_bytes(M, K):
+    return 2 * M * K + M * K + 4 * M
+
+
+# ----------------------------------------------------------------- timing helpers
+class GraphEvent:
+    """A timing event that becomes an event-record node inside a CUDA graph."""
+
+    def __init__(self):
+        try:
+            self.ev = torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:  # torch without external events: plain events, eager use only
+            self.ev = torch.cuda.Event(enable_timing=True)
+
+    def record(self, stream=None):
+        self.ev.record(stream)
+
+    def elapsed_ms(self, other: "GraphEvent") -> float:
+        return self.ev.elapsed_time(other.ev)
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (100 ms) while the bench runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.t is not None:
+                self.t.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or \
+               [s for (_, s) in self.samples[-3:]]
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ----------------------------------------------------------------- workloads
+class Workload:
+    """Builds resident device operands and exposes one step as a list of
+    (label, fn) launches; `timed_label` marks the dominant kernel."""
+    name = ""
+    n_layers = 1
+    timed_label = ""
+    kernel_bytes = 0       # algorithmic bytes of one launch of the dominant kernel
+    kernel_flops = 0
+    bytes_per_step = 0
+    flops_per_step = 0
+    dtype = ""
+    bound = "hbm"
+    kernel_desc = ""
+
+    def launches(self):
+        raise NotImplementedError
+
+    def e2e_step(self):
+        raise NotImplementedError
+
+
+class OprojChain(Workload):
+    """A4W4 o_proj layers: fused dynamic MXFP4 activation quantization +
+    block-scaled GEMM per layer."""
+
+    def __init__(self, mx, synth, dev, M, layers, w_seeds, cfg, row_scale=False, name=""):
+        self.mx, self.dev = mx, dev
+        N, K = synth.OPROJ_N, synth.OPROJ_K
+        self.M, self.N, self.K = M, N, K
+        self.n_layers = layers
+        self.name = name
+        self.w = []
+        for s in w_seeds:
+            wc, wsf = mx.mx_quantize_weight(synth.weight(N, K, seed=s).to(dev))
+            self.w.append((wc, wsf))
+        self.x_host = [synth.activation(M, K, seed=synth.act_seed(cfg, l, 0), row_scale=row_scale).pin_memory()
+                       for l in range(layers)]
+        self.x = [h.to(dev) for h in self.x_host]
+        self.y = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+        self.y_host = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+        self.ac = [torch.empty(M, K // 2, dtype=torch.uint8, device=dev) for _ in range(layers)]
+        self.asf = [torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(layers)]
+        self.ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(mx.KIND_A4W4, True, M, N, K)),
+                              dtype=torch.uint8, device=dev)
+        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+        self.timed_label = "a4w4_gemm"
+        self.kernel_bytes = a4w4_gemm_bytes(M, N, K)
+        self.kernel_flops = 2 * M * N * K
+        self.bytes_per_step = layers * a4w4_fused_bytes(M, N, K)
+        self.flops_per_step = layers * 2 * M * N * K
+        self.dtype = "e2m1 x e2m1 -> f32 (bf16 out)"
+        self.bound = "hbm" if M <= 512 else "tensor"
+        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
+        self.kernel_desc = f"gemm_kernel<A4W4, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
+        self.h2d = layers * M * K * 2
+        self.d2h = layers * M * N * 2
+
+    def launches(self):
+        mx = self.mx
+        out = []
+        for l in range(self.n_layers):
+            wc, wsf = self.w[l]
+            out.append(("mx_quant", lambda l=l: mx.mx_quantize_act(self.x[l], codes=self.ac[l], sf=self.asf[l])))
+            out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
+                wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws)))
+        return out
+
+    def e2e_step(self):
+        mx = self.mx
+        for l in range(self.n_layers):
+            self.x[l].copy_(self.x_host[l], non_blocking=True)
+            wc, wsf = self.w[l]
+            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws)
+        for l in range(self.n_layers):
+            self.y_host[l].copy_(self.y[l], non_blocking=True)
+
+
+class MlpFp8(Workload):
+    """FP8 PTPC gate_up (7168 -> 2 x 18432) + down (18432 -> 7168)."""
+
+    def __init__(self, mx, synth, dev, M, name):
+        self.mx, self.dev, self.M = mx, dev, M
+        self.name = name
+        I2, H = 2 * synth.MLP_I, 7168
+        self.qg, self.sg = mx.fp8_quantize_act(synth.weight(I2, H, seed=synth.SEED_CFG3_GATE_UP).to(dev))
+        self.qd, self.sd = mx.fp8_quantize_act(synth.weight(H, synth.MLP_I, seed=synth.SEED_CFG3_DOWN).to(dev))
+        self.xg_host = synth.activation(M, H, seed=synth.act_seed(3, 0, 0)).pin_memory()
+        self.xd_host = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1)).pin_memory()
+        self.xg, self.xd = self.xg_host.to(dev), self.xd_host.to(dev)
+        self.qa_g = torch.empty(M, H, dtype=torch.uint8, device=dev)
+        self.sa_g = torch.empty(M, dtype=torch.float32, device=dev)
+        self.qa_d = torch.empty(M, synth.MLP_I, dtype=torch.uint8, device=dev)
+        self.sa_d = torch.empty(M, dtype=torch.float32, device=dev)
+        self.yg = torch.empty(M, I2, dtype=torch.bfloat16, device=dev)
+        self.yd = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        self.yg_host = torch.empty(M, I2, dtype=torch.bfloat16).pin_memory()
+        self.yd_host = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        wsb = max(mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, I2, H),
+                  mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, H, synth.MLP_I), 1 << 20)
+        self.ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+        self.plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm)
+        self.timed_label = "ptpc_gate_up"
+        self.kernel_bytes = ptpc_gemm_bytes(M, I2, H)
+        self.kernel_flops = 2 * M * I2 * H
+        self.bytes_per_step = (fp8_quant_bytes(M, H) + ptpc_gemm_bytes(M, I2, H) +
+                               fp8_quant_bytes(M, synth.MLP_I) + ptpc_gemm_bytes(M, H, synth.MLP_I))
+        self.flops_per_step = 2 * M * I2 * H + 2 * M * H * synth.MLP_I
+        self.dtype = "e4m3 x e4m3 -> f32 (bf16 out)"
+        self.bound = "hbm" if M <= 256 else "tensor"
+        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
+        self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
+        self.h2d = 2 * M * H + 2 * M * synth.MLP_I
+        self.d2h = 2 * M * I2 + 2 * M * H
+
+    def launches(self):
+        mx = self.mx
+        return [("fp8_quant", lambda: mx.fp8_quantize_act(self.xg, q=self.qa_g, scale=self.sa_g)),
+                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg, ws=self.ws)),
+                ("fp8_quant", lambda: mx.fp8_quantize_act(self.xd, q=self.qa_d, scale=self.sa_d)),
+                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd, ws=self.ws))]
+
+    def e2e_step(self):
+        mx = self.mx
+        self.xg.copy_(self.xg_host, non_blocking=True)
+        self.xd.copy_(self.xd_host, non_blocking=True)
+        for _, fn in self.launches():
+            fn()
+        self.yg_host.copy_(self.yg, non_blocking=True)
+        self.yd_host.copy_(self.yd, non_blocking=True)
+
+
+def make_workload(name, mx, synth, dev):
+    if name == "oproj_decode":
+        return OprojChain(mx, synth, dev, 64, 5, synth.SEEDS_CFG1_W, 1,
+                          name="A4W4 o_proj decode chain: M=64 (conc 8 x 8 tokens), N=7168, K=8192, 5 layers")
+    if name == "oproj_m8":
+        return OprojChain(mx, synth, dev, 8, 1, (synth.SEED_CFG0_W,), 0,
+                          name="A4W4 o_proj single layer: M=8 (1 verified + 7 drafted), N=7168, K=8192")
+    if name == "oproj_prefill":
+        return OprojChain(mx, synth, dev, 8192, 1, (synth.SEED_CFG2_W,), 2, row_scale=True,
+                          name="A4W4 o_proj prefill: M=8192 (8 x 1024 tokens), N=7168, K=8192")
+    if name in ("mlp_fp8_m64", "mlp_fp8_m8192"):
+        M = 64 if name.endswith("m64") else 8192
+        return MlpFp8(mx, synth, dev, M, name=f"FP8 PTPC MLP pair: M={M}, gate_up 7168->36864, down 18432->7168")
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ----------------------------------------------------------------- our arm
+def traffic_record(workload: str):
+    """ncu DRAM bytes per launch of the dominant kernel, if the committed
+    profile summary was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    rec = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("kernel_sources_sha256") != kernel_sources_hash():
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
+    for f in ("gemm.cu", "ptx.cuh", "quant.cu"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def run_ours(args, rank, world, local_rank):
+    import fp8_block_scaled_dynamic_gb300 as mx
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    mx.lib()
+    wl = make_workload(args.workload, mx, synth, dev)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    launches = wl.launches()
+    n_timed = sum(1 for lab, _ in launches if lab == wl.timed_label)
+
+    # eager warm-up (sets kernel attributes), then capture one step as a graph
+    with torch.cuda.stream(stream):
+        for _, fn in launches:
+            fn()
+    stream.synchronize()
+    ev_pairs = [(GraphEvent(), GraphEvent()) for _ in range(n_timed)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        k = 0
+        for lab, fn in launches:
+            if lab == wl.timed_label:
+                ev_pairs[k][0].record()
+                fn()
+                ev_pairs[k][1].record()
+                k += 1
+            else:
+                fn()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # warm-up: at least W steps and ~0.5 s of load so clocks settle
+    t_w = time.time()
+    i = 0
+    with torch.cuda.stream(stream):
+        while i < args.warmup or time.time() - t_w < args.min_warmup_s:
+            flush.zero_()
+            graph.replay()
+            i += 1
+            if i % 50 == 0:
+                stream.synchronize()
+    stream.synchronize()
+
+    K = args.steps
+    st_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    st_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kern_ms = []
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            st_s[i].record(stream)
+            graph.replay()
+            st_e[i].record(stream)
+            stream.synchronize()
+            kern_ms.extend(a.elapsed_ms(b) for a, b in ev_pairs)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(st_s, st_e)]
+    ms = statistics.mean(step_ms)
+    kms = statistics.mean(kern_ms)
+    if world > 1:
+        t = torch.tensor([ms, kms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, kms = float(t[0]), float(t[1])
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e_ms = []
+    ke = max(3, min(K, 50))
+    with torch.cuda.stream(stream):
+        for i in range(ke + 2):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            wl.e2e_step()
+            b.record(stream)
+            stream.synchronize()
+            if i >= 2:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(t[0])
+
+    if rank != 0:
+        return
+    hbm, bf16, peak_src = load_peaks()
+    gbs = world * wl.bytes_per_step / (ms * 1e-3) / 1e9
+    achieved_gbs = wl.kernel_bytes / (kms * 1e-3) / 1e9
+    achieved_tf = wl.kernel_flops / (kms * 1e-3) / 1e12
+    if wl.bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4)}
+    else:
+        # FP4/FP8 dense tensor peak: the measured bf16 cuBLAS peak x the nominal ratio
+        ratio = 6.0 if "e2m1" in wl.dtype else 2.0
+        pk = bf16 * ratio
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": round(pk, 1),
+                "unit": "TFLOP/s", "frac": round(achieved_tf / pk, 4),
+                "peak_note": f"{peak_src} bf16 {bf16} TFLOP/s x nominal {'fp4' if ratio == 6 else 'fp8'}/bf16 ratio {ratio}"}
+    roof["traffic"] = traffic_record(args.workload)
+    roof["kernel"] = wl.kernel_desc
+    roof["kernel_ms"] = round(kms, 5)
+    roof["peak_source"] = peak_src
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic (seeded bf16 N(0,1) activations with 0.1% x50 outliers, N(0,0.02) weights)",
+        "config": {"workload": wl.name, "key": args.workload, "l2": "flushed between steps (256 MiB write)",
+                   "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
+                   "dispatch": {k: wl.plan[k] for k in ("variant", "bn", "ctas", "seg_max")}},
+        "tflops": round(world * wl.flops_per_step / (ms * 1e-3) / 1e12, 2),
+        "roofline": roof,
+        "e2e": {"value": round(world * wl.bytes_per_step / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
+                "path": "public API (Python binding -> C ABI), eager launches, pinned host buffers"},
+        "gpu_launches": K * len(launches),
+        "clocks": sampler.summary(t0, t1),
+    }
+    if args.cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- CPU oracle legs
+_ORACLE_CACHE = {}
+
+
+def _oracle_operands(workload: str):
+    """Quantized weights (offline conversion, not timed) and bf16 activations
+    of one layer of the workload, prepared once."""
+    if workload in _ORACLE_CACHE:
+        return _ORACLE_CACHE[workload]
+    import oracle
+    import synth
+    if workload.startswith("oproj"):
+        M, layers, cfg, seed = {"oproj_decode": (64, 5, 1, synth.SEEDS_CFG1_W[0]),
+                                "oproj_m8": (8, 1, 0, synth.SEED_CFG0_W),
+                                "oproj_prefill": (8192, 1, 2, synth.SEED_CFG2_W)}[workload]
+        wq = oracle.mx_quantize_rows(synth.weight(synth.OPROJ_N, synth.OPROJ_K, seed=seed))
+        x = synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(cfg, 0, 0), row_scale=(cfg == 2))
+        ops = ("a4w4", M, layers, wq, x)
+    else:
+        M = 64 if workload.endswith("m64") else 8192
+        qg = oracle.fp8_quantize_rows(synth.weight(2 * synth.MLP_I, 7168, seed=synth.SEED_CFG3_GATE_UP))
+        qd = oracle.fp8_quantize_rows(synth.weight(7168, synth.MLP_I, seed=synth.SEED_CFG3_DOWN))
+        xg = synth.activation(M, 7168, seed=synth.act_seed(3, 0, 0))
+        xd = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1))
+        ops = ("ptpc", M, 1, (qg, qd), (xg, xd))
+    _ORACLE_CACHE[workload] = ops
+    return ops
+
+
+def oracle_sample(workload: str, rows: int):
+    """Time the oracle (activation quantization + reference GEMM, all output
+    channels) on `rows` token rows of one layer.  Returns (raw seconds,
+    factor that scales it to one full step -- linear in rows and layers --,
+    description)."""
+    import oracle
+    kind, M, layers, w, x = _oracle_operands(workload)
+    rows = max(1, min(rows, M))
+    if kind == "a4w4":
+        xs = x[:rows].contiguous()
+        t = time.perf_counter()
+        ac, asf = oracle.mx_quantize_rows(xs)
+        oracle.gemm_a4w4(ac, asf, w[0], w[1])
+        dt = time.perf_counter() - t
+        f = (M / rows) * layers
+        return dt, f, f"1 layer, {rows} of {M} token rows, all 7168 outputs; time x{f:g} (rows, layers)"
+    (qg, sg), (qd, sd) = w
+    xg, xd = x[0][:rows].contiguous(), x[1][:rows].contiguous()
+    t = time.perf_counter()
+    qa, sa = oracle.fp8_quantize_rows(xg)
+    oracle.gemm_ptpc(qa, sa, qg, sg)
+    qa, sa = oracle.fp8_quantize_rows(xd)
+    oracle.gemm_ptpc(qa, sa, qd, sd)
+    dt = time.perf_counter() - t
+    f = M / rows
+    return dt, f, f"gate_up + down, {rows} of {M} token rows, all outputs; time x{f:g} (rows)"
+
+
+def step_bytes(workload: str):
+    N, K = 7168, 8192
+    if workload == "oproj_decode":
+        return 5 * a4w4_fused_bytes(64, N, K)
+    if workload == "oproj_m8":
+        return a4w4_fused_bytes(8, N, K)
+    if workload == "oproj_prefill":
+        return a4w4_fused_bytes(8192, N, K)
+    M = 64 if workload.endswith("m64") else 8192
+    return (fp8_quant_bytes(M, 7168) + ptpc_gemm_bytes(M, 36864, 7168) +
+            fp8_quant_bytes(M, 18432) + ptpc_gemm_bytes(M, 7168, 18432))
+
+
+def cpu_baseline(workload: str, budget_s: float = 20.0):
+    """The oracle as it stands, on this host's cores, on a bounded sample
+    (about budget_s of CPU work) of the benchmarked workload."""
+    import oracle
+    M = _oracle_operands(workload)[1]
+    dt1, _, _ = oracle_sample(workload, 1)  # calibration on one row
+    rows = max(1, min(M, int(budget_s / max(dt1, 1e-6))))
+    dt, f, desc = oracle_sample(workload, rows)
+    t_full = dt * f
+    return {"value": round(step_bytes(workload) / t_full / 1e9, 5), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+            "sample_s": round(dt, 3), "s_per_step_extrapolated": round(t_full, 3)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, on this machine's host
+    cores, each step a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    # rows per step: as many as keep the whole run (warm-up + steps) near two minutes
+    M = _oracle_operands(args.workload)[1]
+    per_step = 120.0 / (args.steps + args.warmup)
+    rows = 1
+    for r in (M, 256, 64, 16, 4):
+        if r <= M:
+            dt, _, _ = oracle_sample(args.workload, r)
+            if dt <= per_step:
+                rows = r
+                break
+    for _ in range(max(0, args.warmup)):
+        oracle_sample(args.workload, rows)
+    ts = []
+    descs = None
+    for _ in range(args.steps):
+        dt, f, descs = oracle_sample(args.workload, rows)
+        ts.append(dt * f)
+    s = statistics.mean(ts)
+    v = step_bytes(args.workload) / s / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload},
+        "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": descs},
+        "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="oproj_decode",
+                    choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--min-warmup-s", type=float, default=0.5,
+                    help="keep warming up at least this long so clocks settle (0 under a profiler)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

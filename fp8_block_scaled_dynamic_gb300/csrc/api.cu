@@ -1,0 +1,362 @@
+// api.cu -- the C ABI declared in include/mxgemm.h: argument checks, device
+// checks, the dispatcher, TMA tensor-map encoding and kernel launches.
+// Every host-detectable error is returned before anything is launched.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "mxgemm.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Workspace layout, fixed for every call so that no call's data can land in
+// another call's counters: [0, 64 KiB) split-K arrival counters (zero before
+// the first call, left zero by every completed call), then the quantized
+// activations of the fused A4W4 path, then the split-K partial tiles.
+constexpr size_t kCounterBytes = 64 * 1024;
+constexpr long long kMaxSplitTiles = kCounterBytes / sizeof(int);
+
+struct DevInfo {
+  bool init = false;
+  int major = 0, minor = 0, sm_count = 0;
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+
+// Current device must be compute capability 10.3; returns its SM count.
+mxg_status check_device(int *sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MXG_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.init) {
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MXG_ERR_CUDA;
+    d.init = true;
+  }
+  if (d.major != 10 || d.minor != 3) return MXG_ERR_UNSUPPORTED_DEVICE;
+  if (sm_count) *sm_count = d.sm_count;
+  return MXG_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D byte matrix (rows x row_bytes, contiguous) read in boxes of 128 bytes x
+// box_rows rows with the 128-byte swizzle; rows past the end read as zero.
+mxg_status make_operand_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes, uint64_t rows,
+                            uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return MXG_ERR_CUDA;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+// CTA that owns stream-K unit u (must equal the device-side owner_of).
+long long owner_of(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
+
+mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm_opts *opts,
+                     mxg_plan *pl) {
+  if (!pl || (kind != 0 && kind != 1) || M < 1 || N < 1 || K < 1 || sm_count < 1)
+    return MXG_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  int variant = opts ? opts->variant : MXG_VARIANT_AUTO;
+  if (variant < MXG_VARIANT_AUTO || variant > MXG_VARIANT_SPLITK) return MXG_ERR_INVALID_ARG;
+  const int kstage = kind == 0 ? 256 : 128;
+  const int KB = (K + kstage - 1) / kstage;
+  if (variant == MXG_VARIANT_AUTO) variant = (M <= 256) ? MXG_VARIANT_SPLITK : MXG_VARIANT_FULL;
+  std::memset(pl, 0, sizeof(*pl));
+  pl->variant = variant;
+  pl->kblocks = KB;
+  pl->bm = 128;
+  if (variant == MXG_VARIANT_FULL) {
+    pl->bn = 256;
+    const long long tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
+    if (tiles > (1LL << 30)) return MXG_ERR_UNSUPPORTED_SHAPE;
+    pl->tiles = (int)tiles;
+    pl->ctas = (int)(tiles < sm_count ? tiles : sm_count);
+    pl->seg_max = 1;
+    pl->ws_bytes = 0;
+  } else {
+    pl->bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+    const long long tilesA = N / 128, tilesB = (M + pl->bn - 1) / pl->bn;
+    const long long tiles = tilesA * tilesB;
+    const long long U = tiles * KB;
+    if (U > (1LL << 40) / 4) return MXG_ERR_UNSUPPORTED_SHAPE;
+    long long G = (opts && opts->ctas > 0) ? opts->ctas : sm_count;
+    if (G > U) G = U;
+    int seg_max = 1;
+    for (long long t = 0; t < tiles; ++t) {
+      const long long n = owner_of(t * KB + KB - 1, U, G) - owner_of(t * KB, U, G) + 1;
+      if (n > seg_max) seg_max = (int)n;
+    }
+    if (seg_max > 1 && tiles > kMaxSplitTiles) return MXG_ERR_UNSUPPORTED_SHAPE;
+    pl->tiles = (int)tiles;
+    pl->ctas = (int)G;
+    pl->seg_max = seg_max;
+    pl->ws_bytes = seg_max > 1 ? kCounterBytes +
+                                     (size_t)tiles * seg_max * pl->bn * 128 * sizeof(float)
+                               : 0;
+  }
+  return MXG_OK;
+}
+
+mxg_status check_rows_arg(const void *x, int rows, int K, int ld) {
+  if (!x || rows < 1 || K < 1 || ld < K) return MXG_ERR_INVALID_ARG;
+  if (K % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || (ld % 8) != 0) return MXG_ERR_MISALIGNED;
+  return MXG_OK;
+}
+
+size_t fused_act_bytes(int M, int K) {
+  return align256((size_t)M * (K / 2)) + align256(mxg_sf_bytes(M, K, MXG_SF_SWIZZLED));
+}
+
+struct GemmOperands {
+  const uint8_t *a, *a_sf, *w, *w_sf;  // codes (A4W4) or E4M3 bytes (PTPC)
+  const float *sa, *sw;                // PTPC scales
+};
+
+// ws: the caller's workspace base; part_off: where the partial tiles start
+// (after the counters and, on the fused path, the quantized activations).
+mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void *y, int ldy,
+                    mxg_out_dtype out_dtype, const mxg_gemm_opts *opts, void *ws, size_t ws_bytes,
+                    size_t part_off, int sm_count, cudaStream_t stream) {
+  mxg_plan pl;
+  mxg_status st = plan_impl(kind, M, N, K, sm_count, opts, &pl);
+  if (st != MXG_OK) return st;
+  if (pl.ws_bytes > 0) {
+    if (!ws || ws_bytes < part_off + (pl.ws_bytes - kCounterBytes)) return MXG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
+  }
+
+  const bool swap = pl.variant == MXG_VARIANT_SPLITK;
+  const uint64_t row_bytes = kind == 0 ? (uint64_t)K / 2 : (uint64_t)K;
+  CUtensorMap tmA, tmB;
+  const uint8_t *A = swap ? op.w : op.a;
+  const uint8_t *B = swap ? op.a : op.w;
+  const int rowsA = swap ? N : M, rowsB = swap ? M : N;
+  if ((st = make_operand_map(&tmA, A, row_bytes, rowsA, 128)) != MXG_OK) return st;
+  if ((st = make_operand_map(&tmB, B, row_bytes, rowsB, (uint32_t)pl.bn)) != MXG_OK) return st;
+
+  mxg::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.sfA = swap ? op.w_sf : op.a_sf;
+  p.sfB = swap ? op.a_sf : op.w_sf;
+  p.tok_scale = op.sa;
+  p.chan_scale = op.sw;
+  p.y = y;
+  p.ldy = ldy;
+  p.out_f32 = out_dtype == MXG_OUT_F32 ? 1 : 0;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.swap = swap ? 1 : 0;
+  p.rowsA = rowsA;
+  p.rowsB = rowsB;
+  p.tilesA = (rowsA + 127) / 128;
+  p.tilesB = (rowsB + pl.bn - 1) / pl.bn;
+  p.kblocks = pl.kblocks;
+  p.G4 = K / 128;
+  p.splitk = swap ? 1 : 0;
+  p.units = (long long)p.tilesA * p.tilesB * p.kblocks;
+  if (pl.ws_bytes > 0) {
+    p.counters = static_cast<int *>(ws);
+    p.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + part_off);
+  }
+  p.seg_max = pl.seg_max;
+  p.status = opts ? opts->dev_status : nullptr;
+  const uint32_t tmo = (opts && opts->timeout_ms) ? opts->timeout_ms : 1000u;
+  p.timeout_ns = (unsigned long long)tmo * 1000000ull;
+  p.debug_stall = opts ? opts->debug_stall : 0;
+  cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_out_dtype od,
+                             const mxg_gemm_opts *opts) {
+  if (M < 1 || N < 1 || K < 1 || !y || ldy < N) return MXG_ERR_INVALID_ARG;
+  if (od != MXG_OUT_BF16 && od != MXG_OUT_F32) return MXG_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(y) || ((size_t)ldy * (od == MXG_OUT_F32 ? 4 : 2)) % 16 != 0)
+    return MXG_ERR_MISALIGNED;
+  if (opts && (opts->variant < 0 || opts->variant > 2 || opts->ctas < 0))
+    return MXG_ERR_INVALID_ARG;
+  return MXG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxg_sf_bytes(int rows, int K, mxg_sf_layout layout) {
+  if (rows < 1 || K < 32) return 0;
+  const size_t G = (size_t)K / 32;
+  if (layout == MXG_SF_SWIZZLED) return (size_t)((rows + 127) / 128) * 128u * G;
+  return (size_t)rows * G;
+}
+
+mxg_status mxg_plan_gemm(int kind, int M, int N, int K, int sm_count, const mxg_gemm_opts *opts,
+                         mxg_plan *plan) {
+  return plan_impl(kind, M, N, K, sm_count, opts, plan);
+}
+
+size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
+                                const mxg_gemm_opts *opts) {
+  int sm = 0;
+  if (check_device(&sm) != MXG_OK) return 0;
+  mxg_plan pl;
+  if (plan_impl(kind, M, N, K, sm, opts, &pl) != MXG_OK) return 0;
+  const size_t act = (kind == 0 && fused) ? fused_act_bytes(M, K) : 0;
+  if (pl.ws_bytes == 0 && act == 0) return 0;
+  return kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
+}
+
+mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t *codes,
+                              uint8_t *sf, mxg_sf_layout layout, mxg_stream_t stream) {
+  mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
+  if (st != MXG_OK) return st;
+  if (!codes || !sf || (layout != MXG_SF_ROWMAJOR && layout != MXG_SF_SWIZZLED))
+    return MXG_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(sf)) return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaError_t e = mxg::launch_mx_quant(w_bf16, ldw, N, K, codes, sf, layout == MXG_SF_SWIZZLED, sm,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+mxg_status mx_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *codes, uint8_t *sf,
+                           mxg_stream_t stream) {
+  return mx_quantize_weight(x_bf16, M, K, ldx, codes, sf, MXG_SF_SWIZZLED, stream);
+}
+
+mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *q, float *scale,
+                            mxg_stream_t stream) {
+  mxg_status st = check_rows_arg(x_bf16, M, K, ldx);
+  if (st != MXG_OK) return st;
+  if (!q || !scale) return MXG_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaError_t e =
+      mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, sm, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void *x_bf16, int ldx,
+                        const uint8_t *w_codes, const uint8_t *w_sf, int M, int N, int K, void *y,
+                        int ldy, mxg_out_dtype out_dtype, const mxg_gemm_opts *opts,
+                        mxg_stream_t stream) {
+  mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, opts);
+  if (st != MXG_OK) return st;
+  if (!w_codes || !w_sf) return MXG_ERR_INVALID_ARG;
+  const bool fused = a_codes == nullptr;
+  if (fused) {
+    if (!x_bf16 || a_sf) return MXG_ERR_INVALID_ARG;
+    if ((st = check_rows_arg(x_bf16, M, K, ldx)) != MXG_OK) return st;
+  } else if (!a_sf) {
+    return MXG_ERR_INVALID_ARG;
+  }
+  if (!aligned16(w_codes) || !aligned16(w_sf) || (a_codes && (!aligned16(a_codes) || !aligned16(a_sf))))
+    return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = opts ? static_cast<uint8_t *>(opts->workspace) : nullptr;
+  size_t ws_bytes = opts ? opts->ws_bytes : 0;
+  size_t part_off = kCounterBytes;
+  if (fused) {
+    const size_t need = fused_act_bytes(M, K);
+    if (!ws || ws_bytes < kCounterBytes + need) return MXG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
+    // plan first so that a too-small workspace is reported before any launch
+    mxg_plan pl;
+    if ((st = plan_impl(0, M, N, K, sm, opts, &pl)) != MXG_OK) return st;
+    if (pl.ws_bytes > 0 && ws_bytes < kCounterBytes + need + (pl.ws_bytes - kCounterBytes))
+      return MXG_ERR_WORKSPACE;
+    uint8_t *codes = ws + kCounterBytes;
+    uint8_t *sf = codes + align256((size_t)M * (K / 2));
+    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, sm, s);
+    if (e != cudaSuccess) return MXG_ERR_CUDA;
+    a_codes = codes;
+    a_sf = sf;
+    part_off += need;
+  }
+  GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
+  return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, sm, s);
+}
+
+mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
+                         int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
+                         const mxg_gemm_opts *opts, mxg_stream_t stream) {
+  mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, opts);
+  if (st != MXG_OK) return st;
+  if (!qa || !sa || !qw || !sw) return MXG_ERR_INVALID_ARG;
+  if (!aligned16(qa) || !aligned16(qw) || (reinterpret_cast<uintptr_t>(sa) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sw) & 3u))
+    return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  GemmOperands op{qa, nullptr, qw, nullptr, sa, sw};
+  return run_gemm(1, op, M, N, K, y, ldy, out_dtype, opts, opts ? opts->workspace : nullptr,
+                  opts ? opts->ws_bytes : 0, kCounterBytes, sm, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MXG_ERR_CUDA;
+  if (!dev_status) return MXG_OK;
+  int h = 0;
+  if (cudaMemcpy(&h, dev_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MXG_ERR_CUDA;
+  if (h != 0 && cudaMemset(dev_status, 0, sizeof(int)) != cudaSuccess) return MXG_ERR_CUDA;
+  if (h & MXG_DEV_TIMEOUT) return MXG_ERR_TIMEOUT;
+  if (h != 0) return MXG_ERR_CUDA;
+  return MXG_OK;
+}
+
+const char *mxg_status_string(mxg_status s) {
+  switch (s) {
+    case MXG_OK: return "MXG_OK";
+    case MXG_ERR_INVALID_ARG: return "MXG_ERR_INVALID_ARG";
+    case MXG_ERR_UNSUPPORTED_SHAPE: return "MXG_ERR_UNSUPPORTED_SHAPE";
+    case MXG_ERR_MISALIGNED: return "MXG_ERR_MISALIGNED";
+    case MXG_ERR_UNSUPPORTED_DEVICE: return "MXG_ERR_UNSUPPORTED_DEVICE";
+    case MXG_ERR_CUDA: return "MXG_ERR_CUDA";
+    case MXG_ERR_TIMEOUT: return "MXG_ERR_TIMEOUT";
+    case MXG_ERR_WORKSPACE: return "MXG_ERR_WORKSPACE";
+  }
+  return "MXG_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,528 @@
+// gemm.cu -- block-scaled A4W4 (tcgen05 kind::mxf4) and FP8 PTPC A8W8
+// (tcgen05 kind::f8f6f4) GEMMs for sm_103a.
+//
+// What is computed (page "Kimi-K3 DSpark O-Proj-only MXFP4", section "Exact
+// quantization coverage": "dynamic MXFP4 activations with A4W4 dispatch";
+// page "Kimi-K3-DSpark-FP8-PTPC", section "Phase 1 FP8 PTPC Quantization"):
+//   A4W4: y[m][n] = sum_g 2^(ea[m,g]-127) 2^(ew[n,g]-127) sum_{k in g} a[m,k] w[n,k]
+//   PTPC: y[m][n] = (sum_k a[m,k] w[n,k] * sa[m]) * sw[n]
+// with fp32 accumulation in TMEM and a bf16 (or fp32) epilogue.
+//
+// One kernel template serves both variants the dispatcher chooses from:
+//   full tile  (swap = 0): MMA-A = 128 token rows, MMA-B = 256 weight rows,
+//              each CTA owns whole tiles and all of K (persistent, strided).
+//   split-K    (swap = 1): MMA-A = 128 weight rows, MMA-B = the (padded)
+//              token rows; the (tile, K-block) units are cut evenly over the
+//              CTAs (stream-K); a CTA that ends a tile part-way writes an
+//              fp32 partial tile, and the last CTA to finish a tile (arrival
+//              counter) sums the partials in slot order -- a fixed order, so
+//              results are deterministic -- and writes y.
+//
+// Warp roles (192 threads): warp 0 = TMA producer (operand tiles with the
+// 128-byte swizzle, scale-factor tiles with plain bulk copies); warp 1 =
+// TMEM allocator and the single MMA-issuing thread (tcgen05.cp of the scale
+// tiles into TMEM, then the MMAs); warps 2-5 = epilogue (tcgen05.ld of their
+// 32-lane quarter).  All hand-offs are mbarriers; every wait is bounded.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mxg {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileA = 128;      // MMA M: rows of the MMA-A operand per tile
+constexpr int kRowBytes = 128;   // K bytes per row per stage (one 128-byte swizzle row)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, BN)
+constexpr uint32_t kSfaCol = 256;  // A scales: 2 tiles x 4 columns
+constexpr uint32_t kSfbCol = 264;  // B scales: 2 K-tiles x (<= 2 row blocks) x 4 columns
+constexpr int kSmemBudget = 220 * 1024;
+
+template <int KIND, int BN>
+struct Cfg {
+  static constexpr int kSfBlocksB = BN >= 128 ? BN / 128 : 1;
+  static constexpr int kABytes = kTileA * kRowBytes;
+  static constexpr int kBBytes = BN * kRowBytes;
+  static constexpr int kSfaBytes = KIND == 0 ? 1024 : 0;
+  static constexpr int kSfbBytes = KIND == 0 ? 1024 * kSfBlocksB : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 6) + 16;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+  static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(kStages >= 2, "pipeline depth");
+};
+
+struct Item {
+  int t, ta, tb, kb0, kb1, seg, nseg;
+};
+
+// CTA that owns stream-K unit u when U units are cut into G equal ranges
+// [c*U/G, (c+1)*U/G): the largest c with c*U < (u+1)*G.
+__device__ __forceinline__ long long owner_of(long long u, long long U, long long G) {
+  return ((u + 1) * G - 1) / U;
+}
+
+__device__ __forceinline__ long long first_cursor(const GemmParams &p) {
+  return p.splitk ? ((long long)blockIdx.x * p.units) / gridDim.x : (long long)blockIdx.x;
+}
+
+// The work items of this CTA, in order; every role walks the same list.
+__device__ __forceinline__ bool next_item(const GemmParams &p, long long &cur, Item &it) {
+  const long long G = gridDim.x;
+  if (!p.splitk) {
+    if (cur >= (long long)p.tilesA * p.tilesB) return false;
+    it.t = (int)cur;
+    it.kb0 = 0;
+    it.kb1 = p.kblocks;
+    it.seg = 0;
+    it.nseg = 1;
+    cur += G;
+  } else {
+    const long long U = p.units;
+    const long long u1 = ((long long)(blockIdx.x + 1) * U) / G;
+    if (cur >= u1) return false;
+    const int KB = p.kblocks;
+    it.t = (int)(cur / KB);
+    it.kb0 = (int)(cur % KB);
+    const long long room = u1 - cur;
+    it.kb1 = (int)((long long)(KB - it.kb0) < room ? KB : it.kb0 + room);
+    cur += it.kb1 - it.kb0;
+    const long long first = (long long)it.t * KB;
+    const long long o0 = owner_of(first, U, G);
+    it.seg = (int)(blockIdx.x - o0);
+    it.nseg = (int)(owner_of(first + KB - 1, U, G) - o0 + 1);
+  }
+  it.ta = it.t / p.tilesB;
+  it.tb = it.t % p.tilesB;
+  return true;
+}
+
+// A wait every lane of the warp takes; the outcome is made warp-uniform so
+// that the .sync.aligned tcgen05 loads that follow stay convergent.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Wait that ignores the abort flag (used only to let in-flight async copies
+// and MMAs land before the CTA exits); bounded by the same limit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           int *status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > timeout_ns) {
+      if (status) atomicOr(status, 0x1);
+      return;
+    }
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<16>(uint32_t taddr, uint32_t (&r)[16]) {
+  tmem_ld16(taddr, r);
+}
+
+__device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, float v) {
+  if (p.out_f32)
+    reinterpret_cast<float *>(p.y)[(size_t)m * p.ldy + n] = v;
+  else
+    reinterpret_cast<uint16_t *>(p.y)[(size_t)m * p.ldy + n] =
+        static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+}
+
+template <int KIND, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  using C = Cfg<KIND, BN>;
+  constexpr int S = C::kStages;
+  constexpr int CH = C::kChunk;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sA = base;
+  const uint32_t sB = sA + S * C::kABytes;
+  const uint32_t sSFA = sB + S * C::kBBytes;
+  const uint32_t sSFB = sSFA + S * C::kSfaBytes;
+  const uint32_t bars = sSFB + S * C::kSfbBytes;
+  const uint32_t acc_full = bars + 8 * (2 * S);
+  const uint32_t acc_empty = acc_full + 8;
+  const uint32_t part_bar = acc_full + 16;
+  const uint32_t dec_bar = acc_full + 24;
+  const uint32_t stall_bar = acc_full + 32;
+  const uint32_t mma_done = acc_full + 40;
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (2 * S + 6);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
+  volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(part_bar, 128);
+    mbar_init(dec_bar, 1);
+    mbar_init(stall_bar, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    *decision = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint64_t polA = p.swap ? pol_stream : pol_keep;  // swapped: A = weights, read once
+      const uint64_t polB = pol_keep;
+      long long cur = first_cursor(p);
+      Item it;
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      while (ok && next_item(p, cur, it)) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          uint32_t bytes = C::kABytes + C::kBBytes;
+          int natoms = 0, nblk = 0, rb0 = 0;
+          if (KIND == 0) {
+            natoms = min(2, p.G4 - 2 * kb);
+            rb0 = (it.tb * BN) / 128;
+            nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+            bytes += (uint32_t)(natoms * 512 * (1 + nblk));
+          }
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
+          tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
+          if (KIND == 0) {
+            bulk_load(sSFA + stage * C::kSfaBytes,
+                      p.sfA + ((size_t)it.ta * p.G4 + 2 * kb) * 512u, natoms * 512, fb, polA);
+            for (int j = 0; j < nblk; ++j)
+              bulk_load(sSFB + stage * C::kSfbBytes + j * 1024,
+                        p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * kb) * 512u, natoms * 512, fb,
+                        polB);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        // let every copy still in flight land before the CTA can exit
+        const long long n = issued < S ? issued : S;
+        for (long long k = 1; k <= n; ++k) {
+          const long long pos = issued - k;
+          drain_wait(full_bar((int)(pos % S)), (uint32_t)((pos / S) & 1), p.timeout_ns, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc0 = KIND == 0 ? idesc_mxf4(kTileA, BN) : idesc_f8(kTileA, BN);
+      long long cur = first_cursor(p);
+      Item it;
+      int stage = 0;
+      uint32_t phase = 0;
+      int i = 0;
+      bool ok = true;
+      while (ok && next_item(p, cur, it)) {
+        if (i > 0 && !mbar_wait(acc_empty, (uint32_t)((i - 1) & 1), ctl)) break;
+        tc_fence_after();
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sA + stage * C::kABytes;
+          const uint32_t b0 = sB + stage * C::kBBytes;
+          if (KIND == 0) {
+            const int natoms = min(2, p.G4 - 2 * kb);
+            const int rb0 = (it.tb * BN) / 128;
+            const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+            for (int a = 0; a < natoms; ++a)
+              tc_cp_sf(tmem + kSfaCol + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
+            for (int j = 0; j < nblk; ++j)
+              for (int a = 0; a < natoms; ++a)
+                tc_cp_sf(tmem + kSfbCol + 8 * a + 4 * j,
+                         sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * 1024 + a * 512));
+            const int nk = min(4, (p.K - kb * 256) / 64);
+            for (int s = 0; s < nk; ++s) {
+              const uint32_t sel = (uint32_t)(s & 1) * 2u;
+              mma_mxf4(tmem + kAccCol, sdesc_kmajor_sw128(a0 + 32 * s),
+                       sdesc_kmajor_sw128(b0 + 32 * s), idesc_sf_ids(idesc0, sel, sel),
+                       tmem + kSfaCol + 4 * (s >> 1), tmem + kSfbCol + 8 * (s >> 1),
+                       (kb > it.kb0 || s > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_f8(tmem + kAccCol, sdesc_kmajor_sw128(a0 + 32 * s),
+                     sdesc_kmajor_sw128(b0 + 32 * s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        ++i;
+      }
+      // every MMA issued so far must finish before TMEM is released
+      tc_commit(mma_done);
+      drain_wait(mma_done, 0, p.timeout_ns, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int r_in = q * 32 + lane;    // row of the MMA-A tile
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + kAccCol;
+    long long cur = first_cursor(p);
+    Item it;
+    int i = 0;
+    uint32_t part_phase = 0;
+    while (next_item(p, cur, it)) {
+      if (p.debug_stall && i == 0) {
+        // test hook: a barrier nothing arrives at; the bounded wait gives up
+        if (!warp_wait(stall_bar, 0, ctl)) break;
+      }
+      if (!warp_wait(acc_full, (uint32_t)(i & 1), ctl)) break;
+      tc_fence_after();
+      const int ra = it.ta * kTileA + r_in;  // MMA-A row: token (full tile) / weight row (split)
+      const int cb0 = it.tb * BN;            // first MMA-B row of the tile
+      const int ncols = min(BN, p.rowsB - cb0);
+      const bool whole = (it.kb0 == 0 && it.kb1 == p.kblocks);
+      bool ok = true;
+      if (whole && !p.swap) {
+        // rows = tokens, columns = output channels: each thread writes a row run
+        const bool mvalid = ra < p.M;
+        const float sa = (KIND == 1 && mvalid) ? p.tok_scale[ra] : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_wait();
+          const int n0 = cb0 + c * CH;
+          if (!mvalid || n0 >= p.N) continue;
+          float f[CH];
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            f[j] = __uint_as_float(v[j]);
+            if (KIND == 1) f[j] = (f[j] * sa) * p.chan_scale[min(n0 + j, p.N - 1)];
+          }
+          if (n0 + CH <= p.N) {
+            if (p.out_f32) {
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) +
+                                                       (size_t)ra * p.ldy + n0);
+#pragma unroll
+              for (int j = 0; j < CH / 4; ++j)
+                dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+            } else {
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) +
+                                                     (size_t)ra * p.ldy + n0);
+#pragma unroll
+              for (int j = 0; j < CH / 8; ++j)
+                dst[j] = make_uint4(pack_bf16x2(f[8 * j], f[8 * j + 1]),
+                                    pack_bf16x2(f[8 * j + 2], f[8 * j + 3]),
+                                    pack_bf16x2(f[8 * j + 4], f[8 * j + 5]),
+                                    pack_bf16x2(f[8 * j + 6], f[8 * j + 7]));
+            }
+          } else {
+            for (int j = 0; j < CH && n0 + j < p.N; ++j) store_out(p, ra, n0 + j, f[j]);
+          }
+        }
+      } else if (whole) {
+        // swapped, one CTA covered all of K: rows = output channels, columns = tokens
+        const int n = ra;
+        const float sw = (KIND == 1 && n < p.N) ? p.chan_scale[n] : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CH; ++j) {
+            const int m = cb0 + c * CH + j;
+            if (m < p.M && n < p.N) {
+              float f = __uint_as_float(v[j]);
+              if (KIND == 1) f = (f * p.tok_scale[m]) * sw;
+              store_out(p, m, n, f);
+            }
+          }
+        }
+      } else {
+        // swapped, part of K: publish an fp32 partial tile, then the last
+        // CTA of the tile reduces all partials in slot order
+        const size_t slot_elems = (size_t)BN * kTileA;
+        float *tile_ws = p.ws + (size_t)it.t * p.seg_max * slot_elems;
+        float *mine = tile_ws + (size_t)it.seg * slot_elems;
+#pragma unroll 1
+        for (int c = 0; c < BN / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
+        }
+        __threadfence();
+        mbar_arrive(part_bar);
+        if (warp == 2 && lane == 0) {
+          const bool okp = mbar_wait(part_bar, part_phase, ctl);
+          int last = 0;
+          if (okp) {
+            __threadfence();
+            const int old = atomicAdd(&p.counters[it.t], 1);
+            last = (old == it.nseg - 1) ? 1 : 0;
+            if (last) atomicExch(&p.counters[it.t], 0);  // left zero for the next call
+          }
+          *decision = okp ? last : -1;
+          mbar_arrive(dec_bar);
+        }
+        ok = warp_wait(dec_bar, part_phase, ctl);
+        part_phase ^= 1u;
+        const int dec = ok ? *decision : -1;
+        if (dec < 0) {
+          ok = false;
+        } else if (dec == 1) {
+          __threadfence();
+          const int n = ra;
+          const float sw = (KIND == 1 && n < p.N) ? p.chan_scale[n] : 1.0f;
+          for (int c = 0; c < ncols; ++c) {
+            float acc = 0.0f;
+            for (int s = 0; s < it.nseg; ++s)
+              acc += ld_cg_f32(tile_ws + (size_t)s * slot_elems + (size_t)c * kTileA + r_in);
+            const int m = cb0 + c;
+            if (n < p.N) {
+              float f = acc;
+              if (KIND == 1) f = (f * p.tok_scale[m]) * sw;
+              store_out(p, m, n, f);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      if (!ok) break;
+      ++i;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int KIND, int BN>
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p, int ctas,
+                     cudaStream_t stream) {
+  using C = Cfg<KIND, BN>;
+  auto kern = gemm_kernel<KIND, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<ctas, kThreads, C::kSmem, stream>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const GemmParams &p, int ctas, cudaStream_t stream) {
+  switch (bn) {
+    case 16: return launch_t<KIND, 16>(tmA, tmB, p, ctas, stream);
+    case 32: return launch_t<KIND, 32>(tmA, tmB, p, ctas, stream);
+    case 64: return launch_t<KIND, 64>(tmA, tmB, p, ctas, stream);
+    case 128: return launch_t<KIND, 128>(tmA, tmB, p, ctas, stream);
+    case 256: return launch_t<KIND, 256>(tmA, tmB, p, ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int KIND>
+int stages_kind(int bn) {
+  switch (bn) {
+    case 16: return Cfg<KIND, 16>::kStages;
+    case 32: return Cfg<KIND, 32>::kStages;
+    case 64: return Cfg<KIND, 64>::kStages;
+    case 128: return Cfg<KIND, 128>::kStages;
+    case 256: return Cfg<KIND, 256>::kStages;
+    default: return 0;
+  }
+}
+
+template <int KIND>
+size_t smem_kind(int bn) {
+  switch (bn) {
+    case 16: return Cfg<KIND, 16>::kSmem;
+    case 32: return Cfg<KIND, 32>::kSmem;
+    case 64: return Cfg<KIND, 64>::kSmem;
+    case 128: return Cfg<KIND, 128>::kSmem;
+    case 256: return Cfg<KIND, 256>::kSmem;
+    default: return 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        const GemmParams &p, int ctas, cudaStream_t stream) {
+  return kind == 0 ? launch_kind<0>(bn, tmA, tmB, p, ctas, stream)
+                   : launch_kind<1>(bn, tmA, tmB, p, ctas, stream);
+}
+
+int gemm_stages(int kind, int bn) { return kind == 0 ? stages_kind<0>(bn) : stages_kind<1>(bn); }
+
+size_t gemm_smem_bytes(int kind, int bn) {
+  return kind == 0 ? smem_kind<0>(bn) : smem_kind<1>(bn);
+}
+
+}  // namespace mxg

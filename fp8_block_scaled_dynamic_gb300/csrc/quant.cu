@@ -1,0 +1,252 @@
+// quant.cu -- HBM-bound quantizer kernels.
+//
+//  * mx_quant_kernel: OCP-MX MXFP4 quantization of bf16 rows ("Kimi-K3 DSpark
+//    O-Proj-only MXFP4", "Exact quantization coverage": E2M1 codes, one E8M0
+//    scale per 32 consecutive input channels).  One thread owns one 16-byte
+//    chunk (8 values = a quarter block); the block amax is a max over 4
+//    lanes by warp shuffles; codes leave as packed nibbles and scales go
+//    straight into the row-major or the 128x4-tile layout.
+//  * fp8_quant_kernel: per-row E4M3 quantization with an FP32 scale
+//    ("Kimi-K3-DSpark-FP8-PTPC", "Phase 1 FP8 PTPC Quantization": dynamic
+//    per-token activations; per-output-channel weights are per-row of W).
+//
+// Numerics (shared readings, see the public header): MX scale e =
+// clamp(floor(log2 amax) - 2, -127, 127), code = E2M1_RNE_sat(x * 2^-e) with
+// the sign of x; FP8 s = amax / 448 (1 for an all-zero row), q =
+// E4M3_RNE_sat(x / s).  Built without fast-math: x * 2^-e is an exact fp32
+// product (subnormal inputs included) and x / s is IEEE division.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace mxg {
+
+namespace {
+
+// Two fp32 values -> one byte of two E2M1 codes (lo in the low nibble),
+// round to nearest even, saturating to +-6.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 values -> two E4M3 bytes (lo in the low byte), RNE, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Sign bits of the two bf16 in `w`, moved to bits 3 and 7 of a byte (the sign
+// bits of the two E2M1 nibbles).
+__device__ __forceinline__ uint32_t nibble_signs(uint32_t w) {
+  return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
+}
+
+// Sign bits of the two bf16 in `w`, moved to bits 7 and 15 (the sign bits
+// of the two E4M3 bytes).
+__device__ __forceinline__ uint32_t byte_signs(uint32_t w) {
+  return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+constexpr int kMxThreads = 256;
+constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in flight per thread
+
+// grid: x = chunk groups along the row, y = rows (grid-stride).
+// rows_iter >= rows: rows in [rows, rows_iter) are padding (swizzled layout
+// only) -- their scales are written as 0 and no codes are stored.
+template <bool kSwizzled>
+__global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
+                                                              long long ldx, int rows,
+                                                              int rows_iter, int K,
+                                                              uint8_t *__restrict__ codes,
+                                                              uint8_t *__restrict__ sf) {
+  const int cpr = K >> 3;  // 16-byte chunks per row; K % 128 == 0 => cpr % 16 == 0
+  const int G = K >> 5;    // MX blocks per row
+  const int lane = threadIdx.x & 31;
+  const unsigned kFull = 0xFFFFFFFFu;
+  for (int r = blockIdx.y; r < rows_iter; r += gridDim.y) {
+    const bool real_row = r < rows;
+    uint4 v[kMxChunksPerThread];
+    int cc[kMxChunksPerThread];
+#pragma unroll
+    for (int i = 0; i < kMxChunksPerThread; ++i) {
+      cc[i] = (blockIdx.x * kMxChunksPerThread + i) * kMxThreads + threadIdx.x;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (real_row && cc[i] < cpr) v[i] = ld_stream_v4(x + (size_t)r * ldx + (size_t)cc[i] * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < kMxChunksPerThread; ++i) {
+      // cpr % 16 == 0: a half-warp is wholly inside the row or wholly past
+      // it; past the row it runs on zeros (the shuffles need every lane)
+      // and stores nothing.
+      const bool in_row = cc[i] < cpr;
+      const uint4 w = v[i];
+      // |x| as bf16 bits; unsigned max orders finite < inf < nan.
+      uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                             __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+      uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
+      amax = max(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = max(amax, __shfl_xor_sync(kFull, amax, 2));
+      uint32_t scode, packed;
+      if (amax >= 0x7F80u) {  // the block holds Inf or NaN
+        scode = 0xFFu;
+        packed = 0u;
+      } else {
+        // floor(log2 amax) = ef - 127 for a normal amax; a zero or subnormal
+        // amax clamps to e = -127 like ef in {1, 2}: e = max(ef, 2) - 129.
+        const int ef = max(static_cast<int>(amax >> 7), 2);
+        scode = static_cast<uint32_t>(ef - 2);
+        const float inv = __uint_as_float(static_cast<uint32_t>(256 - ef) << 23);  // 2^-e
+        packed = e2m1x2(bf16_lo(w.x) * inv, bf16_hi(w.x) * inv) |
+                 (e2m1x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 8) |
+                 (e2m1x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) << 16) |
+                 (e2m1x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 24);
+        packed |= nibble_signs(w.x) | (nibble_signs(w.y) << 8) | (nibble_signs(w.z) << 16) |
+                  (nibble_signs(w.w) << 24);
+      }
+      if (real_row && in_row)
+        *reinterpret_cast<uint32_t *>(codes + (size_t)r * (K >> 1) + (size_t)cc[i] * 4) = packed;
+      // Gather the scales of 4 consecutive blocks (lanes 0,4,8,12 of each
+      // half-warp) into one 32-bit word.
+      const uint32_t s1 = __shfl_down_sync(kFull, scode, 4);
+      const uint32_t s2 = __shfl_down_sync(kFull, scode, 8);
+      const uint32_t s3 = __shfl_down_sync(kFull, scode, 12);
+      if (in_row && (lane & 15) == 0) {
+        const uint32_t word = scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        const int g = cc[i] >> 2;  // first of the 4 blocks, g % 4 == 0
+        size_t off;
+        if (kSwizzled)
+          off = ((size_t)(r >> 7) * (size_t)(G >> 2) + (size_t)(g >> 2)) * 512u +
+                (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u;
+        else
+          off = (size_t)r * G + g;
+        *reinterpret_cast<uint32_t *>(sf + off) = word;
+      }
+    }
+  }
+}
+
+constexpr int kF8Threads = 256;
+constexpr int kF8RegChunks = 12;  // rows of up to 12*256*8 = 24576 values stay in registers
+
+// One CTA per row (grid-stride over rows).
+__global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *__restrict__ x,
+                                                               long long ldx, int rows, int K,
+                                                               uint8_t *__restrict__ q,
+                                                               float *__restrict__ scale) {
+  __shared__ uint32_t red[kF8Threads / 32];
+  const int cpr = K >> 3;
+  const int tid = threadIdx.x;
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t *xr = x + (size_t)r * ldx;
+    uint4 v[kF8RegChunks];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < kF8RegChunks; ++i) {
+      const int c = i * kF8Threads + tid;
+      v[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < cpr) v[i] = ld_stream_v4(xr + (size_t)c * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < kF8RegChunks; ++i) {
+      uint32_t m2 = __vmaxu2(__vmaxu2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
+                             __vmaxu2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
+      amax = max(amax, max(m2 & 0xFFFFu, m2 >> 16));
+    }
+    for (int c = kF8RegChunks * kF8Threads + tid; c < cpr; c += kF8Threads) {  // long rows
+      const uint4 w = ld_stream_v4(xr + (size_t)c * 8);
+      uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                             __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+      amax = max(amax, max(m2 & 0xFFFFu, m2 >> 16));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kF8Threads / 32; ++i) amax = max(amax, red[i]);
+    __syncthreads();  // red[] is reused by the next row
+
+    uint8_t *qr = q + (size_t)r * K;
+    if (amax >= 0x7F80u) {  // Inf or NaN in the row
+      if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
+      for (int c = tid; c < cpr; c += kF8Threads)
+        *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = make_uint2(0u, 0u);
+      continue;
+    }
+    const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
+    if (tid == 0) scale[r] = s;
+    auto quant8 = [&](const uint4 &w) {
+      uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w.x), s), __fdiv_rn(bf16_hi(w.x), s)) |
+                    (e4m3x2(__fdiv_rn(bf16_lo(w.y), s), __fdiv_rn(bf16_hi(w.y), s)) << 16);
+      uint32_t hi = e4m3x2(__fdiv_rn(bf16_lo(w.z), s), __fdiv_rn(bf16_hi(w.z), s)) |
+                    (e4m3x2(__fdiv_rn(bf16_lo(w.w), s), __fdiv_rn(bf16_hi(w.w), s)) << 16);
+      // keep the sign of x on codes that round to zero
+      lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
+      hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
+      return make_uint2(lo, hi);
+    };
+#pragma unroll
+    for (int i = 0; i < kF8RegChunks; ++i) {
+      const int c = i * kF8Threads + tid;
+      if (c < cpr) *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = quant8(v[i]);
+    }
+    for (int c = kF8RegChunks * kF8Threads + tid; c < cpr; c += kF8Threads)
+      *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = quant8(ld_stream_v4(xr + (size_t)c * 8));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
+                            uint8_t *sf, bool swizzled, int sm_count, cudaStream_t stream) {
+  const int cpr = K / 8;
+  const int per_block = kMxThreads * kMxChunksPerThread;
+  const int gx = (cpr + per_block - 1) / per_block;
+  const int rows_iter = swizzled ? ((rows + 127) / 128) * 128 : rows;
+  // enough CTAs for ~8 resident per SM, rows beyond that are grid-strided
+  int gy = rows_iter;
+  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
+  if (gy * gx > cap) gy = (cap + gx - 1) / gx;
+  if (gy > 65535) gy = 65535;
+  if (gy < 1) gy = 1;
+  dim3 grid(gx, gy);
+  if (swizzled)
+    mx_quant_kernel<true><<<grid, kMxThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, codes, sf);
+  else
+    mx_quant_kernel<false><<<grid, kMxThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, codes, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
+                             float *scale, int sm_count, cudaStream_t stream) {
+  int g = rows;
+  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
+  if (g > cap) g = cap;
+  fp8_quant_kernel<<<g, kF8Threads, 0, stream>>>(static_cast<const uint16_t *>(x), ldx, rows, K,
+                                                 q, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

@@ -1,0 +1,193 @@
+/*
+ * mxgemm.h -- C ABI of the GB300 (sm_103a) MXFP4 A4W4 / FP8 PTPC A8W8 library.
+ *
+ * The library implements the quantized linear layers of a mixed-precision
+ * speculative-decoding draft model:
+ *
+ *   - MXFP4 (page "Kimi-K3 DSpark O-Proj-only MXFP4", section "Exact
+ *     quantization coverage"): E2M1 element codes, one E8M0 scale per 32
+ *     consecutive input-channel values, weight stored (N, K) = (7168, 8192)
+ *     with scale (7168, 256); at run time "dynamic MXFP4 activations with
+ *     A4W4 dispatch" (the same section).  "OCP MXFP4" names the standard
+ *     (page "Kimi-K3-Quark-MXFP4-AttnFP8", section "Model Overview").
+ *   - FP8 PTPC (page "Kimi-K3-DSpark-FP8-PTPC", section "Phase 1 FP8 PTPC
+ *     Quantization"): E4M3 weights with one FP32 scale per output channel
+ *     (shape (out_features, 1)); activations quantized per token at run time,
+ *     never calibrated or stored.
+ *
+ * Conventions for every entry point:
+ *   - Linear layout y = x . W^T: x (M, K) and W (N, K) are row-major and
+ *     K-contiguous (leading dimensions in ELEMENTS); y (M, N) row-major.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory and keeps no pointer after a call
+ *     returns.  Scratch memory, where needed, is the caller's workspace.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     do not synchronise the host, except mxg_query_status.
+ *   - Host-detectable errors (bad shape, alignment, device, workspace) are
+ *     returned before anything is launched.  A failed launch returns
+ *     MXG_ERR_CUDA.  Device-side waits are bounded; a wait that runs out
+ *     ORs MXG_DEV_TIMEOUT into opts->dev_status (if given) and the kernel
+ *     returns early, leaving the context usable.
+ *   - Requirements: compute capability 10.3 (GB300); K % 128 == 0; M, N >= 1
+ *     (N % 128 == 0 for the GEMMs); every pointer 16-byte aligned; every
+ *     leading dimension a multiple of 16 bytes.
+ *   - Quantization rules (the pages fix the formats, not the rounding; these
+ *     are the readings the library and its CPU oracle share):
+ *       MX: per block of 32, amax = max|x|; e = clamp(floor(log2 amax) - 2,
+ *           -127, 127) (an all-zero block gets e = -127); scale code = e+127;
+ *           code = E2M1(x * 2^-e), round to nearest even, saturating, sign
+ *           kept (also for -0).  A block holding NaN/Inf gets scale 0xFF and
+ *           zero codes.  Two codes per byte, the lower k in the low nibble.
+ *       FP8: per row, s = amax / 448 (fp32 division); s = 1 for an all-zero
+ *           row; q = E4M3(x / s) (fp32 division, then round to nearest even,
+ *           saturating at +-448, sign kept).  A row holding NaN/Inf gets
+ *           s = NaN and zero codes.
+ */
+#ifndef MXGEMM_H
+#define MXGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *mxg_stream_t;
+
+typedef enum {
+    MXG_OK = 0,
+    MXG_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad enum */
+    MXG_ERR_UNSUPPORTED_SHAPE = 2,  /* K % 128 != 0, N % 128 != 0, size too large */
+    MXG_ERR_MISALIGNED = 3,         /* pointer or leading dimension not 16-byte aligned */
+    MXG_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    MXG_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+    MXG_ERR_TIMEOUT = 6,            /* a device-side bounded wait ran out (mxg_query_status) */
+    MXG_ERR_WORKSPACE = 7           /* workspace missing or smaller than required */
+} mxg_status;
+
+/* Bits a kernel ORs into the optional device status word. */
+#define MXG_DEV_TIMEOUT 0x1
+#define MXG_DEV_BAD_INDEX 0x2
+
+typedef enum {
+    MXG_SF_ROWMAJOR = 0, /* (rows, K/32) bytes, row-major: the stored checkpoint layout */
+    MXG_SF_SWIZZLED = 1  /* 128x4 tiles of 512 bytes (see mxg_sf_bytes); the GEMM operand layout */
+} mxg_sf_layout;
+
+typedef enum {
+    MXG_OUT_BF16 = 0, /* y rounded to bf16 (round to nearest even) */
+    MXG_OUT_F32 = 1   /* y in fp32 before the bf16 cast (test / parity mode) */
+} mxg_out_dtype;
+
+typedef enum {
+    MXG_VARIANT_AUTO = 0,   /* the dispatcher chooses from (M, N, K, SM count) */
+    MXG_VARIANT_FULL = 1,   /* one CTA owns a whole output tile and all of K */
+    MXG_VARIANT_SPLITK = 2  /* operands swapped (weights fill the 128-row MMA side),
+                               K split across CTAs (stream-K), fixed-order reduction */
+} mxg_variant;
+
+typedef struct {
+    int variant;          /* mxg_variant */
+    int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over; 0 = SM count */
+    void *workspace;      /* device scratch of >= mxg_gemm_workspace_bytes() bytes,
+                             256-byte aligned.  Its first 64 KiB hold split-K arrival
+                             counters: zero them before the first call; every completed
+                             call leaves them zero again (after MXG_ERR_TIMEOUT, zero them
+                             again).  Calls that overlap on the GPU need separate
+                             workspaces.  NULL only when the call needs none. */
+    size_t ws_bytes;      /* size of workspace */
+    int *dev_status;      /* optional device int; kernels OR MXG_DEV_* bits into it */
+    uint32_t timeout_ms;  /* limit of every device-side wait; 0 = 1000 ms */
+    int debug_stall;      /* test hook: 1 makes the epilogue wait on a barrier nothing
+                             arrives at, so the timeout path runs (no fault, no hang) */
+} mxg_gemm_opts;
+
+typedef struct {
+    int variant;       /* MXG_VARIANT_FULL or MXG_VARIANT_SPLITK */
+    int bm, bn;        /* MMA tile: bm rows of the 128-row operand, bn of the other */
+    int ctas;          /* grid size */
+    int tiles;         /* output tiles */
+    int kblocks;       /* K-blocks per tile (256 K for A4W4, 128 K for PTPC) */
+    int seg_max;       /* SPLITK: most CTAs contributing to one tile */
+    size_t ws_bytes;   /* workspace this plan needs */
+} mxg_plan;
+
+/* Bytes of a scale-factor array for `rows` rows of K elements (K/32 groups).
+ * ROWMAJOR: rows * K/32.  SWIZZLED: ceil(rows/128)*128 * K/32: the scale of
+ * (row r, group g) sits at ((r/128)*(G/4) + g/4)*512 + (r%32)*16 +
+ * ((r%128)/32)*4 + g%4 with G = K/32; padding rows hold 0. */
+size_t mxg_sf_bytes(int rows, int K, mxg_sf_layout layout);
+
+/* Dispatcher, pure host logic (no GPU needed): the variant, tile and grid a
+ * GEMM of kind 0 (A4W4) or 1 (PTPC) at (M, N, K) would use on a device with
+ * `sm_count` SMs under `opts` (nullable), and the workspace it needs. */
+mxg_status mxg_plan_gemm(int kind, int M, int N, int K, int sm_count,
+                         const mxg_gemm_opts *opts, mxg_plan *plan);
+
+/* Workspace bytes mx_gemm_a4w4 (kind 0, fused == 0), mx_gemm_a4w4 with bf16
+ * activations (kind 0, fused == 1) or fp8_gemm_ptpc (kind 1) needs on the
+ * current device with `opts` (nullable); 0 if none. */
+size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
+                                const mxg_gemm_opts *opts);
+
+/* Offline MXFP4 weight conversion ("Exact quantization coverage": E2M1 codes,
+ * E8M0 scale per 32 consecutive input channels).
+ *   w_bf16: (N, K) bf16, leading dimension ldw elements.
+ *   codes:  (N, K/2) bytes, two codes per byte, lower k in the low nibble.
+ *   sf:     mxg_sf_bytes(N, K, layout) bytes, ROWMAJOR (the stored (N, K/32)
+ *           checkpoint layout) or SWIZZLED (the GEMM operand layout). */
+mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw,
+                              uint8_t *codes, uint8_t *sf, mxg_sf_layout layout,
+                              mxg_stream_t stream);
+
+/* Dynamic MXFP4 activation quantization ("dynamic MXFP4 activations with
+ * A4W4 dispatch"): per row of x (M, K) bf16, per block of 32.
+ *   codes: (M, K/2) bytes.  sf: mxg_sf_bytes(M, K, MXG_SF_SWIZZLED) bytes
+ *   (padding rows are written as 0). */
+mxg_status mx_quantize_act(const void *x_bf16, int M, int K, int ldx,
+                           uint8_t *codes, uint8_t *sf, mxg_stream_t stream);
+
+/* Block-scaled A4W4 GEMM ("A4W4 dispatch"): y[m][n] = sum_g 2^(ea[m,g]-127) *
+ * 2^(ew[n,g]-127) * sum_{k in g} v(a[m,k]) v(w[n,k]), fp32 accumulation,
+ * then bf16 (or fp32) output.
+ *   a_codes (M, K/2) + a_sf (swizzled): pre-quantized activations, OR
+ *   a_codes == NULL and x_bf16 (M, K) with leading dimension ldx: the
+ *   activations are quantized inside the call (codes and scales identical to
+ *   mx_quantize_act) into the workspace.
+ *   w_codes (N, K/2), w_sf (swizzled): the weight.
+ *   y: (M, N) with leading dimension ldy elements, bf16 or fp32. */
+mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf,
+                        const void *x_bf16, int ldx,
+                        const uint8_t *w_codes, const uint8_t *w_sf,
+                        int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
+                        const mxg_gemm_opts *opts, mxg_stream_t stream);
+
+/* Dynamic per-token FP8 quantization (and, applied to W rows, the
+ * per-output-channel weight conversion of "Phase 1 FP8 PTPC Quantization").
+ *   x_bf16 (M, K), leading dimension ldx.  q: (M, K) E4M3 bytes.
+ *   scale: M floats (the (out_features, 1) scale when x is a weight). */
+mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx,
+                            uint8_t *q, float *scale, mxg_stream_t stream);
+
+/* FP8 PTPC A8W8 GEMM: y[m][n] = (acc[m][n] * sa[m]) * sw[n] with
+ * acc = sum_k v(qa[m,k]) v(qw[n,k]) accumulated in fp32.
+ *   qa (M, K), sa (M); qw (N, K), sw (N); y (M, N), leading dimension ldy. */
+mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
+                         const uint8_t *qw, const float *sw,
+                         int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
+                         const mxg_gemm_opts *opts, mxg_stream_t stream);
+
+/* Synchronises `stream`, reads the device status word, clears it, and maps
+ * it: MXG_OK, MXG_ERR_TIMEOUT (MXG_DEV_TIMEOUT set) or MXG_ERR_CUDA. */
+mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *mxg_status_string(mxg_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXGEMM_H */

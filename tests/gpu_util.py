@@ -1,0 +1,50 @@
+"""Helpers for the GPU parity tests: device handles, oracle comparisons."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+# Tolerance for GEMM outputs (fp32 before the bf16 cast): the stated bound
+# |gpu - oracle| <= 1e-5 * sum_k |a_k w_k| per element.
+GEMM_REL_TOL = 1e-5
+
+
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda", 0)
+
+
+def np_u8(t):
+    return t.detach().cpu().numpy().astype(np.uint8)
+
+
+def assert_codes_equal(got, want, what):
+    got = np.asarray(got)
+    want = np.asarray(want)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, f"{what}: {len(bad)} mismatches, first at {bad[:5].tolist()}: " \
+                          f"got {got[tuple(bad[0])]} want {want[tuple(bad[0])]}"
+
+
+def assert_gemm_close(y, ref, bound, what, tol=GEMM_REL_TOL):
+    y = np.asarray(y, dtype=np.float64)
+    assert y.shape == ref.shape, (what, y.shape, ref.shape)
+    nan_ref = np.isnan(ref)
+    assert (np.isnan(y) == nan_ref).all(), f"{what}: NaN pattern differs"
+    err = np.abs(y - ref)
+    ok = np.where(nan_ref, True, err <= tol * bound)
+    if not ok.all():
+        idx = np.argwhere(~ok)[:5]
+        i0 = tuple(idx[0])
+        raise AssertionError(f"{what}: {int((~ok).sum())} elements outside tolerance; first {idx.tolist()}"
+                             f" got {y[i0]!r} ref {ref[i0]!r} bound {bound[i0]!r}")
+    rel = np.where(bound > 0, err / np.where(bound > 0, bound, 1), 0)
+    return float(np.nanmax(rel)) if rel.size else 0.0
+
+
+def bf16_rne(y_f32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(y_f32, dtype=np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)

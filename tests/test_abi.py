@@ -1,0 +1,128 @@
+"""CPU-side checks of the C ABI: the library loads without a GPU, exports
+every function include/mxgemm.h declares, rejects bad arguments before any
+launch, and its dispatcher (pure host logic) plans the stream-K split the
+way an independent simulation says it must."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import fp8_block_scaled_dynamic_gb300 as mx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = ""
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src += open(os.path.join(ROOT, "include", f)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s*([a-z_][a-z_0-9]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert {"mx_quantize_weight", "mx_quantize_act", "mx_gemm_a4w4", "fp8_quantize_act",
+            "fp8_gemm_ptpc"} <= set(names)
+    L = mx.lib()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_sf_bytes():
+    assert mx.mxg_sf_bytes(7168, 8192, mx.SF_ROWMAJOR) == 7168 * 256
+    assert mx.mxg_sf_bytes(7168, 8192, mx.SF_SWIZZLED) == 7168 * 256
+    assert mx.mxg_sf_bytes(8, 8192, mx.SF_SWIZZLED) == 128 * 256
+    assert mx.mxg_sf_bytes(129, 256, mx.SF_SWIZZLED) == 256 * 8
+    assert mx.mxg_sf_bytes(0, 256, mx.SF_SWIZZLED) == 0
+
+
+def test_status_strings():
+    L = mx.lib()
+    for code, name in mx.STATUS_NAMES.items():
+        assert L.mxg_status_string(code).decode() == name
+
+
+FAKE = 1 << 20  # a 16-byte aligned pointer value; nothing is dereferenced on these paths
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, 8, 100, 100, FAKE, FAKE, None), 2),   # K % 128
+    ((None, 8, 128, 128, FAKE, FAKE, None), 1),   # null input
+    ((FAKE, 0, 128, 128, FAKE, FAKE, None), 1),   # M = 0
+    ((FAKE, 8, 128, 64, FAKE, FAKE, None), 1),    # ld < K
+    ((FAKE + 2, 8, 128, 128, FAKE, FAKE, None), 3),  # misaligned x
+    ((FAKE, 8, 128, 132, FAKE, FAKE, None), 3),   # ld*2 not a multiple of 16
+    ((FAKE, 8, 128, 128, FAKE + 8, FAKE, None), 3),  # misaligned codes
+])
+def test_quantizer_argument_errors_before_launch(args, want):
+    assert mx.lib().mx_quantize_act(*args) == want
+
+
+def test_gemm_argument_errors_before_launch():
+    L = mx.lib()
+    o = mx.GemmOpts()
+    # N % 128
+    assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 100, 128, FAKE, 100, 0, ctypes.byref(o), None) == 2
+    # bad output dtype
+    assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, 7, ctypes.byref(o), None) == 1
+    # ldy < N
+    assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, FAKE, 8, 256, 256, FAKE, 128, 0, None, None) == 1
+    # fused path without x
+    assert L.mx_gemm_a4w4(None, None, None, 0, FAKE, FAKE, 8, 256, 256, FAKE, 256, 0, None, None) == 1
+    # misaligned y
+    assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, FAKE, 8, 256, 256, FAKE + 4, 256, 0, None, None) == 3
+    # bad variant
+    o.variant = 9
+    assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, FAKE, 8, 256, 256, FAKE, 256, 0, ctypes.byref(o), None) == 1
+
+
+def owner_sim(U, G):
+    """Independent statement of the even stream-K cut: CTA c takes units
+    [floor(c U / G), floor((c+1) U / G))."""
+    own = np.empty(U, np.int64)
+    for c in range(G):
+        own[(c * U) // G:((c + 1) * U) // G] = c
+    return own
+
+
+@pytest.mark.parametrize("kind,M,N,K,sm", [(0, 8, 7168, 8192, 152), (0, 64, 7168, 8192, 152),
+                                           (1, 64, 36864, 7168, 152), (1, 64, 7168, 18432, 152),
+                                           (0, 200, 1024, 2048, 7), (1, 1, 128, 128, 152)])
+def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
+    p = mx.mxg_plan_gemm(kind, M, N, K, sm)
+    assert p["variant"] == 2 and p["bm"] == 128
+    assert p["bn"] >= M and p["bn"] in (16, 32, 64, 128, 256) and (p["bn"] // 2 < M or p["bn"] == 16)
+    kstage = 256 if kind == 0 else 128
+    KB = -(-K // kstage)
+    assert p["kblocks"] == KB
+    tiles = (N // 128) * (-(-M // p["bn"]))
+    assert p["tiles"] == tiles
+    U = tiles * KB
+    G = min(sm, U)
+    assert p["ctas"] == G
+    own = owner_sim(U, G)
+    seg = max(len(set(own[t * KB:(t + 1) * KB])) for t in range(tiles))
+    assert p["seg_max"] == seg
+    if seg > 1:
+        assert p["ws_bytes"] >= tiles * seg * p["bn"] * 128 * 4
+
+
+def test_plan_full_tile_for_large_m():
+    p = mx.mxg_plan_gemm(0, 8192, 7168, 8192, 152)
+    assert p["variant"] == 1 and p["bn"] == 256 and p["tiles"] == 64 * 28 and p["ctas"] == 152
+    assert p["ws_bytes"] == 0
+    p = mx.mxg_plan_gemm(1, 300, 384, 1024, 152, variant="splitk")
+    assert p["variant"] == 2 and p["bn"] == 256 and p["tiles"] == 3 * 2
+
+
+def test_plan_errors():
+    with pytest.raises(mx.MxgError):
+        mx.mxg_plan_gemm(0, 8, 7168, 8000, 152)  # K % 128
+    with pytest.raises(mx.MxgError):
+        mx.mxg_plan_gemm(2, 8, 7168, 8192, 152)  # kind

@@ -1,0 +1,44 @@
+"""Failure detection without a GPU fault: the debug_stall hook makes the
+epilogue wait on a barrier that nothing arrives at; the bounded wait must
+give up, the kernel must record MXG_DEV_TIMEOUT in the caller's status word
+and return, and the context must stay usable for the next (correct) call."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_dynamic_gb300 as mx
+import oracle
+import synth
+from gpu_util import assert_gemm_close, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("kind,variant", [(0, "full"), (0, "splitk"), (1, "splitk")])
+def test_stall_times_out_then_next_call_is_correct(kind, variant):
+    d = dev()
+    M, N, K = 16, 512, 1024
+    x = synth.activation(M, K, seed=50)
+    w = synth.weight(N, K, seed=51)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device=d)
+    if kind == 0:
+        wc, wsf = mx.mx_quantize_weight(w.to(d))
+        run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant=variant, ws=ws, **kw)
+        ac, asf = oracle.mx_quantize_rows(x)
+        wr, wsr = oracle.mx_quantize_rows(w)
+        ref, bound = oracle.gemm_a4w4(ac, asf, wr, wsr)
+    else:
+        qw, sw = mx.fp8_quantize_act(w.to(d))
+        qa, sa = mx.fp8_quantize_act(x.to(d))
+        run = lambda **kw: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant=variant, ws=ws, **kw)
+        qar, sar = oracle.fp8_quantize_rows(x)
+        qwr, swr = oracle.fp8_quantize_rows(w)
+        ref, bound = oracle.gemm_ptpc(qar, sar, qwr, swr)
+    run(dev_status=status, timeout_ms=20, debug_stall=1)
+    assert mx.mxg_query_status(status) == 6  # MXG_ERR_TIMEOUT
+    assert int(status.item()) == 0           # cleared by the query
+    ws.zero_()                               # a timed-out call may leave counters behind
+    y = run(dev_status=status)
+    assert mx.mxg_query_status(status) == 0
+    assert_gemm_close(y.cpu().numpy(), ref, bound, "after timeout")
