@@ -215,7 +215,8 @@ class OprojChain(Workload):
             wc, wsf = self.w[l]
             out.append(("mx_quant", lambda l=l: mx.mx_quantize_act(self.x[l], codes=self.ac[l], sf=self.asf[l])))
             out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
-                wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws)))
+                wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws,
+                weights_static=True)))
         return out
 
     def e2e_step(self):
@@ -269,9 +270,11 @@ class MlpFp8(Workload):
     def launches(self):
         mx = self.mx
         return [("fp8_quant", lambda: mx.fp8_quantize_act(self.xg, q=self.qa_g, scale=self.sa_g)),
-                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg, ws=self.ws)),
+                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg,
+                                                          ws=self.ws, weights_static=True)),
                 ("fp8_quant", lambda: mx.fp8_quantize_act(self.xd, q=self.qa_d, scale=self.sa_d)),
-                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd, ws=self.ws))]
+                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd,
+                                                       ws=self.ws, weights_static=True))]
 
     def e2e_step(self):
         mx = self.mx

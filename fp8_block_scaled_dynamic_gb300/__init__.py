@@ -44,7 +44,8 @@ class GemmOpts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("ctas", ctypes.c_int),
                 ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
                 ("dev_status", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint32),
-                ("debug_stall", ctypes.c_int)]
+                ("debug_stall", ctypes.c_int), ("weights_static", ctypes.c_int),
+                ("trace", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -198,8 +199,10 @@ def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
 
 
 # ---------------------------------------------------------------- GEMMs
-def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall) -> GemmOpts:
-    return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas),
+def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static=False,
+          trace=None) -> GemmOpts:
+    return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas), weights_static=int(weights_static),
+                    trace=0 if trace is None else trace.data_ptr(),
                     workspace=0 if ws is None else ws.data_ptr(),
                     ws_bytes=0 if ws is None else ws.numel() * ws.element_size(),
                     dev_status=0 if dev_status is None else dev_status.data_ptr(),
@@ -216,7 +219,8 @@ def _out(out, M, N, out_f32, device):
 
 def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_sf=None, x=None,
                  out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
-                 ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0, stream=None):
+                 ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
+                 weights_static: bool = False, trace=None, stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
     x (M, K) bf16 (quantized inside the call).  w_sf must be SWIZZLED."""
     N, K2 = w_codes.shape
@@ -232,7 +236,7 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
     out = _out(out, M, N, out_f32, w_codes.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_A4W4, fused, M, N, K, variant, ctas), w_codes.device)
-    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall)
+    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace)
     _check("mx_gemm_a4w4", lib().mx_gemm_a4w4(
         _ptr(a_codes), _ptr(a_sf), _ptr(x), ldx, _ptr(w_codes), _ptr(w_sf), M, N, K,
         _ptr(out), out.stride(0), OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
@@ -241,14 +245,15 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
 
 def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor, *,
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
-                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0, stream=None):
+                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
+                  weights_static: bool = False, trace=None, stream=None):
     """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM."""
     M, K = qa.shape
     N = qw.shape[0]
     out = _out(out, M, N, out_f32, qa.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)
-    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall)
+    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))

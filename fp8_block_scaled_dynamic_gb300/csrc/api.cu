@@ -101,7 +101,7 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
   if (variant == MXG_VARIANT_FULL) {
     pl->bn = 256;
     const long long tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
-    if (tiles > (1LL << 30)) return MXG_ERR_UNSUPPORTED_SHAPE;
+    if (tiles + sm_count >= (1LL << 31)) return MXG_ERR_UNSUPPORTED_SHAPE;
     pl->tiles = (int)tiles;
     pl->ctas = (int)(tiles < sm_count ? tiles : sm_count);
     pl->seg_max = 1;
@@ -120,6 +120,8 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
       if (n > seg_max) seg_max = (int)n;
     }
     if (seg_max > 1 && tiles > kMaxSplitTiles) return MXG_ERR_UNSUPPORTED_SHAPE;
+    // the kernel walks its stream-K range in 32-bit arithmetic
+    if ((U + 1) * G >= (1LL << 32)) return MXG_ERR_UNSUPPORTED_SHAPE;
     pl->tiles = (int)tiles;
     pl->ctas = (int)G;
     pl->seg_max = seg_max;
@@ -150,7 +152,7 @@ struct GemmOperands {
 // (after the counters and, on the fused path, the quantized activations).
 mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void *y, int ldy,
                     mxg_out_dtype out_dtype, const mxg_gemm_opts *opts, void *ws, size_t ws_bytes,
-                    size_t part_off, int sm_count, cudaStream_t stream) {
+                    size_t part_off, bool early_w, int sm_count, cudaStream_t stream) {
   mxg_plan pl;
   mxg_status st = plan_impl(kind, M, N, K, sm_count, opts, &pl);
   if (st != MXG_OK) return st;
@@ -198,6 +200,8 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   const uint32_t tmo = (opts && opts->timeout_ms) ? opts->timeout_ms : 1000u;
   p.timeout_ns = (unsigned long long)tmo * 1000000ull;
   p.debug_stall = opts ? opts->debug_stall : 0;
+  p.early_w = (early_w || (opts && opts->weights_static)) ? 1 : 0;
+  p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
   cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
@@ -313,7 +317,9 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
     part_off += need;
   }
   GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
-  return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, sm, s);
+  // fused: the kernel just before the GEMM is the activation quantizer, which
+  // does not write the weights
+  return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, fused, sm, s);
 }
 
 mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
@@ -329,7 +335,8 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, 
   if ((st = check_device(&sm)) != MXG_OK) return st;
   GemmOperands op{qa, nullptr, qw, nullptr, sa, sw};
   return run_gemm(1, op, M, N, K, y, ldy, out_dtype, opts, opts ? opts->workspace : nullptr,
-                  opts ? opts->ws_bytes : 0, kCounterBytes, sm, reinterpret_cast<cudaStream_t>(stream));
+                  opts ? opts->ws_bytes : 0, kCounterBytes, false, sm,
+                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream) {

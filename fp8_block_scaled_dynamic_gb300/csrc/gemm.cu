@@ -37,8 +37,11 @@ constexpr int kTileA = 128;      // MMA M: rows of the MMA-A operand per tile
 constexpr int kRowBytes = 128;   // K bytes per row per stage (one 128-byte swizzle row)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, BN)
-constexpr uint32_t kSfaCol = 256;  // A scales: 2 tiles x 4 columns
-constexpr uint32_t kSfbCol = 264;  // B scales: 2 K-tiles x (<= 2 row blocks) x 4 columns
+// Scale factors: every pipeline stage has its own TMEM columns from kSfCol on
+// (A: 2 K-tiles x 4 columns, then B: 2 K-tiles x row blocks x 4 columns), so
+// the copy for the next stage never waits for the MMAs still reading the
+// scales of this one.
+constexpr uint32_t kSfCol = 256;
 constexpr int kSmemBudget = 220 * 1024;
 
 template <int KIND, int BN>
@@ -54,8 +57,10 @@ struct Cfg {
   static constexpr int kBarBytes = 8 * (2 * kStages + 6) + 16;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
   static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
+  static constexpr uint32_t kSfColsPerStage = 8u + 8u * (uint32_t)kSfBlocksB;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert(KIND != 0 || kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 };
 
 struct Item {
@@ -63,20 +68,22 @@ struct Item {
 };
 
 // CTA that owns stream-K unit u when U units are cut into G equal ranges
-// [c*U/G, (c+1)*U/G): the largest c with c*U < (u+1)*G.
-__device__ __forceinline__ long long owner_of(long long u, long long U, long long G) {
+// [c*U/G, (c+1)*U/G): the largest c with c*U < (u+1)*G.  The host checks
+// that (U+1)*G fits in 32 bits (64-bit division costs ~1 us per item on
+// the single producer thread).
+__device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t G) {
   return ((u + 1) * G - 1) / U;
 }
 
-__device__ __forceinline__ long long first_cursor(const GemmParams &p) {
-  return p.splitk ? ((long long)blockIdx.x * p.units) / gridDim.x : (long long)blockIdx.x;
+__device__ __forceinline__ uint32_t first_cursor(const GemmParams &p) {
+  return p.splitk ? (blockIdx.x * (uint32_t)p.units) / gridDim.x : blockIdx.x;
 }
 
 // The work items of this CTA, in order; every role walks the same list.
-__device__ __forceinline__ bool next_item(const GemmParams &p, long long &cur, Item &it) {
-  const long long G = gridDim.x;
+__device__ __forceinline__ bool next_item(const GemmParams &p, uint32_t &cur, Item &it) {
+  const uint32_t G = gridDim.x;
   if (!p.splitk) {
-    if (cur >= (long long)p.tilesA * p.tilesB) return false;
+    if (cur >= (uint32_t)(p.tilesA * p.tilesB)) return false;
     it.t = (int)cur;
     it.kb0 = 0;
     it.kb1 = p.kblocks;
@@ -84,22 +91,23 @@ __device__ __forceinline__ bool next_item(const GemmParams &p, long long &cur, I
     it.nseg = 1;
     cur += G;
   } else {
-    const long long U = p.units;
-    const long long u1 = ((long long)(blockIdx.x + 1) * U) / G;
+    const uint32_t U = (uint32_t)p.units;
+    const uint32_t u1 = ((blockIdx.x + 1) * U) / G;
     if (cur >= u1) return false;
-    const int KB = p.kblocks;
-    it.t = (int)(cur / KB);
-    it.kb0 = (int)(cur % KB);
-    const long long room = u1 - cur;
-    it.kb1 = (int)((long long)(KB - it.kb0) < room ? KB : it.kb0 + room);
-    cur += it.kb1 - it.kb0;
-    const long long first = (long long)it.t * KB;
-    const long long o0 = owner_of(first, U, G);
+    const uint32_t KB = (uint32_t)p.kblocks;
+    const uint32_t t = cur / KB;
+    it.t = (int)t;
+    it.kb0 = (int)(cur - t * KB);
+    const uint32_t room = u1 - cur;
+    it.kb1 = (KB - (uint32_t)it.kb0) < room ? (int)KB : it.kb0 + (int)room;
+    cur += (uint32_t)(it.kb1 - it.kb0);
+    const uint32_t first = t * KB;
+    const uint32_t o0 = owner_of(first, U, G);
     it.seg = (int)(blockIdx.x - o0);
     it.nseg = (int)(owner_of(first + KB - 1, U, G) - o0 + 1);
   }
   it.ta = it.t / p.tilesB;
-  it.tb = it.t % p.tilesB;
+  it.tb = it.t - it.ta * p.tilesB;
   return true;
 }
 
@@ -123,6 +131,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
+// Optional timeline: one SM-clock stamp per trace point per CTA (plus the
+// global timer at entry and exit, to line CTAs up against each other).
+__device__ __forceinline__ void trace_mark(const GemmParams &p, int point) {
+  if (p.trace) p.trace[(size_t)blockIdx.x * kTracePoints + point] = clock64();
+}
+__device__ __forceinline__ void trace_set(const GemmParams &p, int point, unsigned long long v) {
+  if (p.trace) p.trace[(size_t)blockIdx.x * kTracePoints + point] = v;
+}
+
 template <int N>
 __device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, uint32_t (&r)[N]);
 template <>
@@ -140,6 +157,78 @@ __device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, flo
   else
     reinterpret_cast<uint16_t *>(p.y)[(size_t)m * p.ldy + n] =
         static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+}
+
+// Sum the nseg partial tiles of one output tile in slot order and write y.
+// Each slot is [column][128 rows] fp32; the 128 epilogue threads take float4
+// groups (4 consecutive rows of one column) so that loads and stores are
+// coalesced, with the loads of up to 4 slots x kU groups in flight at once.
+template <int KIND>
+__device__ __forceinline__ void reduce_partials(const GemmParams &p, const float *tile_ws,
+                                                size_t slot_elems, int nseg, int ncols, int row0,
+                                                int col0, int tid) {
+  constexpr int kU = 4;
+  const int ngrp = ncols * (kTileA / 4);
+  const float4 *base = reinterpret_cast<const float4 *>(tile_ws);
+  const size_t slot4 = slot_elems / 4;
+#pragma unroll 1
+  for (int g0 = tid; g0 < ngrp; g0 += 128 * kU) {
+    float4 acc[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[4][kU];
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int g = g0 + 128 * u;
+        v[s][u] = (s < nseg && g < ngrp) ? __ldcg(base + s * slot4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        acc[u].x += v[s][u].x;
+        acc[u].y += v[s][u].y;
+        acc[u].z += v[s][u].z;
+        acc[u].w += v[s][u].w;
+      }
+#pragma unroll 1
+    for (int s = 4; s < nseg; ++s)
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int g = g0 + 128 * u;
+        if (g < ngrp) {
+          const float4 t = __ldcg(base + s * slot4 + g);
+          acc[u].x += t.x;
+          acc[u].y += t.y;
+          acc[u].z += t.z;
+          acc[u].w += t.w;
+        }
+      }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int g = g0 + 128 * u;
+      if (g >= ngrp) continue;
+      const int c = g / (kTileA / 4);
+      const int r = (g % (kTileA / 4)) * 4;
+      const int m = col0 + c;  // token
+      const int n = row0 + r;  // output channel (N % 128 == 0: always in range)
+      float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+      if (KIND == 1) {
+        const float sa = p.tok_scale[m];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
+      }
+      if (p.out_f32) {
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
+            make_float4(f[0], f[1], f[2], f[3]);
+      } else {
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
+            make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+      }
+    }
+  }
 }
 
 template <int KIND, int BN>
@@ -173,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    trace_mark(p, kTrEntry);
+    trace_set(p, kTrEntryNs, global_timer_ns());
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -202,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+  if (threadIdx.x == 0) trace_mark(p, kTrSetup);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -210,7 +304,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_keep = policy_evict_last();
       const uint64_t polA = p.swap ? pol_stream : pol_keep;  // swapped: A = weights, read once
       const uint64_t polB = pol_keep;
-      long long cur = first_cursor(p);
+      // the operand and scale bytes one stage receives
+      auto stage_bytes = [&](const Item &it, int kb) {
+        uint32_t bytes = C::kABytes + C::kBBytes;
+        if (KIND == 0) {
+          const int natoms = min(2, p.G4 - 2 * kb);
+          const int rb0 = (it.tb * BN) / 128;
+          const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+          bytes += (uint32_t)(natoms * 512 * (1 + nblk));
+        }
+        return bytes;
+      };
+      auto issue_a = [&](int stage, const Item &it, int kb, uint32_t fb) {
+        tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
+        if (KIND == 0)
+          bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * kb) * 512u,
+                    min(2, p.G4 - 2 * kb) * 512, fb, polA);
+      };
+      auto issue_b = [&](int stage, const Item &it, int kb, uint32_t fb) {
+        tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
+        if (KIND == 0) {
+          const int natoms = min(2, p.G4 - 2 * kb);
+          const int rb0 = (it.tb * BN) / 128;
+          const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+          for (int j = 0; j < nblk; ++j)
+            bulk_load(sSFB + stage * C::kSfbBytes + j * 1024,
+                      p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * kb) * 512u, natoms * 512, fb, polB);
+        }
+      };
+      // Weights that the previous kernel did not write may stream in before
+      // griddepcontrol.wait: arm the first stages and issue their weight
+      // operand now, the activation operand after the wait.
+      const bool w_is_a = p.swap != 0;
+      int pre = 0;
+      if (p.early_w) {
+        uint32_t c2 = first_cursor(p);
+        Item it2;
+        while (pre < S && next_item(p, c2, it2)) {
+          for (int kb = it2.kb0; kb < it2.kb1 && pre < S; ++kb, ++pre) {
+            const uint32_t fb = full_bar(pre);
+            mbar_arrive_expect_tx(fb, stage_bytes(it2, kb));
+            if (w_is_a)
+              issue_a(pre, it2, kb, fb);
+            else
+              issue_b(pre, it2, kb, fb);
+          }
+        }
+      }
+      pdl_wait();
+      // Dependents may start only after this kernel's own wait: an early
+      // start then overlaps one kernel at most, never the one before it.
+      pdl_trigger();
+      uint32_t cur = first_cursor(p);
       Item it;
       int stage = 0;
       uint32_t phase = 0;
@@ -218,30 +363,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && next_item(p, cur, it)) {
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
-            ok = false;
-            break;
-          }
           const uint32_t fb = full_bar(stage);
-          uint32_t bytes = C::kABytes + C::kBBytes;
-          int natoms = 0, nblk = 0, rb0 = 0;
-          if (KIND == 0) {
-            natoms = min(2, p.G4 - 2 * kb);
-            rb0 = (it.tb * BN) / 128;
-            nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-            bytes += (uint32_t)(natoms * 512 * (1 + nblk));
+          if (issued < pre) {  // armed before the wait: only the other operand is left
+            if (w_is_a)
+              issue_b(stage, it, kb, fb);
+            else
+              issue_a(stage, it, kb, fb);
+          } else {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, stage_bytes(it, kb));
+            issue_a(stage, it, kb, fb);
+            issue_b(stage, it, kb, fb);
           }
-          mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
-          tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
-          if (KIND == 0) {
-            bulk_load(sSFA + stage * C::kSfaBytes,
-                      p.sfA + ((size_t)it.ta * p.G4 + 2 * kb) * 512u, natoms * 512, fb, polA);
-            for (int j = 0; j < nblk; ++j)
-              bulk_load(sSFB + stage * C::kSfbBytes + j * 1024,
-                        p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * kb) * 512u, natoms * 512, fb,
-                        polB);
-          }
+          if (issued == 0) trace_mark(p, kTrFirstLoad);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -249,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      trace_mark(p, kTrLastLoad);
       if (!ok || *abort_flag) {
         // let every copy still in flight land before the CTA can exit
         const long long n = issued < S ? issued : S;
@@ -256,13 +394,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const long long pos = issued - k;
           drain_wait(full_bar((int)(pos % S)), (uint32_t)((pos / S) & 1), p.timeout_ns, p.status);
         }
+        // stages armed before the wait but never completed by the loop
+        for (long long k = issued; k < pre; ++k)
+          drain_wait(full_bar((int)k), 0, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc0 = KIND == 0 ? idesc_mxf4(kTileA, BN) : idesc_f8(kTileA, BN);
-      long long cur = first_cursor(p);
+      uint32_t cur = first_cursor(p);
       Item it;
       int stage = 0;
       uint32_t phase = 0;
@@ -276,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (i == 0 && kb == it.kb0) trace_mark(p, kTrFirstFull);
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::kABytes;
           const uint32_t b0 = sB + stage * C::kBBytes;
@@ -283,18 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int natoms = min(2, p.G4 - 2 * kb);
             const int rb0 = (it.tb * BN) / 128;
             const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+            const uint32_t sfa_t = tmem + kSfCol + (uint32_t)stage * C::kSfColsPerStage;
+            const uint32_t sfb_t = sfa_t + 8u;
             for (int a = 0; a < natoms; ++a)
-              tc_cp_sf(tmem + kSfaCol + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
+              tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
             for (int j = 0; j < nblk; ++j)
               for (int a = 0; a < natoms; ++a)
-                tc_cp_sf(tmem + kSfbCol + 8 * a + 4 * j,
+                tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
                          sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * 1024 + a * 512));
             const int nk = min(4, (p.K - kb * 256) / 64);
             for (int s = 0; s < nk; ++s) {
               const uint32_t sel = (uint32_t)(s & 1) * 2u;
               mma_mxf4(tmem + kAccCol, sdesc_kmajor_sw128(a0 + 32 * s),
                        sdesc_kmajor_sw128(b0 + 32 * s), idesc_sf_ids(idesc0, sel, sel),
-                       tmem + kSfaCol + 4 * (s >> 1), tmem + kSfbCol + 8 * (s >> 1),
+                       sfa_t + 4 * (s >> 1), sfb_t + 4 * C::kSfBlocksB * (s >> 1),
                        (kb > it.kb0 || s > 0) ? 1u : 0u);
             }
           } else {
@@ -311,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(acc_full);
+        trace_mark(p, kTrLastCommit);
         ++i;
       }
       // every MMA issued so far must finish before TMEM is released
@@ -322,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r_in = q * 32 + lane;    // row of the MMA-A tile
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + kAccCol;
-    long long cur = first_cursor(p);
+    pdl_wait();  // scales, counters and partial tiles may come from the previous kernel
+    uint32_t cur = first_cursor(p);
     Item it;
     int i = 0;
     uint32_t part_phase = 0;
@@ -332,12 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_wait(stall_bar, 0, ctl)) break;
       }
       if (!warp_wait(acc_full, (uint32_t)(i & 1), ctl)) break;
+      if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrAcc0 : kTrAcc1);
       tc_fence_after();
       const int ra = it.ta * kTileA + r_in;  // MMA-A row: token (full tile) / weight row (split)
       const int cb0 = it.tb * BN;            // first MMA-B row of the tile
       const int ncols = min(BN, p.rowsB - cb0);
       const bool whole = (it.kb0 == 0 && it.kb1 == p.kblocks);
       bool ok = true;
+      bool released = false;
+      // hand the accumulator back to the MMA warp once its TMEM reads are done
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+        released = true;
+      };
       if (whole && !p.swap) {
         // rows = tokens, columns = output channels: each thread writes a row run
         const bool mvalid = ra < p.M;
@@ -373,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     pack_bf16x2(f[8 * j + 6], f[8 * j + 7]));
             }
           } else {
-            for (int j = 0; j < CH && n0 + j < p.N; ++j) store_out(p, ra, n0 + j, f[j]);
+#pragma unroll
+            for (int j = 0; j < CH; ++j)
+              if (n0 + j < p.N) store_out(p, ra, n0 + j, f[j]);
           }
         }
       } else if (whole) {
@@ -410,7 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < CH; ++j)
             if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
         }
-        __threadfence();
+        release_acc();  // the MMA may start the next item during the hand-off
+        if (threadIdx.x == 64 && p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
+          trace_mark(p, kTrPartStored);
+        // the arrive orders this thread's partial stores before the leader's
+        // release fence (cumulative) and counter increment
         mbar_arrive(part_bar);
         if (warp == 2 && lane == 0) {
           const bool okp = mbar_wait(part_bar, part_phase, ctl);
@@ -419,9 +580,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __threadfence();
             const int old = atomicAdd(&p.counters[it.t], 1);
             last = (old == it.nseg - 1) ? 1 : 0;
-            if (last) atomicExch(&p.counters[it.t], 0);  // left zero for the next call
+            if (last) {
+              atomicExch(&p.counters[it.t], 0);  // left zero for the next call
+              __threadfence();
+            }
           }
           *decision = okp ? last : -1;
+          if (p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrDecision] == 0)
+            trace_mark(p, kTrDecision);
           mbar_arrive(dec_bar);
         }
         ok = warp_wait(dec_bar, part_phase, ctl);
@@ -430,32 +596,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (dec < 0) {
           ok = false;
         } else if (dec == 1) {
-          __threadfence();
-          const int n = ra;
-          const float sw = (KIND == 1 && n < p.N) ? p.chan_scale[n] : 1.0f;
-          for (int c = 0; c < ncols; ++c) {
-            float acc = 0.0f;
-            for (int s = 0; s < it.nseg; ++s)
-              acc += ld_cg_f32(tile_ws + (size_t)s * slot_elems + (size_t)c * kTileA + r_in);
-            const int m = cb0 + c;
-            if (n < p.N) {
-              float f = acc;
-              if (KIND == 1) f = (f * p.tok_scale[m]) * sw;
-              store_out(p, m, n, f);
-            }
-          }
+          reduce_partials<KIND>(p, tile_ws, slot_elems, it.nseg, ncols, it.ta * kTileA, cb0,
+                                threadIdx.x - 64);
+          if (threadIdx.x == 64) trace_mark(p, kTrReduced);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (!released) release_acc();
+      if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrItem0Done : kTrItem1Done);
       if (!ok) break;
       ++i;
+    }
+    if (threadIdx.x == 64) {
+      trace_mark(p, kTrEpiDone);
+      trace_set(p, kTrItems, (unsigned long long)i);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    trace_mark(p, kTrExit);
+    trace_set(p, kTrExitNs, global_timer_ns());
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -470,8 +632,10 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<ctas, kThreads, C::kSmem, stream>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
 template <int KIND>

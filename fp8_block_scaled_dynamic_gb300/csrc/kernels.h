@@ -7,6 +7,25 @@
 
 namespace mxg {
 
+// Launch configuration with programmatic stream serialization: the kernel
+// may begin while the previous kernel in the stream is still running; every
+// kernel of this library calls griddepcontrol.wait before it touches memory
+// the previous kernel may write or read.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  return cfg;
+}
+inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
                             uint8_t *sf, bool swizzled, int sm_count, cudaStream_t stream);
 
@@ -36,6 +55,17 @@ struct GemmParams {
   int *status;         // optional device status word
   unsigned long long timeout_ns;
   int debug_stall;
+  unsigned long long *trace;  // optional: kTracePoints SM-clock stamps per CTA
+  int early_w;         // 1: the weights were not written by the previous kernel in the
+                       //    stream, so their first stages may load before griddepcontrol.wait
+};
+
+// Timeline trace points (index into a CTA's 16 slots): SM clock64 values.
+enum TracePoint {
+  kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrLastLoad = 3, kTrFirstFull = 4,
+  kTrLastCommit = 5, kTrAcc0 = 6, kTrItem0Done = 7, kTrAcc1 = 8, kTrItem1Done = 9,
+  kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12, kTrDecision = 13, kTrReduced = 14,
+  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTracePoints = 20
 };
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.

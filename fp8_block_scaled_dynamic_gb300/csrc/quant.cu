@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace mxg {
 
@@ -82,6 +83,11 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   const int G = K >> 5;    // MX blocks per row
   const int lane = threadIdx.x & 31;
   const unsigned kFull = 0xFFFFFFFFu;
+  // x may be the previous kernel's output and codes/sf may still be read by
+  // it; only once it is complete may the next kernel start its prologue
+  // (triggering after the wait keeps every early start one kernel deep).
+  pdl_wait();
+  pdl_trigger();
   for (int r = blockIdx.y; r < rows_iter; r += gridDim.y) {
     const bool real_row = r < rows;
     uint4 v[kMxChunksPerThread];
@@ -155,6 +161,8 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *_
   __shared__ uint32_t red[kF8Threads / 32];
   const int cpr = K >> 3;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint16_t *xr = x + (size_t)r * ldx;
     uint4 v[kF8RegChunks];
@@ -229,14 +237,13 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   if (gy * gx > cap) gy = (cap + gx - 1) / gx;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
-  dim3 grid(gx, gy);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(gx, gy), dim3(kMxThreads), 0, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  const uint16_t *xp = static_cast<const uint16_t *>(x);
   if (swizzled)
-    mx_quant_kernel<true><<<grid, kMxThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, codes, sf);
-  else
-    mx_quant_kernel<false><<<grid, kMxThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, codes, sf);
-  return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true>, xp, ldx, rows, rows_iter, K, codes, sf);
+  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false>, xp, ldx, rows, rows_iter, K, codes, sf);
 }
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
@@ -244,9 +251,11 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   int g = rows;
   const int cap = (sm_count > 0 ? sm_count : 152) * 8;
   if (g > cap) g = cap;
-  fp8_quant_kernel<<<g, kF8Threads, 0, stream>>>(static_cast<const uint16_t *>(x), ldx, rows, K,
-                                                 q, scale);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows, K,
+                            q, scale);
 }
 
 }  // namespace mxg

@@ -22,7 +22,10 @@
  *     library allocates no device memory and keeps no pointer after a call
  *     returns.  Scratch memory, where needed, is the caller's workspace.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
- *     do not synchronise the host, except mxg_query_status.
+ *     do not synchronise the host, except mxg_query_status.  Kernels are
+ *     launched with programmatic stream serialization: each may begin its
+ *     prologue while the kernel before it finishes, and touches no memory
+ *     that kernel may use before that kernel has completed.
  *   - Host-detectable errors (bad shape, alignment, device, workspace) are
  *     returned before anything is launched.  A failed launch returns
  *     MXG_ERR_CUDA.  Device-side waits are bounded; a wait that runs out
@@ -102,6 +105,16 @@ typedef struct {
     uint32_t timeout_ms;  /* limit of every device-side wait; 0 = 1000 ms */
     int debug_stall;      /* test hook: 1 makes the epilogue wait on a barrier nothing
                              arrives at, so the timeout path runs (no fault, no hang) */
+    int weights_static;   /* 1: the kernel enqueued on `stream` just before this call did
+                             not write the weight operands (w_codes/w_sf or qw), so the
+                             GEMM may start streaming them while that kernel finishes
+                             (programmatic dependent launch).  The fused A4W4 path does
+                             this for its own quantization kernel without being asked. */
+    void *trace;          /* optional device buffer of ctas x 20 uint64, zero-filled: each
+                             CTA records SM clock64 stamps of its timeline (entry, setup,
+                             first/last load, first stage ready, last MMA commit, epilogue
+                             items, split-K hand-off, exit; slot 15 = items; slots 16/17 =
+                             global timer ns at entry/exit).  NULL = off. */
 } mxg_gemm_opts;
 
 typedef struct {
