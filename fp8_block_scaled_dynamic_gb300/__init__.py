@@ -28,7 +28,8 @@ MXG_OK = 0
 STATUS_NAMES = {0: "MXG_OK", 1: "MXG_ERR_INVALID_ARG", 2: "MXG_ERR_UNSUPPORTED_SHAPE",
                 3: "MXG_ERR_MISALIGNED", 4: "MXG_ERR_UNSUPPORTED_DEVICE", 5: "MXG_ERR_CUDA",
                 6: "MXG_ERR_TIMEOUT", 7: "MXG_ERR_WORKSPACE"}
-SF_ROWMAJOR, SF_SWIZZLED = 0, 1
+SF_ROWMAJOR, SF_SWIZZLED, TILED = 0, 1, 2
+TILE_BYTES = 16384
 OUT_BF16, OUT_F32 = 0, 1
 VARIANTS = {"auto": 0, "full": 1, "splitk": 2}
 KIND_A4W4, KIND_PTPC = 0, 1
@@ -45,7 +46,7 @@ class GemmOpts(ctypes.Structure):
                 ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
                 ("dev_status", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint32),
                 ("debug_stall", ctypes.c_int), ("weights_static", ctypes.c_int),
-                ("trace", ctypes.c_void_p)]
+                ("weights_tiled", ctypes.c_int), ("trace", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.mx_gemm_a4w4.restype = i
             L.fp8_quantize_act.argtypes = [vp, i, i, i, vp, vp, vp]
             L.fp8_quantize_act.restype = i
+            L.fp8_quantize_weight.argtypes = [vp, i, i, i, vp, vp, i, vp]
+            L.fp8_quantize_weight.restype = i
             L.fp8_gemm_ptpc.argtypes = [vp, vp, vp, vp, i, i, i, vp, i, i,
                                         ctypes.POINTER(GemmOpts), vp]
             L.fp8_gemm_ptpc.restype = i
@@ -153,8 +156,10 @@ def workspace(nbytes: int, device=None) -> torch.Tensor | None:
 
 # ---------------------------------------------------------------- quantizers
 def mx_quantize_weight(w: torch.Tensor, layout: int = SF_SWIZZLED, codes=None, sf=None, stream=None):
-    """Offline MXFP4 weight conversion: w (N, K) bf16 -> (codes (N, K/2) u8,
-    sf u8 in `layout`: SF_ROWMAJOR (N, K/32) or SF_SWIZZLED flat)."""
+    """Offline MXFP4 weight conversion: w (N, K) bf16 -> (codes u8, sf u8).
+    layout SF_ROWMAJOR: codes (N, K/2), sf (N, K/32); SF_SWIZZLED: codes
+    (N, K/2), sf flat 128x4 tiles; TILED: codes in 16 KiB weight tiles
+    (shape (N, K/2) bytes, tile-ordered), sf flat 128x4 tiles."""
     _need(w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1,
           "w must be a CUDA bf16 (N, K) tensor with unit inner stride")
     N, K = w.shape
@@ -183,6 +188,21 @@ def mx_quantize_act(x: torch.Tensor, codes=None, sf=None, stream=None):
     return codes, sf
 
 
+def fp8_quantize_weight(w: torch.Tensor, layout: int = SF_ROWMAJOR, q=None, scale=None, stream=None):
+    """Per-output-channel E4M3 weight conversion: w (N, K) bf16 -> (q (N, K)
+    bytes, row-major or in 16 KiB weight tiles (layout TILED), scale (N,) f32)."""
+    _need(w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1,
+          "w must be a CUDA bf16 (N, K) tensor with unit inner stride")
+    N, K = w.shape
+    if q is None:
+        q = torch.empty(N, K, dtype=torch.uint8, device=w.device)
+    if scale is None:
+        scale = torch.empty(N, dtype=torch.float32, device=w.device)
+    _check("fp8_quantize_weight", lib().fp8_quantize_weight(
+        _ptr(w), N, K, w.stride(0), _ptr(q), _ptr(scale), layout, _stream(stream)))
+    return q, scale
+
+
 def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
     """Per-row E4M3 quantization: x (M, K) bf16 -> (q (M, K) u8, scale (M,) f32).
     Applied to a weight W (N, K) it gives the per-output-channel conversion."""
@@ -200,8 +220,9 @@ def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
 
 # ---------------------------------------------------------------- GEMMs
 def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static=False,
-          trace=None) -> GemmOpts:
+          trace=None, weights_tiled=False) -> GemmOpts:
     return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas), weights_static=int(weights_static),
+                    weights_tiled=int(weights_tiled),
                     trace=0 if trace is None else trace.data_ptr(),
                     workspace=0 if ws is None else ws.data_ptr(),
                     ws_bytes=0 if ws is None else ws.numel() * ws.element_size(),
@@ -220,9 +241,11 @@ def _out(out, M, N, out_f32, device):
 def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_sf=None, x=None,
                  out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
-                 weights_static: bool = False, trace=None, stream=None):
+                 weights_static: bool = False, trace=None, weights_tiled: bool = False,
+                 stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
-    x (M, K) bf16 (quantized inside the call).  w_sf must be SWIZZLED."""
+    x (M, K) bf16 (quantized inside the call).  w_sf must be in the 128x4
+    tiles; w_codes row-major, or in weight tiles with weights_tiled=True."""
     N, K2 = w_codes.shape
     K = 2 * K2
     fused = a_codes is None
@@ -236,7 +259,8 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
     out = _out(out, M, N, out_f32, w_codes.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_A4W4, fused, M, N, K, variant, ctas), w_codes.device)
-    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace)
+    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
+              weights_tiled)
     _check("mx_gemm_a4w4", lib().mx_gemm_a4w4(
         _ptr(a_codes), _ptr(a_sf), _ptr(x), ldx, _ptr(w_codes), _ptr(w_sf), M, N, K,
         _ptr(out), out.stride(0), OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
@@ -246,14 +270,17 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
 def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor, *,
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                   ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
-                  weights_static: bool = False, trace=None, stream=None):
-    """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM."""
+                  weights_static: bool = False, trace=None, weights_tiled: bool = False,
+                  stream=None):
+    """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM; qw
+    row-major, or in weight tiles with weights_tiled=True."""
     M, K = qa.shape
     N = qw.shape[0]
     out = _out(out, M, N, out_f32, qa.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)
-    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace)
+    o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
+              weights_tiled)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))

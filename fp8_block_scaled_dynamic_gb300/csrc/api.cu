@@ -163,6 +163,8 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
 
   const bool swap = pl.variant == MXG_VARIANT_SPLITK;
   const uint64_t row_bytes = kind == 0 ? (uint64_t)K / 2 : (uint64_t)K;
+  const bool w_tiled = opts && opts->weights_tiled;
+  if (w_tiled && (row_bytes % 128 != 0 || N % 128 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tmA, tmB;
   const uint8_t *A = swap ? op.w : op.a;
   const uint8_t *B = swap ? op.a : op.w;
@@ -202,6 +204,13 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.debug_stall = opts ? opts->debug_stall : 0;
   p.early_w = (early_w || (opts && opts->weights_static)) ? 1 : 0;
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
+  p.kc_per_row = (int)(row_bytes / 128);
+  if (w_tiled) {  // the tensor map encoded above is then unused for that operand
+    if (swap)
+      p.a_tiles = op.w;
+    else
+      p.b_tiles = op.w;
+  }
   cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
@@ -249,12 +258,15 @@ mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t
                               uint8_t *sf, mxg_sf_layout layout, mxg_stream_t stream) {
   mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
   if (st != MXG_OK) return st;
-  if (!codes || !sf || (layout != MXG_SF_ROWMAJOR && layout != MXG_SF_SWIZZLED))
+  if (!codes || !sf ||
+      (layout != MXG_SF_ROWMAJOR && layout != MXG_SF_SWIZZLED && layout != MXG_TILED))
     return MXG_ERR_INVALID_ARG;
+  if (layout == MXG_TILED && (N % 128 != 0 || K % 256 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(codes) || !aligned16(sf)) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  cudaError_t e = mxg::launch_mx_quant(w_bf16, ldw, N, K, codes, sf, layout == MXG_SF_SWIZZLED, sm,
+  cudaError_t e = mxg::launch_mx_quant(w_bf16, ldw, N, K, codes, sf, layout != MXG_SF_ROWMAJOR,
+                                       layout == MXG_TILED, sm,
                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
@@ -272,8 +284,22 @@ mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *
   if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  cudaError_t e =
-      mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, sm, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, false, sm,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t *q, float *scale,
+                               mxg_sf_layout layout, mxg_stream_t stream) {
+  mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
+  if (st != MXG_OK) return st;
+  if (!q || !scale || (layout != MXG_SF_ROWMAJOR && layout != MXG_TILED)) return MXG_ERR_INVALID_ARG;
+  if (layout == MXG_TILED && N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaError_t e = mxg::launch_fp8_quant(w_bf16, ldw, N, K, q, scale, layout == MXG_TILED, sm,
+                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 
@@ -310,7 +336,7 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
       return MXG_ERR_WORKSPACE;
     uint8_t *codes = ws + kCounterBytes;
     uint8_t *sf = codes + align256((size_t)M * (K / 2));
-    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, sm, s);
+    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, false, sm, s);
     if (e != cudaSuccess) return MXG_ERR_CUDA;
     a_codes = codes;
     a_sf = sf;

@@ -162,12 +162,13 @@ __device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, flo
 // Sum the nseg partial tiles of one output tile in slot order and write y.
 // Each slot is [column][128 rows] fp32; the 128 epilogue threads take float4
 // groups (4 consecutive rows of one column) so that loads and stores are
-// coalesced, with the loads of up to 4 slots x kU groups in flight at once.
+// coalesced, with the loads of up to 4 slots x kU groups in flight at once
+// (one round of L2 latency per 128 * kU groups).
 template <int KIND>
 __device__ __forceinline__ void reduce_partials(const GemmParams &p, const float *tile_ws,
                                                 size_t slot_elems, int nseg, int ncols, int row0,
                                                 int col0, int tid) {
-  constexpr int kU = 4;
+  constexpr int kU = 8;
   const int ngrp = ncols * (kTileA / 4);
   const float4 *base = reinterpret_cast<const float4 *>(tile_ws);
   const size_t slot4 = slot_elems / 4;
@@ -315,14 +316,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return bytes;
       };
+      // A weight tile (128 rows x 128 bytes) is one contiguous 16 KiB bulk copy;
+      // row-major operands go through the tensor map (128-byte swizzle box)
       auto issue_a = [&](int stage, const Item &it, int kb, uint32_t fb) {
-        tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
+        if (p.a_tiles)
+          bulk_load(sA + stage * C::kABytes,
+                    p.a_tiles + ((size_t)it.ta * p.kc_per_row + kb) * (size_t)C::kABytes,
+                    C::kABytes, fb, polA);
+        else
+          tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
         if (KIND == 0)
           bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * kb) * 512u,
                     min(2, p.G4 - 2 * kb) * 512, fb, polA);
       };
       auto issue_b = [&](int stage, const Item &it, int kb, uint32_t fb) {
-        tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
+        if (p.b_tiles) {  // BN is a multiple of 128 here: one tile per 128-row block
+          for (int j = 0; j < BN / 128; ++j)
+            bulk_load(sB + stage * C::kBBytes + j * 16384,
+                      p.b_tiles + ((size_t)(it.tb * (BN / 128) + j) * p.kc_per_row + kb) * 16384u,
+                      16384, fb, polB);
+        } else {
+          tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
+        }
         if (KIND == 0) {
           const int natoms = min(2, p.G4 - 2 * kb);
           const int rb0 = (it.tb * BN) / 128;
@@ -570,20 +585,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         release_acc();  // the MMA may start the next item during the hand-off
         if (threadIdx.x == 64 && p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
           trace_mark(p, kTrPartStored);
-        // the arrive orders this thread's partial stores before the leader's
-        // release fence (cumulative) and counter increment
+        // the arrive (release, CTA scope) orders this thread's partial stores
+        // before the leader's acquire-release counter increment (GPU scope)
         mbar_arrive(part_bar);
         if (warp == 2 && lane == 0) {
           const bool okp = mbar_wait(part_bar, part_phase, ctl);
           int last = 0;
           if (okp) {
-            __threadfence();
-            const int old = atomicAdd(&p.counters[it.t], 1);
-            last = (old == it.nseg - 1) ? 1 : 0;
-            if (last) {
-              atomicExch(&p.counters[it.t], 0);  // left zero for the next call
-              __threadfence();
-            }
+            // one acquire-release increment both publishes this CTA's partial
+            // (the part_bar arrivals order the other threads' stores before
+            // it) and, for the last arriver, makes the other partials visible
+            const unsigned old =
+                atom_add_acq_rel_gpu(reinterpret_cast<unsigned *>(p.counters) + it.t, 1u);
+            last = (old == (unsigned)(it.nseg - 1)) ? 1 : 0;
+            if (last) p.counters[it.t] = 0;  // every segment arrived: left zero for the next call
           }
           *decision = okp ? last : -1;
           if (p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrDecision] == 0)

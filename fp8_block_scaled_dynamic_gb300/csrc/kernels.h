@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -19,7 +20,16 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
   cfg.stream = stream;
   return cfg;
 }
+// MXG_DISABLE_PDL=1 in the environment turns the overlap off (for A/B timing).
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char *e = std::getenv("MXG_DISABLE_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
+}
 inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
+  if (!pdl_enabled()) return;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
@@ -27,10 +37,11 @@ inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) 
 }
 
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
-                            uint8_t *sf, bool swizzled, int sm_count, cudaStream_t stream);
+                            uint8_t *sf, bool swizzled, bool tiled_codes, int sm_count,
+                            cudaStream_t stream);
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
-                             float *scale, int sm_count, cudaStream_t stream);
+                             float *scale, bool tiled, int sm_count, cudaStream_t stream);
 
 // Everything one GEMM launch needs besides the two tensor maps.
 struct GemmParams {
@@ -56,6 +67,9 @@ struct GemmParams {
   unsigned long long timeout_ns;
   int debug_stall;
   unsigned long long *trace;  // optional: kTracePoints SM-clock stamps per CTA
+  const uint8_t *a_tiles;  // non-null: the MMA-A operand in the weight tile layout (bulk copies)
+  const uint8_t *b_tiles;  // non-null: the MMA-B operand in the weight tile layout
+  int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int early_w;         // 1: the weights were not written by the previous kernel in the
                        //    stream, so their first stages may load before griddepcontrol.wait
 };

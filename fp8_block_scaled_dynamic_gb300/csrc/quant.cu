@@ -67,13 +67,22 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
   return v;
 }
 
+// Byte offset of (row r, byte b of the row) in the weight tile layout: 16 KiB
+// tiles of 128 rows x 128 bytes, tile (r / 128, b / 128) at ((r/128)*KC +
+// b/128) * 16384, 16-byte unit j of row r at (r % 128) * 128 + ((j ^ (r % 8)) * 16).
+__device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row) {
+  const int j = (b >> 4) & 7;
+  return ((size_t)(r >> 7) * kc_per_row + (b >> 7)) * 16384u + (size_t)(r & 127) * 128u +
+         (size_t)((j ^ (r & 7)) << 4) + (b & 15);
+}
+
 constexpr int kMxThreads = 256;
 constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in flight per thread
 
 // grid: x = chunk groups along the row, y = rows (grid-stride).
 // rows_iter >= rows: rows in [rows, rows_iter) are padding (swizzled layout
 // only) -- their scales are written as 0 and no codes are stored.
-template <bool kSwizzled>
+template <bool kSwizzled, bool kTiledCodes>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
                                                               long long ldx, int rows,
                                                               int rows_iter, int K,
@@ -128,8 +137,11 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
         packed |= nibble_signs(w.x) | (nibble_signs(w.y) << 8) | (nibble_signs(w.z) << 16) |
                   (nibble_signs(w.w) << 24);
       }
-      if (real_row && in_row)
-        *reinterpret_cast<uint32_t *>(codes + (size_t)r * (K >> 1) + (size_t)cc[i] * 4) = packed;
+      if (real_row && in_row) {
+        const size_t off = kTiledCodes ? tiled_offset(r, cc[i] * 4, K >> 8)
+                                       : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
+        *reinterpret_cast<uint32_t *>(codes + off) = packed;
+      }
       // Gather the scales of 4 consecutive blocks (lanes 0,4,8,12 of each
       // half-warp) into one 32-bit word.
       const uint32_t s1 = __shfl_down_sync(kFull, scode, 4);
@@ -153,7 +165,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
 constexpr int kF8Threads = 256;
 constexpr int kF8RegChunks = 12;  // rows of up to 12*256*8 = 24576 values stay in registers
 
-// One CTA per row (grid-stride over rows).
+// One CTA per row (grid-stride over rows).  kTiled: q in the weight tile layout.
+template <bool kTiled>
 __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *__restrict__ x,
                                                                long long ldx, int rows, int K,
                                                                uint8_t *__restrict__ q,
@@ -194,11 +207,14 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *_
     for (int i = 1; i < kF8Threads / 32; ++i) amax = max(amax, red[i]);
     __syncthreads();  // red[] is reused by the next row
 
-    uint8_t *qr = q + (size_t)r * K;
+    // destination of the 8 bytes of chunk c of this row
+    auto qdst = [&](int c) -> uint2 * {
+      return reinterpret_cast<uint2 *>(q + (kTiled ? tiled_offset(r, c * 8, K >> 7)
+                                                   : (size_t)r * K + (size_t)c * 8));
+    };
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
-      for (int c = tid; c < cpr; c += kF8Threads)
-        *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
       continue;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
@@ -216,17 +232,18 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *_
 #pragma unroll
     for (int i = 0; i < kF8RegChunks; ++i) {
       const int c = i * kF8Threads + tid;
-      if (c < cpr) *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = quant8(v[i]);
+      if (c < cpr) *qdst(c) = quant8(v[i]);
     }
     for (int c = kF8RegChunks * kF8Threads + tid; c < cpr; c += kF8Threads)
-      *reinterpret_cast<uint2 *>(qr + (size_t)c * 8) = quant8(ld_stream_v4(xr + (size_t)c * 8));
+      *qdst(c) = quant8(ld_stream_v4(xr + (size_t)c * 8));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
-                            uint8_t *sf, bool swizzled, int sm_count, cudaStream_t stream) {
+                            uint8_t *sf, bool swizzled, bool tiled_codes, int sm_count,
+                            cudaStream_t stream) {
   const int cpr = K / 8;
   const int per_block = kMxThreads * kMxChunksPerThread;
   const int gx = (cpr + per_block - 1) / per_block;
@@ -241,21 +258,29 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
+  if (tiled_codes)
+    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true, true>, xp, ldx, rows, rows_iter, K, codes,
+                              sf);
   if (swizzled)
-    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true>, xp, ldx, rows, rows_iter, K, codes, sf);
-  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false>, xp, ldx, rows, rows_iter, K, codes, sf);
+    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true, false>, xp, ldx, rows, rows_iter, K,
+                              codes, sf);
+  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false, false>, xp, ldx, rows, rows_iter, K, codes,
+                            sf);
 }
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
-                             float *scale, int sm_count, cudaStream_t stream) {
+                             float *scale, bool tiled, int sm_count, cudaStream_t stream) {
   int g = rows;
   const int cap = (sm_count > 0 ? sm_count : 152) * 8;
   if (g > cap) g = cap;
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
-  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows, K,
-                            q, scale);
+  if (tiled)
+    return cudaLaunchKernelEx(&cfg, fp8_quant_kernel<true>, static_cast<const uint16_t *>(x), ldx,
+                              rows, K, q, scale);
+  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel<false>, static_cast<const uint16_t *>(x), ldx,
+                            rows, K, q, scale);
 }
 
 }  // namespace mxg

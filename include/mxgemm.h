@@ -76,8 +76,20 @@ typedef enum {
 
 typedef enum {
     MXG_SF_ROWMAJOR = 0, /* (rows, K/32) bytes, row-major: the stored checkpoint layout */
-    MXG_SF_SWIZZLED = 1  /* 128x4 tiles of 512 bytes (see mxg_sf_bytes); the GEMM operand layout */
+    MXG_SF_SWIZZLED = 1, /* 128x4 tiles of 512 bytes (see mxg_sf_bytes); the GEMM operand layout */
+    MXG_TILED = 2        /* scales as MXG_SF_SWIZZLED, and the codes in the GEMM's weight tile
+                            layout (see MXG_TILE_BYTES); needs rows % 128 == 0 and, for MXFP4,
+                            K % 256 == 0 */
 } mxg_sf_layout;
+
+/* Weight tile layout (MXG_TILED), for MXFP4 codes and for FP8 E4M3 bytes alike:
+ * a row is cut into 128-byte chunks (256 FP4 or 128 FP8 values, KC = row bytes
+ * / 128 chunks); the 128 rows x 128 bytes of row block rb and chunk kc form one
+ * 16 KiB tile at byte ((rb * KC) + kc) * 16384; inside it, the 16-byte unit j
+ * (0..7) of row r (0..127) sits at r * 128 + ((j ^ (r % 8)) * 16).  That is the
+ * shared-memory image the tensor cores read (K-major, 128-byte swizzle), so a
+ * GEMM stage fetches a weight tile with one contiguous bulk copy. */
+#define MXG_TILE_BYTES 16384
 
 typedef enum {
     MXG_OUT_BF16 = 0, /* y rounded to bf16 (round to nearest even) */
@@ -110,6 +122,8 @@ typedef struct {
                              GEMM may start streaming them while that kernel finishes
                              (programmatic dependent launch).  The fused A4W4 path does
                              this for its own quantization kernel without being asked. */
+    int weights_tiled;    /* 1: w_codes (A4W4) / qw (PTPC) are in the MXG_TILED weight tile
+                             layout; 0: row-major */
     void *trace;          /* optional device buffer of ctas x 20 uint64, zero-filled: each
                              CTA records SM clock64 stamps of its timeline (entry, setup,
                              first/last load, first stage ready, last MMA commit, epilogue
@@ -148,9 +162,10 @@ size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
 /* Offline MXFP4 weight conversion ("Exact quantization coverage": E2M1 codes,
  * E8M0 scale per 32 consecutive input channels).
  *   w_bf16: (N, K) bf16, leading dimension ldw elements.
- *   codes:  (N, K/2) bytes, two codes per byte, lower k in the low nibble.
+ *   codes:  N * K/2 bytes, two codes per byte, lower k in the low nibble:
+ *           row-major (N, K/2) for ROWMAJOR / SWIZZLED, weight tiles for TILED.
  *   sf:     mxg_sf_bytes(N, K, layout) bytes, ROWMAJOR (the stored (N, K/32)
- *           checkpoint layout) or SWIZZLED (the GEMM operand layout). */
+ *           checkpoint layout) or the 128x4 tiles (SWIZZLED, TILED). */
 mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw,
                               uint8_t *codes, uint8_t *sf, mxg_sf_layout layout,
                               mxg_stream_t stream);
@@ -183,6 +198,16 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf,
  *   scale: M floats (the (out_features, 1) scale when x is a weight). */
 mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx,
                             uint8_t *q, float *scale, mxg_stream_t stream);
+
+/* Per-output-channel FP8 weight conversion ("Phase 1 FP8 PTPC Quantization":
+ * E4M3 weight, FP32 scale of shape (out_features, 1)); the same arithmetic as
+ * fp8_quantize_act applied to the rows of W.
+ *   w_bf16 (N, K), leading dimension ldw.  q: N * K bytes, row-major (N, K)
+ *   for MXG_SF_ROWMAJOR or weight tiles for MXG_TILED (N % 128 == 0).
+ *   scale: N floats. */
+mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw,
+                               uint8_t *q, float *scale, mxg_sf_layout layout,
+                               mxg_stream_t stream);
 
 /* FP8 PTPC A8W8 GEMM: y[m][n] = (acc[m][n] * sa[m]) * sw[n] with
  * acc = sum_k v(qa[m,k]) v(qw[n,k]) accumulated in fp32.

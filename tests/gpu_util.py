@@ -48,3 +48,15 @@ def assert_gemm_close(y, ref, bound, what, tol=GEMM_REL_TOL):
 def bf16_rne(y_f32: np.ndarray) -> np.ndarray:
     return torch.from_numpy(np.ascontiguousarray(y_f32, dtype=np.float32)).to(torch.bfloat16) \
         .view(torch.int16).numpy().view(np.uint16)
+
+
+def untile(tiled: np.ndarray, rows: int, row_bytes: int) -> np.ndarray:
+    """Weight tile layout -> row-major (rows, row_bytes): 16 KiB tiles of
+    128 rows x 128 bytes ordered (row block, chunk); the 16-byte unit j of
+    row r is stored at unit position j ^ (r % 8)."""
+    kc = row_bytes // 128
+    a = np.asarray(tiled, dtype=np.uint8).reshape(rows // 128, kc, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    logical = a[:, :, r, j ^ (r % 8), :]          # [rb][kc][128][8][16]
+    return logical.transpose(0, 2, 1, 3, 4).reshape(rows, row_bytes)
