@@ -392,4 +392,66 @@ const char *mxg_status_string(mxg_status s) {
   return "MXG_UNKNOWN";
 }
 
+// ---------------------------------------------------------------------------
+// mx_gemm_a4w4_noalloc: the A4W4 GEMM for callers that cannot allocate device
+// memory.  Its scratch (split-K arrival counters, fused activations, partial
+// tiles -- the same layout as the caller workspace of mx_gemm_a4w4) lives in
+// this file-scope device array, which every GPU that loads the library holds
+// until the process exits.  Host code must not use the array's name as a
+// device address: the address comes from cudaGetSymbolAddress, once per
+// device, with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MXG_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+
+// Device address of the scratch array on the current device (looked up on
+// the first call for that device).
+mxg_status noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MXG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MXG_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MXG_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MXG_OK;
+}
+}  // namespace
+
+mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, const void *x_bf16,
+                                int ldx, const uint8_t *w_codes, const uint8_t *w_sf, int M, int N,
+                                int K, void *y, int ldy, mxg_out_dtype out_dtype, int weights_tiled,
+                                mxg_stream_t stream) {
+  mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, nullptr);
+  if (st != MXG_OK) return st;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  // the scratch this call needs, exactly as mx_gemm_a4w4 would ask for it
+  mxg_plan pl;
+  if ((st = plan_impl(0, M, N, K, sm, nullptr, &pl)) != MXG_OK) return st;
+  const bool fused = a_codes == nullptr;
+  const size_t act = fused ? fused_act_bytes(M, K) : 0;
+  const size_t need = kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
+  if (need > (size_t)MXG_NOALLOC_SCRATCH_BYTES) return MXG_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MXG_OK) return st;
+  // the arrival counters must start at zero; the array keeps whatever the
+  // previous call (on any stream) left in it
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, kCounterBytes, s) != cudaSuccess) return MXG_ERR_CUDA;
+  mxg_gemm_opts opts;
+  std::memset(&opts, 0, sizeof(opts));
+  opts.variant = MXG_VARIANT_AUTO;
+  opts.workspace = scratch;
+  opts.ws_bytes = MXG_NOALLOC_SCRATCH_BYTES;
+  opts.weights_tiled = weights_tiled ? 1 : 0;
+  return mx_gemm_a4w4(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype, &opts,
+                      stream);
+}
+
 }  // extern "C"

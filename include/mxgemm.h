@@ -217,6 +217,37 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
                          int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
                          const mxg_gemm_opts *opts, mxg_stream_t stream);
 
+/* Size of the library-owned scratch array used by mx_gemm_a4w4_noalloc. */
+#define MXG_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* mx_gemm_a4w4 for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a library convenience, not part of the method.
+ * Some callers own every device byte themselves and hand a kernel only its
+ * inputs and outputs -- for example the custom-op or plugin interface of an
+ * inference engine that plans all memory up front, or a serving loop that
+ * must not allocate on its hot path because an allocation can stall on a
+ * device-wide synchronisation or fail when memory is fragmented.  This entry
+ * point takes the same operands as mx_gemm_a4w4 (default dispatch; weights in
+ * the MXG_TILED layout when weights_tiled != 0) and no workspace: its scratch
+ * is a file-scope device array of MXG_NOALLOC_SCRATCH_BYTES (16 MiB) inside
+ * the library, which every GPU that loads the library keeps until the
+ * process exits.  It calls no cudaMalloc/cudaFree or any allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Shapes whose scratch would exceed the array (see
+ *     mxg_gemm_workspace_bytes) return MXG_ERR_WORKSPACE before any launch.
+ *   - Each call clears the array's arrival counters (a 64 KiB memset on
+ *     `stream`), then runs the GEMM.  All calls share the one array, which
+ *     keeps the last call's contents: calls that overlap on the GPU (other
+ *     streams, other threads) race on it and must be serialised by the
+ *     caller. */
+mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf,
+                                const void *x_bf16, int ldx,
+                                const uint8_t *w_codes, const uint8_t *w_sf,
+                                int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
+                                int weights_tiled, mxg_stream_t stream);
+
 /* Synchronises `stream`, reads the device status word, clears it, and maps
  * it: MXG_OK, MXG_ERR_TIMEOUT (MXG_DEV_TIMEOUT set) or MXG_ERR_CUDA. */
 mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream);
