@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -76,6 +77,14 @@ mxg_status make_operand_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
+}
+
+bool splitk_inkernel() {
+  static const bool on = [] {
+    const char *e = std::getenv("MXG_SPLITK_INKERNEL");
+    return e && e[0] == '1';
+  }();
+  return on;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -211,7 +220,12 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
     else
       p.b_tiles = op.w;
   }
+  // Split-K partial tiles are summed by a separate reduce kernel spread over
+  // every SM (MXG_SPLITK_INKERNEL=1: by the last CTA of each tile instead).
+  p.defer_reduce = (pl.seg_max > 1 && !splitk_inkernel()) ? 1 : 0;
   cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
+  if (e == cudaSuccess && p.defer_reduce)
+    e = mxg::launch_splitk_reduce(kind, pl.bn, p, pl.ctas, sm_count, stream);
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 

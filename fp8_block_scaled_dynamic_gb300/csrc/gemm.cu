@@ -501,6 +501,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = (it.kb0 == 0 && it.kb1 == p.kblocks);
       bool ok = true;
       bool released = false;
+      // write this CTA's fp32 partial of the tile ([column][128 rows]) into
+      // its slot of the workspace; returns the tile's first slot
+      auto publish_partial = [&]() -> float * {
+        const size_t slot_elems = (size_t)BN * kTileA;
+        float *tile_ws = p.ws + (size_t)it.t * p.seg_max * slot_elems;
+        float *mine = tile_ws + (size_t)it.seg * slot_elems;
+#pragma unroll 1
+        for (int c = 0; c < BN / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < CH; ++j)
+            if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
+        }
+        return tile_ws;
+      };
       // hand the accumulator back to the MMA warp once its TMEM reads are done
       auto release_acc = [&]() {
         tc_fence_before();
@@ -567,24 +584,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else {
-        // swapped, part of K: publish an fp32 partial tile, then the last
-        // CTA of the tile reduces all partials in slot order
-        const size_t slot_elems = (size_t)BN * kTileA;
-        float *tile_ws = p.ws + (size_t)it.t * p.seg_max * slot_elems;
-        float *mine = tile_ws + (size_t)it.seg * slot_elems;
-#pragma unroll 1
-        for (int c = 0; c < BN / CH; ++c) {
-          uint32_t v[CH];
-          tmem_ld_chunk<CH>(t_row + c * CH, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < CH; ++j)
-            if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
-        }
+      } else if (p.defer_reduce) {
+        // swapped, part of K: publish this CTA's fp32 partial tile into its
+        // slot; the split-K reduce kernel that follows sums the slots
+        publish_partial();
         release_acc();  // the MMA may start the next item during the hand-off
         if (threadIdx.x == 64 && p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
           trace_mark(p, kTrPartStored);
+      } else if (!whole) {
+        // (in-kernel variant) the last CTA of the tile reduces the partials
+        const size_t slot_elems = (size_t)BN * kTileA;
+        float *tile_ws = publish_partial();
+        release_acc();
         // the arrive (release, CTA scope) orders this thread's partial stores
         // before the leader's acquire-release counter increment (GPU scope)
         mbar_arrive(part_bar);
@@ -636,6 +647,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Split-K reduction for the deferred variant: for every tile that more than
+// one CTA touched, y = sum of the partial slots in slot order (fixed order:
+// deterministic), then the PTPC scales, then bf16 (or fp32).  One thread per
+// float4 group of a slot ([column][128 rows]), grid-strided over all tiles, so
+// the ~nseg x 32 KB per tile is read by every SM instead of by one CTA.
+template <int KIND>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, int bn,
+                                                            unsigned gemm_ctas) {
+  pdl_wait();  // the GEMM that wrote the partial slots has completed
+  pdl_trigger();
+  const unsigned U = (unsigned)p.units, KB = (unsigned)p.kblocks;
+  const int per_col = kTileA / 4;
+  const int per_tile = bn * per_col;
+  const int total = p.tilesA * p.tilesB * per_tile;
+  const size_t slot4 = (size_t)bn * kTileA / 4;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const int t = e / per_tile;
+    const int g = e - t * per_tile;
+    const unsigned first = (unsigned)t * KB;
+    const unsigned o0 = owner_of(first, U, gemm_ctas);
+    const int nseg = (int)(owner_of(first + KB - 1, U, gemm_ctas) - o0 + 1);
+    if (nseg == 1) continue;  // one CTA owned the whole tile and wrote y itself
+    const int ta = t / p.tilesB, tb = t - (t / p.tilesB) * p.tilesB;
+    const int c = g / per_col, r = (g - c * per_col) * 4;
+    if (c >= min(bn, p.rowsB - tb * bn)) continue;
+    const float4 *src = reinterpret_cast<const float4 *>(p.ws) + (size_t)t * p.seg_max * slot4 + g;
+    float4 v[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) v[s] = s < nseg ? __ldcg(src + s * slot4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      acc.x += v[s].x;
+      acc.y += v[s].y;
+      acc.z += v[s].z;
+      acc.w += v[s].w;
+    }
+    for (int s = 4; s < nseg; ++s) {
+      const float4 w = __ldcg(src + s * slot4);
+      acc.x += w.x;
+      acc.y += w.y;
+      acc.z += w.z;
+      acc.w += w.w;
+    }
+    const int m = tb * bn + c;      // token
+    const int n = ta * kTileA + r;  // output channel
+    float f[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (KIND == 1) {
+      const float sa = p.tok_scale[m];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
+    }
+    if (p.out_f32)
+      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
+          make_float4(f[0], f[1], f[2], f[3]);
+    else
+      *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
+          make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
   }
 }
 
@@ -691,6 +763,20 @@ size_t smem_kind(int bn) {
 }
 
 }  // namespace
+
+cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
+                                 int sm_count, cudaStream_t stream) {
+  const long long total = (long long)p.tilesA * p.tilesB * bn * (kTileA / 4);
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)(sm_count > 0 ? sm_count : 152) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(256), 0, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  if (kind == 0) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<0>, p, bn, (unsigned)gemm_ctas);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1>, p, bn, (unsigned)gemm_ctas);
+}
 
 cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const GemmParams &p, int ctas, cudaStream_t stream) {

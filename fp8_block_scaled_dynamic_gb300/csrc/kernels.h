@@ -70,6 +70,8 @@ struct GemmParams {
   const uint8_t *a_tiles;  // non-null: the MMA-A operand in the weight tile layout (bulk copies)
   const uint8_t *b_tiles;  // non-null: the MMA-B operand in the weight tile layout
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
+  int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
+                           //          the last CTA of each tile
   int early_w;         // 1: the weights were not written by the previous kernel in the
                        //    stream, so their first stages may load before griddepcontrol.wait
 };
@@ -85,6 +87,11 @@ enum TracePoint {
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.
 cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const GemmParams &p, int ctas, cudaStream_t stream);
+
+// Split-K reduction of a GEMM launched with p.defer_reduce = 1 (the same
+// params, its grid size gemm_ctas); launched right after it on the stream.
+cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
+                                 int sm_count, cudaStream_t stream);
 
 // Pipeline stages a (kind, bn) kernel uses, and its dynamic shared memory.
 int gemm_stages(int kind, int bn);
