@@ -160,6 +160,12 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workloads
+def act_tile_rows(plan: dict) -> int:
+    """Token-tile height of the activation tile layout a GEMM plan reads:
+    the MMA-N tile in split-K (tokens are the MMA-B operand), else 128."""
+    return plan["bn"] if plan["variant"] == 2 else 128
+
+
 class Workload:
     """Builds resident device operands and exposes one step as a list of
     (label, fn) launches; `timed_label` marks the dominant kernel."""
@@ -201,11 +207,14 @@ class OprojChain(Workload):
         self.x = [h.to(dev) for h in self.x_host]
         self.y = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
         self.y_host = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
-        self.ac = [torch.empty(M, K // 2, dtype=torch.uint8, device=dev) for _ in range(layers)]
+        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+        # activation codes in the tile layout the GEMM fetches by bulk copy
+        self.T = act_tile_rows(self.plan)
+        self.ac = [torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_A4W4, M, K, self.T), dtype=torch.uint8, device=dev)
+                   for _ in range(layers)]
         self.asf = [torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(layers)]
         self.ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(mx.KIND_A4W4, True, M, N, K)),
                               dtype=torch.uint8, device=dev)
-        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
         self.timed_label = "a4w4_gemm"
         self.kernel_bytes = a4w4_gemm_bytes(M, N, K)
         self.kernel_flops = 2 * M * N * K
@@ -223,10 +232,11 @@ class OprojChain(Workload):
         out = []
         for l in range(self.n_layers):
             wc, wsf = self.w[l]
-            out.append(("mx_quant", lambda l=l: mx.mx_quantize_act(self.x[l], codes=self.ac[l], sf=self.asf[l])))
+            out.append(("mx_quant", lambda l=l: mx.mx_quantize_act_tiled(self.x[l], self.T, codes=self.ac[l],
+                                                                         sf=self.asf[l])))
             out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
                 wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws,
-                weights_static=True, weights_tiled=True)))
+                weights_static=True, weights_tiled=True, act_tile_rows=self.T, m=self.M)))
         return out
 
     def e2e_step(self):
@@ -234,7 +244,8 @@ class OprojChain(Workload):
         for l in range(self.n_layers):
             self.x[l].copy_(self.x_host[l], non_blocking=True)
             wc, wsf = self.w[l]
-            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_tiled=True)
+            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_tiled=True,
+                            weights_static=True)
         for l in range(self.n_layers):
             self.y_host[l].copy_(self.y[l], non_blocking=True)
 
@@ -253,15 +264,19 @@ class MlpFp8(Workload):
         self.xg_host = synth.activation(M, H, seed=synth.act_seed(3, 0, 0)).pin_memory()
         self.xd_host = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1)).pin_memory()
         self.xg, self.xd = self.xg_host.to(dev), self.xd_host.to(dev)
-        self.qa_g = torch.empty(M, H, dtype=torch.uint8, device=dev)
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        # activations in the tile layout of each GEMM's plan
+        self.Tg = act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm))
+        self.Td = act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm))
+        self.qa_g = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, H, self.Tg), dtype=torch.uint8, device=dev)
         self.sa_g = torch.empty(M, dtype=torch.float32, device=dev)
-        self.qa_d = torch.empty(M, synth.MLP_I, dtype=torch.uint8, device=dev)
+        self.qa_d = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, synth.MLP_I, self.Td), dtype=torch.uint8,
+                                device=dev)
         self.sa_d = torch.empty(M, dtype=torch.float32, device=dev)
         self.yg = torch.empty(M, I2, dtype=torch.bfloat16, device=dev)
         self.yd = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
         self.yg_host = torch.empty(M, I2, dtype=torch.bfloat16).pin_memory()
         self.yd_host = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
-        sm = torch.cuda.get_device_properties(dev).multi_processor_count
         wsb = max(mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, I2, H),
                   mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, H, synth.MLP_I), 1 << 20)
         self.ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
@@ -281,12 +296,14 @@ class MlpFp8(Workload):
 
     def launches(self):
         mx = self.mx
-        return [("fp8_quant", lambda: mx.fp8_quantize_act(self.xg, q=self.qa_g, scale=self.sa_g)),
+        return [("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xg, self.Tg, q=self.qa_g, scale=self.sa_g)),
                 ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg,
-                                                          ws=self.ws, weights_static=True, weights_tiled=True)),
-                ("fp8_quant", lambda: mx.fp8_quantize_act(self.xd, q=self.qa_d, scale=self.sa_d)),
+                                                          ws=self.ws, weights_static=True, weights_tiled=True,
+                                                          act_tile_rows=self.Tg)),
+                ("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xd, self.Td, q=self.qa_d, scale=self.sa_d)),
                 ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd,
-                                                       ws=self.ws, weights_static=True, weights_tiled=True))]
+                                                       ws=self.ws, weights_static=True, weights_tiled=True,
+                                                       act_tile_rows=self.Td))]
 
     def e2e_step(self):
         mx = self.mx

@@ -46,7 +46,8 @@ class GemmOpts(ctypes.Structure):
                 ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
                 ("dev_status", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint32),
                 ("debug_stall", ctypes.c_int), ("weights_static", ctypes.c_int),
-                ("weights_tiled", ctypes.c_int), ("trace", ctypes.c_void_p)]
+                ("weights_tiled", ctypes.c_int), ("act_tile_rows", ctypes.c_int),
+                ("trace", ctypes.c_void_p)]
 
 
 class Plan(ctypes.Structure):
@@ -87,6 +88,12 @@ def lib() -> ctypes.CDLL:
             L.fp8_quantize_act.restype = i
             L.fp8_quantize_weight.argtypes = [vp, i, i, i, vp, vp, i, vp]
             L.fp8_quantize_weight.restype = i
+            L.mxg_act_tiled_bytes.argtypes = [i, i, i, i]
+            L.mxg_act_tiled_bytes.restype = sz
+            L.mx_quantize_act_tiled.argtypes = [vp, i, i, i, i, vp, vp, vp]
+            L.mx_quantize_act_tiled.restype = i
+            L.fp8_quantize_act_tiled.argtypes = [vp, i, i, i, i, vp, vp, vp]
+            L.fp8_quantize_act_tiled.restype = i
             L.fp8_gemm_ptpc.argtypes = [vp, vp, vp, vp, i, i, i, vp, i, i,
                                         ctypes.POINTER(GemmOpts), vp]
             L.fp8_gemm_ptpc.restype = i
@@ -203,6 +210,39 @@ def fp8_quantize_weight(w: torch.Tensor, layout: int = SF_ROWMAJOR, q=None, scal
     return q, scale
 
 
+def mxg_act_tiled_bytes(kind: int, M: int, K: int, tile_rows: int) -> int:
+    return int(lib().mxg_act_tiled_bytes(kind, M, K, tile_rows))
+
+
+def mx_quantize_act_tiled(x: torch.Tensor, tile_rows: int, codes=None, sf=None, stream=None):
+    """mx_quantize_act with the codes in the activation tile layout (tiles of
+    tile_rows rows; flat u8 of mxg_act_tiled_bytes bytes)."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+          "x must be a CUDA bf16 (M, K) tensor with unit inner stride")
+    M, K = x.shape
+    if codes is None:
+        codes = torch.empty(mxg_act_tiled_bytes(KIND_A4W4, M, K, tile_rows), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(mxg_sf_bytes(M, K, SF_SWIZZLED), dtype=torch.uint8, device=x.device)
+    _check("mx_quantize_act_tiled", lib().mx_quantize_act_tiled(
+        _ptr(x), M, K, x.stride(0), tile_rows, _ptr(codes), _ptr(sf), _stream(stream)))
+    return codes, sf
+
+
+def fp8_quantize_act_tiled(x: torch.Tensor, tile_rows: int, q=None, scale=None, stream=None):
+    """fp8_quantize_act with q in the activation tile layout."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+          "x must be a CUDA bf16 (M, K) tensor with unit inner stride")
+    M, K = x.shape
+    if q is None:
+        q = torch.empty(mxg_act_tiled_bytes(KIND_PTPC, M, K, tile_rows), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check("fp8_quantize_act_tiled", lib().fp8_quantize_act_tiled(
+        _ptr(x), M, K, x.stride(0), tile_rows, _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
 def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
     """Per-row E4M3 quantization: x (M, K) bf16 -> (q (M, K) u8, scale (M,) f32).
     Applied to a weight W (N, K) it gives the per-output-channel conversion."""
@@ -220,9 +260,9 @@ def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
 
 # ---------------------------------------------------------------- GEMMs
 def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static=False,
-          trace=None, weights_tiled=False) -> GemmOpts:
+          trace=None, weights_tiled=False, act_tile_rows=0) -> GemmOpts:
     return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas), weights_static=int(weights_static),
-                    weights_tiled=int(weights_tiled),
+                    weights_tiled=int(weights_tiled), act_tile_rows=int(act_tile_rows),
                     trace=0 if trace is None else trace.data_ptr(),
                     workspace=0 if ws is None else ws.data_ptr(),
                     ws_bytes=0 if ws is None else ws.numel() * ws.element_size(),
@@ -242,10 +282,12 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
                  out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                  weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                 stream=None):
+                 act_tile_rows: int = 0, m: int = 0, stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
     x (M, K) bf16 (quantized inside the call).  w_sf must be in the 128x4
-    tiles; w_codes row-major, or in weight tiles with weights_tiled=True."""
+    tiles; w_codes row-major, or in weight tiles with weights_tiled=True.
+    With act_tile_rows, a_codes is flat in the activation tile layout and
+    m gives M."""
     N, K2 = w_codes.shape
     K = 2 * K2
     fused = a_codes is None
@@ -254,13 +296,13 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
         M = x.shape[0]
         ldx = x.stride(0)
     else:
-        M = a_codes.shape[0]
+        M = m if m else a_codes.shape[0]
         ldx = 0
     out = _out(out, M, N, out_f32, w_codes.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_A4W4, fused, M, N, K, variant, ctas), w_codes.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled)
+              weights_tiled, act_tile_rows)
     _check("mx_gemm_a4w4", lib().mx_gemm_a4w4(
         _ptr(a_codes), _ptr(a_sf), _ptr(x), ldx, _ptr(w_codes), _ptr(w_sf), M, N, K,
         _ptr(out), out.stride(0), OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
@@ -271,16 +313,17 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                   ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                   weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                  stream=None):
+                  act_tile_rows: int = 0, stream=None):
     """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM; qw
-    row-major, or in weight tiles with weights_tiled=True."""
-    M, K = qa.shape
-    N = qw.shape[0]
+    row-major, or in weight tiles with weights_tiled=True; qa row-major, or
+    flat in the activation tile layout with act_tile_rows (M = len(sa))."""
+    M = sa.numel()
+    N, K = qw.shape
     out = _out(out, M, N, out_f32, qa.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled)
+              weights_tiled, act_tile_rows)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))

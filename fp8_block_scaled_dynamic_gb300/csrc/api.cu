@@ -148,9 +148,27 @@ mxg_status check_rows_arg(const void *x, int rows, int K, int ld) {
   return MXG_OK;
 }
 
-size_t fused_act_bytes(int M, int K) {
-  return align256((size_t)M * (K / 2)) + align256(mxg_sf_bytes(M, K, MXG_SF_SWIZZLED));
+// Bytes of activation codes (row bytes `row_bytes`) for M rows, row-major
+// (tile_rows == 0) or in tiles of tile_rows rows (the last tile padded).
+size_t act_code_bytes(int M, size_t row_bytes, int tile_rows) {
+  const size_t rows = tile_rows ? (size_t)((M + tile_rows - 1) / tile_rows) * tile_rows : (size_t)M;
+  return rows * row_bytes;
 }
+
+// Token-tile height of the activation codes a plan reads as tiles: the MMA-N
+// tile in the split-K variant (tokens are the MMA-B operand), 128 otherwise.
+int plan_act_tile_rows(const mxg_plan &pl) {
+  return pl.variant == MXG_VARIANT_SPLITK ? pl.bn : 128;
+}
+
+// Workspace bytes of the fused path's quantized activations (codes in tiles
+// of tile_rows rows, then the 128x4-tile scales).
+size_t fused_act_bytes(int M, int K, int tile_rows) {
+  return align256(act_code_bytes(M, (size_t)K / 2, tile_rows)) +
+         align256(mxg_sf_bytes(M, K, MXG_SF_SWIZZLED));
+}
+
+bool valid_tile_rows(int t) { return t == 16 || t == 32 || t == 64 || t == 128 || t == 256; }
 
 struct GemmOperands {
   const uint8_t *a, *a_sf, *w, *w_sf;  // codes (A4W4) or E4M3 bytes (PTPC)
@@ -159,9 +177,12 @@ struct GemmOperands {
 
 // ws: the caller's workspace base; part_off: where the partial tiles start
 // (after the counters and, on the fused path, the quantized activations).
+// act_tile_rows: 0 = activations row-major, else in the tile layout with
+// tiles of that many rows (must match the plan: plan_act_tile_rows).
 mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void *y, int ldy,
                     mxg_out_dtype out_dtype, const mxg_gemm_opts *opts, void *ws, size_t ws_bytes,
-                    size_t part_off, bool early_w, int sm_count, cudaStream_t stream) {
+                    size_t part_off, int act_tile_rows, int sm_count,
+                    cudaStream_t stream) {
   mxg_plan pl;
   mxg_status st = plan_impl(kind, M, N, K, sm_count, opts, &pl);
   if (st != MXG_OK) return st;
@@ -174,6 +195,8 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   const uint64_t row_bytes = kind == 0 ? (uint64_t)K / 2 : (uint64_t)K;
   const bool w_tiled = opts && opts->weights_tiled;
   if (w_tiled && (row_bytes % 128 != 0 || N % 128 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (act_tile_rows && act_tile_rows != plan_act_tile_rows(pl)) return MXG_ERR_INVALID_ARG;
+  if (act_tile_rows && row_bytes % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tmA, tmB;
   const uint8_t *A = swap ? op.w : op.a;
   const uint8_t *B = swap ? op.a : op.w;
@@ -211,14 +234,26 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   const uint32_t tmo = (opts && opts->timeout_ms) ? opts->timeout_ms : 1000u;
   p.timeout_ns = (unsigned long long)tmo * 1000000ull;
   p.debug_stall = opts ? opts->debug_stall : 0;
-  p.early_w = (early_w || (opts && opts->weights_static)) ? 1 : 0;
+  p.early_w = (opts && opts->weights_static) ? 1 : 0;
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
   p.kc_per_row = (int)(row_bytes / 128);
-  if (w_tiled) {  // the tensor map encoded above is then unused for that operand
-    if (swap)
+  // operands in the tile layout are fetched by bulk copy (their tensor map
+  // above is then unused)
+  if (w_tiled) {
+    if (swap) {
       p.a_tiles = op.w;
-    else
+    } else {
       p.b_tiles = op.w;
+      p.b_tile_rows = 128;
+    }
+  }
+  if (act_tile_rows) {
+    if (swap) {
+      p.b_tiles = op.a;
+      p.b_tile_rows = act_tile_rows;
+    } else {
+      p.a_tiles = op.a;
+    }
   }
   // Split-K partial tiles are summed by a separate reduce kernel spread over
   // every SM (MXG_SPLITK_INKERNEL=1: by the last CTA of each tile instead).
@@ -237,6 +272,8 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
   if (!aligned16(y) || ((size_t)ldy * (od == MXG_OUT_F32 ? 4 : 2)) % 16 != 0)
     return MXG_ERR_MISALIGNED;
   if (opts && (opts->variant < 0 || opts->variant > 2 || opts->ctas < 0))
+    return MXG_ERR_INVALID_ARG;
+  if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
     return MXG_ERR_INVALID_ARG;
   return MXG_OK;
 }
@@ -263,13 +300,14 @@ size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
   if (check_device(&sm) != MXG_OK) return 0;
   mxg_plan pl;
   if (plan_impl(kind, M, N, K, sm, opts, &pl) != MXG_OK) return 0;
-  const size_t act = (kind == 0 && fused) ? fused_act_bytes(M, K) : 0;
+  const size_t act = (kind == 0 && fused) ? fused_act_bytes(M, K, plan_act_tile_rows(pl)) : 0;
   if (pl.ws_bytes == 0 && act == 0) return 0;
   return kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
 }
 
-mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t *codes,
-                              uint8_t *sf, mxg_sf_layout layout, mxg_stream_t stream) {
+namespace {
+mxg_status mx_quantize_rows(const void *w_bf16, int N, int K, int ldw, uint8_t *codes, uint8_t *sf,
+                            mxg_sf_layout layout, bool act, mxg_stream_t stream) {
   mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
   if (st != MXG_OK) return st;
   if (!codes || !sf ||
@@ -280,14 +318,20 @@ mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
   cudaError_t e = mxg::launch_mx_quant(w_bf16, ldw, N, K, codes, sf, layout != MXG_SF_ROWMAJOR,
-                                       layout == MXG_TILED, sm,
+                                       layout == MXG_TILED ? 128 : 0, act, sm,
                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+}  // namespace
+
+mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t *codes,
+                              uint8_t *sf, mxg_sf_layout layout, mxg_stream_t stream) {
+  return mx_quantize_rows(w_bf16, N, K, ldw, codes, sf, layout, false, stream);
 }
 
 mxg_status mx_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *codes, uint8_t *sf,
                            mxg_stream_t stream) {
-  return mx_quantize_weight(x_bf16, M, K, ldx, codes, sf, MXG_SF_SWIZZLED, stream);
+  return mx_quantize_rows(x_bf16, M, K, ldx, codes, sf, MXG_SF_SWIZZLED, true, stream);
 }
 
 mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *q, float *scale,
@@ -298,7 +342,39 @@ mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx, uint8_t *
   if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  cudaError_t e = mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, false, sm,
+  cudaError_t e = mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, 0, true, sm,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+size_t mxg_act_tiled_bytes(int kind, int M, int K, int tile_rows) {
+  if ((kind != 0 && kind != 1) || M < 1 || K < 1 || !valid_tile_rows(tile_rows)) return 0;
+  return act_code_bytes(M, kind == 0 ? (size_t)K / 2 : (size_t)K, tile_rows);
+}
+
+mxg_status mx_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int tile_rows,
+                                 uint8_t *codes, uint8_t *sf, mxg_stream_t stream) {
+  mxg_status st = check_rows_arg(x_bf16, M, K, ldx);
+  if (st != MXG_OK) return st;
+  if (!codes || !sf || !valid_tile_rows(tile_rows)) return MXG_ERR_INVALID_ARG;
+  if (K % 256 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(codes) || !aligned16(sf)) return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, tile_rows, true, sm,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
+mxg_status fp8_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int tile_rows,
+                                  uint8_t *q, float *scale, mxg_stream_t stream) {
+  mxg_status st = check_rows_arg(x_bf16, M, K, ldx);
+  if (st != MXG_OK) return st;
+  if (!q || !scale || !valid_tile_rows(tile_rows)) return MXG_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  if ((st = check_device(&sm)) != MXG_OK) return st;
+  cudaError_t e = mxg::launch_fp8_quant(x_bf16, ldx, M, K, q, scale, tile_rows, true, sm,
                                         reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
@@ -312,8 +388,8 @@ mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_
   if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  cudaError_t e = mxg::launch_fp8_quant(w_bf16, ldw, N, K, q, scale, layout == MXG_TILED, sm,
-                                        reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = mxg::launch_fp8_quant(w_bf16, ldw, N, K, q, scale, layout == MXG_TILED ? 128 : 0, false,
+                                        sm, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 
@@ -339,27 +415,30 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
   uint8_t *ws = opts ? static_cast<uint8_t *>(opts->workspace) : nullptr;
   size_t ws_bytes = opts ? opts->ws_bytes : 0;
   size_t part_off = kCounterBytes;
+  int act_tile_rows = opts ? opts->act_tile_rows : 0;
   if (fused) {
-    const size_t need = fused_act_bytes(M, K);
-    if (!ws || ws_bytes < kCounterBytes + need) return MXG_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
-    // plan first so that a too-small workspace is reported before any launch
+    // plan first: the activations are quantized straight into the tile
+    // layout the plan reads, and a too-small workspace is reported before
+    // any launch
     mxg_plan pl;
     if ((st = plan_impl(0, M, N, K, sm, opts, &pl)) != MXG_OK) return st;
+    act_tile_rows = K % 256 == 0 ? plan_act_tile_rows(pl) : 0;
+    const size_t need = fused_act_bytes(M, K, act_tile_rows);
+    if (!ws || ws_bytes < kCounterBytes + need) return MXG_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
     if (pl.ws_bytes > 0 && ws_bytes < kCounterBytes + need + (pl.ws_bytes - kCounterBytes))
       return MXG_ERR_WORKSPACE;
     uint8_t *codes = ws + kCounterBytes;
-    uint8_t *sf = codes + align256((size_t)M * (K / 2));
-    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, false, sm, s);
+    uint8_t *sf = codes + align256(act_code_bytes(M, (size_t)K / 2, act_tile_rows));
+    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s);
     if (e != cudaSuccess) return MXG_ERR_CUDA;
     a_codes = codes;
     a_sf = sf;
     part_off += need;
   }
   GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
-  // fused: the kernel just before the GEMM is the activation quantizer, which
-  // does not write the weights
-  return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, fused, sm, s);
+  return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, act_tile_rows,
+                  sm, s);
 }
 
 mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
@@ -375,7 +454,7 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, 
   if ((st = check_device(&sm)) != MXG_OK) return st;
   GemmOperands op{qa, nullptr, qw, nullptr, sa, sw};
   return run_gemm(1, op, M, N, K, y, ldy, out_dtype, opts, opts ? opts->workspace : nullptr,
-                  opts ? opts->ws_bytes : 0, kCounterBytes, false, sm,
+                  opts ? opts->ws_bytes : 0, kCounterBytes, opts ? opts->act_tile_rows : 0, sm,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -449,7 +528,8 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, con
   mxg_plan pl;
   if ((st = plan_impl(0, M, N, K, sm, nullptr, &pl)) != MXG_OK) return st;
   const bool fused = a_codes == nullptr;
-  const size_t act = fused ? fused_act_bytes(M, K) : 0;
+  const size_t act =
+      fused ? fused_act_bytes(M, K, K % 256 == 0 ? plan_act_tile_rows(pl) : 0) : 0;
   const size_t need = kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
   if (need > (size_t)MXG_NOALLOC_SCRATCH_BYTES) return MXG_ERR_WORKSPACE;
   void *scratch = nullptr;

@@ -233,7 +233,7 @@ __device__ __forceinline__ void reduce_partials(const GemmParams &p, const float
 }
 
 template <int KIND, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small kernels beside it
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
   using C = Cfg<KIND, BN>;
@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     trace_mark(p, kTrEntry);
     trace_set(p, kTrEntryNs, global_timer_ns());
   }
+  // The next kernel may launch now: it touches no memory this one writes or
+  // reads before its own griddepcontrol.wait, which returns only when this
+  // grid has completed.  Its CTAs take an SM as this kernel's leave it.
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -330,7 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     min(2, p.G4 - 2 * kb) * 512, fb, polA);
       };
       auto issue_b = [&](int stage, const Item &it, int kb, uint32_t fb) {
-        if (p.b_tiles) {  // BN is a multiple of 128 here: one tile per 128-row block
+        if (p.b_tiles && p.b_tile_rows == BN) {  // one tile of BN rows (activations)
+          bulk_load(sB + stage * C::kBBytes,
+                    p.b_tiles + ((size_t)it.tb * p.kc_per_row + kb) * (size_t)C::kBBytes,
+                    C::kBBytes, fb, polB);
+        } else if (p.b_tiles) {  // 128-row weight tiles, BN / 128 of them
           for (int j = 0; j < BN / 128; ++j)
             bulk_load(sB + stage * C::kBBytes + j * 16384,
                       p.b_tiles + ((size_t)(it.tb * (BN / 128) + j) * p.kc_per_row + kb) * 16384u,
@@ -367,9 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       pdl_wait();
-      // Dependents may start only after this kernel's own wait: an early
-      // start then overlaps one kernel at most, never the one before it.
-      pdl_trigger();
+      trace_mark(p, kTrWaited);
       uint32_t cur = first_cursor(p);
       Item it;
       int stage = 0;
@@ -418,6 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc0 = KIND == 0 ? idesc_mxf4(kTileA, BN) : idesc_f8(kTileA, BN);
+      // the bounded waits below start counting only once the kernels this
+      // one depends on have finished
+      pdl_wait();
+      trace_mark(p, kTrWaited);
       uint32_t cur = first_cursor(p);
       Item it;
       int stage = 0;
@@ -658,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int KIND>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, int bn,
                                                             unsigned gemm_ctas) {
-  pdl_wait();  // the GEMM that wrote the partial slots has completed
-  pdl_trigger();
+  pdl_trigger();  // touches nothing before the wait below
+  pdl_wait();     // the GEMM that wrote the partial slots has completed
   const unsigned U = (unsigned)p.units, KB = (unsigned)p.kblocks;
   const int per_col = kTileA / 4;
   const int per_tile = bn * per_col;
@@ -768,7 +778,10 @@ cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm
                                  int sm_count, cudaStream_t stream) {
   const long long total = (long long)p.tilesA * p.tilesB * bn * (kTileA / 4);
   long long blocks = (total + 255) / 256;
-  const long long cap = (long long)(sm_count > 0 ? sm_count : 152) * 4;
+  // one CTA per SM: launched early (programmatic launch), the reduce CTAs sit
+  // beside the GEMM CTAs, and the next GEMM's CTAs must still fit beside
+  // them and the next quantizer's (registers: 24K + 8K + 8-12K of 64K)
+  const long long cap = (long long)(sm_count > 0 ? sm_count : 152);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(256), 0, stream);

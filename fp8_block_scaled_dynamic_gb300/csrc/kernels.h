@@ -36,12 +36,17 @@ inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) 
   cfg.numAttrs = 1;
 }
 
+// tile_rows: 0 = row-major codes / bytes, else the tile layout with tiles of
+// that many rows (128 for weights, the GEMM's token tile for activations).
+// act: the input is an activation; the next kernel may launch at once.  For
+// weights (act = false) no later kernel starts before this one has finished.
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
-                            uint8_t *sf, bool swizzled, bool tiled_codes, int sm_count,
+                            uint8_t *sf, bool swizzled, int tile_rows, bool act, int sm_count,
                             cudaStream_t stream);
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
-                             float *scale, bool tiled, int sm_count, cudaStream_t stream);
+                             float *scale, int tile_rows, bool act, int sm_count,
+                             cudaStream_t stream);
 
 // Everything one GEMM launch needs besides the two tensor maps.
 struct GemmParams {
@@ -68,12 +73,13 @@ struct GemmParams {
   int debug_stall;
   unsigned long long *trace;  // optional: kTracePoints SM-clock stamps per CTA
   const uint8_t *a_tiles;  // non-null: the MMA-A operand in the weight tile layout (bulk copies)
-  const uint8_t *b_tiles;  // non-null: the MMA-B operand in the weight tile layout
+  const uint8_t *b_tiles;  // non-null: the MMA-B operand in the tile layout, b_tile_rows rows
+  int b_tile_rows;         //   per tile: 128 (weights, full-tile mode) or BN (activations)
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
                            //          the last CTA of each tile
-  int early_w;         // 1: the weights were not written by the previous kernel in the
-                       //    stream, so their first stages may load before griddepcontrol.wait
+  int early_w;         // 1: no kernel still in flight writes the weights, so their first
+                       //    stages may load before griddepcontrol.wait
 };
 
 // Timeline trace points (index into a CTA's 16 slots): SM clock64 values.
@@ -81,7 +87,7 @@ enum TracePoint {
   kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrLastLoad = 3, kTrFirstFull = 4,
   kTrLastCommit = 5, kTrAcc0 = 6, kTrItem0Done = 7, kTrAcc1 = 8, kTrItem1Done = 9,
   kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12, kTrDecision = 13, kTrReduced = 14,
-  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTracePoints = 20
+  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18, kTracePoints = 20
 };
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.

@@ -67,12 +67,14 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
   return v;
 }
 
-// Byte offset of (row r, byte b of the row) in the weight tile layout: 16 KiB
-// tiles of 128 rows x 128 bytes, tile (r / 128, b / 128) at ((r/128)*KC +
-// b/128) * 16384, 16-byte unit j of row r at (r % 128) * 128 + ((j ^ (r % 8)) * 16).
-__device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row) {
+// Byte offset of (row r, byte b of the row) in the tile layout with T-row
+// tiles (T = 128 for weights; the GEMM's token tile for activations): tile
+// (r / T, b / 128) of T rows x 128 bytes at ((r/T)*KC + b/128) * T * 128, and
+// the 16-byte unit j of row r at (r % T) * 128 + ((j ^ (r % 8)) * 16).
+__device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row, int T) {
   const int j = (b >> 4) & 7;
-  return ((size_t)(r >> 7) * kc_per_row + (b >> 7)) * 16384u + (size_t)(r & 127) * 128u +
+  const int rt = r / T;
+  return ((size_t)rt * kc_per_row + (b >> 7)) * (size_t)T * 128u + (size_t)(r - rt * T) * 128u +
          (size_t)((j ^ (r & 7)) << 4) + (b & 15);
 }
 
@@ -82,21 +84,32 @@ constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in fligh
 // grid: x = chunk groups along the row, y = rows (grid-stride).
 // rows_iter >= rows: rows in [rows, rows_iter) are padding (swizzled layout
 // only) -- their scales are written as 0 and no codes are stored.
-template <bool kSwizzled, bool kTiledCodes>
+// tile_rows: 0 = row-major codes, else the tile layout with that tile height.
+template <bool kSwizzled>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
                                                               long long ldx, int rows,
-                                                              int rows_iter, int K,
+                                                              int rows_iter, int K, int tile_rows,
+                                                              int early_trigger,
                                                               uint8_t *__restrict__ codes,
                                                               uint8_t *__restrict__ sf) {
   const int cpr = K >> 3;  // 16-byte chunks per row; K % 128 == 0 => cpr % 16 == 0
   const int G = K >> 5;    // MX blocks per row
   const int lane = threadIdx.x & 31;
   const unsigned kFull = 0xFFFFFFFFu;
-  // x may be the previous kernel's output and codes/sf may still be read by
-  // it; only once it is complete may the next kernel start its prologue
-  // (triggering after the wait keeps every early start one kernel deep).
+  // An activation quantizer lets the next kernel launch at once: every kernel
+  // of this library waits for its predecessor before it touches memory that
+  // one may write.  A weight quantizer never triggers, so no later kernel
+  // starts (and streams weights before its own wait) until it has finished.
+  if (early_trigger) pdl_trigger();
+  // Warm L2 with this CTA's part of its first row while the kernel ahead
+  // finishes; the loads below come after the wait.
+  if (threadIdx.x == 0 && (int)blockIdx.y < rows) {
+    const int c0 = blockIdx.x * kMxChunksPerThread * kMxThreads;
+    const int nc = min(kMxChunksPerThread * kMxThreads, cpr - c0);
+    if (nc > 0) prefetch_l2_bulk(x + (size_t)blockIdx.y * ldx + (size_t)c0 * 8, (uint32_t)nc * 16u);
+  }
+  // x may be the previous kernel's output and codes/sf may still be read by it
   pdl_wait();
-  pdl_trigger();
   for (int r = blockIdx.y; r < rows_iter; r += gridDim.y) {
     const bool real_row = r < rows;
     uint4 v[kMxChunksPerThread];
@@ -138,8 +151,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
                   (nibble_signs(w.w) << 24);
       }
       if (real_row && in_row) {
-        const size_t off = kTiledCodes ? tiled_offset(r, cc[i] * 4, K >> 8)
-                                       : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
+        const size_t off = tile_rows ? tiled_offset(r, cc[i] * 4, K >> 8, tile_rows)
+                                     : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
         *reinterpret_cast<uint32_t *>(codes + off) = packed;
       }
       // Gather the scales of 4 consecutive blocks (lanes 0,4,8,12 of each
@@ -163,41 +176,53 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
 }
 
 constexpr int kF8Threads = 256;
-constexpr int kF8RegChunks = 12;  // rows of up to 12*256*8 = 24576 values stay in registers
 
-// One CTA per row (grid-stride over rows).  kTiled: q in the weight tile layout.
-template <bool kTiled>
-__global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *__restrict__ x,
+// Read-only 16-byte load that stays in L1: the second pass over a row finds it there.
+__device__ __forceinline__ uint4 ld_keep_v4(const uint16_t *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::evict_last.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t amax_bf16x8(const uint4 &w) {
+  const uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  return max(m2 & 0xFFFFu, m2 >> 16);
+}
+
+// One CTA per row (grid-stride over rows), two passes over the row: the
+// amax, then the codes (the row is re-read from L1).  Few registers, so the
+// CTAs fit beside a resident GEMM CTA.  tile_rows: 0 = row-major q, else the
+// tile layout with that tile height.
+__global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
                                                                long long ldx, int rows, int K,
+                                                               int tile_rows, int early_trigger,
                                                                uint8_t *__restrict__ q,
                                                                float *__restrict__ scale) {
   __shared__ uint32_t red[kF8Threads / 32];
   const int cpr = K >> 3;
   const int tid = threadIdx.x;
+  if (early_trigger) pdl_trigger();  // activations only, as in mx_quant_kernel
+  if (threadIdx.x == 0 && (int)blockIdx.x < rows) {  // warm L2 with the first row
+    const uint16_t *xr = x + (size_t)blockIdx.x * ldx;
+    for (int c = 0; c < cpr; c += 1024)  // 16 KiB pieces
+      prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
+  }
   pdl_wait();
-  pdl_trigger();
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint16_t *xr = x + (size_t)r * ldx;
-    uint4 v[kF8RegChunks];
     uint32_t amax = 0;
-#pragma unroll
-    for (int i = 0; i < kF8RegChunks; ++i) {
-      const int c = i * kF8Threads + tid;
-      v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (c < cpr) v[i] = ld_stream_v4(xr + (size_t)c * 8);
+    int c = tid;
+    for (; c + 3 * kF8Threads < cpr; c += 4 * kF8Threads) {  // 4 loads in flight
+      const uint4 a = ld_keep_v4(xr + (size_t)c * 8);
+      const uint4 b = ld_keep_v4(xr + (size_t)(c + kF8Threads) * 8);
+      const uint4 d = ld_keep_v4(xr + (size_t)(c + 2 * kF8Threads) * 8);
+      const uint4 e = ld_keep_v4(xr + (size_t)(c + 3 * kF8Threads) * 8);
+      amax = max(max(amax, amax_bf16x8(a)), max(amax_bf16x8(b), max(amax_bf16x8(d), amax_bf16x8(e))));
     }
-#pragma unroll
-    for (int i = 0; i < kF8RegChunks; ++i) {
-      uint32_t m2 = __vmaxu2(__vmaxu2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                             __vmaxu2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-      amax = max(amax, max(m2 & 0xFFFFu, m2 >> 16));
-    }
-    for (int c = kF8RegChunks * kF8Threads + tid; c < cpr; c += kF8Threads) {  // long rows
-      const uint4 w = ld_stream_v4(xr + (size_t)c * 8);
-      uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                             __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-      amax = max(amax, max(m2 & 0xFFFFu, m2 >> 16));
-    }
+    for (; c < cpr; c += kF8Threads) amax = max(amax, amax_bf16x8(ld_keep_v4(xr + (size_t)c * 8)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     if ((tid & 31) == 0) red[tid >> 5] = amax;
@@ -209,8 +234,8 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *_
 
     // destination of the 8 bytes of chunk c of this row
     auto qdst = [&](int c) -> uint2 * {
-      return reinterpret_cast<uint2 *>(q + (kTiled ? tiled_offset(r, c * 8, K >> 7)
-                                                   : (size_t)r * K + (size_t)c * 8));
+      return reinterpret_cast<uint2 *>(q + (tile_rows ? tiled_offset(r, c * 8, K >> 7, tile_rows)
+                                                      : (size_t)r * K + (size_t)c * 8));
     };
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
@@ -229,20 +254,14 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_kernel(const uint16_t *_
       hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
       return make_uint2(lo, hi);
     };
-#pragma unroll
-    for (int i = 0; i < kF8RegChunks; ++i) {
-      const int c = i * kF8Threads + tid;
-      if (c < cpr) *qdst(c) = quant8(v[i]);
-    }
-    for (int c = kF8RegChunks * kF8Threads + tid; c < cpr; c += kF8Threads)
-      *qdst(c) = quant8(ld_stream_v4(xr + (size_t)c * 8));
+    for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
-                            uint8_t *sf, bool swizzled, bool tiled_codes, int sm_count,
+                            uint8_t *sf, bool swizzled, int tile_rows, bool act, int sm_count,
                             cudaStream_t stream) {
   const int cpr = K / 8;
   const int per_block = kMxThreads * kMxChunksPerThread;
@@ -258,29 +277,24 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
-  if (tiled_codes)
-    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true, true>, xp, ldx, rows, rows_iter, K, codes,
-                              sf);
   if (swizzled)
-    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true, false>, xp, ldx, rows, rows_iter, K,
-                              codes, sf);
-  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false, false>, xp, ldx, rows, rows_iter, K, codes,
-                            sf);
+    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true>, xp, ldx, rows, rows_iter, K, tile_rows,
+                              act ? 1 : 0, codes, sf);
+  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false>, xp, ldx, rows, rows_iter, K, tile_rows,
+                            act ? 1 : 0, codes, sf);
 }
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
-                             float *scale, bool tiled, int sm_count, cudaStream_t stream) {
+                             float *scale, int tile_rows, bool act, int sm_count,
+                             cudaStream_t stream) {
   int g = rows;
   const int cap = (sm_count > 0 ? sm_count : 152) * 8;
   if (g > cap) g = cap;
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
-  if (tiled)
-    return cudaLaunchKernelEx(&cfg, fp8_quant_kernel<true>, static_cast<const uint16_t *>(x), ldx,
-                              rows, K, q, scale);
-  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel<false>, static_cast<const uint16_t *>(x), ldx,
-                            rows, K, q, scale);
+  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows, K,
+                            tile_rows, act ? 1 : 0, q, scale);
 }
 
 }  // namespace mxg

@@ -24,8 +24,11 @@
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
  *     do not synchronise the host, except mxg_query_status.  Kernels are
  *     launched with programmatic stream serialization: each may begin its
- *     prologue while the kernel before it finishes, and touches no memory
- *     that kernel may use before that kernel has completed.
+ *     prologue while the kernels before it finish, and touches no memory
+ *     they may use before the kernel just before it has completed (which in
+ *     turn waited for its own predecessor).  The one exception is the GEMMs'
+ *     opts->weights_static.  The weight quantizers (mx_quantize_weight,
+ *     fp8_quantize_weight) never let a later kernel start before they end.
  *   - Host-detectable errors (bad shape, alignment, device, workspace) are
  *     returned before anything is launched.  A failed launch returns
  *     MXG_ERR_CUDA.  Device-side waits are bounded; a wait that runs out
@@ -117,18 +120,28 @@ typedef struct {
     uint32_t timeout_ms;  /* limit of every device-side wait; 0 = 1000 ms */
     int debug_stall;      /* test hook: 1 makes the epilogue wait on a barrier nothing
                              arrives at, so the timeout path runs (no fault, no hang) */
-    int weights_static;   /* 1: the kernel enqueued on `stream` just before this call did
-                             not write the weight operands (w_codes/w_sf or qw), so the
-                             GEMM may start streaming them while that kernel finishes
-                             (programmatic dependent launch).  The fused A4W4 path does
-                             this for its own quantization kernel without being asked. */
+    int weights_static;   /* 1: no kernel that may still be running when the GEMM starts
+                             writes the weight operands (w_codes/w_sf or qw/sw), so the
+                             GEMM may stream them in before the kernels ahead of it on
+                             `stream` have finished (programmatic dependent launch).
+                             Weights written by mx_quantize_weight / fp8_quantize_weight,
+                             by a kernel without programmatic launch, or before a
+                             synchronisation qualify; weights written by this library's
+                             activation quantizers, GEMMs or reduce do not. */
     int weights_tiled;    /* 1: w_codes (A4W4) / qw (PTPC) are in the MXG_TILED weight tile
                              layout; 0: row-major */
+    int act_tile_rows;    /* 0: a_codes (A4W4) / qa (PTPC) are row-major; else they are in
+                             the activation tile layout with tiles of this many rows, as
+                             written by mx_quantize_act_tiled / fp8_quantize_act_tiled; it
+                             must equal the plan's MMA-N tile (mxg_plan_gemm().bn) for the
+                             SPLITK variant and 128 for the FULL variant.  (The fused A4W4
+                             path picks its own layout and ignores this field.) */
     void *trace;          /* optional device buffer of ctas x 20 uint64, zero-filled: each
                              CTA records SM clock64 stamps of its timeline (entry, setup,
                              first/last load, first stage ready, last MMA commit, epilogue
                              items, split-K hand-off, exit; slot 15 = items; slots 16/17 =
-                             global timer ns at entry/exit).  NULL = off. */
+                             global timer ns at entry/exit; slot 18 = the producer's
+                             dependency wait returned).  NULL = off. */
 } mxg_gemm_opts;
 
 typedef struct {
@@ -208,6 +221,24 @@ mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx,
 mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw,
                                uint8_t *q, float *scale, mxg_sf_layout layout,
                                mxg_stream_t stream);
+
+/* Activation tile layout: the weight tile layout (MXG_TILE_BYTES) with tiles
+ * of T = tile_rows rows instead of 128 (T in {16, 32, 64, 128, 256}): tile
+ * (r / T, chunk kc) of T rows x 128 bytes at byte ((r/T) * KC + kc) * T * 128,
+ * the 16-byte unit j of row r at (r % T) * 128 + ((j ^ (r % 8)) * 16).  The
+ * GEMM fetches a token tile with one bulk copy.  Rows past M in the last tile
+ * are left unwritten (they only feed output columns past M, which are not
+ * stored).  Bytes: mxg_act_tiled_bytes. */
+size_t mxg_act_tiled_bytes(int kind, int M, int K, int tile_rows);
+
+/* mx_quantize_act with the codes in the activation tile layout (K % 256 == 0);
+ * the scales as mx_quantize_act (128x4 tiles, padding rows 0). */
+mxg_status mx_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int tile_rows,
+                                 uint8_t *codes, uint8_t *sf, mxg_stream_t stream);
+
+/* fp8_quantize_act with q in the activation tile layout. */
+mxg_status fp8_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int tile_rows,
+                                  uint8_t *q, float *scale, mxg_stream_t stream);
 
 /* FP8 PTPC A8W8 GEMM: y[m][n] = (acc[m][n] * sa[m]) * sw[n] with
  * acc = sum_k v(qa[m,k]) v(qw[n,k]) accumulated in fp32.

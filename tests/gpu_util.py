@@ -60,3 +60,13 @@ def untile(tiled: np.ndarray, rows: int, row_bytes: int) -> np.ndarray:
     j = np.arange(8)[None, :]
     logical = a[:, :, r, j ^ (r % 8), :]          # [rb][kc][128][8][16]
     return logical.transpose(0, 2, 1, 3, 4).reshape(rows, row_bytes)
+
+
+def untile_rows(tiled: np.ndarray, rows: int, row_bytes: int, T: int) -> np.ndarray:
+    """Activation tile layout with T-row tiles -> row-major (rows, row_bytes)."""
+    kc = row_bytes // 128
+    a = np.asarray(tiled, dtype=np.uint8).reshape(rows // T, kc, T, 8, 16)
+    r = np.arange(T)[:, None]
+    j = np.arange(8)[None, :]
+    logical = a[:, :, r, j ^ (r % 8), :]
+    return logical.transpose(0, 2, 1, 3, 4).reshape(rows, row_bytes)
