@@ -191,7 +191,7 @@ class OprojChain(Workload):
     """A4W4 o_proj layers: fused dynamic MXFP4 activation quantization +
     block-scaled GEMM per layer."""
 
-    def __init__(self, mx, synth, dev, M, layers, w_seeds, cfg, row_scale=False, name=""):
+    def __init__(self, mx, synth, dev, M, layers, w_seeds, cfg, row_scale=False, name="", fused=False):
         self.mx, self.dev = mx, dev
         N, K = synth.OPROJ_N, synth.OPROJ_K
         self.M, self.N, self.K = M, N, K
@@ -215,8 +215,12 @@ class OprojChain(Workload):
         self.asf = [torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(layers)]
         self.ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(mx.KIND_A4W4, True, M, N, K)),
                               dtype=torch.uint8, device=dev)
-        self.timed_label = "a4w4_gemm"
-        self.kernel_bytes = a4w4_gemm_bytes(M, N, K)
+        # fused: one launch per layer -- the GEMM's CTAs quantize x themselves
+        # (split-K plans only; slower than the three-kernel chain, kept for
+        # comparison); else the standalone quantizer, then the GEMM
+        self.fused = fused and self.plan["variant"] == 2 and K % 256 == 0
+        self.timed_label = "a4w4_fused" if self.fused else "a4w4_gemm"
+        self.kernel_bytes = a4w4_fused_bytes(M, N, K) if self.fused else a4w4_gemm_bytes(M, N, K)
         self.kernel_flops = 2 * M * N * K
         self.bytes_per_step = layers * a4w4_fused_bytes(M, N, K)
         self.flops_per_step = layers * 2 * M * N * K
@@ -224,6 +228,9 @@ class OprojChain(Workload):
         self.bound = "hbm" if M <= 512 else "tensor"
         v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
         self.kernel_desc = f"gemm_kernel<A4W4, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
+        if self.fused:
+            self.kernel_desc += (", one cooperative launch: activation quantization, grid barrier, "
+                                 "GEMM, grid barrier, split-K reduction")
         self.h2d = layers * M * K * 2
         self.d2h = layers * M * N * 2
 
@@ -232,6 +239,11 @@ class OprojChain(Workload):
         out = []
         for l in range(self.n_layers):
             wc, wsf = self.w[l]
+            if self.fused:
+                out.append(("a4w4_fused", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
+                    wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_static=True, weights_tiled=True,
+                    splitk_reduce="grid")))
+                continue
             out.append(("mx_quant", lambda l=l: mx.mx_quantize_act_tiled(self.x[l], self.T, codes=self.ac[l],
                                                                          sf=self.asf[l])))
             out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(

@@ -47,7 +47,10 @@ class GemmOpts(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint32),
                 ("debug_stall", ctypes.c_int), ("weights_static", ctypes.c_int),
                 ("weights_tiled", ctypes.c_int), ("act_tile_rows", ctypes.c_int),
-                ("trace", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("splitk_reduce", ctypes.c_int)]
+
+
+REDUCE = {"default": 0, "kernel": 1, "grid": 2, "lastcta": 3}
 
 
 class Plan(ctypes.Structure):
@@ -260,9 +263,10 @@ def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
 
 # ---------------------------------------------------------------- GEMMs
 def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static=False,
-          trace=None, weights_tiled=False, act_tile_rows=0) -> GemmOpts:
+          trace=None, weights_tiled=False, act_tile_rows=0, splitk_reduce="default") -> GemmOpts:
     return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas), weights_static=int(weights_static),
                     weights_tiled=int(weights_tiled), act_tile_rows=int(act_tile_rows),
+                    splitk_reduce=REDUCE[splitk_reduce],
                     trace=0 if trace is None else trace.data_ptr(),
                     workspace=0 if ws is None else ws.data_ptr(),
                     ws_bytes=0 if ws is None else ws.numel() * ws.element_size(),
@@ -282,7 +286,7 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
                  out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                  weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                 act_tile_rows: int = 0, m: int = 0, stream=None):
+                 act_tile_rows: int = 0, m: int = 0, splitk_reduce: str = "default", stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
     x (M, K) bf16 (quantized inside the call).  w_sf must be in the 128x4
     tiles; w_codes row-major, or in weight tiles with weights_tiled=True.
@@ -302,7 +306,7 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_A4W4, fused, M, N, K, variant, ctas), w_codes.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled, act_tile_rows)
+              weights_tiled, act_tile_rows, splitk_reduce)
     _check("mx_gemm_a4w4", lib().mx_gemm_a4w4(
         _ptr(a_codes), _ptr(a_sf), _ptr(x), ldx, _ptr(w_codes), _ptr(w_sf), M, N, K,
         _ptr(out), out.stride(0), OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
@@ -313,7 +317,7 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                   ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                   weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                  act_tile_rows: int = 0, stream=None):
+                  act_tile_rows: int = 0, splitk_reduce: str = "default", stream=None):
     """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM; qw
     row-major, or in weight tiles with weights_tiled=True; qa row-major, or
     flat in the activation tile layout with act_tile_rows (M = len(sa))."""
@@ -323,7 +327,7 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled, act_tile_rows)
+              weights_tiled, act_tile_rows, splitk_reduce)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))

@@ -21,7 +21,10 @@ constexpr int kMaxDevices = 64;
 // the first call, left zero by every completed call), then the quantized
 // activations of the fused A4W4 path, then the split-K partial tiles.
 constexpr size_t kCounterBytes = 64 * 1024;
-constexpr long long kMaxSplitTiles = kCounterBytes / sizeof(int);
+// the last 512 bytes of the counter region hold the grid barrier words
+// (one 128-byte line each)
+constexpr size_t kGridBarrierOff = kCounterBytes - 512;
+constexpr long long kMaxSplitTiles = kGridBarrierOff / sizeof(int);
 
 struct DevInfo {
   bool init = false;
@@ -79,12 +82,23 @@ mxg_status make_operand_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes,
   return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
 }
 
-bool splitk_inkernel() {
-  static const bool on = [] {
-    const char *e = std::getenv("MXG_SPLITK_INKERNEL");
-    return e && e[0] == '1';
+// How split-K partial tiles are summed on the two-kernel path:
+//   kernel (default): a reduce kernel launched right after the GEMM;
+//   grid: by every CTA of the GEMM after a grid barrier (one launch);
+//   lastcta: by the last CTA to finish each tile (arrival counter).
+// MXG_SPLITK_REDUCE=kernel|grid|lastcta selects it (MXG_SPLITK_INKERNEL=1 =
+// lastcta).  The single-kernel fused A4W4 path always sums in-grid.
+enum class ReduceMode { kKernel, kGrid, kLastCta };
+ReduceMode reduce_mode() {
+  static const ReduceMode m = [] {
+    const char *e = std::getenv("MXG_SPLITK_REDUCE");
+    if (e && std::strcmp(e, "grid") == 0) return ReduceMode::kGrid;
+    if (e && std::strcmp(e, "lastcta") == 0) return ReduceMode::kLastCta;
+    const char *f = std::getenv("MXG_SPLITK_INKERNEL");
+    if (f && f[0] == '1') return ReduceMode::kLastCta;
+    return ReduceMode::kKernel;
   }();
-  return on;
+  return m;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -100,9 +114,13 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
   if (K % 128 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   int variant = opts ? opts->variant : MXG_VARIANT_AUTO;
   if (variant < MXG_VARIANT_AUTO || variant > MXG_VARIANT_SPLITK) return MXG_ERR_INVALID_ARG;
-  const int kstage = kind == 0 ? 256 : 128;
-  const int KB = (K + kstage - 1) / kstage;
   if (variant == MXG_VARIANT_AUTO) variant = (M <= 256) ? MXG_VARIANT_SPLITK : MXG_VARIANT_FULL;
+  // pipeline stages along K: 128-byte K columns (256 E2M1 / 128 E4M3
+  // values), one per stage in the full-tile kernel, two in the split-K one
+  const int kcol = kind == 0 ? 256 : 128;
+  const int KC = (K + kcol - 1) / kcol;
+  const int per = mxg::gemm_cols_per_stage(variant == MXG_VARIANT_SPLITK);
+  const int KB = (KC + per - 1) / per;
   std::memset(pl, 0, sizeof(*pl));
   pl->variant = variant;
   pl->kblocks = KB;
@@ -121,7 +139,8 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
     const long long tiles = tilesA * tilesB;
     const long long U = tiles * KB;
     if (U > (1LL << 40) / 4) return MXG_ERR_UNSUPPORTED_SHAPE;
-    long long G = (opts && opts->ctas > 0) ? opts->ctas : sm_count;
+    // persistent: at most one CTA per SM (grid barriers need them all resident)
+    long long G = (opts && opts->ctas > 0 && opts->ctas < sm_count) ? opts->ctas : sm_count;
     if (G > U) G = U;
     int seg_max = 1;
     for (long long t = 0; t < tiles; ++t) {
@@ -173,6 +192,8 @@ bool valid_tile_rows(int t) { return t == 16 || t == 32 || t == 64 || t == 128 |
 struct GemmOperands {
   const uint8_t *a, *a_sf, *w, *w_sf;  // codes (A4W4) or E4M3 bytes (PTPC)
   const float *sa, *sw;                // PTPC scales
+  const void *x;                       // single-kernel fused A4W4: bf16 activations that the
+  long long ldx;                       //   GEMM quantizes into a / a_sf itself
 };
 
 // ws: the caller's workspace base; part_off: where the partial tiles start
@@ -236,7 +257,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.debug_stall = opts ? opts->debug_stall : 0;
   p.early_w = (opts && opts->weights_static) ? 1 : 0;
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
-  p.kc_per_row = (int)(row_bytes / 128);
+  p.kc_per_row = (int)((row_bytes + 127) / 128);  // the last column may be half (TMA pads it)
   // operands in the tile layout are fetched by bulk copy (their tensor map
   // above is then unused)
   if (w_tiled) {
@@ -255,9 +276,23 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
       p.a_tiles = op.a;
     }
   }
-  // Split-K partial tiles are summed by a separate reduce kernel spread over
-  // every SM (MXG_SPLITK_INKERNEL=1: by the last CTA of each tile instead).
-  p.defer_reduce = (pl.seg_max > 1 && !splitk_inkernel()) ? 1 : 0;
+  if (op.x) {
+    // single kernel: quantize x into the token tiles, grid barrier, GEMM
+    p.x = static_cast<const uint16_t *>(op.x);
+    p.ldx = op.ldx;
+    p.fuse_quant = 1;
+  }
+  ReduceMode mode = reduce_mode();
+  if (opts && opts->splitk_reduce == MXG_REDUCE_KERNEL) mode = ReduceMode::kKernel;
+  if (opts && opts->splitk_reduce == MXG_REDUCE_GRID) mode = ReduceMode::kGrid;
+  if (opts && opts->splitk_reduce == MXG_REDUCE_LAST_CTA) mode = ReduceMode::kLastCta;
+  if (op.x) mode = ReduceMode::kGrid;
+  p.grid_reduce = (pl.seg_max > 1 && mode == ReduceMode::kGrid) ? 1 : 0;
+  p.defer_reduce = (pl.seg_max > 1 && mode == ReduceMode::kKernel) ? 1 : 0;
+  if (p.fuse_quant || p.grid_reduce) {
+    if (!ws) return MXG_ERR_WORKSPACE;
+    p.gbar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + kGridBarrierOff);
+  }
   cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
   if (e == cudaSuccess && p.defer_reduce)
     e = mxg::launch_splitk_reduce(kind, pl.bn, p, pl.ctas, sm_count, stream);
@@ -272,6 +307,8 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
   if (!aligned16(y) || ((size_t)ldy * (od == MXG_OUT_F32 ? 4 : 2)) % 16 != 0)
     return MXG_ERR_MISALIGNED;
   if (opts && (opts->variant < 0 || opts->variant > 2 || opts->ctas < 0))
+    return MXG_ERR_INVALID_ARG;
+  if (opts && (opts->splitk_reduce < MXG_REDUCE_DEFAULT || opts->splitk_reduce > MXG_REDUCE_LAST_CTA))
     return MXG_ERR_INVALID_ARG;
   if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
     return MXG_ERR_INVALID_ARG;
@@ -430,13 +467,20 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
       return MXG_ERR_WORKSPACE;
     uint8_t *codes = ws + kCounterBytes;
     uint8_t *sf = codes + align256(act_code_bytes(M, (size_t)K / 2, act_tile_rows));
-    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s);
-    if (e != cudaSuccess) return MXG_ERR_CUDA;
     a_codes = codes;
     a_sf = sf;
     part_off += need;
+    if (pl.variant == MXG_VARIANT_SPLITK && act_tile_rows && opts &&
+        opts->splitk_reduce == MXG_REDUCE_GRID) {
+      // one kernel: its CTAs quantize x into the token tiles themselves
+      GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr, x_bf16, ldx};
+      return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off,
+                      act_tile_rows, sm, s);
+    }
+    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s);
+    if (e != cudaSuccess) return MXG_ERR_CUDA;
   }
-  GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
+  GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr, nullptr, 0};
   return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, act_tile_rows,
                   sm, s);
 }
@@ -452,7 +496,7 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, 
     return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  GemmOperands op{qa, nullptr, qw, nullptr, sa, sw};
+  GemmOperands op{qa, nullptr, qw, nullptr, sa, sw, nullptr, 0};
   return run_gemm(1, op, M, N, K, y, ldy, out_dtype, opts, opts ? opts->workspace : nullptr,
                   opts ? opts->ws_bytes : 0, kCounterBytes, opts ? opts->act_tile_rows : 0, sm,
                   reinterpret_cast<cudaStream_t>(stream));

@@ -28,6 +28,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace mxg {
 namespace {
@@ -44,20 +45,27 @@ constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, BN)
 constexpr uint32_t kSfCol = 256;
 constexpr int kSmemBudget = 220 * 1024;
 
-template <int KIND, int BN>
+// KS: 128-byte K columns per pipeline stage (one column = 256 E2M1 or 128
+// E4M3 values of every row).  Two columns per stage halve the number of bulk
+// copies per byte, which is what bounds the weight-streaming (split-K) rate.
+template <int KIND, int BN, int KS>
 struct Cfg {
   static constexpr int kSfBlocksB = BN >= 128 ? BN / 128 : 1;
-  static constexpr int kABytes = kTileA * kRowBytes;
-  static constexpr int kBBytes = BN * kRowBytes;
-  static constexpr int kSfaBytes = KIND == 0 ? 1024 : 0;
-  static constexpr int kSfbBytes = KIND == 0 ? 1024 * kSfBlocksB : 0;
+  static constexpr int kAColBytes = kTileA * kRowBytes;  // one column of the A operand
+  static constexpr int kBColBytes = BN * kRowBytes;
+  static constexpr int kABytes = kAColBytes * KS;
+  static constexpr int kBBytes = kBColBytes * KS;
+  static constexpr int kSfaBytes = KIND == 0 ? 1024 * KS : 0;  // 2 scale atoms per column
+  static constexpr int kSfbBytes = KIND == 0 ? 1024 * KS * kSfBlocksB : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 6) + 16;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 7) + 16;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
   static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
-  static constexpr uint32_t kSfColsPerStage = 8u + 8u * (uint32_t)kSfBlocksB;
+  static constexpr int kSteps = 4 * KS;              // MMAs (K = 64 / 32) per stage
+  static constexpr uint32_t kSfColsA = 8u * KS;      // 4 TMEM columns per scale atom
+  static constexpr uint32_t kSfColsPerStage = kSfColsA + 8u * KS * (uint32_t)kSfBlocksB;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(KIND != 0 || kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
@@ -232,11 +240,152 @@ __device__ __forceinline__ void reduce_partials(const GemmParams &p, const float
   }
 }
 
-template <int KIND, int BN>
-__global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small kernels beside it
+// Split-K reduction: for every tile that more than one CTA touched, y = sum
+// of the partial slots in slot order (fixed order: deterministic), then the
+// PTPC scales, then bf16 (or fp32).  One thread per float4 group of a slot
+// ([column][128 rows]), kRedJ groups per thread with all their loads issued
+// before the first sum (one round of L2 latency); threads first, first +
+// stride, ... so that every SM pulls a share.
+constexpr int kRedThreads = 128;
+constexpr int kRedJ = 2;
+
+template <int KIND>
+__device__ __forceinline__ void reduce_share(const GemmParams &p, int bn, unsigned gemm_ctas,
+                                             int first, int stride) {
+  const unsigned U = (unsigned)p.units, KB = (unsigned)p.kblocks;
+  const int per_col = kTileA / 4;
+  const int per_tile = bn * per_col;
+  const int total = p.tilesA * p.tilesB * per_tile;
+  const size_t slot4 = (size_t)bn * kTileA / 4;
+  for (int e0 = first; e0 < total; e0 += stride * kRedJ) {
+    int nseg[kRedJ];
+    const float4 *src[kRedJ];
+    float4 v[kRedJ][4];
+#pragma unroll
+    for (int j = 0; j < kRedJ; ++j) {
+      const int e = e0 + j * stride;
+      nseg[j] = 0;
+      src[j] = nullptr;
+      if (e < total) {
+        const int t = e / per_tile;
+        const int g = e - t * per_tile;
+        const unsigned first_u = (unsigned)t * KB;
+        const unsigned o0 = owner_of(first_u, U, gemm_ctas);
+        const int ns = (int)(owner_of(first_u + KB - 1, U, gemm_ctas) - o0 + 1);
+        const int tb = t - (t / p.tilesB) * p.tilesB;
+        const int c = g / per_col;
+        // one CTA owned the whole tile and wrote y itself; padding columns
+        if (ns > 1 && c < min(bn, p.rowsB - tb * bn)) {
+          nseg[j] = ns;
+          src[j] = reinterpret_cast<const float4 *>(p.ws) + (size_t)t * p.seg_max * slot4 + g;
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        v[j][s] = s < nseg[j] ? __ldcg(src[j] + s * slot4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < kRedJ; ++j) {
+      if (nseg[j] == 0) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        acc.x += v[j][s].x;
+        acc.y += v[j][s].y;
+        acc.z += v[j][s].z;
+        acc.w += v[j][s].w;
+      }
+      for (int s = 4; s < nseg[j]; ++s) {
+        const float4 w = __ldcg(src[j] + s * slot4);
+        acc.x += w.x;
+        acc.y += w.y;
+        acc.z += w.z;
+        acc.w += w.w;
+      }
+      const int e = e0 + j * stride;
+      const int t = e / per_tile;
+      const int g = e - t * per_tile;
+      const int ta = t / p.tilesB, tb = t - ta * p.tilesB;
+      const int c = g / per_col, r = (g - c * per_col) * 4;
+      const int m = tb * bn + c;      // token
+      const int n = ta * kTileA + r;  // output channel
+      float f[4] = {acc.x, acc.y, acc.z, acc.w};
+      if (KIND == 1) {
+        const float sa = p.tok_scale[m];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f[q] = (f[q] * sa) * p.chan_scale[n + q];
+      }
+      if (p.out_f32)
+        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
+            make_float4(f[0], f[1], f[2], f[3]);
+      else
+        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
+            make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+    }
+  }
+}
+
+// Fused activation phase (A4W4 split-K): the M x K/128 units (one row, 128
+// values = 16 chunks of 8) are cut evenly over the CTAs; 128 threads = 8
+// half-warps take one unit each per round, two rounds' loads in flight.
+// Codes go to the token tiles (T = BN rows, 128-byte columns), scales to the
+// 128x4-tile layout; padding rows stay unwritten (their columns of the
+// accumulator are never stored).  Every lane of a warp runs every round:
+// the block amax is a 4-lane shuffle.
+__device__ __forceinline__ void quant_share(const GemmParams &p, int T, int tid) {
+  const int upr = p.K >> 7;
+  const long long W = (long long)p.M * upr;
+  const long long u0 = (long long)blockIdx.x * W / gridDim.x;
+  const long long u1 = (long long)(blockIdx.x + 1) * W / gridDim.x;
+  const int hw = tid >> 4, hl = tid & 15;
+  const int kc = p.K >> 8;  // 128-byte code columns per row
+  const int G = p.K >> 5;   // MX blocks per row
+  uint8_t *codes = const_cast<uint8_t *>(p.b_tiles);
+  uint8_t *sf = const_cast<uint8_t *>(p.sfB);
+  for (long long base = u0; base < u1; base += 16) {
+    uint4 v[2];
+    int r[2], ch[2];
+    bool ok[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const long long u = base + hw + 8 * j;
+      ok[j] = u < u1;
+      r[j] = ok[j] ? (int)(u / upr) : 0;
+      ch[j] = ok[j] ? (int)(u - (long long)r[j] * upr) * 16 + hl : 0;
+      v[j] = ok[j] ? ld_stream_v4(p.x + (size_t)r[j] * p.ldx + (size_t)ch[j] * 8)
+                   : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t scode;
+      const uint32_t packed = mx_encode_chunk(v[j], scode);
+      if (ok[j]) *reinterpret_cast<uint32_t *>(codes + tiled_offset(r[j], ch[j] * 4, kc, T)) = packed;
+      const uint32_t word = mx_scale_word(scode);
+      if (ok[j] && hl == 0)
+        *reinterpret_cast<uint32_t *>(sf + sf_swizzled_offset(r[j], ch[j] >> 2, G)) = word;
+    }
+  }
+}
+
+// L2 prefetch of this CTA's share of x (contiguous runs within a row).
+__device__ __forceinline__ void prefetch_x_share(const GemmParams &p) {
+  const int upr = p.K >> 7;
+  const long long W = (long long)p.M * upr;
+  long long u = (long long)blockIdx.x * W / gridDim.x;
+  const long long u1 = (long long)(blockIdx.x + 1) * W / gridDim.x;
+  while (u < u1) {
+    const long long r = u / upr;
+    const long long hi = min(u1, (r + 1) * upr);
+    prefetch_l2_bulk(p.x + (size_t)r * p.ldx + (size_t)(u - r * upr) * 128, (uint32_t)(hi - u) * 256u);
+    u = hi;
+  }
+}
+
+template <int KIND, int BN, int KS>
+__global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small kernels beside it
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmParams p) {
-  using C = Cfg<KIND, BN>;
+  using C = Cfg<KIND, BN, KS>;
   constexpr int S = C::kStages;
   constexpr int CH = C::kChunk;
 
@@ -254,10 +403,12 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
   const uint32_t dec_bar = acc_full + 24;
   const uint32_t stall_bar = acc_full + 32;
   const uint32_t mma_done = acc_full + 40;
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (2 * S + 6);
+  const uint32_t acts_ready = acc_full + 48;  // fused path: token tiles of every CTA written
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (2 * S + 7);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
+  volatile int *reduce_go = reinterpret_cast<volatile int *>(misc + 12);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
 
@@ -283,8 +434,10 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
     mbar_init(dec_bar, 1);
     mbar_init(stall_bar, 1);
     mbar_init(mma_done, 1);
+    mbar_init(acts_ready, 1);
     *abort_flag = 0;
     *decision = 0;
+    *reduce_go = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -309,50 +462,64 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
       const uint64_t pol_keep = policy_evict_last();
       const uint64_t polA = p.swap ? pol_stream : pol_keep;  // swapped: A = weights, read once
       const uint64_t polB = pol_keep;
+      // Stage kb covers the 128-byte K columns [kb*KS, kb*KS + ncol(kb)).
+      auto ncol_of = [&](int kb) { return min(KS, p.kc_per_row - kb * KS); };
+      // A4W4 scale atoms (512 bytes: 128 rows x 4 blocks of 32) of stage kb
+      auto natoms_of = [&](int kb) { return min(2 * KS, p.G4 - 2 * KS * kb); };
       // the operand and scale bytes one stage receives
       auto stage_bytes = [&](const Item &it, int kb) {
-        uint32_t bytes = C::kABytes + C::kBBytes;
+        uint32_t bytes = (uint32_t)ncol_of(kb) * (C::kAColBytes + C::kBColBytes);
         if (KIND == 0) {
-          const int natoms = min(2, p.G4 - 2 * kb);
           const int rb0 = (it.tb * BN) / 128;
           const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-          bytes += (uint32_t)(natoms * 512 * (1 + nblk));
+          bytes += (uint32_t)(natoms_of(kb) * 512 * (1 + nblk));
         }
         return bytes;
       };
-      // A weight tile (128 rows x 128 bytes) is one contiguous 16 KiB bulk copy;
-      // row-major operands go through the tensor map (128-byte swizzle box)
+      // Operands in the tile layout: the columns of one stage are adjacent
+      // (tile (row tile, column) at (row tile * KC + column) * tile bytes), so
+      // a stage of a 128-row A tile or of a BN-row token tile is one bulk copy.
+      // Row-major operands go through the tensor map (128-byte swizzle box per
+      // column).
       auto issue_a = [&](int stage, const Item &it, int kb, uint32_t fb) {
+        const int nc = ncol_of(kb);
         if (p.a_tiles)
           bulk_load(sA + stage * C::kABytes,
-                    p.a_tiles + ((size_t)it.ta * p.kc_per_row + kb) * (size_t)C::kABytes,
-                    C::kABytes, fb, polA);
+                    p.a_tiles + ((size_t)it.ta * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kAColBytes,
+                    (uint32_t)nc * C::kAColBytes, fb, polA);
         else
-          tma_load_2d(sA + stage * C::kABytes, &tmA, kb * kRowBytes, it.ta * kTileA, fb, polA);
+          for (int j = 0; j < nc; ++j)
+            tma_load_2d(sA + stage * C::kABytes + j * C::kAColBytes, &tmA, (kb * KS + j) * kRowBytes,
+                        it.ta * kTileA, fb, polA);
         if (KIND == 0)
-          bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * kb) * 512u,
-                    min(2, p.G4 - 2 * kb) * 512, fb, polA);
+          bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
+                    natoms_of(kb) * 512, fb, polA);
       };
       auto issue_b = [&](int stage, const Item &it, int kb, uint32_t fb) {
-        if (p.b_tiles && p.b_tile_rows == BN) {  // one tile of BN rows (activations)
+        const int nc = ncol_of(kb);
+        if (p.b_tiles && p.b_tile_rows == BN) {  // token tiles of BN rows
           bulk_load(sB + stage * C::kBBytes,
-                    p.b_tiles + ((size_t)it.tb * p.kc_per_row + kb) * (size_t)C::kBBytes,
-                    C::kBBytes, fb, polB);
-        } else if (p.b_tiles) {  // 128-row weight tiles, BN / 128 of them
-          for (int j = 0; j < BN / 128; ++j)
-            bulk_load(sB + stage * C::kBBytes + j * 16384,
-                      p.b_tiles + ((size_t)(it.tb * (BN / 128) + j) * p.kc_per_row + kb) * 16384u,
-                      16384, fb, polB);
+                    p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kBColBytes,
+                    (uint32_t)nc * C::kBColBytes, fb, polB);
+        } else if (p.b_tiles) {  // 128-row weight tiles, BN / 128 of them per column
+          for (int j = 0; j < nc; ++j)
+            for (int r = 0; r < BN / 128; ++r)
+              bulk_load(sB + stage * C::kBBytes + j * C::kBColBytes + r * 16384,
+                        p.b_tiles + ((size_t)(it.tb * (BN / 128) + r) * p.kc_per_row +
+                                     (size_t)kb * KS + j) * 16384u,
+                        16384, fb, polB);
         } else {
-          tma_load_2d(sB + stage * C::kBBytes, &tmB, kb * kRowBytes, it.tb * BN, fb, polB);
+          for (int j = 0; j < nc; ++j)
+            tma_load_2d(sB + stage * C::kBBytes + j * C::kBColBytes, &tmB, (kb * KS + j) * kRowBytes,
+                        it.tb * BN, fb, polB);
         }
         if (KIND == 0) {
-          const int natoms = min(2, p.G4 - 2 * kb);
+          const int natoms = natoms_of(kb);
           const int rb0 = (it.tb * BN) / 128;
           const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
           for (int j = 0; j < nblk; ++j)
-            bulk_load(sSFB + stage * C::kSfbBytes + j * 1024,
-                      p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * kb) * 512u, natoms * 512, fb, polB);
+            bulk_load(sSFB + stage * C::kSfbBytes + j * (1024 * KS),
+                      p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * KS * kb) * 512u, natoms * 512, fb, polB);
         }
       };
       // Weights that the previous kernel did not write may stream in before
@@ -376,12 +543,33 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
       }
       pdl_wait();
       trace_mark(p, kTrWaited);
+      bool ok = true;
+      if (p.fuse_quant) {
+        // the token tiles are written by every CTA of this grid; the epilogue
+        // warps signal once the grid barrier after that phase has passed
+        ok = mbar_wait(acts_ready, 0, ctl) && !*abort_flag;
+        fence_proxy_async_global();
+      }
       uint32_t cur = first_cursor(p);
       Item it;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      bool ok = true;
+      if (!ok && pre > 0) {
+        // give the stages armed before the wait their other operand (in
+        // bounds, contents irrelevant) so that they complete and drain
+        uint32_t c2 = first_cursor(p);
+        Item it2;
+        int k = 0;
+        while (k < pre && next_item(p, c2, it2))
+          for (int kb = it2.kb0; kb < it2.kb1 && k < pre; ++kb, ++k) {
+            if (w_is_a)
+              issue_b(k, it2, kb, full_bar(k));
+            else
+              issue_a(k, it2, kb, full_bar(k));
+          }
+        issued = pre;
+      }
       while (ok && next_item(p, cur, it)) {
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
           const uint32_t fb = full_bar(stage);
@@ -446,31 +634,36 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
           tc_fence_after();
           const uint32_t a0 = sA + stage * C::kABytes;
           const uint32_t b0 = sB + stage * C::kBBytes;
+          // K step s of the stage: column s / 4, 32 bytes per step within it
+          auto a_desc = [&](int s) {
+            return sdesc_kmajor_sw128(a0 + (uint32_t)(s >> 2) * C::kAColBytes + 32u * (s & 3));
+          };
+          auto b_desc = [&](int s) {
+            return sdesc_kmajor_sw128(b0 + (uint32_t)(s >> 2) * C::kBColBytes + 32u * (s & 3));
+          };
           if (KIND == 0) {
-            const int natoms = min(2, p.G4 - 2 * kb);
+            const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
             const int rb0 = (it.tb * BN) / 128;
             const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
             const uint32_t sfa_t = tmem + kSfCol + (uint32_t)stage * C::kSfColsPerStage;
-            const uint32_t sfb_t = sfa_t + 8u;
+            const uint32_t sfb_t = sfa_t + C::kSfColsA;
             for (int a = 0; a < natoms; ++a)
               tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
             for (int j = 0; j < nblk; ++j)
               for (int a = 0; a < natoms; ++a)
                 tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
-                         sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * 1024 + a * 512));
-            const int nk = min(4, (p.K - kb * 256) / 64);
+                         sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * (1024 * KS) + a * 512));
+            const int nk = min(C::kSteps, (p.K - kb * 256 * KS) / 64);
             for (int s = 0; s < nk; ++s) {
               const uint32_t sel = (uint32_t)(s & 1) * 2u;
-              mma_mxf4(tmem + kAccCol, sdesc_kmajor_sw128(a0 + 32 * s),
-                       sdesc_kmajor_sw128(b0 + 32 * s), idesc_sf_ids(idesc0, sel, sel),
+              mma_mxf4(tmem + kAccCol, a_desc(s), b_desc(s), idesc_sf_ids(idesc0, sel, sel),
                        sfa_t + 4 * (s >> 1), sfb_t + 4 * C::kSfBlocksB * (s >> 1),
                        (kb > it.kb0 || s > 0) ? 1u : 0u);
             }
           } else {
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-              mma_f8(tmem + kAccCol, sdesc_kmajor_sw128(a0 + 32 * s),
-                     sdesc_kmajor_sw128(b0 + 32 * s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
+            const int nk = min(C::kSteps, (p.K - kb * 128 * KS) / 32);
+            for (int s = 0; s < nk; ++s)
+              mma_f8(tmem + kAccCol, a_desc(s), b_desc(s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
           }
           tc_commit(empty_bar(stage));
           if (++stage == S) {
@@ -492,7 +685,21 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r_in = q * 32 + lane;    // row of the MMA-A tile
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + kAccCol;
-    pdl_wait();  // scales, counters and partial tiles may come from the previous kernel
+    if (p.fuse_quant && threadIdx.x == 64) prefetch_x_share(p);  // L2 only: safe before the wait
+    pdl_wait();  // x, scales, counters and partial tiles may come from the previous kernel
+    if (p.fuse_quant) {
+      quant_share(p, BN, threadIdx.x - 64);
+      fence_proxy_async_global();  // these generic stores are read by other CTAs' bulk copies
+      named_barrier(1, 128);
+      if (threadIdx.x == 64) {
+        trace_mark(p, kTrQuantDone);
+        grid_barrier(p.gbar, p.gbar + 32, gridDim.x, ctl);  // raises the abort flag on failure
+        trace_mark(p, kTrPartStored);  // (fused path: the first grid barrier passed)
+        fence_proxy_async_global();
+        mbar_arrive(acts_ready);
+      }
+      __syncwarp();
+    }
     uint32_t cur = first_cursor(p);
     Item it;
     int i = 0;
@@ -594,12 +801,14 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
             }
           }
         }
-      } else if (p.defer_reduce) {
+      } else if (p.defer_reduce || p.grid_reduce) {
         // swapped, part of K: publish this CTA's fp32 partial tile into its
-        // slot; the split-K reduce kernel that follows sums the slots
+        // slot; the split-K reduce kernel that follows (or every CTA of this
+        // grid, after a grid barrier) sums the slots
         publish_partial();
         release_acc();  // the MMA may start the next item during the hand-off
-        if (threadIdx.x == 64 && p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
+        if (threadIdx.x == 64 && !p.fuse_quant && p.trace &&
+            p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
           trace_mark(p, kTrPartStored);
       } else if (!whole) {
         // (in-kernel variant) the last CTA of the tile reduces the partials
@@ -646,6 +855,19 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
       trace_mark(p, kTrEpiDone);
       trace_set(p, kTrItems, (unsigned long long)i);
     }
+    if (p.grid_reduce) {
+      // every CTA's partial slots are stored: sum a share of all of them
+      named_barrier(1, 128);
+      if (threadIdx.x == 64) {
+        *reduce_go = (!*abort_flag && grid_barrier(p.gbar + 64, p.gbar + 96, gridDim.x, ctl)) ? 1 : 0;
+        trace_mark(p, kTrDecision);
+      }
+      named_barrier(1, 128);
+      if (*reduce_go) {
+        reduce_share<KIND>(p, BN, gridDim.x, blockIdx.x * 128 + (threadIdx.x - 64), gridDim.x * 128);
+        if (threadIdx.x == 64) trace_mark(p, kTrReduced);
+      }
+    }
   }
 
   tc_fence_before();
@@ -660,114 +882,83 @@ __global__ void __maxnreg__(128)  // 24K registers a CTA: room for the small ker
   }
 }
 
-// Split-K reduction for the deferred variant: for every tile that more than
-// one CTA touched, y = sum of the partial slots in slot order (fixed order:
-// deterministic), then the PTPC scales, then bf16 (or fp32).  One thread per
-// float4 group of a slot ([column][128 rows]), grid-strided over all tiles, so
-// the ~nseg x 32 KB per tile is read by every SM instead of by one CTA.
+// The split-K reduction as its own kernel, launched right after the GEMM.
 template <int KIND>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const GemmParams p, int bn,
-                                                            unsigned gemm_ctas) {
+__global__ void __launch_bounds__(kRedThreads) splitk_reduce_kernel(const GemmParams p, int bn,
+                                                                    unsigned gemm_ctas) {
   pdl_trigger();  // touches nothing before the wait below
   pdl_wait();     // the GEMM that wrote the partial slots has completed
-  const unsigned U = (unsigned)p.units, KB = (unsigned)p.kblocks;
-  const int per_col = kTileA / 4;
-  const int per_tile = bn * per_col;
-  const int total = p.tilesA * p.tilesB * per_tile;
-  const size_t slot4 = (size_t)bn * kTileA / 4;
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
-    const int t = e / per_tile;
-    const int g = e - t * per_tile;
-    const unsigned first = (unsigned)t * KB;
-    const unsigned o0 = owner_of(first, U, gemm_ctas);
-    const int nseg = (int)(owner_of(first + KB - 1, U, gemm_ctas) - o0 + 1);
-    if (nseg == 1) continue;  // one CTA owned the whole tile and wrote y itself
-    const int ta = t / p.tilesB, tb = t - (t / p.tilesB) * p.tilesB;
-    const int c = g / per_col, r = (g - c * per_col) * 4;
-    if (c >= min(bn, p.rowsB - tb * bn)) continue;
-    const float4 *src = reinterpret_cast<const float4 *>(p.ws) + (size_t)t * p.seg_max * slot4 + g;
-    float4 v[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) v[s] = s < nseg ? __ldcg(src + s * slot4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      acc.x += v[s].x;
-      acc.y += v[s].y;
-      acc.z += v[s].z;
-      acc.w += v[s].w;
-    }
-    for (int s = 4; s < nseg; ++s) {
-      const float4 w = __ldcg(src + s * slot4);
-      acc.x += w.x;
-      acc.y += w.y;
-      acc.z += w.z;
-      acc.w += w.w;
-    }
-    const int m = tb * bn + c;      // token
-    const int n = ta * kTileA + r;  // output channel
-    float f[4] = {acc.x, acc.y, acc.z, acc.w};
-    if (KIND == 1) {
-      const float sa = p.tok_scale[m];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
-    }
-    if (p.out_f32)
-      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
-          make_float4(f[0], f[1], f[2], f[3]);
-    else
-      *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
-          make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-  }
+  reduce_share<KIND>(p, bn, gemm_ctas, blockIdx.x * kRedThreads + threadIdx.x,
+                     gridDim.x * kRedThreads);
 }
 
-template <int KIND, int BN>
+template <int KIND, int BN, int KS>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p, int ctas,
                      cudaStream_t stream) {
-  using C = Cfg<KIND, BN>;
-  auto kern = gemm_kernel<KIND, BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C::kSmem);
+  using C = Cfg<KIND, BN, KS>;
+  auto kern = gemm_kernel<KIND, BN, KS>;
+  static DeviceOnce once;  // per instantiation and device (a repeat sets the same value)
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (!once.done(dev)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    once.set(dev);
+  }
   cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attach_pdl(cfg, attr);
+  if (p.fuse_quant || p.grid_reduce) {
+    // grid barriers: every CTA must be resident at once, also when other
+    // streams run kernels of their own (a cooperative launch guarantees it)
+    if (cooperative_enabled()) {
+      attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+      attr[cfg.numAttrs].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs += 1;
+    }
+  }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
 }
 
+// Full-tile kernels (BN = 256) take one K column per stage; split-K kernels two.
 template <int KIND>
 cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const GemmParams &p, int ctas, cudaStream_t stream) {
+  if (!p.splitk) return bn == 256 ? launch_t<KIND, 256, 1>(tmA, tmB, p, ctas, stream) : cudaErrorInvalidValue;
   switch (bn) {
-    case 16: return launch_t<KIND, 16>(tmA, tmB, p, ctas, stream);
-    case 32: return launch_t<KIND, 32>(tmA, tmB, p, ctas, stream);
-    case 64: return launch_t<KIND, 64>(tmA, tmB, p, ctas, stream);
-    case 128: return launch_t<KIND, 128>(tmA, tmB, p, ctas, stream);
-    case 256: return launch_t<KIND, 256>(tmA, tmB, p, ctas, stream);
+    case 16: return launch_t<KIND, 16, 2>(tmA, tmB, p, ctas, stream);
+    case 32: return launch_t<KIND, 32, 2>(tmA, tmB, p, ctas, stream);
+    case 64: return launch_t<KIND, 64, 2>(tmA, tmB, p, ctas, stream);
+    case 128: return launch_t<KIND, 128, 2>(tmA, tmB, p, ctas, stream);
+    case 256: return launch_t<KIND, 256, 2>(tmA, tmB, p, ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int KIND>
-int stages_kind(int bn) {
+int stages_kind(int bn, bool splitk) {
+  if (!splitk) return bn == 256 ? Cfg<KIND, 256, 1>::kStages : 0;
   switch (bn) {
-    case 16: return Cfg<KIND, 16>::kStages;
-    case 32: return Cfg<KIND, 32>::kStages;
-    case 64: return Cfg<KIND, 64>::kStages;
-    case 128: return Cfg<KIND, 128>::kStages;
-    case 256: return Cfg<KIND, 256>::kStages;
+    case 16: return Cfg<KIND, 16, 2>::kStages;
+    case 32: return Cfg<KIND, 32, 2>::kStages;
+    case 64: return Cfg<KIND, 64, 2>::kStages;
+    case 128: return Cfg<KIND, 128, 2>::kStages;
+    case 256: return Cfg<KIND, 256, 2>::kStages;
     default: return 0;
   }
 }
 
 template <int KIND>
-size_t smem_kind(int bn) {
+size_t smem_kind(int bn, bool splitk) {
+  if (!splitk) return bn == 256 ? Cfg<KIND, 256, 1>::kSmem : 0;
   switch (bn) {
-    case 16: return Cfg<KIND, 16>::kSmem;
-    case 32: return Cfg<KIND, 32>::kSmem;
-    case 64: return Cfg<KIND, 64>::kSmem;
-    case 128: return Cfg<KIND, 128>::kSmem;
-    case 256: return Cfg<KIND, 256>::kSmem;
+    case 16: return Cfg<KIND, 16, 2>::kSmem;
+    case 32: return Cfg<KIND, 32, 2>::kSmem;
+    case 64: return Cfg<KIND, 64, 2>::kSmem;
+    case 128: return Cfg<KIND, 128, 2>::kSmem;
+    case 256: return Cfg<KIND, 256, 2>::kSmem;
     default: return 0;
   }
 }
@@ -777,16 +968,18 @@ size_t smem_kind(int bn) {
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream) {
   const long long total = (long long)p.tilesA * p.tilesB * bn * (kTileA / 4);
-  long long blocks = (total + 255) / 256;
-  // one CTA per SM: launched early (programmatic launch), the reduce CTAs sit
-  // beside the GEMM CTAs, and the next GEMM's CTAs must still fit beside
-  // them and the next quantizer's (registers: 24K + 8K + 8-12K of 64K)
-  const long long cap = (long long)(sm_count > 0 ? sm_count : 152);
+  long long blocks = (total + kRedThreads * kRedJ - 1) / (kRedThreads * kRedJ);
+  // launched early (programmatic launch), every reduce CTA must fit beside a
+  // resident GEMM CTA: 3 small CTAs per SM at most
+  const long long cap = (long long)(sm_count > 0 ? sm_count : 152) * 3;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(256), 0, stream);
+  cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(kRedThreads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
+  cudaError_t e = kind == 0 ? prefer_shared_carveout(splitk_reduce_kernel<0>)
+                            : prefer_shared_carveout(splitk_reduce_kernel<1>);
+  if (e != cudaSuccess) return e;
   if (kind == 0) return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<0>, p, bn, (unsigned)gemm_ctas);
   return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<1>, p, bn, (unsigned)gemm_ctas);
 }
@@ -797,10 +990,14 @@ cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensor
                    : launch_kind<1>(bn, tmA, tmB, p, ctas, stream);
 }
 
-int gemm_stages(int kind, int bn) { return kind == 0 ? stages_kind<0>(bn) : stages_kind<1>(bn); }
-
-size_t gemm_smem_bytes(int kind, int bn) {
-  return kind == 0 ? smem_kind<0>(bn) : smem_kind<1>(bn);
+int gemm_stages(int kind, int bn, bool splitk) {
+  return kind == 0 ? stages_kind<0>(bn, splitk) : stages_kind<1>(bn, splitk);
 }
+
+size_t gemm_smem_bytes(int kind, int bn, bool splitk) {
+  return kind == 0 ? smem_kind<0>(bn, splitk) : smem_kind<1>(bn, splitk);
+}
+
+int gemm_cols_per_stage(bool splitk) { return splitk ? 2 : 1; }
 
 }  // namespace mxg

@@ -28,12 +28,49 @@ inline bool pdl_enabled() {
   }();
   return on;
 }
-inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[1]) {
+template <int N>
+inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[N]) {
   if (!pdl_enabled()) return;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+}
+// MXG_NO_COOPERATIVE=1 launches the grid-synchronised GEMM without the
+// cooperative attribute (for A/B timing; co-residency is then only likely).
+inline bool cooperative_enabled() {
+  static const bool on = [] {
+    const char *e = std::getenv("MXG_NO_COOPERATIVE");
+    return !(e && e[0] == '1');
+  }();
+  return on;
+}
+
+// Small kernels (quantizers, split-K reduce) run beside, and just before,
+// GEMM CTAs that need ~210 KB of shared memory.  An SM whose L1/shared split
+// was set for an L1-preferring kernel cannot take a GEMM CTA until it drains,
+// so these kernels ask for the maximum shared-memory carveout (set once per
+// kernel; a repeated or concurrent call sets the same value).
+// A per-device "already done" bit set (devices 0..63; beyond that, always redo).
+struct DeviceOnce {
+  unsigned long long bits = 0;
+  bool done(int dev) const { return dev >= 0 && dev < 64 && ((bits >> dev) & 1ull); }
+  void set(int dev) {
+    if (dev >= 0 && dev < 64) __atomic_fetch_or(&bits, 1ull << dev, __ATOMIC_RELAXED);
+  }
+};
+
+template <class Kernel>
+inline cudaError_t prefer_shared_carveout(Kernel *kern) {
+  static DeviceOnce once;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (once.done(dev)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) once.set(dev);
+  return e;
 }
 
 // tile_rows: 0 = row-major codes / bytes, else the tile layout with tiles of
@@ -61,7 +98,7 @@ struct GemmParams {
   int swap;            // 1: MMA-A = weight rows (N), MMA-B = token rows (M)
   int rowsA, rowsB;    // rows of the MMA-A / MMA-B operand
   int tilesA, tilesB;  // ceil(rowsA / 128), ceil(rowsB / BN)
-  int kblocks;         // K-blocks per tile (one pipeline stage each)
+  int kblocks;         // pipeline stages along K per tile (gemm_cols_per_stage columns each)
   int G4;              // K / 128: 512-byte scale tiles per 128-row block
   int splitk;          // 1: stream-K over (tile, K-block) units
   long long units;     // tilesA * tilesB * kblocks
@@ -80,6 +117,16 @@ struct GemmParams {
                            //          the last CTA of each tile
   int early_w;         // 1: no kernel still in flight writes the weights, so their first
                        //    stages may load before griddepcontrol.wait
+  // Single-kernel split-K (swap) path: the CTAs first quantize the bf16
+  // activations x into the token tiles (b_tiles, T = BN rows) and their
+  // 128x4-tile scales (sfB), then a grid barrier, then the GEMM; partial
+  // tiles are summed after a second grid barrier by all CTAs (grid_reduce).
+  const uint16_t *x;
+  long long ldx;
+  int fuse_quant;
+  int grid_reduce;
+  unsigned *gbar;      // grid barrier words: [0] / [32] count / generation of barrier 1,
+                       //   [64] / [96] of barrier 2 (zero-initialised, 128 bytes apart)
 };
 
 // Timeline trace points (index into a CTA's 16 slots): SM clock64 values.
@@ -87,7 +134,8 @@ enum TracePoint {
   kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrLastLoad = 3, kTrFirstFull = 4,
   kTrLastCommit = 5, kTrAcc0 = 6, kTrItem0Done = 7, kTrAcc1 = 8, kTrItem1Done = 9,
   kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12, kTrDecision = 13, kTrReduced = 14,
-  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18, kTracePoints = 20
+  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18, kTrQuantDone = 19,
+  kTracePoints = 20  // fused path: kTrDecision = second grid barrier passed
 };
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.
@@ -99,8 +147,11 @@ cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensor
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream);
 
-// Pipeline stages a (kind, bn) kernel uses, and its dynamic shared memory.
-int gemm_stages(int kind, int bn);
-size_t gemm_smem_bytes(int kind, int bn);
+// Pipeline stages a (kind, bn, variant) kernel uses, its dynamic shared
+// memory, and the 128-byte K columns one stage covers (p.kblocks counts
+// stages of that many columns).
+int gemm_stages(int kind, int bn, bool splitk);
+size_t gemm_smem_bytes(int kind, int bn, bool splitk);
+int gemm_cols_per_stage(bool splitk);
 
 }  // namespace mxg

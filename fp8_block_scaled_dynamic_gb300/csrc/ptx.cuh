@@ -74,6 +74,55 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// ---------------------------------------------------------------- grid barrier
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (bulk copy / TMA) ones: the writer side and the reader side of data that
+// one CTA stores with st.global and another loads with cp.async.bulk.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Barrier of all G CTAs of a launch, taken by one thread per CTA once the
+// CTA's own writes are ordered before it (bar.sync among the writers).
+// `cnt` and `gen` are zero-initialised words of the caller's workspace;
+// completed barriers leave `cnt` at zero, `gen` only ever advances.  Every
+// CTA must be resident at the same time (the persistent grid is at most one
+// CTA per SM); the wait is bounded like every other one.
+__device__ __forceinline__ bool grid_barrier(unsigned *cnt, unsigned *gen, unsigned G,
+                                             const WaitCtl &ctl) {
+  // The generation cannot move before this CTA has arrived.
+  const unsigned g0 = ld_acquire_gpu(gen);
+  __threadfence();
+  const unsigned old = atomicAdd(cnt, 1u);
+  if (old == G - 1) {  // last to arrive: reset the count, open the barrier
+    atomicExch(cnt, 0u);
+    __threadfence();
+    atomicAdd(gen, 1u);
+    return true;
+  }
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire_gpu(gen) == g0) {
+    __nanosleep(32);  // fewer polls of the line the arrivals update
+    if (*ctl.abort_flag) return false;
+    if (global_timer_ns() - t0 > ctl.timeout_ns) {
+      *ctl.abort_flag = 1;
+      if (ctl.status) atomicOr(ctl.status, 0x1 /* MXG_DEV_TIMEOUT */);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Named barrier among `n` threads (whole warps) of the CTA; id 0 is __syncthreads.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");

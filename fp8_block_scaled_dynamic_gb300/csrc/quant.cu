@@ -20,63 +20,11 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace mxg {
 
 namespace {
-
-// Two fp32 values -> one byte of two E2M1 codes (lo in the low nibble),
-// round to nearest even, saturating to +-6.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint16_t r;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "cvt.u16.u8 %0, t;\n\t}"
-      : "=h"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Two fp32 values -> two E4M3 bytes (lo in the low byte), RNE, saturating.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Sign bits of the two bf16 in `w`, moved to bits 3 and 7 of a byte (the sign
-// bits of the two E2M1 nibbles).
-__device__ __forceinline__ uint32_t nibble_signs(uint32_t w) {
-  return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
-}
-
-// Sign bits of the two bf16 in `w`, moved to bits 7 and 15 (the sign bits
-// of the two E4M3 bytes).
-__device__ __forceinline__ uint32_t byte_signs(uint32_t w) {
-  return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
-}
-
-__device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// Byte offset of (row r, byte b of the row) in the tile layout with T-row
-// tiles (T = 128 for weights; the GEMM's token tile for activations): tile
-// (r / T, b / 128) of T rows x 128 bytes at ((r/T)*KC + b/128) * T * 128, and
-// the 16-byte unit j of row r at (r % T) * 128 + ((j ^ (r % 8)) * 16).
-__device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row, int T) {
-  const int j = (b >> 4) & 7;
-  const int rt = r / T;
-  return ((size_t)rt * kc_per_row + (b >> 7)) * (size_t)T * 128u + (size_t)(r - rt * T) * 128u +
-         (size_t)((j ^ (r & 7)) << 4) + (b & 15);
-}
 
 constexpr int kMxThreads = 256;
 constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in flight per thread
@@ -95,7 +43,6 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   const int cpr = K >> 3;  // 16-byte chunks per row; K % 128 == 0 => cpr % 16 == 0
   const int G = K >> 5;    // MX blocks per row
   const int lane = threadIdx.x & 31;
-  const unsigned kFull = 0xFFFFFFFFu;
   // An activation quantizer lets the next kernel launch at once: every kernel
   // of this library waits for its predecessor before it touches memory that
   // one may write.  A weight quantizer never triggers, so no later kernel
@@ -126,49 +73,17 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       // it; past the row it runs on zeros (the shuffles need every lane)
       // and stores nothing.
       const bool in_row = cc[i] < cpr;
-      const uint4 w = v[i];
-      // |x| as bf16 bits; unsigned max orders finite < inf < nan.
-      uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                             __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-      uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
-      amax = max(amax, __shfl_xor_sync(kFull, amax, 1));
-      amax = max(amax, __shfl_xor_sync(kFull, amax, 2));
-      uint32_t scode, packed;
-      if (amax >= 0x7F80u) {  // the block holds Inf or NaN
-        scode = 0xFFu;
-        packed = 0u;
-      } else {
-        // floor(log2 amax) = ef - 127 for a normal amax; a zero or subnormal
-        // amax clamps to e = -127 like ef in {1, 2}: e = max(ef, 2) - 129.
-        const int ef = max(static_cast<int>(amax >> 7), 2);
-        scode = static_cast<uint32_t>(ef - 2);
-        const float inv = __uint_as_float(static_cast<uint32_t>(256 - ef) << 23);  // 2^-e
-        packed = e2m1x2(bf16_lo(w.x) * inv, bf16_hi(w.x) * inv) |
-                 (e2m1x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 8) |
-                 (e2m1x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) << 16) |
-                 (e2m1x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 24);
-        packed |= nibble_signs(w.x) | (nibble_signs(w.y) << 8) | (nibble_signs(w.z) << 16) |
-                  (nibble_signs(w.w) << 24);
-      }
+      uint32_t scode;
+      const uint32_t packed = mx_encode_chunk(v[i], scode);
       if (real_row && in_row) {
         const size_t off = tile_rows ? tiled_offset(r, cc[i] * 4, K >> 8, tile_rows)
                                      : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
         *reinterpret_cast<uint32_t *>(codes + off) = packed;
       }
-      // Gather the scales of 4 consecutive blocks (lanes 0,4,8,12 of each
-      // half-warp) into one 32-bit word.
-      const uint32_t s1 = __shfl_down_sync(kFull, scode, 4);
-      const uint32_t s2 = __shfl_down_sync(kFull, scode, 8);
-      const uint32_t s3 = __shfl_down_sync(kFull, scode, 12);
+      const uint32_t word = mx_scale_word(scode);
       if (in_row && (lane & 15) == 0) {
-        const uint32_t word = scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
         const int g = cc[i] >> 2;  // first of the 4 blocks, g % 4 == 0
-        size_t off;
-        if (kSwizzled)
-          off = ((size_t)(r >> 7) * (size_t)(G >> 2) + (size_t)(g >> 2)) * 512u +
-                (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u;
-        else
-          off = (size_t)r * G + g;
+        const size_t off = kSwizzled ? sf_swizzled_offset(r, g, G) : (size_t)r * G + g;
         *reinterpret_cast<uint32_t *>(sf + off) = word;
       }
     }
@@ -277,6 +192,9 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
+  cudaError_t e = swizzled ? prefer_shared_carveout(mx_quant_kernel<true>)
+                           : prefer_shared_carveout(mx_quant_kernel<false>);
+  if (e != cudaSuccess) return e;
   if (swizzled)
     return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true>, xp, ldx, rows, rows_iter, K, tile_rows,
                               act ? 1 : 0, codes, sf);
@@ -293,6 +211,8 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
+  cudaError_t e = prefer_shared_carveout(fp8_quant_kernel);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows, K,
                             tile_rows, act ? 1 : 0, q, scale);
 }

@@ -1,0 +1,117 @@
+// quant_math.cuh -- the per-value arithmetic of the quantizers, shared by
+// the standalone quantizer kernels and the GEMM's fused activation phase.
+//
+// OCP-MX MXFP4 ("Kimi-K3 DSpark O-Proj-only MXFP4", "Exact quantization
+// coverage"): a 32-value block gets the E8M0 scale e = clamp(floor(log2 amax)
+// - 2, -127, 127) and codes E2M1_RNE_sat(x * 2^-e) with the sign of x.
+// FP8 PTPC ("Kimi-K3-DSpark-FP8-PTPC", "Phase 1 FP8 PTPC Quantization"): s =
+// amax / 448, q = E4M3_RNE_sat(x / s).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxg {
+
+// Two fp32 values -> one byte of two E2M1 codes (lo in the low nibble),
+// round to nearest even, saturating to +-6.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 values -> two E4M3 bytes (lo in the low byte), RNE, saturating.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Sign bits of the two bf16 in `w`, moved to bits 3 and 7 of a byte (the sign
+// bits of the two E2M1 nibbles).
+__device__ __forceinline__ uint32_t nibble_signs(uint32_t w) {
+  return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
+}
+
+// Sign bits of the two bf16 in `w`, moved to bits 7 and 15 (the sign bits
+// of the two E4M3 bytes).
+__device__ __forceinline__ uint32_t byte_signs(uint32_t w) {
+  return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Byte offset of (row r, byte b of the row) in the tile layout with T-row
+// tiles (T = 128 for weights; the GEMM's token tile for activations): tile
+// (r / T, b / 128) of T rows x 128 bytes at ((r/T)*KC + b/128) * T * 128, and
+// the 16-byte unit j of row r at (r % T) * 128 + ((j ^ (r % 8)) * 16).
+__device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row, int T) {
+  const int j = (b >> 4) & 7;
+  const int rt = r / T;
+  return ((size_t)rt * kc_per_row + (b >> 7)) * (size_t)T * 128u + (size_t)(r - rt * T) * 128u +
+         (size_t)((j ^ (r & 7)) << 4) + (b & 15);
+}
+
+// One 16-byte chunk (8 bf16 = a quarter of an MX block) per lane; four
+// consecutive lanes hold one block.  Returns the 8 packed E2M1 codes (value
+// 2i in the low nibble of byte i) and the block's E8M0 code in `scode`.
+// Every lane of the warp must call it (the block amax is a 4-lane shuffle).
+__device__ __forceinline__ uint32_t mx_encode_chunk(const uint4 &w, uint32_t &scode) {
+  const unsigned kFull = 0xFFFFFFFFu;
+  // |x| as bf16 bits; unsigned max orders finite < inf < nan.
+  const uint32_t m2 = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                               __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
+  amax = max(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = max(amax, __shfl_xor_sync(kFull, amax, 2));
+  if (amax >= 0x7F80u) {  // the block holds Inf or NaN
+    scode = 0xFFu;
+    return 0u;
+  }
+  // floor(log2 amax) = ef - 127 for a normal amax; a zero or subnormal amax
+  // clamps to e = -127 like ef in {1, 2}: e = max(ef, 2) - 129.
+  const int ef = max(static_cast<int>(amax >> 7), 2);
+  scode = static_cast<uint32_t>(ef - 2);
+  const float inv = __uint_as_float(static_cast<uint32_t>(256 - ef) << 23);  // 2^-e
+  uint32_t packed = e2m1x2(bf16_lo(w.x) * inv, bf16_hi(w.x) * inv) |
+                    (e2m1x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 8) |
+                    (e2m1x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) << 16) |
+                    (e2m1x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 24);
+  packed |= nibble_signs(w.x) | (nibble_signs(w.y) << 8) | (nibble_signs(w.z) << 16) |
+            (nibble_signs(w.w) << 24);
+  return packed;
+}
+
+// The scales of 4 consecutive blocks (lanes 0, 4, 8, 12 of a half-warp) as
+// one 32-bit word, valid in lanes 0 and 16.  Every lane must call it.
+__device__ __forceinline__ uint32_t mx_scale_word(uint32_t scode) {
+  const unsigned kFull = 0xFFFFFFFFu;
+  const uint32_t s1 = __shfl_down_sync(kFull, scode, 4);
+  const uint32_t s2 = __shfl_down_sync(kFull, scode, 8);
+  const uint32_t s3 = __shfl_down_sync(kFull, scode, 12);
+  return scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+// Byte offset of the scale of (row r, block g) -- g % 4 == 0 for a word -- in
+// the 128x4-tile layout: 512-byte tiles of 128 rows x 4 blocks, row-block
+// major, then (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4.  G = blocks/row.
+__device__ __forceinline__ size_t sf_swizzled_offset(int r, int g, int G) {
+  return ((size_t)(r >> 7) * (size_t)(G >> 2) + (size_t)(g >> 2)) * 512u + (size_t)(r & 31) * 16u +
+         (size_t)((r >> 5) & 3) * 4u;
+}
+
+}  // namespace mxg

@@ -108,7 +108,8 @@ typedef enum {
 
 typedef struct {
     int variant;          /* mxg_variant */
-    int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over; 0 = SM count */
+    int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over; 0 or more
+                             than the SM count = the SM count (one persistent CTA per SM) */
     void *workspace;      /* device scratch of >= mxg_gemm_workspace_bytes() bytes,
                              256-byte aligned.  Its first 64 KiB hold split-K arrival
                              counters: zero them before the first call; every completed
@@ -141,15 +142,39 @@ typedef struct {
                              first/last load, first stage ready, last MMA commit, epilogue
                              items, split-K hand-off, exit; slot 15 = items; slots 16/17 =
                              global timer ns at entry/exit; slot 18 = the producer's
-                             dependency wait returned).  NULL = off. */
+                             dependency wait returned; fused path: slot 19 = activation
+                             share quantized, slot 12 = first and slot 13 = second grid
+                             barrier passed).
+                             NULL = off. */
+    int splitk_reduce;    /* how SPLITK partial tiles are summed when the activations come
+                             pre-quantized: MXG_REDUCE_DEFAULT (= MXG_REDUCE_KERNEL),
+                             MXG_REDUCE_KERNEL (a reduce kernel launched right after the
+                             GEMM), MXG_REDUCE_GRID (every CTA of the GEMM, after a grid
+                             barrier: one launch; the grid is launched cooperatively),
+                             MXG_REDUCE_LAST_CTA (the last CTA to finish each tile).  On
+                             the fused A4W4 path (x given, K % 256 == 0) MXG_REDUCE_GRID
+                             runs everything as one cooperative kernel: quantize, grid
+                             barrier, GEMM, grid barrier, reduce; otherwise the fused path
+                             is the quantizer kernel, the GEMM and the reduce kernel,
+                             chained by programmatic dependent launch (faster on GB300:
+                             a grid barrier costs more than a kernel boundary). */
 } mxg_gemm_opts;
+
+enum {
+    MXG_REDUCE_DEFAULT = 0,
+    MXG_REDUCE_KERNEL = 1,
+    MXG_REDUCE_GRID = 2,
+    MXG_REDUCE_LAST_CTA = 3
+};
 
 typedef struct {
     int variant;       /* MXG_VARIANT_FULL or MXG_VARIANT_SPLITK */
     int bm, bn;        /* MMA tile: bm rows of the 128-row operand, bn of the other */
     int ctas;          /* grid size */
     int tiles;         /* output tiles */
-    int kblocks;       /* K-blocks per tile (256 K for A4W4, 128 K for PTPC) */
+    int kblocks;       /* pipeline stages along K per tile: 128-byte K columns (256 K
+                          for A4W4, 128 K for PTPC), one per stage for FULL, two for
+                          SPLITK */
     int seg_max;       /* SPLITK: most CTAs contributing to one tile */
     size_t ws_bytes;   /* workspace this plan needs */
 } mxg_plan;

@@ -98,8 +98,8 @@ def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
     p = mx.mxg_plan_gemm(kind, M, N, K, sm)
     assert p["variant"] == 2 and p["bm"] == 128
     assert p["bn"] >= M and p["bn"] in (16, 32, 64, 128, 256) and (p["bn"] // 2 < M or p["bn"] == 16)
-    kstage = 256 if kind == 0 else 128
-    KB = -(-K // kstage)
+    kcol = 256 if kind == 0 else 128  # K values in one 128-byte column
+    KB = -(-(-(-K // kcol)) // 2)      # split-K stages take two columns
     assert p["kblocks"] == KB
     tiles = (N // 128) * (-(-M // p["bn"]))
     assert p["tiles"] == tiles

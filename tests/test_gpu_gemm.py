@@ -126,6 +126,43 @@ def test_a4w4_fused_equals_prequantized_and_is_deterministic():
     assert (a.view(np.uint32) == c.view(np.uint32)).all()
 
 
+@pytest.mark.parametrize("M,N,K,ctas", [(64, 1024, 4096, 0), (8, 7168, 8192, 0), (37, 768, 2048, 7),
+                                         (200, 512, 2048, 0), (256, 1280, 1024, 57), (24, 640, 640, 0)])
+def test_a4w4_splitk_reduce_modes_bit_identical(M, N, K, ctas):
+    """The partial tiles are summed in slot order whichever kernel does it: a
+    reduce kernel, every CTA after a grid barrier, the last CTA of the tile;
+    and the fused path gives the same bits, as three kernels or as one
+    (whose CTAs also quantize x themselves)."""
+    d = dev()
+    x, w = quant_pair(M, N, K, seed=M * 7 + N)
+    wc, wsf = mx.mx_quantize_weight(w.to(d))
+    ac, asf = mx.mx_quantize_act(x.to(d))
+    outs = {m: mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out_f32=True, variant="splitk",
+                               ctas=ctas, splitk_reduce=m)
+            for m in ("kernel", "grid", "lastcta")}
+    outs["fused"] = mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant="splitk", ctas=ctas)
+    outs["fused one kernel"] = mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant="splitk",
+                                               ctas=ctas, splitk_reduce="grid")
+    ref, bound = oracle_a4w4(x, w)
+    y0 = outs["kernel"].cpu().numpy()
+    assert_gemm_close(y0, ref, bound, f"splitk {M}x{N}x{K}")
+    for m, y in outs.items():
+        assert (y.cpu().numpy().view(np.uint32) == y0.view(np.uint32)).all(), m
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 1024, 2048), (5, 7168, 1024), (130, 384, 896)])
+def test_ptpc_splitk_reduce_modes_bit_identical(M, N, K):
+    d = dev()
+    x, w = quant_pair(M, N, K, seed=M + 3 * N)
+    qw, sw = mx.fp8_quantize_act(w.to(d))
+    qa, sa = mx.fp8_quantize_act(x.to(d))
+    outs = {m: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant="splitk", splitk_reduce=m)
+            for m in ("kernel", "grid", "lastcta")}
+    y0 = outs["kernel"].cpu().numpy()
+    for m, y in outs.items():
+        assert (y.cpu().numpy().view(np.uint32) == y0.view(np.uint32)).all(), m
+
+
 def test_a4w4_decode_m8_full_size():
     # single o_proj layer, M = 8 (1 verified + 7 drafted tokens), N = 7168, K = 8192
     x = synth.activation(8, synth.OPROJ_K, seed=synth.act_seed(0, 0, 0))
