@@ -457,7 +457,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    {  // all 32 lanes set up the first stages; lane 0 then runs the pipeline
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
       const uint64_t polA = p.swap ? pol_stream : pol_keep;  // swapped: A = weights, read once
@@ -522,27 +522,39 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
                       p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * KS * kb) * 512u, natoms * 512, fb, polB);
         }
       };
-      // Weights that the previous kernel did not write may stream in before
-      // griddepcontrol.wait: arm the first stages and issue their weight
-      // operand now, the activation operand after the wait.
       const bool w_is_a = p.swap != 0;
-      int pre = 0;
-      if (p.early_w) {
-        uint32_t c2 = first_cursor(p);
-        Item it2;
-        while (pre < S && next_item(p, c2, it2)) {
-          for (int kb = it2.kb0; kb < it2.kb1 && pre < S; ++kb, ++pre) {
-            const uint32_t fb = full_bar(pre);
-            mbar_arrive_expect_tx(fb, stage_bytes(it2, kb));
-            if (w_is_a)
-              issue_a(pre, it2, kb, fb);
-            else
-              issue_b(pre, it2, kb, fb);
+      // stage k of this CTA's sequence: its item and K-stage
+      auto stage_of = [&](int k, Item &it, int &kb) -> bool {
+        uint32_t c = first_cursor(p);
+        int n = 0;
+        while (next_item(p, c, it)) {
+          const int len = it.kb1 - it.kb0;
+          if (k < n + len) {
+            kb = it.kb0 + (k - n);
+            return true;
           }
+          n += len;
         }
+        return false;
+      };
+      // The first S stages (fewer if the CTA has fewer) are set up by the
+      // lanes in parallel, one stage each: bulk copies issued by one thread
+      // queue behind each other (~0.1 us apiece).  Weights that no kernel
+      // still in flight writes stream in before griddepcontrol.wait; the
+      // activation operand follows the wait.
+      Item my_it;
+      int my_kb = 0;
+      const bool mine = lane < S && stage_of(lane, my_it, my_kb);
+      const int pre = __popc(__ballot_sync(0xFFFFFFFFu, mine));  // lanes 0 .. pre-1
+      if (p.early_w && mine) {
+        mbar_arrive_expect_tx(full_bar(lane), stage_bytes(my_it, my_kb));
+        if (w_is_a)
+          issue_a(lane, my_it, my_kb, full_bar(lane));
+        else
+          issue_b(lane, my_it, my_kb, full_bar(lane));
       }
       pdl_wait();
-      trace_mark(p, kTrWaited);
+      if (lane == 0) trace_mark(p, kTrWaited);
       bool ok = true;
       if (p.fuse_quant) {
         // the token tiles are written by every CTA of this grid; the epilogue
@@ -550,62 +562,58 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         ok = mbar_wait(acts_ready, 0, ctl) && !*abort_flag;
         fence_proxy_async_global();
       }
-      uint32_t cur = first_cursor(p);
-      Item it;
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      if (!ok && pre > 0) {
-        // give the stages armed before the wait their other operand (in
-        // bounds, contents irrelevant) so that they complete and drain
-        uint32_t c2 = first_cursor(p);
-        Item it2;
-        int k = 0;
-        while (k < pre && next_item(p, c2, it2))
-          for (int kb = it2.kb0; kb < it2.kb1 && k < pre; ++kb, ++k) {
-            if (w_is_a)
-              issue_b(k, it2, kb, full_bar(k));
-            else
-              issue_a(k, it2, kb, full_bar(k));
-          }
-        issued = pre;
+      // the rest of the first stages -- also when the fused phase failed:
+      // every armed stage must land before the CTA exits (contents are then
+      // irrelevant; every address stays in bounds)
+      if (mine) {
+        if (p.early_w) {
+          if (w_is_a)
+            issue_b(lane, my_it, my_kb, full_bar(lane));
+          else
+            issue_a(lane, my_it, my_kb, full_bar(lane));
+        } else {
+          mbar_arrive_expect_tx(full_bar(lane), stage_bytes(my_it, my_kb));
+          issue_a(lane, my_it, my_kb, full_bar(lane));
+          issue_b(lane, my_it, my_kb, full_bar(lane));
+        }
       }
-      while (ok && next_item(p, cur, it)) {
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          const uint32_t fb = full_bar(stage);
-          if (issued < pre) {  // armed before the wait: only the other operand is left
-            if (w_is_a)
-              issue_b(stage, it, kb, fb);
-            else
+      __syncwarp();
+      if (lane == 0) {
+        trace_mark(p, kTrFirstLoad);
+        uint32_t cur = first_cursor(p);
+        Item it;
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        while (ok && next_item(p, cur, it)) {
+          for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            if (issued >= pre) {  // the first `pre` stages are already in flight
+              const uint32_t fb = full_bar(stage);
+              if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(fb, stage_bytes(it, kb));
               issue_a(stage, it, kb, fb);
-          } else {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
-              ok = false;
-              break;
+              issue_b(stage, it, kb, fb);
             }
-            mbar_arrive_expect_tx(fb, stage_bytes(it, kb));
-            issue_a(stage, it, kb, fb);
-            issue_b(stage, it, kb, fb);
-          }
-          if (issued == 0) trace_mark(p, kTrFirstLoad);
-          ++issued;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
+            ++issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
-      }
-      trace_mark(p, kTrLastLoad);
-      if (!ok || *abort_flag) {
-        // let every copy still in flight land before the CTA can exit
-        const long long n = issued < S ? issued : S;
-        for (long long k = 1; k <= n; ++k) {
-          const long long pos = issued - k;
-          drain_wait(full_bar((int)(pos % S)), (uint32_t)((pos / S) & 1), p.timeout_ns, p.status);
+        if (issued < pre) issued = pre;
+        trace_mark(p, kTrLastLoad);
+        if (!ok || *abort_flag) {
+          // let every copy still in flight land before the CTA can exit
+          const long long n = issued < S ? issued : S;
+          for (long long k = 1; k <= n; ++k) {
+            const long long pos = issued - k;
+            drain_wait(full_bar((int)(pos % S)), (uint32_t)((pos / S) & 1), p.timeout_ns, p.status);
+          }
         }
-        // stages armed before the wait but never completed by the loop
-        for (long long k = issued; k < pre; ++k)
-          drain_wait(full_bar((int)k), 0, p.timeout_ns, p.status);
       }
     }
   } else if (warp == 1) {
