@@ -476,50 +476,66 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         }
         return bytes;
       };
-      // Operands in the tile layout: the columns of one stage are adjacent
-      // (tile (row tile, column) at (row tile * KC + column) * tile bytes), so
-      // a stage of a 128-row A tile or of a BN-row token tile is one bulk copy.
-      // Row-major operands go through the tensor map (128-byte swizzle box per
-      // column).
-      auto issue_a = [&](int stage, const Item &it, int kb, uint32_t fb) {
+      // The copies of one stage, numbered: the A operand (one bulk copy in the
+      // tile layout -- the columns of a stage are adjacent, tile (row tile,
+      // column) at (row tile * KC + column) * tile bytes -- else one 128-byte
+      // swizzle box per column), its scales, then the B operand (token tiles:
+      // one copy; 128-row weight tiles: one per column and row tile; else one
+      // box per column), its scales (one per 128-row block).  Lane i issues
+      // copy i: copies from one converged instruction run in parallel, while
+      // copies that one thread issues one after another complete one after
+      // another (~0.2-0.4 us each).
+      auto issue_op = [&](int i, bool want_a, bool want_b, int stage, const Item &it, int kb,
+                          uint32_t fb) {
         const int nc = ncol_of(kb);
-        if (p.a_tiles)
-          bulk_load(sA + stage * C::kABytes,
-                    p.a_tiles + ((size_t)it.ta * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kAColBytes,
-                    (uint32_t)nc * C::kAColBytes, fb, polA);
-        else
-          for (int j = 0; j < nc; ++j)
-            tma_load_2d(sA + stage * C::kABytes + j * C::kAColBytes, &tmA, (kb * KS + j) * kRowBytes,
-                        it.ta * kTileA, fb, polA);
-        if (KIND == 0)
-          bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
-                    natoms_of(kb) * 512, fb, polA);
-      };
-      auto issue_b = [&](int stage, const Item &it, int kb, uint32_t fb) {
-        const int nc = ncol_of(kb);
-        if (p.b_tiles && p.b_tile_rows == BN) {  // token tiles of BN rows
-          bulk_load(sB + stage * C::kBBytes,
-                    p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kBColBytes,
-                    (uint32_t)nc * C::kBColBytes, fb, polB);
-        } else if (p.b_tiles) {  // 128-row weight tiles, BN / 128 of them per column
-          for (int j = 0; j < nc; ++j)
-            for (int r = 0; r < BN / 128; ++r)
-              bulk_load(sB + stage * C::kBBytes + j * C::kBColBytes + r * 16384,
-                        p.b_tiles + ((size_t)(it.tb * (BN / 128) + r) * p.kc_per_row +
-                                     (size_t)kb * KS + j) * 16384u,
-                        16384, fb, polB);
-        } else {
-          for (int j = 0; j < nc; ++j)
-            tma_load_2d(sB + stage * C::kBBytes + j * C::kBColBytes, &tmB, (kb * KS + j) * kRowBytes,
-                        it.tb * BN, fb, polB);
+        const int rb0 = (it.tb * BN) / 128;
+        const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+        if (want_a) {
+          const int na = p.a_tiles ? 1 : nc;
+          if (i < na) {
+            if (p.a_tiles)
+              bulk_load(sA + stage * C::kABytes,
+                        p.a_tiles + ((size_t)it.ta * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kAColBytes,
+                        (uint32_t)nc * C::kAColBytes, fb, polA);
+            else
+              tma_load_2d(sA + stage * C::kABytes + i * C::kAColBytes, &tmA, (kb * KS + i) * kRowBytes,
+                          it.ta * kTileA, fb, polA);
+            return;
+          }
+          i -= na;
+          if (KIND == 0) {
+            if (i == 0) {
+              bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
+                        natoms_of(kb) * 512, fb, polA);
+              return;
+            }
+            i -= 1;
+          }
         }
-        if (KIND == 0) {
-          const int natoms = natoms_of(kb);
-          const int rb0 = (it.tb * BN) / 128;
-          const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-          for (int j = 0; j < nblk; ++j)
-            bulk_load(sSFB + stage * C::kSfbBytes + j * (1024 * KS),
-                      p.sfB + ((size_t)(rb0 + j) * p.G4 + 2 * KS * kb) * 512u, natoms * 512, fb, polB);
+        if (want_b) {
+          const bool tok = p.b_tiles && p.b_tile_rows == BN;
+          const int nb = tok ? 1 : p.b_tiles ? nc * (BN >= 128 ? BN / 128 : 1) : nc;
+          if (i < nb) {
+            if (tok) {
+              bulk_load(sB + stage * C::kBBytes,
+                        p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kBColBytes,
+                        (uint32_t)nc * C::kBColBytes, fb, polB);
+            } else if (p.b_tiles) {  // BN >= 128 here (the dispatcher's weight-tile case)
+              constexpr int kRT = BN >= 128 ? BN / 128 : 1;
+              const int j = i / kRT, r = i % kRT;
+              bulk_load(sB + stage * C::kBBytes + j * C::kBColBytes + r * 16384,
+                        p.b_tiles + ((size_t)(it.tb * kRT + r) * p.kc_per_row + (size_t)kb * KS + j) * 16384u,
+                        16384, fb, polB);
+            } else {
+              tma_load_2d(sB + stage * C::kBBytes + i * C::kBColBytes, &tmB, (kb * KS + i) * kRowBytes,
+                          it.tb * BN, fb, polB);
+            }
+            return;
+          }
+          i -= nb;
+          if (KIND == 0 && i < nblk)
+            bulk_load(sSFB + stage * C::kSfbBytes + i * (1024 * KS),
+                      p.sfB + ((size_t)(rb0 + i) * p.G4 + 2 * KS * kb) * 512u, natoms_of(kb) * 512, fb, polB);
         }
       };
       const bool w_is_a = p.swap != 0;
@@ -537,21 +553,21 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         }
         return false;
       };
-      // The first S stages (fewer if the CTA has fewer) are set up by the
-      // lanes in parallel, one stage each: bulk copies issued by one thread
-      // queue behind each other (~0.1 us apiece).  Weights that no kernel
-      // still in flight writes stream in before griddepcontrol.wait; the
-      // activation operand follows the wait.
-      Item my_it;
-      int my_kb = 0;
-      const bool mine = lane < S && stage_of(lane, my_it, my_kb);
-      const int pre = __popc(__ballot_sync(0xFFFFFFFFu, mine));  // lanes 0 .. pre-1
-      if (p.early_w && mine) {
-        mbar_arrive_expect_tx(full_bar(lane), stage_bytes(my_it, my_kb));
-        if (w_is_a)
-          issue_a(lane, my_it, my_kb, full_bar(lane));
-        else
-          issue_b(lane, my_it, my_kb, full_bar(lane));
+      // The first S stages (fewer if the CTA has fewer): weights that no
+      // kernel still in flight writes stream in before griddepcontrol.wait;
+      // the activation operand follows the wait.
+      int pre = 0;
+      {
+        Item itk;
+        int kbk = 0;
+        while (pre < S && stage_of(pre, itk, kbk)) {
+          if (p.early_w) {
+            if (lane == 0) mbar_arrive_expect_tx(full_bar(pre), stage_bytes(itk, kbk));
+            __syncwarp();
+            issue_op(lane, w_is_a, !w_is_a, pre, itk, kbk, full_bar(pre));
+          }
+          ++pre;
+        }
       }
       pdl_wait();
       if (lane == 0) trace_mark(p, kTrWaited);
@@ -560,51 +576,56 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         // the token tiles are written by every CTA of this grid; the epilogue
         // warps signal once the grid barrier after that phase has passed
         ok = mbar_wait(acts_ready, 0, ctl) && !*abort_flag;
+        ok = __all_sync(0xFFFFFFFFu, ok);
         fence_proxy_async_global();
       }
       // the rest of the first stages -- also when the fused phase failed:
       // every armed stage must land before the CTA exits (contents are then
       // irrelevant; every address stays in bounds)
-      if (mine) {
+      for (int k = 0; k < pre; ++k) {
+        Item itk;
+        int kbk = 0;
+        stage_of(k, itk, kbk);
         if (p.early_w) {
-          if (w_is_a)
-            issue_b(lane, my_it, my_kb, full_bar(lane));
-          else
-            issue_a(lane, my_it, my_kb, full_bar(lane));
+          issue_op(lane, !w_is_a, w_is_a, k, itk, kbk, full_bar(k));
         } else {
-          mbar_arrive_expect_tx(full_bar(lane), stage_bytes(my_it, my_kb));
-          issue_a(lane, my_it, my_kb, full_bar(lane));
-          issue_b(lane, my_it, my_kb, full_bar(lane));
+          if (lane == 0) mbar_arrive_expect_tx(full_bar(k), stage_bytes(itk, kbk));
+          __syncwarp();
+          issue_op(lane, true, true, k, itk, kbk, full_bar(k));
         }
       }
-      __syncwarp();
-      if (lane == 0) {
-        trace_mark(p, kTrFirstLoad);
-        uint32_t cur = first_cursor(p);
-        Item it;
-        int stage = 0;
-        uint32_t phase = 0;
-        long long issued = 0;
-        while (ok && next_item(p, cur, it)) {
-          for (int kb = it.kb0; kb < it.kb1; ++kb) {
-            if (issued >= pre) {  // the first `pre` stages are already in flight
-              const uint32_t fb = full_bar(stage);
-              if (!mbar_wait(empty_bar(stage), phase ^ 1u, ctl)) {
-                ok = false;
-                break;
-              }
-              mbar_arrive_expect_tx(fb, stage_bytes(it, kb));
-              issue_a(stage, it, kb, fb);
-              issue_b(stage, it, kb, fb);
+      if (lane == 0) trace_mark(p, kTrFirstLoad);
+      // steady state: the whole warp walks the stages in order; lane 0 waits
+      // for a free slot and arms it, then every lane issues its copy
+      uint32_t cur = first_cursor(p);
+      Item it;
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      while (ok && next_item(p, cur, it)) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (issued >= pre) {
+            const uint32_t fb = full_bar(stage);
+            bool w_ok = true;
+            if (lane == 0) {
+              w_ok = mbar_wait(empty_bar(stage), phase ^ 1u, ctl);
+              if (w_ok) mbar_arrive_expect_tx(fb, stage_bytes(it, kb));
             }
-            ++issued;
-            if (++stage == S) {
-              stage = 0;
-              phase ^= 1u;
+            if (!__shfl_sync(0xFFFFFFFFu, w_ok ? 1 : 0, 0)) {
+              ok = false;
+              break;
             }
+            issue_op(lane, true, true, stage, it, kb, fb);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        if (issued < pre) issued = pre;
+      }
+      if (issued < pre) issued = pre;
+      if (lane == 0) {
         trace_mark(p, kTrLastLoad);
         if (!ok || *abort_flag) {
           // let every copy still in flight land before the CTA can exit
@@ -650,6 +671,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             return sdesc_kmajor_sw128(b0 + (uint32_t)(s >> 2) * C::kBColBytes + 32u * (s & 3));
           };
           if (KIND == 0) {
+            // scale factors: smem -> the TMEM columns of this ring slot
             const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
             const int rb0 = (it.tb * BN) / 128;
             const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
