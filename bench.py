@@ -366,9 +366,10 @@ def traffic_record(workload: str):
 def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
-    for f in ("gemm.cu", "ptx.cuh", "quant.cu"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")) and f != "api.cu":
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()
 
 
@@ -610,6 +611,10 @@ def run_reference(args, rank, world):
     cores, each step a bounded sample of the same workload."""
     if rank != 0:
         return
+    if args.workload == "sweep":
+        print(json.dumps({"impl": "reference", "unavailable": "the sweep reports per-GEMM GPU rates only; "
+                          "the oracle arm times the single workloads"}), flush=True)
+        return
     import oracle
     oracle.build()
     # rows per step: as many as keep the whole run (warm-up + steps) near two minutes
@@ -642,6 +647,122 @@ def run_reference(args, rank, world):
     }), flush=True)
 
 
+# ----------------------------------------------------------------- sweep
+SWEEP_M = (8, 16, 32, 64, 128, 512, 2048, 8192, 16384)
+
+
+def run_sweep(args, rank, world, local_rank):
+    """Mixed-precision draft layer over M: per layer an FP8 PTPC gate_up
+    (7168 -> 2 x 18432), an FP8 PTPC down (18432 -> 7168) and an A4W4 o_proj
+    (8192 -> 7168), five layers with distinct seeded weights.  For every M
+    and GEMM: one graph of the five layers' launches (activation quantizer +
+    GEMM, as a caller runs them), timed between L2 flushes; one JSON line per M."""
+    import fp8_block_scaled_dynamic_gb300 as mx
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    hbm, bf16, peak_src = load_peaks()
+    H, I2, I, N_O, K_O = 7168, 2 * synth.MLP_I, synth.MLP_I, synth.OPROJ_N, synth.OPROJ_K
+    L = 5
+    # resident weights (tile layout); bf16 originals freed after conversion
+    w = {"gate_up": [], "down": [], "o_proj": []}
+    for l in range(L):
+        w["gate_up"].append(mx.fp8_quantize_weight(
+            synth.weight(I2, H, seed=synth.seed_cfg4("gate_up", l)).to(dev), layout=mx.TILED))
+        w["down"].append(mx.fp8_quantize_weight(
+            synth.weight(H, I, seed=synth.seed_cfg4("down", l)).to(dev), layout=mx.TILED))
+        w["o_proj"].append(mx.mx_quantize_weight(
+            synth.weight(N_O, K_O, seed=synth.seed_cfg4("o_proj", l)).to(dev), layout=mx.TILED))
+    # activations for the largest M (smaller M take the leading rows)
+    MX = max(SWEEP_M)
+    xs = {"gate_up": synth.activation(MX, H, seed=synth.act_seed(4, 0, 0)).to(dev),
+          "down": synth.activation(MX, I, seed=synth.act_seed(4, 0, 1)).to(dev),
+          "o_proj": synth.activation(MX, K_O, seed=synth.act_seed(4, 0, 2)).to(dev)}
+    shapes = {"gate_up": (I2, H, 1), "down": (H, I, 1), "o_proj": (N_O, K_O, 0)}
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    reps = max(3, min(args.steps, 20))
+    for M in SWEEP_M:
+        per = {}
+        total_ms = 0.0
+        for g, (N, K, kind) in shapes.items():
+            plan = mx.mxg_plan_gemm(kind, M, N, K, sm)
+            T = act_tile_rows(plan)
+            x = xs[g][:M]
+            y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(kind, False, M, N, K)),
+                             dtype=torch.uint8, device=dev)
+            if kind == 1:
+                qa = torch.empty(mx.mxg_act_tiled_bytes(1, M, K, T), dtype=torch.uint8, device=dev)
+                sa = torch.empty(M, dtype=torch.float32, device=dev)
+
+                def layer(l, x=x, y=y, ws=ws, qa=qa, sa=sa, T=T, g=g):
+                    mx.fp8_quantize_act_tiled(x, T, q=qa, scale=sa)
+                    qw, sw = w[g][l]
+                    mx.fp8_gemm_ptpc(qa, sa, qw, sw, out=y, ws=ws, weights_static=True,
+                                     weights_tiled=True, act_tile_rows=T)
+                gbytes = ptpc_gemm_bytes(M, N, K) + fp8_quant_bytes(M, K)
+            else:
+                ac = torch.empty(mx.mxg_act_tiled_bytes(0, M, K, T), dtype=torch.uint8, device=dev)
+                asf = torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev)
+
+                def layer(l, x=x, y=y, ws=ws, ac=ac, asf=asf, T=T, M=M, g=g):
+                    mx.mx_quantize_act_tiled(x, T, codes=ac, sf=asf)
+                    wc, wsf = w[g][l]
+                    mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out=y, ws=ws, weights_static=True,
+                                    weights_tiled=True, act_tile_rows=T, m=M)
+                gbytes = a4w4_gemm_bytes(M, N, K) + mx_quant_bytes(M, K)
+            with torch.cuda.stream(stream):
+                for l in range(L):
+                    layer(l)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for l in range(L):
+                    layer(l)
+            ts = []
+            with torch.cuda.stream(stream):
+                for r in range(reps + 2):
+                    flush_l2(flush)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    graph.replay()
+                    b.record(stream)
+                    stream.synchronize()
+                    if r >= 2:
+                        ts.append(a.elapsed_time(b))
+            ms = statistics.median(ts) / L  # one layer's quantizer + GEMM
+            total_ms += ms
+            flops = 2.0 * M * N * K
+            tf = flops / (ms * 1e-3) / 1e12
+            gbs = gbytes / (ms * 1e-3) / 1e9
+            ratio = 6.0 if kind == 0 else 2.0
+            if plan["variant"] == 2:
+                roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                        "frac": round(gbs / hbm, 4)}
+            else:
+                roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": round(bf16 * ratio, 1),
+                        "unit": "TFLOP/s", "frac": round(tf / (bf16 * ratio), 4)}
+            per[g] = {"dtype": "e2m1 x e2m1" if kind == 0 else "e4m3 x e4m3", "N": N, "K": K,
+                      "us": round(ms * 1e3, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
+                      "roofline": roof,
+                      "dispatch": {k: plan[k] for k in ("variant", "bn", "ctas", "seg_max")}}
+            del graph
+        layer_flops = sum(2.0 * M * n * k for n, k, _ in shapes.values())
+        line = {"metric": METRIC, "workload": "sweep", "M": M, "n_gpus": world,
+                "value": round(layer_flops / (total_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "higher_is_better": True, "layer_ms": round(total_ms, 4), "layers": L,
+                "timing": f"median of {reps} graph replays of 5 layers between L2 flushes; per GEMM "
+                          "= activation quantizer + GEMM of one layer",
+                "peak_source": peak_src, "gemms": per,
+                "data": "synthetic (seeded bf16 N(0,1) activations with 0.1% x50 outliers, N(0,0.02) weights)"}
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -649,7 +770,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="oproj_decode",
-                    choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192"])
+                    choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192",
+                             "sweep"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--min-warmup-s", type=float, default=0.5,
@@ -667,7 +789,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
-        run_ours(args, rank, world, local_rank)
+        if args.workload == "sweep":
+            run_sweep(args, rank, world, local_rank)
+        else:
+            run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()
