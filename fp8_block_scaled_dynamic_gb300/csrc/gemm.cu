@@ -60,7 +60,7 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 7) + 16;
+  static constexpr int kBarBytes = 8 * (3 * kStages + 7) + 16;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
   static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
   static constexpr int kSteps = 4 * KS;              // MMAs (K = 64 / 32) per stage
@@ -404,13 +404,20 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   const uint32_t stall_bar = acc_full + 32;
   const uint32_t mma_done = acc_full + 40;
   const uint32_t acts_ready = acc_full + 48;  // fused path: token tiles of every CTA written
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (2 * S + 7);
+  const uint32_t sf_bars = acc_full + 56;     // full tile: a stage's scales are in TMEM
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 7);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
   volatile int *reduce_go = reinterpret_cast<volatile int *>(misc + 12);
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto sf_ready = [&](int s) { return sf_bars + 8u * s; };
+  // Full-tile A4W4: the epilogue warps (idle during a tile's main loop) move
+  // each stage's scale factors into TMEM with tcgen05.st, off the tensor
+  // pipe; a tcgen05.cp there would hold up the MMAs behind it and, through
+  // them, the release of the stage.
+  constexpr bool kEpiScales = KIND == 0 && KS == 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -435,6 +442,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     mbar_init(stall_bar, 1);
     mbar_init(mma_done, 1);
     mbar_init(acts_ready, 1);
+    for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
     *abort_flag = 0;
     *decision = 0;
     *reduce_go = 0;
@@ -655,7 +663,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (i > 0 && !mbar_wait(acc_empty, (uint32_t)((i - 1) & 1), ctl)) break;
         tc_fence_after();
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, ctl)) {
+          // full tile A4W4: the epilogue warps signal once the stage's data is
+          // in and its scales are in TMEM
+          if (!mbar_wait(kEpiScales ? sf_ready(stage) : full_bar(stage), phase, ctl)) {
             ok = false;
             break;
           }
@@ -677,12 +687,14 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
             const uint32_t sfa_t = tmem + kSfCol + (uint32_t)stage * C::kSfColsPerStage;
             const uint32_t sfb_t = sfa_t + C::kSfColsA;
-            for (int a = 0; a < natoms; ++a)
-              tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
-            for (int j = 0; j < nblk; ++j)
+            if (!kEpiScales) {
               for (int a = 0; a < natoms; ++a)
-                tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
-                         sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * (1024 * KS) + a * 512));
+                tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
+              for (int j = 0; j < nblk; ++j)
+                for (int a = 0; a < natoms; ++a)
+                  tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
+                           sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * (1024 * KS) + a * 512));
+            }
             const int nk = min(C::kSteps, (p.K - kb * 256 * KS) / 64);
             for (int s = 0; s < nk; ++s) {
               const uint32_t sel = (uint32_t)(s & 1) * 2u;
@@ -734,7 +746,39 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     Item it;
     int i = 0;
     uint32_t part_phase = 0;
+    long long q_sf = 0;  // stage sequence number (kEpiScales)
     while (next_item(p, cur, it)) {
+      if (kEpiScales) {
+        // The item's stages in order: once the stage's data is in, its scale
+        // atoms go smem -> registers -> this warp's TMEM lane quarter, in the
+        // layout tcgen05.cp 32x128b.warpx4 makes (lane 32q+i, columns c..c+3
+        // = the atom's 16-byte row i, in every quarter q).
+        bool fed = true;
+        for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
+          const int st = (int)(q_sf % S);
+          if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) {
+            fed = false;
+            break;
+          }
+          const int natoms = min(2, p.G4 - 2 * kb);
+          const int rb0 = (it.tb * BN) / 128;
+          const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+          const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+          const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
+          const uint32_t sfb_col = sfa_col + C::kSfColsA;
+          for (int a = 0; a < natoms; ++a)
+            tmem_st4(sfa_col + 4 * a, ld_shared_v4(sSFA + st * C::kSfaBytes + a * 512 + lane * 16));
+          for (int j = 0; j < nblk; ++j)
+            for (int a = 0; a < natoms; ++a)
+              tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
+                       ld_shared_v4(sSFB + st * C::kSfbBytes + j * 1024 + a * 512 + lane * 16));
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sf_ready(st));
+        }
+        if (!fed) break;
+      }
       if (p.debug_stall && i == 0) {
         // test hook: a barrier nothing arrives at; the bounded wait gives up
         if (!warp_wait(stall_bar, 0, ctl)) break;
