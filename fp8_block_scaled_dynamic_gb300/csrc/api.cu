@@ -82,6 +82,21 @@ mxg_status make_operand_map(CUtensorMap *m, const void *ptr, uint64_t row_bytes,
   return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
 }
 
+// y (M rows of N bf16, leading dimension ldy) for the full-tile epilogue's
+// TMA stores: 32 x 32 boxes, no swizzle; out-of-bounds elements are skipped.
+mxg_status make_output_map(CUtensorMap *m, void *y, int M, int N, int ldy) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return MXG_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)ldy * 2u};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, y, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
+}
+
 // How split-K partial tiles are summed on the two-kernel path:
 //   kernel (default): a reduce kernel launched right after the GEMM;
 //   grid: by every CTA of the GEMM after a grid barrier (one launch);
@@ -218,7 +233,8 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   if (w_tiled && (row_bytes % 128 != 0 || N % 128 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
   if (act_tile_rows && act_tile_rows != plan_act_tile_rows(pl)) return MXG_ERR_INVALID_ARG;
   if (act_tile_rows && row_bytes % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmY;
+  std::memset(&tmY, 0, sizeof(tmY));
   const uint8_t *A = swap ? op.w : op.a;
   const uint8_t *B = swap ? op.a : op.w;
   const int rowsA = swap ? N : M, rowsB = swap ? M : N;
@@ -234,6 +250,10 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.y = y;
   p.ldy = ldy;
   p.out_f32 = out_dtype == MXG_OUT_F32 ? 1 : 0;
+  if (!swap && !p.out_f32 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && (ldy % 8) == 0) {
+    if ((st = make_output_map(&tmY, y, M, N, ldy)) != MXG_OK) return st;
+    p.y_tma = 1;
+  }
   p.M = M;
   p.N = N;
   p.K = K;
@@ -293,7 +313,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
     if (!ws) return MXG_ERR_WORKSPACE;
     p.gbar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + kGridBarrierOff);
   }
-  cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, p, pl.ctas, stream);
+  cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, tmY, p, pl.ctas, stream);
   if (e == cudaSuccess && p.defer_reduce)
     e = mxg::launch_splitk_reduce(kind, pl.bn, p, pl.ctas, sm_count, stream);
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;

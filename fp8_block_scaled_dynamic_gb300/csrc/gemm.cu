@@ -61,7 +61,9 @@ struct Cfg {
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kBarBytes = 8 * (3 * kStages + 7) + 16;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+  // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
+  static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
   static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
   static constexpr int kSteps = 4 * KS;              // MMAs (K = 64 / 32) per stage
   static constexpr uint32_t kSfColsA = 8u * KS;      // 4 TMEM columns per scale atom
@@ -384,7 +386,7 @@ __device__ __forceinline__ void prefetch_x_share(const GemmParams &p) {
 template <int KIND, int BN, int KS>
 __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small kernels beside it
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   using C = Cfg<KIND, BN, KS>;
   constexpr int S = C::kStages;
   constexpr int CH = C::kChunk;
@@ -396,7 +398,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   const uint32_t sB = sA + S * C::kABytes;
   const uint32_t sSFA = sB + S * C::kBBytes;
   const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-  const uint32_t bars = sSFB + S * C::kSfbBytes;
+  const uint32_t sEpi = sSFB + S * C::kSfbBytes;
+  const uint32_t bars = sEpi + C::kEpiBytes;
   const uint32_t acc_full = bars + 8 * (2 * S);
   const uint32_t acc_empty = acc_full + 8;
   const uint32_t part_bar = acc_full + 16;
@@ -816,7 +819,44 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (lane == 0) mbar_arrive(acc_empty);
         released = true;
       };
-      if (whole && !p.swap) {
+      if (whole && !p.swap && KS == 1 && p.y_tma) {
+        // rows = tokens, columns = output channels; per 32-column chunk the
+        // warp's 32 x 32 bf16 box goes registers -> smem -> one TMA store
+        // (rows past M and columns past N are clipped by the tensor map)
+        const float sa = (KIND == 1 && ra < p.M) ? p.tok_scale[ra] : 1.0f;
+        const uint32_t ebuf = sEpi + (uint32_t)(warp - 2) * 4096u;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_chunk<32>(t_row + c * 32, v);
+          tmem_ld_wait();
+          const int n0 = cb0 + c * 32;
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            float f0 = __uint_as_float(v[2 * j]), f1 = __uint_as_float(v[2 * j + 1]);
+            if (KIND == 1) {
+              f0 = (f0 * sa) * p.chan_scale[min(n0 + 2 * j, p.N - 1)];
+              f1 = (f1 * sa) * p.chan_scale[min(n0 + 2 * j + 1, p.N - 1)];
+            }
+            w[j] = pack_bf16x2(f0, f1);
+          }
+          const uint32_t buf = ebuf + (uint32_t)(c & 1) * 2048u;
+          if (c >= 2) {  // the box written two chunks ago must have been read out
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(buf + lane * 64u + k * 16u, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, buf, n0, it.ta * kTileA + q * 32);
+            bulk_commit_group();
+          }
+        }
+      } else if (whole && !p.swap) {
         // rows = tokens, columns = output channels: each thread writes a row run
         const bool mvalid = ra < p.M;
         const float sa = (KIND == 1 && mvalid) ? p.tok_scale[ra] : 1.0f;
@@ -925,6 +965,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       if (!ok) break;
       ++i;
     }
+    if (KS == 1 && p.y_tma && lane == 0) bulk_wait_group_all();  // y stores complete
     if (threadIdx.x == 64) {
       trace_mark(p, kTrEpiDone);
       trace_set(p, kTrItems, (unsigned long long)i);
@@ -967,8 +1008,8 @@ __global__ void __launch_bounds__(kRedThreads) splitk_reduce_kernel(const GemmPa
 }
 
 template <int KIND, int BN, int KS>
-cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmParams &p, int ctas,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmY,
+                     const GemmParams &p, int ctas, cudaStream_t stream) {
   using C = Cfg<KIND, BN, KS>;
   auto kern = gemm_kernel<KIND, BN, KS>;
   static DeviceOnce once;  // per instantiation and device (a repeat sets the same value)
@@ -993,20 +1034,21 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmP
       cfg.numAttrs += 1;
     }
   }
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
 }
 
 // Full-tile kernels (BN = 256) take one K column per stage; split-K kernels two.
 template <int KIND>
-cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
+cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmY,
                         const GemmParams &p, int ctas, cudaStream_t stream) {
-  if (!p.splitk) return bn == 256 ? launch_t<KIND, 256, 1>(tmA, tmB, p, ctas, stream) : cudaErrorInvalidValue;
+  if (!p.splitk)
+    return bn == 256 ? launch_t<KIND, 256, 1>(tmA, tmB, tmY, p, ctas, stream) : cudaErrorInvalidValue;
   switch (bn) {
-    case 16: return launch_t<KIND, 16, 2>(tmA, tmB, p, ctas, stream);
-    case 32: return launch_t<KIND, 32, 2>(tmA, tmB, p, ctas, stream);
-    case 64: return launch_t<KIND, 64, 2>(tmA, tmB, p, ctas, stream);
-    case 128: return launch_t<KIND, 128, 2>(tmA, tmB, p, ctas, stream);
-    case 256: return launch_t<KIND, 256, 2>(tmA, tmB, p, ctas, stream);
+    case 16: return launch_t<KIND, 16, 2>(tmA, tmB, tmY, p, ctas, stream);
+    case 32: return launch_t<KIND, 32, 2>(tmA, tmB, tmY, p, ctas, stream);
+    case 64: return launch_t<KIND, 64, 2>(tmA, tmB, tmY, p, ctas, stream);
+    case 128: return launch_t<KIND, 128, 2>(tmA, tmB, tmY, p, ctas, stream);
+    case 256: return launch_t<KIND, 256, 2>(tmA, tmB, tmY, p, ctas, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1059,9 +1101,9 @@ cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm
 }
 
 cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmParams &p, int ctas, cudaStream_t stream) {
-  return kind == 0 ? launch_kind<0>(bn, tmA, tmB, p, ctas, stream)
-                   : launch_kind<1>(bn, tmA, tmB, p, ctas, stream);
+                        const CUtensorMap &tmY, const GemmParams &p, int ctas, cudaStream_t stream) {
+  return kind == 0 ? launch_kind<0>(bn, tmA, tmB, tmY, p, ctas, stream)
+                   : launch_kind<1>(bn, tmA, tmB, tmY, p, ctas, stream);
 }
 
 int gemm_stages(int kind, int bn, bool splitk) {

@@ -121,6 +121,7 @@ struct GemmParams {
   // activations x into the token tiles (b_tiles, T = BN rows) and their
   // 128x4-tile scales (sfB), then a grid barrier, then the GEMM; partial
   // tiles are summed after a second grid barrier by all CTAs (grid_reduce).
+  int y_tma;           // full tile, bf16 out: the epilogue stores y through tensor map tmY
   const uint16_t *x;
   long long ldx;
   int fuse_quant;
@@ -140,7 +141,7 @@ enum TracePoint {
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.
 cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        const GemmParams &p, int ctas, cudaStream_t stream);
+                        const CUtensorMap &tmY, const GemmParams &p, int ctas, cudaStream_t stream);
 
 // Split-K reduction of a GEMM launched with p.defer_reduce = 1 (the same
 // params, its grid size gemm_ctas); launched right after it on the stream.
