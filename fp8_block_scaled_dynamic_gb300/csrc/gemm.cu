@@ -60,7 +60,7 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (3 * kStages + 7) + 16;
+  static constexpr int kBarBytes = 8 * (3 * kStages + 8) + 16;
   // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
   static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
@@ -408,7 +408,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   const uint32_t mma_done = acc_full + 40;
   const uint32_t acts_ready = acc_full + 48;  // fused path: token tiles of every CTA written
   const uint32_t sf_bars = acc_full + 56;     // full tile: a stage's scales are in TMEM
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 7);
+  const uint32_t pull_bar = sf_bars + 8 * S;  // last-CTA split-K: the partial tiles are in smem
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 8);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
@@ -446,6 +447,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     mbar_init(mma_done, 1);
     mbar_init(acts_ready, 1);
     for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
+    mbar_init(pull_bar, 1);
     *abort_flag = 0;
     *decision = 0;
     *reduce_go = 0;
@@ -928,6 +930,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         // (in-kernel variant) the last CTA of the tile reduces the partials
         const size_t slot_elems = (size_t)BN * kTileA;
         float *tile_ws = publish_partial();
+        fence_proxy_async_global();  // the last CTA may read them with bulk copies
         release_acc();
         // the arrive (release, CTA scope) orders this thread's partial stores
         // before the leader's acquire-release counter increment (GPU scope)
@@ -955,8 +958,61 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (dec < 0) {
           ok = false;
         } else if (dec == 1) {
-          reduce_partials<KIND>(p, tile_ws, slot_elems, it.nseg, ncols, it.ta * kTileA, cb0,
-                                threadIdx.x - 64);
+          // The tile's last item in this CTA's range and nothing after it: the
+          // pipeline's shared memory is idle (the MMAs behind acc_full have
+          // consumed every stage), so the partial slots come in by bulk copies,
+          // one lane per slot, and are summed from smem.
+          uint32_t cur2 = cur;
+          Item nxt;
+          const bool more = next_item(p, cur2, nxt);
+          const uint32_t slot_bytes = (uint32_t)(slot_elems * sizeof(float));
+          if (!more && (size_t)it.nseg * slot_bytes <= (size_t)S * C::kStageBytes) {
+            if (warp == 2) {
+              fence_proxy_async_global();  // the slots were stored by other CTAs' generic stores
+              if (lane == 0) mbar_arrive_expect_tx(pull_bar, (uint32_t)it.nseg * slot_bytes);
+              __syncwarp();
+              if (lane < it.nseg)
+                bulk_load(sA + (uint32_t)lane * slot_bytes,
+                          reinterpret_cast<const uint8_t *>(tile_ws + (size_t)lane * slot_elems), slot_bytes,
+                          pull_bar, policy_evict_first());
+            }
+            ok = warp_wait(pull_bar, 0, ctl);
+            if (ok) {
+              const int tid = threadIdx.x - 64;
+              const int ngrp = ncols * (kTileA / 4);
+              const int row0 = it.ta * kTileA;
+              for (int g = tid; g < ngrp; g += 128) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sgi = 0; sgi < it.nseg; ++sgi) {
+                  const uint32_t a = sA + (uint32_t)sgi * slot_bytes + (uint32_t)g * 16u;
+                  const uint4 u = ld_shared_v4(a);
+                  acc.x += __uint_as_float(u.x);
+                  acc.y += __uint_as_float(u.y);
+                  acc.z += __uint_as_float(u.z);
+                  acc.w += __uint_as_float(u.w);
+                }
+                const int c = g / (kTileA / 4);
+                const int r = (g % (kTileA / 4)) * 4;
+                const int m = cb0 + c;    // token
+                const int n = row0 + r;   // output channel
+                float f[4] = {acc.x, acc.y, acc.z, acc.w};
+                if (KIND == 1) {
+                  const float sa = p.tok_scale[m];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
+                }
+                if (p.out_f32)
+                  *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
+                      make_float4(f[0], f[1], f[2], f[3]);
+                else
+                  *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
+                      make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+              }
+            }
+          } else {
+            reduce_partials<KIND>(p, tile_ws, slot_elems, it.nseg, ncols, it.ta * kTileA, cb0,
+                                  threadIdx.x - 64);
+          }
           if (threadIdx.x == 64) trace_mark(p, kTrReduced);
         }
       }
