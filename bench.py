@@ -39,6 +39,8 @@ import torch  # noqa: E402
 
 METRIC = "MXFP4 A4W4 / FP8 A8W8 GEMM TFLOPS & HBM GB/s vs GB300 roofline by M"
 FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 7900.0               # GB300 HBM3e, nominal
+DATASHEET_TFLOPS = {0: 13500.0, 1: 4500.0}  # GB300 dense FP4 / FP8 tensor, nominal
 
 
 def flush_l2(buf: torch.Tensor):
@@ -497,6 +499,16 @@ def run_ours(args, rank, world, local_rank):
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": round(pk, 1),
                 "unit": "TFLOP/s", "frac": round(achieved_tf / pk, 4),
                 "peak_note": f"{peak_src} bf16 {bf16} TFLOP/s x nominal {'fp4' if ratio == 6 else 'fp8'}/bf16 ratio {ratio}"}
+    if wl.bound == "hbm":
+        roof["nominal_peak"] = NOMINAL_HBM_GBS
+        roof["frac_of_nominal"] = round(achieved_gbs / NOMINAL_HBM_GBS, 4)
+    else:
+        kind = 0 if "e2m1" in wl.dtype else 1
+        loop = mx.mxg_mma_peak(kind, 256)
+        roof["mma_loop_peak"] = round(loop, 1)
+        roof["frac_of_mma_loop"] = round(achieved_tf / loop, 4)
+        roof["datasheet_peak"] = DATASHEET_TFLOPS[kind]
+        roof["frac_of_datasheet"] = round(achieved_tf / DATASHEET_TFLOPS[kind], 4)
     roof["traffic"] = traffic_record(args.workload)
     roof["kernel"] = wl.kernel_desc
     roof["kernel_ms"] = round(kms, 5)
@@ -684,6 +696,7 @@ def run_sweep(args, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     reps = max(3, min(args.steps, 20))
+    loop_peak = {k: mx.mxg_mma_peak(k, 256) for k in (0, 1)}
     for M in SWEEP_M:
         per = {}
         total_ms = 0.0
@@ -745,7 +758,9 @@ def run_sweep(args, rank, world, local_rank):
                         "frac": round(gbs / hbm, 4)}
             else:
                 roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": round(bf16 * ratio, 1),
-                        "unit": "TFLOP/s", "frac": round(tf / (bf16 * ratio), 4)}
+                        "unit": "TFLOP/s", "frac": round(tf / (bf16 * ratio), 4),
+                        "mma_loop_peak": round(loop_peak[kind], 1),
+                        "frac_of_mma_loop": round(tf / loop_peak[kind], 4)}
             per[g] = {"dtype": "e2m1 x e2m1" if kind == 0 else "e4m3 x e4m3", "N": N, "K": K,
                       "us": round(ms * 1e3, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
                       "roofline": roof,

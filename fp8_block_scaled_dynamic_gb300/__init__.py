@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
             L.fp8_gemm_ptpc.argtypes = [vp, vp, vp, vp, i, i, i, vp, i, i,
                                         ctypes.POINTER(GemmOpts), vp]
             L.fp8_gemm_ptpc.restype = i
+            L.mxg_mma_peak.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_double), vp]
+            L.mxg_mma_peak.restype = i
             L.mxg_query_status.argtypes = [vp, vp]
             L.mxg_query_status.restype = i
             L.mxg_status_string.argtypes = [i]
@@ -332,6 +334,14 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
     return out
+
+
+def mxg_mma_peak(kind: int, n: int = 256, iters: int = 20000, stream=None) -> float:
+    """TFLOP/s of the GEMMs' MMA instruction shape on operands resident in
+    shared memory (all SMs); synchronises the stream."""
+    out = ctypes.c_double(0.0)
+    _check("mxg_mma_peak", lib().mxg_mma_peak(kind, n, iters, ctypes.byref(out), _stream(stream)))
+    return float(out.value)
 
 
 def mxg_query_status(dev_status: torch.Tensor | None, stream=None) -> int:

@@ -522,6 +522,36 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, 
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
+mxg_status mxg_mma_peak(int kind, int n, int iters, double *tflops, mxg_stream_t stream) {
+  if ((kind != 0 && kind != 1) || (n != 128 && n != 256) || iters < 1 || iters > (1 << 22) || !tflops)
+    return MXG_ERR_INVALID_ARG;
+  int sm = 0;
+  mxg_status st = check_device(&sm);
+  if (st != MXG_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *status = nullptr;
+  if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) return MXG_ERR_CUDA;
+  cudaEvent_t a = nullptr, b = nullptr;
+  float ms = 0.0f;
+  bool ok = cudaMemsetAsync(status, 0, sizeof(int), s) == cudaSuccess &&
+            cudaEventCreate(&a) == cudaSuccess && cudaEventCreate(&b) == cudaSuccess &&
+            mxg::launch_mma_peak(kind, n, iters / 8 + 1, sm, status, s) == cudaSuccess &&  // warm-up
+            cudaEventRecord(a, s) == cudaSuccess &&
+            mxg::launch_mma_peak(kind, n, iters, sm, status, s) == cudaSuccess &&
+            cudaEventRecord(b, s) == cudaSuccess && cudaEventSynchronize(b) == cudaSuccess &&
+            cudaEventElapsedTime(&ms, a, b) == cudaSuccess;
+  int h = 0;
+  ok = ok && cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (a) cudaEventDestroy(a);
+  if (b) cudaEventDestroy(b);
+  cudaFree(status);
+  if (!ok) return MXG_ERR_CUDA;
+  if (h) return MXG_ERR_TIMEOUT;
+  const double k = kind == 0 ? 64.0 : 32.0;
+  *tflops = (double)sm * iters * 4.0 * 2.0 * 128.0 * n * k / (ms * 1e-3) / 1e12;
+  return MXG_OK;
+}
+
 mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return MXG_ERR_CUDA;

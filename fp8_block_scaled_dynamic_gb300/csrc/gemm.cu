@@ -1135,7 +1135,77 @@ size_t smem_kind(int bn, bool splitk) {
   }
 }
 
+// The tensor pipe's own rate for this GEMM's instruction shapes: one CTA per
+// SM, one thread issuing `iters` x 4 MMAs (M = 128, N = bn; K = 64 E2M1 with
+// block scales already in TMEM, or K = 32 E4M3) on operands resident in
+// shared memory (zeros: finite codes and scales), one TMEM accumulator.  The
+// final commit is waited on with a bound.
+template <int KIND>
+__global__ void __launch_bounds__(128) mma_peak_kernel(int iters, int bn, int *status,
+                                                       unsigned long long timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tslot;
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sA = base, sB = base + 16384, sSFA = sB + 32768, sSFB = sSFA + 1024;
+  for (uint32_t o = threadIdx.x * 16u; o < 16384u + 32768u + 3072u; o += 128u * 16u)
+    st_shared_v4(base + o, 0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();  // the zeros are read by the tensor pipe
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_addr(&tslot), 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (threadIdx.x == 0) {
+    const uint32_t idesc = KIND == 0 ? idesc_mxf4(128, bn) : idesc_f8(128, bn);
+    const uint32_t sfa_t = tmem + 256, sfb_t = tmem + 264;
+    if (KIND == 0) {
+      for (int a = 0; a < 2; ++a) tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + a * 512));
+      for (int j = 0; j < 2; ++j)
+        for (int a = 0; a < 2; ++a) tc_cp_sf(sfb_t + 8 * a + 4 * j, sdesc_sf_block(sSFB + j * 1024 + a * 512));
+    }
+    for (int it = 0; it < iters; ++it)
+      for (int s = 0; s < 4; ++s) {
+        if (KIND == 0) {
+          const uint32_t sel = (uint32_t)(s & 1) * 2u;
+          mma_mxf4(tmem, sdesc_kmajor_sw128(sA + 32 * s), sdesc_kmajor_sw128(sB + 32 * s),
+                   idesc_sf_ids(idesc, sel, sel), sfa_t + 4 * (s >> 1), sfb_t + 8 * (s >> 1), 1u);
+        } else {
+          mma_f8(tmem, sdesc_kmajor_sw128(sA + 32 * s), sdesc_kmajor_sw128(sB + 32 * s), idesc, 1u);
+        }
+      }
+    tc_commit(smem_addr(&bar));
+    drain_wait(smem_addr(&bar), 0, timeout_ns, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
+
+cudaError_t launch_mma_peak(int kind, int bn, int iters, int sm_count, int *status,
+                            cudaStream_t stream) {
+  const int smem = 200 * 1024;  // one CTA per SM
+  cudaError_t e = kind == 0
+                      ? cudaFuncSetAttribute(mma_peak_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                      : cudaFuncSetAttribute(mma_peak_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned long long tmo = 2000000000ull;
+  if (kind == 0)
+    mma_peak_kernel<0><<<sm_count, 128, smem, stream>>>(iters, bn, status, tmo);
+  else
+    mma_peak_kernel<1><<<sm_count, 128, smem, stream>>>(iters, bn, status, tmo);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream) {

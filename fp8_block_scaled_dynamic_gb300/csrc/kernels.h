@@ -148,6 +148,10 @@ cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensor
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream);
 
+// The tensor-pipe rate probe behind mxg_mma_peak: sm_count CTAs, one per SM.
+cudaError_t launch_mma_peak(int kind, int bn, int iters, int sm_count, int *status,
+                            cudaStream_t stream);
+
 // Pipeline stages a (kind, bn, variant) kernel uses, its dynamic shared
 // memory, and the 128-byte K columns one stage covers (p.kblocks counts
 // stages of that many columns).

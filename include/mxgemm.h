@@ -308,6 +308,16 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf,
  * it: MXG_OK, MXG_ERR_TIMEOUT (MXG_DEV_TIMEOUT set) or MXG_ERR_CUDA. */
 mxg_status mxg_query_status(int *dev_status, mxg_stream_t stream);
 
+/* Measurement utility (no counterpart on the pages): the rate of this
+ * library's tcgen05 MMA instruction shape with the operands already in shared
+ * memory -- the ceiling the GEMMs' main loops run against.  One CTA per SM,
+ * one thread issuing `iters` x 4 MMAs of M = 128, N = n (128 or 256), K = 64
+ * block-scaled E2M1 (kind 0, scales resident in TMEM) or K = 32 E4M3 (kind 1)
+ * into one TMEM accumulator; timed with CUDA events on `stream`, which it
+ * synchronises.  *tflops = dense TFLOP/s over all SMs.  It allocates (and
+ * frees) one int of device memory. */
+mxg_status mxg_mma_peak(int kind, int n, int iters, double *tflops, mxg_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *mxg_status_string(mxg_status s);
 

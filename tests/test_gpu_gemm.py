@@ -233,3 +233,11 @@ def test_ptpc_mlp_pair_sampled_rows(M):
     y = run_ptpc(xd, wd, "auto").cpu().numpy()
     ref, bound = oracle_ptpc(xd, wd, rows=rows)
     assert_gemm_close(y[rows], ref, bound, f"down M={M}")
+
+
+@pytest.mark.parametrize("kind,lo,hi", [(0, 1000.0, 20000.0), (1, 500.0, 10000.0)])
+def test_mma_loop_peak_is_plausible(kind, lo, hi):
+    """The measurement utility runs and lands between a tenth of and above the
+    nominal dense rate (13.5 PF/s E2M1, 4.5 PF/s E4M3 on GB300)."""
+    t = mx.mxg_mma_peak(kind, 256, iters=2000)
+    assert lo < t < hi, t
