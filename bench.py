@@ -189,6 +189,16 @@ class Workload:
         raise NotImplementedError
 
 
+# resident weight layout of every workload: "panel" (256-row panels, the
+# MXFP4 scales inside; one copy per full-tile stage) or "tiled" (128-row tiles)
+WEIGHTS = "panel"
+
+
+def weight_layout(mx):
+    """(quantizer layout, GEMM weights_tiled value) of the chosen layout."""
+    return (mx.PANEL, mx.W_PANEL) if WEIGHTS == "panel" else (mx.TILED, mx.W_TILED)
+
+
 class OprojChain(Workload):
     """A4W4 o_proj layers: fused dynamic MXFP4 activation quantization +
     block-scaled GEMM per layer."""
@@ -200,9 +210,10 @@ class OprojChain(Workload):
         self.n_layers = layers
         self.name = name
         self.w = []
+        layout, self.wt = weight_layout(mx)
         for s in w_seeds:
-            # resident weights in the GEMM's tile layout
-            wc, wsf = mx.mx_quantize_weight(synth.weight(N, K, seed=s).to(dev), layout=mx.TILED)
+            # resident weights in the layout the GEMM fetches by bulk copy
+            wc, wsf = mx.mx_quantize_weight(synth.weight(N, K, seed=s).to(dev), layout=layout)
             self.w.append((wc, wsf))
         # all layers' inputs / outputs in one pinned host and one device tensor,
         # so that the end-to-end step moves them with one copy each way
@@ -245,14 +256,14 @@ class OprojChain(Workload):
             wc, wsf = self.w[l]
             if self.fused:
                 out.append(("a4w4_fused", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
-                    wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_static=True, weights_tiled=True,
-                    splitk_reduce="grid")))
+                    wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_static=True, weights_tiled=self.wt,
+                    n=self.N, k=self.K, splitk_reduce="grid")))
                 continue
             out.append(("mx_quant", lambda l=l: mx.mx_quantize_act_tiled(self.x[l], self.T, codes=self.ac[l],
                                                                          sf=self.asf[l])))
             out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
                 wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws,
-                weights_static=True, weights_tiled=True, act_tile_rows=self.T, m=self.M)))
+                weights_static=True, weights_tiled=self.wt, act_tile_rows=self.T, m=self.M, n=self.N, k=self.K)))
         return out
 
     def e2e_step(self):
@@ -260,8 +271,8 @@ class OprojChain(Workload):
         self.x.copy_(self.x_host, non_blocking=True)
         for l in range(self.n_layers):
             wc, wsf = self.w[l]
-            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_tiled=True,
-                            weights_static=True)
+            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_tiled=self.wt,
+                            weights_static=True, n=self.N, k=self.K)
         self.y_host.copy_(self.y, non_blocking=True)
 
 
@@ -272,10 +283,12 @@ class MlpFp8(Workload):
         self.mx, self.dev, self.M = mx, dev, M
         self.name = name
         I2, H = 2 * synth.MLP_I, 7168
+        self.H, self.I = H, synth.MLP_I
+        layout, self.wt = weight_layout(mx)
         self.qg, self.sg = mx.fp8_quantize_weight(synth.weight(I2, H, seed=synth.SEED_CFG3_GATE_UP).to(dev),
-                                                  layout=mx.TILED)
+                                                  layout=layout)
         self.qd, self.sd = mx.fp8_quantize_weight(synth.weight(H, synth.MLP_I, seed=synth.SEED_CFG3_DOWN).to(dev),
-                                                  layout=mx.TILED)
+                                                  layout=layout)
         self.xg_host = synth.activation(M, H, seed=synth.act_seed(3, 0, 0)).pin_memory()
         self.xd_host = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1)).pin_memory()
         self.xg, self.xd = self.xg_host.to(dev), self.xd_host.to(dev)
@@ -313,12 +326,12 @@ class MlpFp8(Workload):
         mx = self.mx
         return [("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xg, self.Tg, q=self.qa_g, scale=self.sa_g)),
                 ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg,
-                                                          ws=self.ws, weights_static=True, weights_tiled=True,
-                                                          act_tile_rows=self.Tg)),
+                                                          ws=self.ws, weights_static=True, weights_tiled=self.wt,
+                                                          act_tile_rows=self.Tg, k=self.H)),
                 ("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xd, self.Td, q=self.qa_d, scale=self.sa_d)),
                 ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd,
-                                                       ws=self.ws, weights_static=True, weights_tiled=True,
-                                                       act_tile_rows=self.Td))]
+                                                       ws=self.ws, weights_static=True, weights_tiled=self.wt,
+                                                       act_tile_rows=self.Td, k=self.I))]
 
     def e2e_step(self):
         mx = self.mx
@@ -533,6 +546,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded bf16 N(0,1) activations with 0.1% x50 outliers, N(0,0.02) weights)",
         "config": {"workload": wl.name, "key": args.workload, "l2": "flushed between steps (256 MiB write + read back, outside the timed interval)",
                    "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
+                   "weights": f"{WEIGHTS} layout, resident in HBM",
                    "dispatch": {k: wl.plan[k] for k in ("variant", "bn", "ctas", "seg_max")}},
         "tflops": round(world * wl.flops_per_step / (ms * 1e-3) / 1e12, 2),
         "roofline": roof,
@@ -694,15 +708,16 @@ def run_sweep(args, rank, world, local_rank):
     hbm, bf16, peak_src = load_peaks()
     H, I2, I, N_O, K_O = 7168, 2 * synth.MLP_I, synth.MLP_I, synth.OPROJ_N, synth.OPROJ_K
     L = 5
-    # resident weights (tile layout); bf16 originals freed after conversion
+    # resident weights (panel or tile layout); bf16 originals freed after conversion
+    layout, wt = weight_layout(mx)
     w = {"gate_up": [], "down": [], "o_proj": []}
     for l in range(L):
         w["gate_up"].append(mx.fp8_quantize_weight(
-            synth.weight(I2, H, seed=synth.seed_cfg4("gate_up", l)).to(dev), layout=mx.TILED))
+            synth.weight(I2, H, seed=synth.seed_cfg4("gate_up", l)).to(dev), layout=layout))
         w["down"].append(mx.fp8_quantize_weight(
-            synth.weight(H, I, seed=synth.seed_cfg4("down", l)).to(dev), layout=mx.TILED))
+            synth.weight(H, I, seed=synth.seed_cfg4("down", l)).to(dev), layout=layout))
         w["o_proj"].append(mx.mx_quantize_weight(
-            synth.weight(N_O, K_O, seed=synth.seed_cfg4("o_proj", l)).to(dev), layout=mx.TILED))
+            synth.weight(N_O, K_O, seed=synth.seed_cfg4("o_proj", l)).to(dev), layout=layout))
     # activations for the largest M (smaller M take the leading rows)
     MX = max(SWEEP_M)
     xs = {"gate_up": synth.activation(MX, H, seed=synth.act_seed(4, 0, 0)).to(dev),
@@ -727,21 +742,21 @@ def run_sweep(args, rank, world, local_rank):
                 qa = torch.empty(mx.mxg_act_tiled_bytes(1, M, K, T), dtype=torch.uint8, device=dev)
                 sa = torch.empty(M, dtype=torch.float32, device=dev)
 
-                def layer(l, x=x, y=y, ws=ws, qa=qa, sa=sa, T=T, g=g):
+                def layer(l, x=x, y=y, ws=ws, qa=qa, sa=sa, T=T, g=g, K=K):
                     mx.fp8_quantize_act_tiled(x, T, q=qa, scale=sa)
                     qw, sw = w[g][l]
                     mx.fp8_gemm_ptpc(qa, sa, qw, sw, out=y, ws=ws, weights_static=True,
-                                     weights_tiled=True, act_tile_rows=T)
+                                     weights_tiled=wt, act_tile_rows=T, k=K)
                 gbytes = ptpc_gemm_bytes(M, N, K) + fp8_quant_bytes(M, K)
             else:
                 ac = torch.empty(mx.mxg_act_tiled_bytes(0, M, K, T), dtype=torch.uint8, device=dev)
                 asf = torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev)
 
-                def layer(l, x=x, y=y, ws=ws, ac=ac, asf=asf, T=T, M=M, g=g):
+                def layer(l, x=x, y=y, ws=ws, ac=ac, asf=asf, T=T, M=M, g=g, N=N, K=K):
                     mx.mx_quantize_act_tiled(x, T, codes=ac, sf=asf)
                     wc, wsf = w[g][l]
                     mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out=y, ws=ws, weights_static=True,
-                                    weights_tiled=True, act_tile_rows=T, m=M)
+                                    weights_tiled=wt, act_tile_rows=T, m=M, n=N, k=K)
                 gbytes = a4w4_gemm_bytes(M, N, K) + mx_quant_bytes(M, K)
             with torch.cuda.stream(stream):
                 for l in range(L):
@@ -803,11 +818,15 @@ def main():
     ap.add_argument("--workload", default="oproj_decode",
                     choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192",
                              "sweep"])
+    ap.add_argument("--weights", default="panel", choices=["panel", "tiled"],
+                    help="resident weight layout: 256-row panels (scales inside) or 128-row tiles")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--min-warmup-s", type=float, default=0.5,
                     help="keep warming up at least this long so clocks settle (0 under a profiler)")
     args = ap.parse_args()
+    global WEIGHTS
+    WEIGHTS = args.weights
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

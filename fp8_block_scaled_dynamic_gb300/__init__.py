@@ -28,8 +28,11 @@ MXG_OK = 0
 STATUS_NAMES = {0: "MXG_OK", 1: "MXG_ERR_INVALID_ARG", 2: "MXG_ERR_UNSUPPORTED_SHAPE",
                 3: "MXG_ERR_MISALIGNED", 4: "MXG_ERR_UNSUPPORTED_DEVICE", 5: "MXG_ERR_CUDA",
                 6: "MXG_ERR_TIMEOUT", 7: "MXG_ERR_WORKSPACE"}
-SF_ROWMAJOR, SF_SWIZZLED, TILED = 0, 1, 2
+SF_ROWMAJOR, SF_SWIZZLED, TILED, PANEL = 0, 1, 2, 3
 TILE_BYTES = 16384
+PANEL_ROWS = 256
+# weights_tiled values of the GEMM calls: the weight codes' layout
+W_ROWMAJOR, W_TILED, W_PANEL = 0, 1, 2
 OUT_BF16, OUT_F32 = 0, 1
 VARIANTS = {"auto": 0, "full": 1, "splitk": 2}
 KIND_A4W4, KIND_PTPC = 0, 1
@@ -91,6 +94,8 @@ def lib() -> ctypes.CDLL:
             L.fp8_quantize_act.restype = i
             L.fp8_quantize_weight.argtypes = [vp, i, i, i, vp, vp, i, vp]
             L.fp8_quantize_weight.restype = i
+            L.mxg_weight_bytes.argtypes = [i, i, i, i]
+            L.mxg_weight_bytes.restype = sz
             L.mxg_act_tiled_bytes.argtypes = [i, i, i, i]
             L.mxg_act_tiled_bytes.restype = sz
             L.mx_quantize_act_tiled.argtypes = [vp, i, i, i, i, vp, vp, vp]
@@ -134,6 +139,10 @@ def mxg_sf_bytes(rows: int, K: int, layout: int = SF_SWIZZLED) -> int:
     return int(lib().mxg_sf_bytes(rows, K, layout))
 
 
+def mxg_weight_bytes(kind: int, N: int, K: int, layout: int) -> int:
+    return int(lib().mxg_weight_bytes(kind, N, K, layout))
+
+
 def mxg_plan_gemm(kind: int, M: int, N: int, K: int, sm_count: int,
                   variant: str = "auto", ctas: int = 0) -> dict:
     """Pure host dispatcher: the variant/tile/grid/workspace of a GEMM."""
@@ -171,10 +180,20 @@ def mx_quantize_weight(w: torch.Tensor, layout: int = SF_SWIZZLED, codes=None, s
     """Offline MXFP4 weight conversion: w (N, K) bf16 -> (codes u8, sf u8).
     layout SF_ROWMAJOR: codes (N, K/2), sf (N, K/32); SF_SWIZZLED: codes
     (N, K/2), sf flat 128x4 tiles; TILED: codes in 16 KiB weight tiles
-    (shape (N, K/2) bytes, tile-ordered), sf flat 128x4 tiles."""
+    (shape (N, K/2) bytes, tile-ordered), sf flat 128x4 tiles; PANEL: codes
+    flat (mxg_weight_bytes bytes) in 256-row panels holding the scales too,
+    sf None."""
     _need(w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1,
           "w must be a CUDA bf16 (N, K) tensor with unit inner stride")
     N, K = w.shape
+    if layout == PANEL:
+        if codes is None:
+            nbytes = mxg_weight_bytes(KIND_A4W4, N, K, PANEL)
+            _need(nbytes > 0, "the panel layout needs K % 256 == 0")
+            codes = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+        _check("mx_quantize_weight", lib().mx_quantize_weight(
+            _ptr(w), N, K, w.stride(0), _ptr(codes), None, layout, _stream(stream)))
+        return codes, None
     if codes is None:
         codes = torch.empty(N, K // 2, dtype=torch.uint8, device=w.device)
     if sf is None:
@@ -202,12 +221,14 @@ def mx_quantize_act(x: torch.Tensor, codes=None, sf=None, stream=None):
 
 def fp8_quantize_weight(w: torch.Tensor, layout: int = SF_ROWMAJOR, q=None, scale=None, stream=None):
     """Per-output-channel E4M3 weight conversion: w (N, K) bf16 -> (q (N, K)
-    bytes, row-major or in 16 KiB weight tiles (layout TILED), scale (N,) f32)."""
+    bytes, row-major or in 16 KiB weight tiles (layout TILED), or flat in
+    256-row panels (layout PANEL, mxg_weight_bytes bytes), scale (N,) f32)."""
     _need(w.is_cuda and w.dtype == torch.bfloat16 and w.dim() == 2 and w.stride(1) == 1,
           "w must be a CUDA bf16 (N, K) tensor with unit inner stride")
     N, K = w.shape
     if q is None:
-        q = torch.empty(N, K, dtype=torch.uint8, device=w.device)
+        q = (torch.empty(mxg_weight_bytes(KIND_PTPC, N, K, PANEL), dtype=torch.uint8, device=w.device)
+             if layout == PANEL else torch.empty(N, K, dtype=torch.uint8, device=w.device))
     if scale is None:
         scale = torch.empty(N, dtype=torch.float32, device=w.device)
     _check("fp8_quantize_weight", lib().fp8_quantize_weight(
@@ -284,18 +305,24 @@ def _out(out, M, N, out_f32, device):
     return out
 
 
-def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_sf=None, x=None,
+def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf, *, a_codes=None, a_sf=None, x=None,
                  out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
-                 weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                 act_tile_rows: int = 0, m: int = 0, splitk_reduce: str = "default", stream=None):
+                 weights_static: bool = False, trace=None, weights_tiled: int = W_ROWMAJOR,
+                 act_tile_rows: int = 0, m: int = 0, n: int = 0, k: int = 0,
+                 splitk_reduce: str = "default", stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
     x (M, K) bf16 (quantized inside the call).  w_sf must be in the 128x4
-    tiles; w_codes row-major, or in weight tiles with weights_tiled=True.
-    With act_tile_rows, a_codes is flat in the activation tile layout and
-    m gives M."""
-    N, K2 = w_codes.shape
-    K = 2 * K2
+    tiles; w_codes row-major, or in weight tiles with weights_tiled=W_TILED
+    (or True); with weights_tiled=W_PANEL w_codes is flat in 256-row panels
+    (scales inside, w_sf None) and n, k give N, K.  With act_tile_rows,
+    a_codes is flat in the activation tile layout and m gives M."""
+    if w_codes.dim() == 1:
+        _need(n > 0 and k > 0, "flat weight codes need n and k")
+        N, K = n, k
+    else:
+        N, K2 = w_codes.shape
+        K = 2 * K2
     fused = a_codes is None
     if fused:
         _need(x is not None and x.dtype == torch.bfloat16 and x.stride(1) == 1, "x (M, K) bf16 needed")
@@ -318,13 +345,21 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf: torch.Tensor, *, a_codes=None, a_s
 def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torch.Tensor, *,
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                   ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
-                  weights_static: bool = False, trace=None, weights_tiled: bool = False,
-                  act_tile_rows: int = 0, splitk_reduce: str = "default", stream=None):
+                  weights_static: bool = False, trace=None, weights_tiled: int = W_ROWMAJOR,
+                  act_tile_rows: int = 0, k: int = 0, splitk_reduce: str = "default", stream=None):
     """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM; qw
-    row-major, or in weight tiles with weights_tiled=True; qa row-major, or
-    flat in the activation tile layout with act_tile_rows (M = len(sa))."""
+    row-major, or in weight tiles with weights_tiled=W_TILED (or True), or
+    flat in 256-row panels with weights_tiled=W_PANEL (k gives K); qa
+    row-major, or flat in the activation tile layout with act_tile_rows
+    (M = len(sa), N = len(sw))."""
     M = sa.numel()
-    N, K = qw.shape
+    N = sw.numel()
+    if qw.dim() == 1:
+        _need(k > 0, "flat weight bytes need k")
+        K = k
+    else:
+        _need(qw.shape[0] == N, "qw rows and len(sw) differ")
+        K = qw.shape[1]
     out = _out(out, M, N, out_f32, qa.device)
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)

@@ -230,7 +230,11 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   const bool swap = pl.variant == MXG_VARIANT_SPLITK;
   const uint64_t row_bytes = kind == 0 ? (uint64_t)K / 2 : (uint64_t)K;
   const bool w_tiled = opts && opts->weights_tiled;
+  const bool w_panels = opts && opts->weights_tiled == 2;
+  if (opts && (opts->weights_tiled < 0 || opts->weights_tiled > 2)) return MXG_ERR_INVALID_ARG;
   if (w_tiled && (row_bytes % 128 != 0 || N % 128 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
+  // a full-tile GEMM takes a whole 256-row panel as its B tile
+  if (w_panels && !swap && pl.bn != mxg::kPanelRows) return MXG_ERR_UNSUPPORTED_SHAPE;
   if (act_tile_rows && act_tile_rows != plan_act_tile_rows(pl)) return MXG_ERR_INVALID_ARG;
   if (act_tile_rows && row_bytes % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   CUtensorMap tmA, tmB, tmY;
@@ -285,8 +289,9 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
       p.a_tiles = op.w;
     } else {
       p.b_tiles = op.w;
-      p.b_tile_rows = 128;
+      p.b_tile_rows = w_panels ? mxg::kPanelRows : 128;
     }
+    p.w_panels = w_panels ? 1 : 0;
   }
   if (act_tile_rows) {
     if (swap) {
@@ -342,8 +347,22 @@ extern "C" {
 size_t mxg_sf_bytes(int rows, int K, mxg_sf_layout layout) {
   if (rows < 1 || K < 32) return 0;
   const size_t G = (size_t)K / 32;
-  if (layout == MXG_SF_SWIZZLED) return (size_t)((rows + 127) / 128) * 128u * G;
+  if (layout == MXG_PANEL) return 0;  // the scales live inside the panels
+  if (layout == MXG_SF_SWIZZLED || layout == MXG_TILED) return (size_t)((rows + 127) / 128) * 128u * G;
   return (size_t)rows * G;
+}
+
+size_t mxg_weight_bytes(int kind, int N, int K, mxg_sf_layout layout) {
+  if ((kind != 0 && kind != 1) || N < 1 || K < 1) return 0;
+  const size_t row_bytes = kind == 0 ? (size_t)K / 2 : (size_t)K;
+  if (layout == MXG_PANEL) {
+    if (row_bytes % 128 != 0) return 0;
+    return (size_t)((N + mxg::kPanelRows - 1) / mxg::kPanelRows) * (row_bytes / 128) *
+           (size_t)(kind == 0 ? mxg::kMxPanelBytes : mxg::kF8PanelBytes);
+  }
+  if (layout == MXG_SF_ROWMAJOR || layout == MXG_SF_SWIZZLED || layout == MXG_TILED)
+    return (size_t)N * row_bytes;
+  return 0;
 }
 
 mxg_status mxg_plan_gemm(int kind, int M, int N, int K, int sm_count, const mxg_gemm_opts *opts,
@@ -367,16 +386,20 @@ mxg_status mx_quantize_rows(const void *w_bf16, int N, int K, int ldw, uint8_t *
                             mxg_sf_layout layout, bool act, mxg_stream_t stream) {
   mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
   if (st != MXG_OK) return st;
-  if (!codes || !sf ||
-      (layout != MXG_SF_ROWMAJOR && layout != MXG_SF_SWIZZLED && layout != MXG_TILED))
+  const bool panel = layout == MXG_PANEL;
+  if (!codes || (!sf && !panel) ||
+      (layout != MXG_SF_ROWMAJOR && layout != MXG_SF_SWIZZLED && layout != MXG_TILED && !panel))
     return MXG_ERR_INVALID_ARG;
   if (layout == MXG_TILED && (N % 128 != 0 || K % 256 != 0)) return MXG_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(codes) || !aligned16(sf)) return MXG_ERR_MISALIGNED;
+  if (panel && K % 256 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(codes) || (!panel && !aligned16(sf))) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
   cudaError_t e = mxg::launch_mx_quant(w_bf16, ldw, N, K, codes, sf, layout != MXG_SF_ROWMAJOR,
-                                       layout == MXG_TILED ? 128 : 0, act, sm,
-                                       reinterpret_cast<cudaStream_t>(stream));
+                                       panel                 ? mxg::kPanelLayout
+                                       : layout == MXG_TILED ? 128
+                                                             : 0,
+                                       act, sm, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 }  // namespace
@@ -440,13 +463,15 @@ mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_
                                mxg_sf_layout layout, mxg_stream_t stream) {
   mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
   if (st != MXG_OK) return st;
-  if (!q || !scale || (layout != MXG_SF_ROWMAJOR && layout != MXG_TILED)) return MXG_ERR_INVALID_ARG;
+  if (!q || !scale || (layout != MXG_SF_ROWMAJOR && layout != MXG_TILED && layout != MXG_PANEL))
+    return MXG_ERR_INVALID_ARG;
   if (layout == MXG_TILED && N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(q) || !aligned16(scale)) return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  cudaError_t e = mxg::launch_fp8_quant(w_bf16, ldw, N, K, q, scale, layout == MXG_TILED ? 128 : 0, false,
-                                        sm, reinterpret_cast<cudaStream_t>(stream));
+  const int tile_rows = layout == MXG_PANEL ? mxg::kPanelLayout : layout == MXG_TILED ? 128 : 0;
+  cudaError_t e = mxg::launch_fp8_quant(w_bf16, ldw, N, K, q, scale, tile_rows, false, sm,
+                                        reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 
@@ -456,7 +481,9 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
                         mxg_stream_t stream) {
   mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, opts);
   if (st != MXG_OK) return st;
-  if (!w_codes || !w_sf) return MXG_ERR_INVALID_ARG;
+  // weight panels carry their scales; w_sf is then unused (may be NULL)
+  const bool w_panels = opts && opts->weights_tiled == 2;
+  if (!w_codes || (!w_sf && !w_panels)) return MXG_ERR_INVALID_ARG;
   const bool fused = a_codes == nullptr;
   if (fused) {
     if (!x_bf16 || a_sf) return MXG_ERR_INVALID_ARG;
@@ -464,7 +491,7 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
   } else if (!a_sf) {
     return MXG_ERR_INVALID_ARG;
   }
-  if (!aligned16(w_codes) || !aligned16(w_sf) || (a_codes && (!aligned16(a_codes) || !aligned16(a_sf))))
+  if (!aligned16(w_codes) || (w_sf && !aligned16(w_sf)) || (a_codes && (!aligned16(a_codes) || !aligned16(a_sf))))
     return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
@@ -637,7 +664,7 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, con
   opts.variant = MXG_VARIANT_AUTO;
   opts.workspace = scratch;
   opts.ws_bytes = MXG_NOALLOC_SCRATCH_BYTES;
-  opts.weights_tiled = weights_tiled ? 1 : 0;
+  opts.weights_tiled = weights_tiled;
   return mx_gemm_a4w4(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype, &opts,
                       stream);
 }

@@ -58,6 +58,8 @@ struct Cfg {
   static constexpr int kSfaBytes = KIND == 0 ? 1024 * KS : 0;  // 2 scale atoms per column
   static constexpr int kSfbBytes = KIND == 0 ? 1024 * KS * kSfBlocksB : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  // one column of a 256-row weight panel: codes, then (E2M1) the 2 x 2 scale atoms
+  static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kBarBytes = 8 * (3 * kStages + 8) + 16;
@@ -394,11 +396,15 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t sA = base;
-  const uint32_t sB = sA + S * C::kABytes;
-  const uint32_t sSFA = sB + S * C::kBBytes;
-  const uint32_t sSFB = sSFA + S * C::kSfaBytes;
-  const uint32_t sEpi = sSFB + S * C::kSfbBytes;
+  // Stage s is one block of kStageBytes: A codes, B codes, B scales, A scales
+  // (every part 1024-byte aligned; an operand's scales follow its codes so
+  // that a weight panel -- codes, then scales -- lands with one copy).
+  const uint32_t sA = base;  // the whole pipeline region starts here
+  auto a_smem = [&](int st) { return sA + (uint32_t)st * C::kStageBytes; };
+  auto b_smem = [&](int st) { return a_smem(st) + C::kABytes; };
+  auto sfb_smem = [&](int st) { return b_smem(st) + C::kBBytes; };
+  auto sfa_smem = [&](int st) { return sfb_smem(st) + C::kSfbBytes; };
+  const uint32_t sEpi = sA + S * C::kStageBytes;
   const uint32_t bars = sEpi + C::kEpiBytes;
   const uint32_t acc_full = bars + 8 * (2 * S);
   const uint32_t acc_empty = acc_full + 8;
@@ -485,7 +491,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (KIND == 0) {
           const int rb0 = (it.tb * BN) / 128;
           const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-          bytes += (uint32_t)(natoms_of(kb) * 512 * (1 + nblk));
+          // a weight panel as B brings the scales of both halves, padding included
+          const int nblk_in = (p.w_panels && !p.swap) ? C::kSfBlocksB : nblk;
+          bytes += (uint32_t)(natoms_of(kb) * 512 * (1 + nblk_in));
         }
         return bytes;
       };
@@ -503,51 +511,82 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         const int nc = ncol_of(kb);
         const int rb0 = (it.tb * BN) / 128;
         const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-        if (want_a) {
+        // weight panels (256 rows: the codes, then the scales of both 128-row
+        // halves, per 128-byte column): split-K takes one half as its A tile
+        // (codes and scales one copy each per column); the full tile takes a
+        // whole panel as its B tile -- codes and scales in one copy
+        const bool a_pan = p.w_panels && p.swap;
+        const bool b_pan = p.w_panels && !p.swap;
+        if (want_a && a_pan) {
+          const uint8_t *blk0 = p.a_tiles + ((size_t)(it.ta >> 1) * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes;
+          const int h = it.ta & 1;
+          if (i < nc) {
+            bulk_load(a_smem(stage) + i * C::kAColBytes, blk0 + (size_t)i * C::kPanelBytes + h * 16384, 16384,
+                      fb, polA);
+            return;
+          }
+          i -= nc;
+          if (KIND == 0) {
+            if (i < nc) {
+              bulk_load(sfa_smem(stage) + i * 1024, blk0 + (size_t)i * C::kPanelBytes + 32768 + h * 1024, 1024,
+                        fb, polA);
+              return;
+            }
+            i -= nc;
+          }
+        } else if (want_a) {
           const int na = p.a_tiles ? 1 : nc;
           if (i < na) {
             if (p.a_tiles)
-              bulk_load(sA + stage * C::kABytes,
+              bulk_load(a_smem(stage),
                         p.a_tiles + ((size_t)it.ta * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kAColBytes,
                         (uint32_t)nc * C::kAColBytes, fb, polA);
             else
-              tma_load_2d(sA + stage * C::kABytes + i * C::kAColBytes, &tmA, (kb * KS + i) * kRowBytes,
+              tma_load_2d(a_smem(stage) + i * C::kAColBytes, &tmA, (kb * KS + i) * kRowBytes,
                           it.ta * kTileA, fb, polA);
             return;
           }
           i -= na;
           if (KIND == 0) {
             if (i == 0) {
-              bulk_load(sSFA + stage * C::kSfaBytes, p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
+              bulk_load(sfa_smem(stage), p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
                         natoms_of(kb) * 512, fb, polA);
               return;
             }
             i -= 1;
           }
         }
-        if (want_b) {
+        if (want_b && b_pan) {  // BN == 256, one column per stage
+          if (i == 0)
+            bulk_load(b_smem(stage),
+                      p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes,
+                      (uint32_t)C::kPanelBytes, fb, polB);
+        } else if (want_b) {
           const bool tok = p.b_tiles && p.b_tile_rows == BN;
           const int nb = tok ? 1 : p.b_tiles ? nc * (BN >= 128 ? BN / 128 : 1) : nc;
           if (i < nb) {
             if (tok) {
-              bulk_load(sB + stage * C::kBBytes,
+              bulk_load(b_smem(stage),
                         p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kBColBytes,
                         (uint32_t)nc * C::kBColBytes, fb, polB);
             } else if (p.b_tiles) {  // BN >= 128 here (the dispatcher's weight-tile case)
               constexpr int kRT = BN >= 128 ? BN / 128 : 1;
               const int j = i / kRT, r = i % kRT;
-              bulk_load(sB + stage * C::kBBytes + j * C::kBColBytes + r * 16384,
-                        p.b_tiles + ((size_t)(it.tb * kRT + r) * p.kc_per_row + (size_t)kb * KS + j) * 16384u,
+              // a row tile past the last weight row (N % BN != 0) re-reads the last
+              // tile: its rows only feed output columns past N, which are not stored
+              const int rt = min(it.tb * kRT + r, (p.rowsB + 127) / 128 - 1);
+              bulk_load(b_smem(stage) + j * C::kBColBytes + r * 16384,
+                        p.b_tiles + ((size_t)rt * p.kc_per_row + (size_t)kb * KS + j) * 16384u,
                         16384, fb, polB);
             } else {
-              tma_load_2d(sB + stage * C::kBBytes + i * C::kBColBytes, &tmB, (kb * KS + i) * kRowBytes,
+              tma_load_2d(b_smem(stage) + i * C::kBColBytes, &tmB, (kb * KS + i) * kRowBytes,
                           it.tb * BN, fb, polB);
             }
             return;
           }
           i -= nb;
           if (KIND == 0 && i < nblk)
-            bulk_load(sSFB + stage * C::kSfbBytes + i * (1024 * KS),
+            bulk_load(sfb_smem(stage) + i * (1024 * KS),
                       p.sfB + ((size_t)(rb0 + i) * p.G4 + 2 * KS * kb) * 512u, natoms_of(kb) * 512, fb, polB);
         }
       };
@@ -676,8 +715,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           }
           if (i == 0 && kb == it.kb0) trace_mark(p, kTrFirstFull);
           tc_fence_after();
-          const uint32_t a0 = sA + stage * C::kABytes;
-          const uint32_t b0 = sB + stage * C::kBBytes;
+          const uint32_t a0 = a_smem(stage);
+          const uint32_t b0 = b_smem(stage);
           // K step s of the stage: column s / 4, 32 bytes per step within it
           auto a_desc = [&](int s) {
             return sdesc_kmajor_sw128(a0 + (uint32_t)(s >> 2) * C::kAColBytes + 32u * (s & 3));
@@ -694,11 +733,11 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             const uint32_t sfb_t = sfa_t + C::kSfColsA;
             if (!kEpiScales) {
               for (int a = 0; a < natoms; ++a)
-                tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sSFA + stage * C::kSfaBytes + a * 512));
+                tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sfa_smem(stage) + a * 512));
               for (int j = 0; j < nblk; ++j)
                 for (int a = 0; a < natoms; ++a)
                   tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
-                           sdesc_sf_block(sSFB + stage * C::kSfbBytes + j * (1024 * KS) + a * 512));
+                           sdesc_sf_block(sfb_smem(stage) + j * (1024 * KS) + a * 512));
             }
             const int nk = min(C::kSteps, (p.K - kb * 256 * KS) / 64);
             for (int s = 0; s < nk; ++s) {
@@ -772,11 +811,11 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
           const uint32_t sfb_col = sfa_col + C::kSfColsA;
           for (int a = 0; a < natoms; ++a)
-            tmem_st4(sfa_col + 4 * a, ld_shared_v4(sSFA + st * C::kSfaBytes + a * 512 + lane * 16));
+            tmem_st4(sfa_col + 4 * a, ld_shared_v4(sfa_smem(st) + a * 512 + lane * 16));
           for (int j = 0; j < nblk; ++j)
             for (int a = 0; a < natoms; ++a)
               tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
-                       ld_shared_v4(sSFB + st * C::kSfbBytes + j * 1024 + a * 512 + lane * 16));
+                       ld_shared_v4(sfb_smem(st) + j * 1024 + a * 512 + lane * 16));
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();

@@ -73,8 +73,14 @@ inline cudaError_t prefer_shared_carveout(Kernel *kern) {
   return e;
 }
 
-// tile_rows: 0 = row-major codes / bytes, else the tile layout with tiles of
-// that many rows (128 for weights, the GEMM's token tile for activations).
+// tile_rows: 0 = row-major codes / bytes, kPanelLayout = the weight panel
+// layout (256-row panels, MXFP4 scales inside them; rows padded to a multiple
+// of 256 with zero codes), else the tile layout with tiles of that many rows
+// (128 for weights, the GEMM's token tile for activations).
+constexpr int kPanelLayout = -1;
+constexpr int kPanelRows = 256;
+constexpr int kMxPanelBytes = 256 * 128 + 2048;  // per 128-byte column
+constexpr int kF8PanelBytes = 256 * 128;
 // act: the input is an activation; the next kernel may launch at once.  For
 // weights (act = false) no later kernel starts before this one has finished.
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
@@ -112,6 +118,8 @@ struct GemmParams {
   const uint8_t *a_tiles;  // non-null: the MMA-A operand in the weight tile layout (bulk copies)
   const uint8_t *b_tiles;  // non-null: the MMA-B operand in the tile layout, b_tile_rows rows
   int b_tile_rows;         //   per tile: 128 (weights, full-tile mode) or BN (activations)
+  int w_panels;            // the weight operand (a_tiles when swapped, else b_tiles) is in
+                           //   256-row panels with their scales appended (MXG_PANEL)
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
                            //          the last CTA of each tile

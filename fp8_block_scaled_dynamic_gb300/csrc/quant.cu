@@ -32,7 +32,9 @@ constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in fligh
 // grid: x = chunk groups along the row, y = rows (grid-stride).
 // rows_iter >= rows: rows in [rows, rows_iter) are padding (swizzled layout
 // only) -- their scales are written as 0 and no codes are stored.
-// tile_rows: 0 = row-major codes, else the tile layout with that tile height.
+// tile_rows: 0 = row-major codes, kPanelLayout = weight panels (codes and
+// scales; padding rows get zero codes), else the tile layout with that tile
+// height.
 template <bool kSwizzled>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
                                                               long long ldx, int rows,
@@ -75,16 +77,20 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       const bool in_row = cc[i] < cpr;
       uint32_t scode;
       const uint32_t packed = mx_encode_chunk(v[i], scode);
-      if (real_row && in_row) {
-        const size_t off = tile_rows ? tiled_offset(r, cc[i] * 4, K >> 8, tile_rows)
-                                     : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
+      const bool panel = tile_rows == kPanelLayout;
+      if ((real_row || panel) && in_row) {
+        const size_t off = panel       ? panel_code_offset(r, cc[i] * 4, K >> 8, kMxPanelBytes)
+                           : tile_rows ? tiled_offset(r, cc[i] * 4, K >> 8, tile_rows)
+                                       : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
         *reinterpret_cast<uint32_t *>(codes + off) = packed;
       }
       const uint32_t word = mx_scale_word(scode);
       if (in_row && (lane & 15) == 0) {
         const int g = cc[i] >> 2;  // first of the 4 blocks, g % 4 == 0
-        const size_t off = kSwizzled ? sf_swizzled_offset(r, g, G) : (size_t)r * G + g;
-        *reinterpret_cast<uint32_t *>(sf + off) = word;
+        const size_t off = panel       ? panel_sf_offset(r, g, K >> 8)
+                           : kSwizzled ? sf_swizzled_offset(r, g, G)
+                                       : (size_t)r * G + g;
+        *reinterpret_cast<uint32_t *>((panel ? codes : sf) + off) = word;
       }
     }
   }
@@ -109,10 +115,13 @@ __device__ __forceinline__ uint32_t amax_bf16x8(const uint4 &w) {
 
 // One CTA per row (grid-stride over rows), two passes over the row: the
 // amax, then the codes (the row is re-read from L1).  Few registers, so the
-// CTAs fit beside a resident GEMM CTA.  tile_rows: 0 = row-major q, else the
-// tile layout with that tile height.
+// CTAs fit beside a resident GEMM CTA.  tile_rows: 0 = row-major q,
+// kPanelLayout = weight panels (rows_iter = rows rounded up to the panel;
+// the padding rows get zero bytes and no scale), else the tile layout with
+// that tile height.
 __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
-                                                               long long ldx, int rows, int K,
+                                                               long long ldx, int rows,
+                                                               int rows_iter, int K,
                                                                int tile_rows, int early_trigger,
                                                                uint8_t *__restrict__ q,
                                                                float *__restrict__ scale) {
@@ -126,7 +135,18 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
       prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
   }
   pdl_wait();
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+  // destination of the 8 bytes of chunk c of row r
+  auto qdst = [&](int r, int c) -> uint2 * {
+    const size_t off = tile_rows == kPanelLayout ? panel_code_offset(r, c * 8, K >> 7, kF8PanelBytes)
+                       : tile_rows               ? tiled_offset(r, c * 8, K >> 7, tile_rows)
+                                                 : (size_t)r * K + (size_t)c * 8;
+    return reinterpret_cast<uint2 *>(q + off);
+  };
+  for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
+    if (r >= rows) {  // panel padding (uniform over the CTA)
+      for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = make_uint2(0u, 0u);
+      continue;
+    }
     const uint16_t *xr = x + (size_t)r * ldx;
     uint32_t amax = 0;
     int c = tid;
@@ -147,14 +167,9 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
     for (int i = 1; i < kF8Threads / 32; ++i) amax = max(amax, red[i]);
     __syncthreads();  // red[] is reused by the next row
 
-    // destination of the 8 bytes of chunk c of this row
-    auto qdst = [&](int c) -> uint2 * {
-      return reinterpret_cast<uint2 *>(q + (tile_rows ? tiled_offset(r, c * 8, K >> 7, tile_rows)
-                                                      : (size_t)r * K + (size_t)c * 8));
-    };
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
-      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = make_uint2(0u, 0u);
       continue;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
@@ -169,7 +184,7 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
       hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
       return make_uint2(lo, hi);
     };
-    for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
+    for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
   }
 }
 
@@ -181,7 +196,9 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   const int cpr = K / 8;
   const int per_block = kMxThreads * kMxChunksPerThread;
   const int gx = (cpr + per_block - 1) / per_block;
-  const int rows_iter = swizzled ? ((rows + 127) / 128) * 128 : rows;
+  const int rows_iter = tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows
+                        : swizzled                   ? ((rows + 127) / 128) * 128
+                                                     : rows;
   // enough CTAs for ~8 resident per SM, rows beyond that are grid-strided
   int gy = rows_iter;
   const int cap = (sm_count > 0 ? sm_count : 152) * 8;
@@ -205,7 +222,9 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
                              float *scale, int tile_rows, bool act, int sm_count,
                              cudaStream_t stream) {
-  int g = rows;
+  const int rows_iter =
+      tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows : rows;
+  int g = rows_iter;
   const int cap = (sm_count > 0 ? sm_count : 152) * 8;
   if (g > cap) g = cap;
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
@@ -213,8 +232,8 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   attach_pdl(cfg, attr);
   cudaError_t e = prefer_shared_carveout(fp8_quant_kernel);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows, K,
-                            tile_rows, act ? 1 : 0, q, scale);
+  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows,
+                            rows_iter, K, tile_rows, act ? 1 : 0, q, scale);
 }
 
 }  // namespace mxg

@@ -66,6 +66,24 @@ __device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row, int
          (size_t)((j ^ (r & 7)) << 4) + (b & 15);
 }
 
+// Weight panel layout: rows in panels of 256; per panel and 128-byte column
+// kc one block of panel_bytes holding the codes of the panel's two 128-row
+// halves (16 KiB each, laid out as a tile above), then -- MXFP4 -- the
+// scale atoms of the two halves (1 KiB each: the column's two 512-byte atoms
+// of the 128x4-tile scale layout).  Byte b of row r's codes:
+__device__ __forceinline__ size_t panel_code_offset(int r, int b, int kc_per_row, int panel_bytes) {
+  const int j = (b >> 4) & 7;
+  return ((size_t)(r >> 8) * kc_per_row + (b >> 7)) * (size_t)panel_bytes +
+         (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u + (size_t)((j ^ (r & 7)) << 4) +
+         (b & 15);
+}
+// ... and the 4-byte scale word of groups g..g+3 (g % 4 == 0) of row r
+// (MXFP4: 8 groups per column, panel_bytes = 34816).
+__device__ __forceinline__ size_t panel_sf_offset(int r, int g, int kc_per_row) {
+  return ((size_t)(r >> 8) * kc_per_row + (g >> 3)) * 34816u + 32768u + (size_t)((r >> 7) & 1) * 1024u +
+         (size_t)((g >> 2) & 1) * 512u + (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u;
+}
+
 // One 16-byte chunk (8 bf16 = a quarter of an MX block) per lane; four
 // consecutive lanes hold one block.  Returns the 8 packed E2M1 codes (value
 // 2i in the low nibble of byte i) and the block's E8M0 code in `scode`.

@@ -80,9 +80,11 @@ typedef enum {
 typedef enum {
     MXG_SF_ROWMAJOR = 0, /* (rows, K/32) bytes, row-major: the stored checkpoint layout */
     MXG_SF_SWIZZLED = 1, /* 128x4 tiles of 512 bytes (see mxg_sf_bytes); the GEMM operand layout */
-    MXG_TILED = 2        /* scales as MXG_SF_SWIZZLED, and the codes in the GEMM's weight tile
+    MXG_TILED = 2,       /* scales as MXG_SF_SWIZZLED, and the codes in the GEMM's weight tile
                             layout (see MXG_TILE_BYTES); needs rows % 128 == 0 and, for MXFP4,
                             K % 256 == 0 */
+    MXG_PANEL = 3        /* weights only: the codes in 256-row panels with the MXFP4 scales
+                            inside them (see MXG_PANEL_ROWS); K % 256 == 0 for MXFP4 */
 } mxg_sf_layout;
 
 /* Weight tile layout (MXG_TILED), for MXFP4 codes and for FP8 E4M3 bytes alike:
@@ -93,6 +95,19 @@ typedef enum {
  * shared-memory image the tensor cores read (K-major, 128-byte swizzle), so a
  * GEMM stage fetches a weight tile with one contiguous bulk copy. */
 #define MXG_TILE_BYTES 16384
+
+/* Weight panel layout (MXG_PANEL): the rows are grouped in panels of 256
+ * (the last panel padded with zero codes).  Panel p and chunk kc form one
+ * block at byte (p * KC + kc) * B, B = 34816 for MXFP4 and 32768 for FP8:
+ * first the two 128-row halves of the panel, each a 16 KiB tile as in
+ * MXG_TILED (half h at h * 16384, row r of the weight being row r % 128 of
+ * half (r / 128) % 2 of panel r / 256); then, MXFP4 only, the scales of the
+ * chunk's 8 groups: half h at 32768 + h * 1024, the 2 x 512-byte 128x4 tiles
+ * of MXG_SF_SWIZZLED for groups 8kc..8kc+3 and 8kc+4..8kc+7 (tile
+ * offsets as in mxg_sf_bytes, with r % 128).  A full-tile GEMM stage (256
+ * weight rows, one chunk) then fetches its whole weight operand, codes and
+ * scales, with one bulk copy.  Bytes: mxg_weight_bytes. */
+#define MXG_PANEL_ROWS 256
 
 typedef enum {
     MXG_OUT_BF16 = 0, /* y rounded to bf16 (round to nearest even) */
@@ -129,8 +144,9 @@ typedef struct {
                              by a kernel without programmatic launch, or before a
                              synchronisation qualify; weights written by this library's
                              activation quantizers, GEMMs or reduce do not. */
-    int weights_tiled;    /* 1: w_codes (A4W4) / qw (PTPC) are in the MXG_TILED weight tile
-                             layout; 0: row-major */
+    int weights_tiled;    /* 0: w_codes (A4W4) / qw (PTPC) are row-major; 1: in the
+                             MXG_TILED weight tile layout; 2: in the MXG_PANEL layout (A4W4:
+                             w_sf is then unused and may be NULL) */
     int act_tile_rows;    /* 0: a_codes (A4W4) / qa (PTPC) are row-major; else they are in
                              the activation tile layout with tiles of this many rows, as
                              written by mx_quantize_act_tiled / fp8_quantize_act_tiled; it
@@ -185,6 +201,12 @@ typedef struct {
  * ((r%128)/32)*4 + g%4 with G = K/32; padding rows hold 0. */
 size_t mxg_sf_bytes(int rows, int K, mxg_sf_layout layout);
 
+/* Bytes of a quantized weight's codes (kind 0: MXFP4, K/2 bytes a row; kind 1:
+ * FP8, K bytes a row) in `layout`: N * row bytes, or for MXG_PANEL
+ * ceil(N/256) * (row bytes / 128) * (34816 | 32768) (scales included);
+ * 0 for an invalid argument. */
+size_t mxg_weight_bytes(int kind, int N, int K, mxg_sf_layout layout);
+
 /* Dispatcher, pure host logic (no GPU needed): the variant, tile and grid a
  * GEMM of kind 0 (A4W4) or 1 (PTPC) at (M, N, K) would use on a device with
  * `sm_count` SMs under `opts` (nullable), and the workspace it needs. */
@@ -201,9 +223,11 @@ size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
  * E8M0 scale per 32 consecutive input channels).
  *   w_bf16: (N, K) bf16, leading dimension ldw elements.
  *   codes:  N * K/2 bytes, two codes per byte, lower k in the low nibble:
- *           row-major (N, K/2) for ROWMAJOR / SWIZZLED, weight tiles for TILED.
+ *           row-major (N, K/2) for ROWMAJOR / SWIZZLED, weight tiles for TILED,
+ *           mxg_weight_bytes(0, N, K, MXG_PANEL) bytes of panels for PANEL.
  *   sf:     mxg_sf_bytes(N, K, layout) bytes, ROWMAJOR (the stored (N, K/32)
- *           checkpoint layout) or the 128x4 tiles (SWIZZLED, TILED). */
+ *           checkpoint layout) or the 128x4 tiles (SWIZZLED, TILED); unused
+ *           (may be NULL) for PANEL, whose scales sit inside the panels. */
 mxg_status mx_quantize_weight(const void *w_bf16, int N, int K, int ldw,
                               uint8_t *codes, uint8_t *sf, mxg_sf_layout layout,
                               mxg_stream_t stream);
@@ -241,7 +265,8 @@ mxg_status fp8_quantize_act(const void *x_bf16, int M, int K, int ldx,
  * E4M3 weight, FP32 scale of shape (out_features, 1)); the same arithmetic as
  * fp8_quantize_act applied to the rows of W.
  *   w_bf16 (N, K), leading dimension ldw.  q: N * K bytes, row-major (N, K)
- *   for MXG_SF_ROWMAJOR or weight tiles for MXG_TILED (N % 128 == 0).
+ *   for MXG_SF_ROWMAJOR, weight tiles for MXG_TILED (N % 128 == 0), or
+ *   mxg_weight_bytes(1, N, K, MXG_PANEL) bytes of panels for MXG_PANEL.
  *   scale: N floats. */
 mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw,
                                uint8_t *q, float *scale, mxg_sf_layout layout,
@@ -284,7 +309,7 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
  * must not allocate on its hot path because an allocation can stall on a
  * device-wide synchronisation or fail when memory is fragmented.  This entry
  * point takes the same operands as mx_gemm_a4w4 (default dispatch; weights in
- * the MXG_TILED layout when weights_tiled != 0) and no workspace: its scratch
+ * the layout weights_tiled names, as in mxg_gemm_opts) and no workspace: its scratch
  * is a file-scope device array of MXG_NOALLOC_SCRATCH_BYTES (16 MiB) inside
  * the library, which every GPU that loads the library keeps until the
  * process exits.  It calls no cudaMalloc/cudaFree or any allocating routine.

@@ -70,3 +70,24 @@ def untile_rows(tiled: np.ndarray, rows: int, row_bytes: int, T: int) -> np.ndar
     j = np.arange(8)[None, :]
     logical = a[:, :, r, j ^ (r % 8), :]
     return logical.transpose(0, 2, 1, 3, 4).reshape(rows, row_bytes)
+
+
+def unpanel(buf: np.ndarray, rows: int, row_bytes: int, panel_bytes: int):
+    """Weight panel layout -> (row-major codes (rows rounded up to 256,
+    row_bytes), the scales in the flat 128x4-tile layout or None).  Per panel
+    P and 128-byte chunk kc one block of panel_bytes: two 128-row tiles
+    (swizzled as in `untile`), then (MXFP4) per 128-row half the chunk's two
+    512-byte scale tiles."""
+    kc = row_bytes // 128
+    P = -(-rows // 256)
+    a = np.asarray(buf, dtype=np.uint8).reshape(P, kc, panel_bytes)
+    tiles = a[:, :, :32768].reshape(P, kc, 2, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    j = np.arange(8)[None, :]
+    logical = tiles[:, :, :, r, j ^ (r % 8), :]       # [P][kc][half][128][8][16]
+    codes = logical.transpose(0, 2, 3, 1, 4, 5).reshape(P * 256, row_bytes)
+    sf = None
+    if panel_bytes > 32768:
+        s = a[:, :, 32768:].reshape(P, kc, 2, 2, 512)  # [P][kc][half][tile][512]
+        sf = s.transpose(0, 2, 1, 3, 4).reshape(-1)     # [row block][scale tile][512]
+    return codes, sf

@@ -40,6 +40,23 @@ def test_sf_bytes():
     assert mx.mxg_sf_bytes(8, 8192, mx.SF_SWIZZLED) == 128 * 256
     assert mx.mxg_sf_bytes(129, 256, mx.SF_SWIZZLED) == 256 * 8
     assert mx.mxg_sf_bytes(0, 256, mx.SF_SWIZZLED) == 0
+    assert mx.mxg_sf_bytes(7168, 8192, mx.TILED) == 7168 * 256
+    assert mx.mxg_sf_bytes(7168, 8192, mx.PANEL) == 0      # the scales sit inside the panels
+
+
+def test_weight_bytes():
+    # row-major and tile layouts: N x row bytes
+    assert mx.mxg_weight_bytes(mx.KIND_A4W4, 7168, 8192, mx.SF_SWIZZLED) == 7168 * 4096
+    assert mx.mxg_weight_bytes(mx.KIND_PTPC, 7168, 8192, mx.TILED) == 7168 * 8192
+    # panels: ceil(N / 256) panels x (row bytes / 128) chunks x (32 KiB codes + 2 KiB MXFP4 scales)
+    assert mx.mxg_weight_bytes(mx.KIND_A4W4, 7168, 8192, mx.PANEL) == 28 * 32 * 34816
+    assert mx.mxg_weight_bytes(mx.KIND_A4W4, 384, 1024, mx.PANEL) == 2 * 4 * 34816
+    assert mx.mxg_weight_bytes(mx.KIND_PTPC, 384, 1152, mx.PANEL) == 2 * 9 * 32768
+    # the codes plus the swizzled scales, re-arranged: the same bytes when N % 256 == 0
+    assert mx.mxg_weight_bytes(mx.KIND_A4W4, 7168, 8192, mx.PANEL) == \
+        7168 * 4096 + mx.mxg_sf_bytes(7168, 8192, mx.SF_SWIZZLED)
+    assert mx.mxg_weight_bytes(mx.KIND_A4W4, 128, 384, mx.PANEL) == 0   # MXFP4 panels need K % 256
+    assert mx.mxg_weight_bytes(2, 128, 256, mx.PANEL) == 0
 
 
 def test_status_strings():

@@ -36,21 +36,23 @@ def ptr(t):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
-@pytest.mark.parametrize("M,fused,tiled", [(64, True, True), (8, False, False), (300, True, False)])
+@pytest.mark.parametrize("M,fused,tiled", [(64, True, 1), (8, False, 0), (300, True, 0), (300, True, 2),
+                                            (64, True, 2)])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(M, fused, tiled):
     d = dev()
     N, K = (7168, 8192) if M <= 64 else (1024, 2048)
     x = synth.activation(M, K, seed=synth.act_seed(1, 0, 0) + M)
     w = synth.weight(N, K, seed=M + 3)
-    layout = mx.TILED if tiled else mx.SF_SWIZZLED
+    layout = {0: mx.SF_SWIZZLED, 1: mx.TILED, 2: mx.PANEL}[tiled]
     wc, wsf = mx.mx_quantize_weight(w.to(d), layout=layout)
     xd = x.to(d)
     if fused:
         ac = asf = None
-        y_ref = mx.mx_gemm_a4w4(wc, wsf, x=xd, out_f32=True, weights_tiled=tiled)
+        y_ref = mx.mx_gemm_a4w4(wc, wsf, x=xd, out_f32=True, weights_tiled=tiled, n=N, k=K)
     else:
         ac, asf = mx.mx_quantize_act(xd)
-        y_ref = mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out_f32=True, weights_tiled=tiled)
+        y_ref = mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out_f32=True, weights_tiled=tiled,
+                                n=N, k=K)
     y_ref = y_ref.cpu().numpy()
     a_c, a_s = oracle.mx_quantize_rows(x)
     w_c, w_s = oracle.mx_quantize_rows(w)
