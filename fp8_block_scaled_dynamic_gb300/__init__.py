@@ -53,13 +53,13 @@ class GemmOpts(ctypes.Structure):
                 ("trace", ctypes.c_void_p), ("splitk_reduce", ctypes.c_int)]
 
 
-REDUCE = {"default": 0, "kernel": 1, "grid": 2, "lastcta": 3}
+REDUCE = {"default": 0, "kernel": 1, "grid": 2, "lastcta": 3, "pair": 4}
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("kblocks", ctypes.c_int),
-                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t)]
+                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t), ("pair", ctypes.c_int)]
 
 
 _lib = None
@@ -144,17 +144,17 @@ def mxg_weight_bytes(kind: int, N: int, K: int, layout: int) -> int:
 
 
 def mxg_plan_gemm(kind: int, M: int, N: int, K: int, sm_count: int,
-                  variant: str = "auto", ctas: int = 0) -> dict:
+                  variant: str = "auto", ctas: int = 0, splitk_reduce: str = "default") -> dict:
     """Pure host dispatcher: the variant/tile/grid/workspace of a GEMM."""
-    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas)
+    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas, splitk_reduce=REDUCE[splitk_reduce])
     p = Plan()
     _check("mxg_plan_gemm", lib().mxg_plan_gemm(kind, M, N, K, sm_count, ctypes.byref(o), ctypes.byref(p)))
     return {f: getattr(p, f) for f, _ in Plan._fields_}
 
 
 def mxg_gemm_workspace_bytes(kind: int, fused: bool, M: int, N: int, K: int,
-                             variant: str = "auto", ctas: int = 0) -> int:
-    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas)
+                             variant: str = "auto", ctas: int = 0, splitk_reduce: str = "default") -> int:
+    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas, splitk_reduce=REDUCE[splitk_reduce])
     return int(lib().mxg_gemm_workspace_bytes(kind, int(fused), M, N, K, ctypes.byref(o)))
 
 

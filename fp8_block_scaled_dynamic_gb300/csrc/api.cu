@@ -103,17 +103,28 @@ mxg_status make_output_map(CUtensorMap *m, void *y, int M, int N, int ldy) {
 //   lastcta: by the last CTA to finish each tile (arrival counter).
 // MXG_SPLITK_REDUCE=kernel|grid|lastcta selects it (MXG_SPLITK_INKERNEL=1 =
 // lastcta).  The single-kernel fused A4W4 path always sums in-grid.
-enum class ReduceMode { kKernel, kGrid, kLastCta };
+enum class ReduceMode { kKernel, kGrid, kLastCta, kPair };
 ReduceMode reduce_mode() {
   static const ReduceMode m = [] {
     const char *e = std::getenv("MXG_SPLITK_REDUCE");
     if (e && std::strcmp(e, "grid") == 0) return ReduceMode::kGrid;
     if (e && std::strcmp(e, "lastcta") == 0) return ReduceMode::kLastCta;
+    if (e && std::strcmp(e, "pair") == 0) return ReduceMode::kPair;
     const char *f = std::getenv("MXG_SPLITK_INKERNEL");
     if (f && f[0] == '1') return ReduceMode::kLastCta;
     return ReduceMode::kKernel;
   }();
   return m;
+}
+// The split-K reduction a call asks for: opts->splitk_reduce, else the
+// MXG_SPLITK_REDUCE environment default.
+ReduceMode requested_reduce(const mxg_gemm_opts *opts) {
+  ReduceMode mode = reduce_mode();
+  if (opts && opts->splitk_reduce == MXG_REDUCE_KERNEL) mode = ReduceMode::kKernel;
+  if (opts && opts->splitk_reduce == MXG_REDUCE_GRID) mode = ReduceMode::kGrid;
+  if (opts && opts->splitk_reduce == MXG_REDUCE_LAST_CTA) mode = ReduceMode::kLastCta;
+  if (opts && opts->splitk_reduce == MXG_REDUCE_PAIR) mode = ReduceMode::kPair;
+  return mode;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -152,6 +163,17 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
     pl->bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     const long long tilesA = N / 128, tilesB = (M + pl->bn - 1) / pl->bn;
     const long long tiles = tilesA * tilesB;
+    if (requested_reduce(opts) == ReduceMode::kPair && KB >= 2 && 2 * tiles <= sm_count &&
+        !(opts && opts->ctas > 0)) {
+      // CTA pairs: the stream-K split with G = 2 x tiles gives CTAs 2t and
+      // 2t + 1 the two halves of tile t's K range
+      pl->tiles = (int)tiles;
+      pl->ctas = (int)(2 * tiles);
+      pl->seg_max = 2;
+      pl->ws_bytes = 0;
+      pl->pair = 1;
+      return MXG_OK;
+    }
     const long long U = tiles * KB;
     if (U > (1LL << 40) / 4) return MXG_ERR_UNSUPPORTED_SHAPE;
     // persistent: at most one CTA per SM (grid barriers need them all resident)
@@ -307,13 +329,15 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
     p.ldx = op.ldx;
     p.fuse_quant = 1;
   }
-  ReduceMode mode = reduce_mode();
-  if (opts && opts->splitk_reduce == MXG_REDUCE_KERNEL) mode = ReduceMode::kKernel;
-  if (opts && opts->splitk_reduce == MXG_REDUCE_GRID) mode = ReduceMode::kGrid;
-  if (opts && opts->splitk_reduce == MXG_REDUCE_LAST_CTA) mode = ReduceMode::kLastCta;
+  ReduceMode mode = requested_reduce(opts);
   if (op.x) mode = ReduceMode::kGrid;
-  p.grid_reduce = (pl.seg_max > 1 && mode == ReduceMode::kGrid) ? 1 : 0;
-  p.defer_reduce = (pl.seg_max > 1 && mode == ReduceMode::kKernel) ? 1 : 0;
+  if (pl.pair && !op.x) {
+    p.pair_reduce = 1;
+  } else {
+    if (mode == ReduceMode::kPair) mode = ReduceMode::kKernel;  // the plan found no room for pairs
+    p.grid_reduce = (pl.seg_max > 1 && mode == ReduceMode::kGrid) ? 1 : 0;
+    p.defer_reduce = (pl.seg_max > 1 && mode == ReduceMode::kKernel) ? 1 : 0;
+  }
   if (p.fuse_quant || p.grid_reduce) {
     if (!ws) return MXG_ERR_WORKSPACE;
     p.gbar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + kGridBarrierOff);
@@ -333,7 +357,7 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
     return MXG_ERR_MISALIGNED;
   if (opts && (opts->variant < 0 || opts->variant > 2 || opts->ctas < 0))
     return MXG_ERR_INVALID_ARG;
-  if (opts && (opts->splitk_reduce < MXG_REDUCE_DEFAULT || opts->splitk_reduce > MXG_REDUCE_LAST_CTA))
+  if (opts && (opts->splitk_reduce < MXG_REDUCE_DEFAULT || opts->splitk_reduce > MXG_REDUCE_PAIR))
     return MXG_ERR_INVALID_ARG;
   if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
     return MXG_ERR_INVALID_ARG;

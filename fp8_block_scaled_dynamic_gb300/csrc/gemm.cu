@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (3 * kStages + 8) + 16;
+  static constexpr int kBarBytes = 8 * (3 * kStages + 10) + 16;
   // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
   static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
@@ -72,6 +72,7 @@ struct Cfg {
   static constexpr uint32_t kSfColsPerStage = kSfColsA + 8u * KS * (uint32_t)kSfBlocksB;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert(KS == 1 || 128 * BN * 4 <= kStages * kStageBytes, "CTA-pair partial tile fits the pipeline");
   static_assert(KIND != 0 || kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 };
 
@@ -415,7 +416,12 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   const uint32_t acts_ready = acc_full + 48;  // fused path: token tiles of every CTA written
   const uint32_t sf_bars = acc_full + 56;     // full tile: a stage's scales are in TMEM
   const uint32_t pull_bar = sf_bars + 8 * S;  // last-CTA split-K: the partial tiles are in smem
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 8);
+  // CTA-pair split-K: rank 0's pair_bar completes once rank 1's partial tile
+  // is in rank 0's shared memory; rank 1's ready_bar once rank 0's pipeline
+  // shared memory is free to receive it
+  const uint32_t pair_bar = pull_bar + 8;
+  const uint32_t ready_bar = pull_bar + 16;
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 10);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
@@ -454,6 +460,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     mbar_init(acts_ready, 1);
     for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
     mbar_init(pull_bar, 1);
+    mbar_init(pair_bar, 128);
+    mbar_init(ready_bar, 1);
     *abort_flag = 0;
     *decision = 0;
     *reduce_go = 0;
@@ -469,6 +477,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   }
   tc_fence_before();
   __syncthreads();
+  // the peer CTA arrives on this CTA's barriers later: their init must be
+  // visible across the cluster first
+  if (p.pair_reduce) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
@@ -956,6 +967,66 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             }
           }
         }
+      } else if (p.pair_reduce) {
+        // A CTA pair (one cluster) shares the tile: rank 0 holds the first
+        // part of K, rank 1 the rest.  Rank 1 pushes its fp32 partial into
+        // rank 0's pipeline shared memory (idle once rank 0's MMAs are done:
+        // each CTA of a pair has this one item); rank 0 adds it to its own,
+        // (partial 0 + partial 1, as the reduce kernel sums the slots) and
+        // writes y.  Row r's 16-byte chunk k sits at r * BN * 4 +
+        // ((k ^ (r % 8)) * 16), so that 8 consecutive rows cover all banks.
+        constexpr int kChunks = BN / 4;
+        constexpr int kSw = kChunks >= 8 ? 7 : kChunks - 1;
+        auto pofs = [&](int r, int k) -> uint32_t {
+          return (uint32_t)r * (uint32_t)(BN * 4) + (uint32_t)((k ^ (r & kSw)) << 4);
+        };
+        if (it.seg == 1) {
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(ready_bar, 0, ctl));
+          if (ok) {
+            const uint32_t dst = mapa_shared(sA, 0);
+#pragma unroll 1
+            for (int c = 0; c < BN / CH; ++c) {
+              uint32_t v[CH];
+              tmem_ld_chunk<CH>(t_row + c * CH, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < CH / 4; ++j)
+                st_cluster_v4(dst + pofs(r_in, c * (CH / 4) + j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                              v[4 * j + 3]);
+            }
+          }
+          release_acc();
+          if (ok) mbar_arrive_remote(mapa_shared(pair_bar, 0));
+        } else {
+          if (threadIdx.x == 64) mbar_arrive_remote(mapa_shared(ready_bar, 1));
+          ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(pair_bar, 0, ctl));
+          if (ok) {
+            const int n = ra;
+            const float sw = (KIND == 1 && n < p.N) ? p.chan_scale[n] : 1.0f;
+#pragma unroll 1
+            for (int c = 0; c < BN / CH; ++c) {
+              uint32_t v[CH];
+              tmem_ld_chunk<CH>(t_row + c * CH, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < CH / 4; ++j) {
+                const uint4 u = ld_shared_v4(sA + pofs(r_in, c * (CH / 4) + j));
+                const uint32_t o[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int m = cb0 + c * CH + 4 * j + e;
+                  if (m < p.M && n < p.N) {
+                    float f = 0.0f;
+                    f += __uint_as_float(v[4 * j + e]);
+                    f += __uint_as_float(o[e]);
+                    if (KIND == 1) f = (f * p.tok_scale[m]) * sw;
+                    store_out(p, m, n, f);
+                  }
+                }
+              }
+            }
+          }
+        }
       } else if (p.defer_reduce || p.grid_reduce) {
         // swapped, part of K: publish this CTA's fp32 partial tile into its
         // slot; the split-K reduce kernel that follows (or every CTA of this
@@ -1117,8 +1188,19 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUten
     once.set(dev);
   }
   cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attach_pdl(cfg, attr);
+  if (p.pair_reduce) {
+    // CTA pairs (2j, 2j + 1) share a tile and exchange partials through
+    // distributed shared memory
+    if (ctas % 2 != 0) return cudaErrorInvalidValue;
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = 2;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
+  }
   if (p.fuse_quant || p.grid_reduce) {
     // grid barriers: every CTA must be resident at once, also when other
     // streams run kernels of their own (a cooperative launch guarantees it)

@@ -123,6 +123,8 @@ struct GemmParams {
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
                            //          the last CTA of each tile
+  int pair_reduce;         // split-K over CTA pairs (2-CTA clusters, grid = 2 x tiles): rank 1
+                           //          pushes its partial into rank 0's shared memory
   int early_w;         // 1: no kernel still in flight writes the weights, so their first
                        //    stages may load before griddepcontrol.wait
   // Single-kernel split-K (swap) path: the CTAs first quantize the bf16

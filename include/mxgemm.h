@@ -167,7 +167,12 @@ typedef struct {
                              MXG_REDUCE_KERNEL (a reduce kernel launched right after the
                              GEMM), MXG_REDUCE_GRID (every CTA of the GEMM, after a grid
                              barrier: one launch; the grid is launched cooperatively),
-                             MXG_REDUCE_LAST_CTA (the last CTA to finish each tile).  On
+                             MXG_REDUCE_LAST_CTA (the last CTA to finish each tile),
+                             MXG_REDUCE_PAIR (when 2 x tiles <= SM count: two CTAs per
+                             tile, launched as a 2-CTA cluster, each taking half of K; the
+                             second pushes its partial into the first one's shared memory,
+                             which adds it and writes y -- no workspace partials and no
+                             second kernel; otherwise as MXG_REDUCE_KERNEL).  On
                              the fused A4W4 path (x given, K % 256 == 0) MXG_REDUCE_GRID
                              runs everything as one cooperative kernel: quantize, grid
                              barrier, GEMM, grid barrier, reduce; otherwise the fused path
@@ -180,7 +185,8 @@ enum {
     MXG_REDUCE_DEFAULT = 0,
     MXG_REDUCE_KERNEL = 1,
     MXG_REDUCE_GRID = 2,
-    MXG_REDUCE_LAST_CTA = 3
+    MXG_REDUCE_LAST_CTA = 3,
+    MXG_REDUCE_PAIR = 4
 };
 
 typedef struct {
@@ -193,6 +199,7 @@ typedef struct {
                           SPLITK */
     int seg_max;       /* SPLITK: most CTAs contributing to one tile */
     size_t ws_bytes;   /* workspace this plan needs */
+    int pair;          /* SPLITK: 1 = CTA pairs (MXG_REDUCE_PAIR), ctas = 2 x tiles */
 } mxg_plan;
 
 /* Bytes of a scale-factor array for `rows` rows of K elements (K/32 groups).
