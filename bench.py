@@ -188,6 +188,34 @@ class Workload:
     def e2e_step(self):
         raise NotImplementedError
 
+    def e2e_pipelined(self, parts):
+        """One end-to-end step as a serving loop runs it: parts = [(inputs,
+        compute, outputs)], inputs / outputs lists of (dst, src) tensor pairs.
+        Every part's pinned host inputs go in on a copy stream at once; part
+        i computes as soon as its own inputs have landed, and its results go
+        out on the copy stream while the parts after it compute."""
+        if not hasattr(self, "copy_stream"):
+            self.copy_stream = torch.cuda.Stream(device=self.dev)
+            self.ev_in = [torch.cuda.Event() for _ in parts]
+            self.ev_out = [torch.cuda.Event() for _ in parts]
+        cur = torch.cuda.current_stream()
+        cs = self.copy_stream
+        cs.wait_stream(cur)
+        with torch.cuda.stream(cs):
+            for i, (ins, _, _) in enumerate(parts):
+                for dst, src in ins:
+                    dst.copy_(src, non_blocking=True)
+                self.ev_in[i].record(cs)
+        for i, (_, fn, outs) in enumerate(parts):
+            cur.wait_event(self.ev_in[i])
+            fn()
+            self.ev_out[i].record(cur)
+            cs.wait_event(self.ev_out[i])
+            with torch.cuda.stream(cs):
+                for dst, src in outs:
+                    dst.copy_(src, non_blocking=True)
+        cur.wait_stream(cs)
+
 
 # resident weight layout of every workload: "panel" (256-row panels, the
 # MXFP4 scales inside; one copy per full-tile stage) or "tiled" (128-row tiles)
@@ -268,12 +296,13 @@ class OprojChain(Workload):
 
     def e2e_step(self):
         mx = self.mx
-        self.x.copy_(self.x_host, non_blocking=True)
-        for l in range(self.n_layers):
+
+        def layer(l):
             wc, wsf = self.w[l]
             mx.mx_gemm_a4w4(wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_tiled=self.wt,
                             weights_static=True, n=self.N, k=self.K)
-        self.y_host.copy_(self.y, non_blocking=True)
+        self.e2e_pipelined([([(self.x[l], self.x_host[l])], lambda l=l: layer(l), [(self.y_host[l], self.y[l])])
+                            for l in range(self.n_layers)])
 
 
 class MlpFp8(Workload):
@@ -334,13 +363,17 @@ class MlpFp8(Workload):
                                                        act_tile_rows=self.Td, k=self.I))]
 
     def e2e_step(self):
-        mx = self.mx
-        self.xg.copy_(self.xg_host, non_blocking=True)
-        self.xd.copy_(self.xd_host, non_blocking=True)
-        for _, fn in self.launches():
-            fn()
-        self.yg_host.copy_(self.yg, non_blocking=True)
-        self.yd_host.copy_(self.yd, non_blocking=True)
+        ln = [fn for _, fn in self.launches()]
+
+        def gate_up():
+            ln[0]()
+            ln[1]()
+
+        def down():
+            ln[2]()
+            ln[3]()
+        self.e2e_pipelined([([(self.xg, self.xg_host)], gate_up, [(self.yg_host, self.yg)]),
+                            ([(self.xd, self.xd_host)], down, [(self.yd_host, self.yd)])])
 
 
 def make_workload(name, mx, synth, dev):
@@ -553,7 +586,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(world * wl.bytes_per_step / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
                 "path": "public API (Python binding -> C ABI) captured in a CUDA graph with the pinned "
-                        "host<->device copies of every step",
+                        "host<->device copies of every step, the copies on a second stream so that "
+                        "each layer waits only for its own input and results leave while later layers run",
                 "eager_ms_per_step": round(e2e_eager, 4),
                 "eager_value": round(world * wl.bytes_per_step / (e2e_eager * 1e-3) / 1e9, 1)},
         "gpu_launches": K * len(launches),
