@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (3 * kStages + 10) + 16;
+  static constexpr int kBarBytes = 8 * (3 * kStages + 12) + 16;
   // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
   static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
@@ -421,7 +421,16 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   // shared memory is free to receive it
   const uint32_t pair_bar = pull_bar + 8;
   const uint32_t ready_bar = pull_bar + 16;
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 10);
+  // FP8 full tile: two accumulators (TMEM columns [0, 256) and [256, 512)),
+  // so that the epilogue of one tile overlaps the MMAs of the next; A4W4
+  // needs TMEM columns for its scale factors and keeps one
+  constexpr int kAccBufs = (KIND == 1 && KS == 1) ? 2 : 1;
+  static_assert(kAccCol + kAccBufs * BN <= (KIND == 0 ? kSfCol : kTmemCols), "TMEM accumulators");
+  const uint32_t acc_full1 = pull_bar + 24;
+  const uint32_t acc_empty1 = pull_bar + 32;
+  auto accf = [&](int b) { return b ? acc_full1 : acc_full; };
+  auto acce = [&](int b) { return b ? acc_empty1 : acc_empty; };
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 12);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
@@ -462,6 +471,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     mbar_init(pull_bar, 1);
     mbar_init(pair_bar, 128);
     mbar_init(ready_bar, 1);
+    mbar_init(acc_full1, 1);
+    mbar_init(acc_empty1, 4);
     *abort_flag = 0;
     *decision = 0;
     *reduce_go = 0;
@@ -715,7 +726,11 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       int i = 0;
       bool ok = true;
       while (ok && next_item(p, cur, it)) {
-        if (i > 0 && !mbar_wait(acc_empty, (uint32_t)((i - 1) & 1), ctl)) break;
+        // accumulator b of item i; its use-th use: wait until the epilogue
+        // has read out its previous tile
+        const int b = i % kAccBufs, use = i / kAccBufs;
+        const uint32_t d_acc = tmem + kAccCol + (uint32_t)(b * BN);
+        if (use > 0 && !mbar_wait(acce(b), (uint32_t)((use - 1) & 1), ctl)) break;
         tc_fence_after();
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
           // full tile A4W4: the epilogue warps signal once the stage's data is
@@ -753,14 +768,14 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             const int nk = min(C::kSteps, (p.K - kb * 256 * KS) / 64);
             for (int s = 0; s < nk; ++s) {
               const uint32_t sel = (uint32_t)(s & 1) * 2u;
-              mma_mxf4(tmem + kAccCol, a_desc(s), b_desc(s), idesc_sf_ids(idesc0, sel, sel),
+              mma_mxf4(d_acc, a_desc(s), b_desc(s), idesc_sf_ids(idesc0, sel, sel),
                        sfa_t + 4 * (s >> 1), sfb_t + 4 * C::kSfBlocksB * (s >> 1),
                        (kb > it.kb0 || s > 0) ? 1u : 0u);
             }
           } else {
             const int nk = min(C::kSteps, (p.K - kb * 128 * KS) / 32);
             for (int s = 0; s < nk; ++s)
-              mma_f8(tmem + kAccCol, a_desc(s), b_desc(s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
+              mma_f8(d_acc, a_desc(s), b_desc(s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
           }
           tc_commit(empty_bar(stage));
           if (++stage == S) {
@@ -769,7 +784,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit(accf(b));
         trace_mark(p, kTrLastCommit);
         ++i;
       }
@@ -838,7 +853,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         // test hook: a barrier nothing arrives at; the bounded wait gives up
         if (!warp_wait(stall_bar, 0, ctl)) break;
       }
-      if (!warp_wait(acc_full, (uint32_t)(i & 1), ctl)) break;
+      const int acc_b = i % kAccBufs, acc_use = i / kAccBufs;
+      if (!warp_wait(accf(acc_b), (uint32_t)(acc_use & 1), ctl)) break;
+      const uint32_t t_acc = t_row + (uint32_t)(acc_b * BN);  // this item's accumulator
       if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrAcc0 : kTrAcc1);
       tc_fence_after();
       const int ra = it.ta * kTileA + r_in;  // MMA-A row: token (full tile) / weight row (split)
@@ -856,7 +873,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
         for (int c = 0; c < BN / CH; ++c) {
           uint32_t v[CH];
-          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_chunk<CH>(t_acc + c * CH, v);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < CH; ++j)
@@ -868,7 +885,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
+        if (lane == 0) mbar_arrive(acce(acc_b));
         released = true;
       };
       if (whole && !p.swap && KS == 1 && p.y_tma) {
@@ -880,7 +897,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t v[32];
-          tmem_ld_chunk<32>(t_row + c * 32, v);
+          tmem_ld_chunk<32>(t_acc + c * 32, v);
           tmem_ld_wait();
           const int n0 = cb0 + c * 32;
           uint32_t w[16];
@@ -915,7 +932,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
         for (int c = 0; c < BN / CH; ++c) {
           uint32_t v[CH];
-          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_chunk<CH>(t_acc + c * CH, v);
           tmem_ld_wait();
           const int n0 = cb0 + c * CH;
           if (!mvalid || n0 >= p.N) continue;
@@ -955,7 +972,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
         for (int c = 0; c < BN / CH; ++c) {
           uint32_t v[CH];
-          tmem_ld_chunk<CH>(t_row + c * CH, v);
+          tmem_ld_chunk<CH>(t_acc + c * CH, v);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < CH; ++j) {
@@ -987,7 +1004,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
             for (int c = 0; c < BN / CH; ++c) {
               uint32_t v[CH];
-              tmem_ld_chunk<CH>(t_row + c * CH, v);
+              tmem_ld_chunk<CH>(t_acc + c * CH, v);
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < CH / 4; ++j)
@@ -1006,7 +1023,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 #pragma unroll 1
             for (int c = 0; c < BN / CH; ++c) {
               uint32_t v[CH];
-              tmem_ld_chunk<CH>(t_row + c * CH, v);
+              tmem_ld_chunk<CH>(t_acc + c * CH, v);
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < CH / 4; ++j) {

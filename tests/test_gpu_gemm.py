@@ -241,3 +241,22 @@ def test_mma_loop_peak_is_plausible(kind, lo, hi):
     nominal dense rate (13.5 PF/s E2M1, 4.5 PF/s E4M3 on GB300)."""
     t = mx.mxg_mma_peak(kind, 256, iters=2000)
     assert lo < t < hi, t
+
+
+@pytest.mark.parametrize("M,N,K", [(2560, 4096, 512), (1100, 9728, 384)])
+def test_ptpc_full_tile_several_tiles_per_cta(M, N, K):
+    """More output tiles than 2 x SMs: every CTA runs 2-3 tiles, so the
+    FP8 full-tile kernel's two TMEM accumulators both cycle (the epilogue of
+    one tile runs beside the MMAs of the next)."""
+    sm = torch.cuda.get_device_properties(dev()).multi_processor_count
+    plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, N, K, sm, variant="full")
+    assert plan["tiles"] > 2 * plan["ctas"]
+    x, w = quant_pair(M, N, K, seed=M + N)
+    y32 = run_ptpc(x, w, "full").cpu().numpy()
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([np.arange(0, M, 128), [M - 1], rng.choice(M, 40, replace=False)]))
+    ref, bound = oracle_ptpc(x, w, rows=rows)
+    assert_gemm_close(y32[rows], ref, bound, f"ptpc full {M}x{N}x{K}")
+    y16 = run_ptpc(x, w, "full", out_f32=False)
+    assert_codes_equal(y16.view(torch.int16).cpu().numpy().view(np.uint16), bf16_rne(y32),
+                       "bf16 output = RNE(fp32 output)")
