@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/mxgemm.h: argument checks, device
 // checks, the dispatcher, TMA tensor-map encoding and kernel launches.
 // Every host-detectable error is returned before anything is launched.
+#include <algorithm>
 #include <cudaTypedefs.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -129,6 +130,12 @@ ReduceMode requested_reduce(const mxg_gemm_opts *opts) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+// Full-tile rasterization: operands above kL2KeepBytes (together) do not stay
+// in the 129 MB L2 across a wave of tiles; a band's activations take up to
+// kL2ActBudget of it.
+constexpr uint64_t kL2KeepBytes = 96ull << 20;
+constexpr uint64_t kL2ActBudget = 64ull << 20;
 
 // CTA that owns stream-K unit u (must equal the device-side owner_of).
 long long owner_of(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
@@ -304,6 +311,18 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.early_w = (opts && opts->weights_static) ? 1 : 0;
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
   p.kc_per_row = (int)((row_bytes + 127) / 128);  // the last column may be half (TMA pads it)
+  if (!swap) {
+    // Full tile: when the two operands together exceed what L2 keeps
+    // (129 MB), walk the tiles in bands of token tiles whose activations fit
+    // in half of it, so that every weight tile is read from HBM once per band
+    // (in row order every wave of CTAs would sweep all the weights).
+    const uint64_t a_tile = 128ull * (row_bytes + (kind == 0 ? row_bytes / 16 : 0));
+    const uint64_t total = (uint64_t)(rowsA + rowsB) * row_bytes;
+    if (total > kL2KeepBytes) {
+      const uint64_t g = kL2ActBudget / a_tile;
+      p.raster_group = (int)std::max<uint64_t>(1, std::min<uint64_t>(g, (uint64_t)p.tilesA));
+    }
+  }
   // operands in the tile layout are fetched by bulk copy (their tensor map
   // above is then unused)
   if (w_tiled) {

@@ -103,6 +103,21 @@ __device__ __forceinline__ bool next_item(const GemmParams &p, uint32_t &cur, It
     it.seg = 0;
     it.nseg = 1;
     cur += G;
+    if (p.raster_group > 0) {
+      // bands of raster_group MMA-A (token) tiles: within a band the token
+      // tile varies fastest, so the CTAs running at one time share a few
+      // weight tiles and the band's activations stay in L2 -- the weights
+      // are read from HBM once per band, not once per token tile
+      const uint32_t g = (uint32_t)p.raster_group;
+      const uint32_t band = g * (uint32_t)p.tilesB;
+      const uint32_t bi = (uint32_t)it.t;
+      const uint32_t b0 = bi / band, r = bi - b0 * band;
+      const uint32_t ta0 = b0 * g;
+      const uint32_t gsz = min(g, (uint32_t)p.tilesA - ta0);
+      it.ta = (int)(ta0 + r % gsz);
+      it.tb = (int)(r / gsz);
+      return true;
+    }
   } else {
     const uint32_t U = (uint32_t)p.units;
     const uint32_t u1 = ((blockIdx.x + 1) * U) / G;

@@ -121,6 +121,8 @@ struct GemmParams {
   int w_panels;            // the weight operand (a_tiles when swapped, else b_tiles) is in
                            //   256-row panels with their scales appended (MXG_PANEL)
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
+  int raster_group;        // full tile: 0 = tiles in row order (token tile slowest), else
+                           //   bands of this many token tiles, the token tile fastest
   int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
                            //          the last CTA of each tile
   int pair_reduce;         // split-K over CTA pairs (2-CTA clusters, grid = 2 x tiles): rank 1
