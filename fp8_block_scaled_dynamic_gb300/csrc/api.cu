@@ -147,11 +147,24 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
   if (K % 128 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   int variant = opts ? opts->variant : MXG_VARIANT_AUTO;
   if (variant < MXG_VARIANT_AUTO || variant > MXG_VARIANT_SPLITK) return MXG_ERR_INVALID_ARG;
-  if (variant == MXG_VARIANT_AUTO) variant = (M <= 256) ? MXG_VARIANT_SPLITK : MXG_VARIANT_FULL;
   // pipeline stages along K: 128-byte K columns (256 E2M1 / 128 E4M3
   // values), one per stage in the full-tile kernel, two in the split-K one
   const int kcol = kind == 0 ? 256 : 128;
   const int KC = (K + kcol - 1) / kcol;
+  if (variant == MXG_VARIANT_AUTO) {
+    // Measured on GB300 (quantizer + GEMM, o_proj / FP8 gate_up / FP8 down):
+    // a full wave of 128 x 256 tiles streams the weights as fast as split-K
+    // and needs no reduction; below a wave, split-K wins for M <= 128, and
+    // up to M = 256 when K is long (a few long tiles leave SMs idle), while
+    // split-K with 256-token tiles (two pipeline stages) loses beyond that.
+    const long long full_tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
+    if (10 * full_tiles >= 9LL * sm_count)
+      variant = MXG_VARIANT_FULL;
+    else if (M <= 128 || (M <= 256 && KC > 64))
+      variant = MXG_VARIANT_SPLITK;
+    else
+      variant = MXG_VARIANT_FULL;
+  }
   const int per = mxg::gemm_cols_per_stage(variant == MXG_VARIANT_SPLITK);
   const int KB = (KC + per - 1) / per;
   std::memset(pl, 0, sizeof(*pl));

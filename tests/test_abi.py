@@ -112,7 +112,7 @@ def owner_sim(U, G):
                                            (1, 64, 36864, 7168, 152), (1, 64, 7168, 18432, 152),
                                            (0, 200, 1024, 2048, 7), (1, 1, 128, 128, 152)])
 def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
-    p = mx.mxg_plan_gemm(kind, M, N, K, sm)
+    p = mx.mxg_plan_gemm(kind, M, N, K, sm, variant="splitk")
     assert p["variant"] == 2 and p["bm"] == 128
     assert p["bn"] >= M and p["bn"] in (16, 32, 64, 128, 256) and (p["bn"] // 2 < M or p["bn"] == 16)
     kcol = 256 if kind == 0 else 128  # K values in one 128-byte column
@@ -158,3 +158,19 @@ def test_plan_pair(kind, M, N, K, sm):
     else:
         assert p["pair"] == 0 and p["ctas"] == base["ctas"] and p["ws_bytes"] == base["ws_bytes"]
     assert base["pair"] == 0
+
+
+@pytest.mark.parametrize("kind,M,N,K,want", [
+    # o_proj (A4W4, 28 full tiles per 128 tokens): split-K up to M = 128, full tile beyond
+    (0, 8, 7168, 8192, 2), (0, 64, 7168, 8192, 2), (0, 128, 7168, 8192, 2),
+    (0, 192, 7168, 8192, 1), (0, 512, 7168, 8192, 1), (0, 8192, 7168, 8192, 1),
+    # FP8 gate_up (144 full tiles >= 0.9 x 152 SMs at any M): full tile
+    (1, 8, 36864, 7168, 1), (1, 64, 36864, 7168, 1), (1, 8192, 36864, 7168, 1),
+    # FP8 down (long K): split-K up to M = 256, full tile beyond
+    (1, 64, 7168, 18432, 2), (1, 256, 7168, 18432, 2), (1, 320, 7168, 18432, 1),
+])
+def test_dispatcher_rule(kind, M, N, K, want):
+    """The automatic variant follows the GB300 measurements of quantizer + GEMM:
+    a full wave of 128 x 256 tiles -> full tile; otherwise split-K for M <= 128,
+    and up to M = 256 when K exceeds 64 128-byte columns."""
+    assert mx.mxg_plan_gemm(kind, M, N, K, 152)["variant"] == want
