@@ -14,8 +14,12 @@ from gpu_util import assert_gemm_close, dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("kind,variant", [(0, "full"), (0, "splitk"), (1, "splitk")])
-def test_stall_times_out_then_next_call_is_correct(kind, variant):
+@pytest.mark.parametrize("kind,variant,reduce", [(0, "full", "default"), (0, "splitk", "default"),
+                                                 (1, "splitk", "default"), (1, "full", "default"),
+                                                 (0, "splitk", "pair"), (1, "splitk", "pair")])
+def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
+    """Also for the 2-CTA-cluster split-K (pair): every CTA of the pair gives
+    up before any exchange with its partner starts."""
     d = dev()
     M, N, K = 16, 512, 1024
     x = synth.activation(M, K, seed=50)
@@ -24,14 +28,16 @@ def test_stall_times_out_then_next_call_is_correct(kind, variant):
     ws = torch.zeros(1 << 22, dtype=torch.uint8, device=d)
     if kind == 0:
         wc, wsf = mx.mx_quantize_weight(w.to(d))
-        run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant=variant, ws=ws, **kw)
+        run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant=variant, ws=ws,
+                                           splitk_reduce=reduce, **kw)
         ac, asf = oracle.mx_quantize_rows(x)
         wr, wsr = oracle.mx_quantize_rows(w)
         ref, bound = oracle.gemm_a4w4(ac, asf, wr, wsr)
     else:
         qw, sw = mx.fp8_quantize_act(w.to(d))
         qa, sa = mx.fp8_quantize_act(x.to(d))
-        run = lambda **kw: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant=variant, ws=ws, **kw)
+        run = lambda **kw: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant=variant, ws=ws,
+                                            splitk_reduce=reduce, **kw)
         qar, sar = oracle.fp8_quantize_rows(x)
         qwr, swr = oracle.fp8_quantize_rows(w)
         ref, bound = oracle.gemm_ptpc(qar, sar, qwr, swr)
