@@ -59,15 +59,44 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   }
   // x may be the previous kernel's output and codes/sf may still be read by it
   pdl_wait();
-  for (int r = blockIdx.y; r < rows_iter; r += gridDim.y) {
-    const bool real_row = r < rows;
-    uint4 v[kMxChunksPerThread];
-    int cc[kMxChunksPerThread];
+  const bool panel = tile_rows == kPanelLayout;
+  const int KC = K >> 8;  // 128-byte code columns per row
+  const int t_shift = (tile_rows > 0) ? __ffs(tile_rows) - 1 : 0;  // tile_rows is a power of 2
+  int cc[kMxChunksPerThread];
+#pragma unroll
+  for (int i = 0; i < kMxChunksPerThread; ++i) cc[i] = (blockIdx.x * kMxChunksPerThread + i) * kMxThreads + threadIdx.x;
+  auto load_row = [&](int r, uint4 (&v)[kMxChunksPerThread]) {
 #pragma unroll
     for (int i = 0; i < kMxChunksPerThread; ++i) {
-      cc[i] = (blockIdx.x * kMxChunksPerThread + i) * kMxThreads + threadIdx.x;
       v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (real_row && cc[i] < cpr) v[i] = ld_stream_v4(x + (size_t)r * ldx + (size_t)cc[i] * 8);
+      if (r < rows && cc[i] < cpr) v[i] = ld_stream_v4(x + (size_t)r * ldx + (size_t)cc[i] * 8);
+    }
+  };
+  uint4 v[kMxChunksPerThread];
+  int r = blockIdx.y;
+  if (r < rows_iter) load_row(r, v);
+  for (; r < rows_iter; r += gridDim.y) {
+    // the next row's loads go out before this row's arithmetic
+    uint4 vn[kMxChunksPerThread] = {};
+    if (r + (int)gridDim.y < rows_iter) load_row(r + gridDim.y, vn);
+    const bool real_row = r < rows;
+    // where this row's codes go: column c of the row at row_base + c *
+    // col_stride, its 16-byte unit j at ((j ^ rsw) * 16) (row-major: rsw = 0)
+    size_t row_base, col_stride;
+    int rsw;
+    if (panel) {
+      row_base = (size_t)(r >> 8) * KC * kMxPanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
+      col_stride = kMxPanelBytes;
+      rsw = r & 7;
+    } else if (tile_rows > 0) {
+      const int rr = r & (tile_rows - 1);
+      row_base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
+      col_stride = (size_t)tile_rows * 128u;
+      rsw = rr & 7;
+    } else {
+      row_base = (size_t)r * (K >> 1);
+      col_stride = 128;
+      rsw = 0;
     }
 #pragma unroll
     for (int i = 0; i < kMxChunksPerThread; ++i) {
@@ -77,22 +106,22 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       const bool in_row = cc[i] < cpr;
       uint32_t scode;
       const uint32_t packed = mx_encode_chunk(v[i], scode);
-      const bool panel = tile_rows == kPanelLayout;
       if ((real_row || panel) && in_row) {
-        const size_t off = panel       ? panel_code_offset(r, cc[i] * 4, K >> 8, kMxPanelBytes)
-                           : tile_rows ? tiled_offset(r, cc[i] * 4, K >> 8, tile_rows)
-                                       : (size_t)r * (K >> 1) + (size_t)cc[i] * 4;
+        const int b = cc[i] * 4;  // byte of the row's codes
+        const size_t off = row_base + (size_t)(b >> 7) * col_stride + (size_t)((((b >> 4) & 7) ^ rsw) << 4) + (b & 15);
         *reinterpret_cast<uint32_t *>(codes + off) = packed;
       }
       const uint32_t word = mx_scale_word(scode);
       if (in_row && (lane & 15) == 0) {
         const int g = cc[i] >> 2;  // first of the 4 blocks, g % 4 == 0
-        const size_t off = panel       ? panel_sf_offset(r, g, K >> 8)
+        const size_t off = panel       ? panel_sf_offset(r, g, KC)
                            : kSwizzled ? sf_swizzled_offset(r, g, G)
                                        : (size_t)r * G + g;
         *reinterpret_cast<uint32_t *>((panel ? codes : sf) + off) = word;
       }
     }
+#pragma unroll
+    for (int i = 0; i < kMxChunksPerThread; ++i) v[i] = vn[i];
   }
 }
 
@@ -135,16 +164,37 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
       prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
   }
   pdl_wait();
-  // destination of the 8 bytes of chunk c of row r
-  auto qdst = [&](int r, int c) -> uint2 * {
-    const size_t off = tile_rows == kPanelLayout ? panel_code_offset(r, c * 8, K >> 7, kF8PanelBytes)
-                       : tile_rows               ? tiled_offset(r, c * 8, K >> 7, tile_rows)
-                                                 : (size_t)r * K + (size_t)c * 8;
-    return reinterpret_cast<uint2 *>(q + off);
+  const int KC = K >> 7;  // 128-byte columns per row
+  const int t_shift = (tile_rows > 0) ? __ffs(tile_rows) - 1 : 0;  // tile_rows is a power of 2
+  // destination of the 8 bytes of chunk c of row r: column c / 16 at
+  // row_base + column * col_stride, 16-byte unit j at ((j ^ rsw) * 16)
+  size_t row_base = 0, col_stride = 128;
+  int rsw = 0;
+  auto set_row = [&](int r) {
+    if (tile_rows == kPanelLayout) {
+      row_base = (size_t)(r >> 8) * KC * kF8PanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
+      col_stride = kF8PanelBytes;
+      rsw = r & 7;
+    } else if (tile_rows > 0) {
+      const int rr = r & (tile_rows - 1);
+      row_base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
+      col_stride = (size_t)tile_rows * 128u;
+      rsw = rr & 7;
+    } else {
+      row_base = (size_t)r * K;
+      col_stride = 128;
+      rsw = 0;
+    }
+  };
+  auto qdst = [&](int c) -> uint2 * {
+    const int b = c * 8;
+    return reinterpret_cast<uint2 *>(q + row_base + (size_t)(b >> 7) * col_stride +
+                                     (size_t)((((b >> 4) & 7) ^ rsw) << 4) + (b & 15));
   };
   for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
+    set_row(r);
     if (r >= rows) {  // panel padding (uniform over the CTA)
-      for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
       continue;
     }
     const uint16_t *xr = x + (size_t)r * ldx;
@@ -169,7 +219,7 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
 
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
-      for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
       continue;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
@@ -184,7 +234,7 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
       hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
       return make_uint2(lo, hi);
     };
-    for (int c = tid; c < cpr; c += kF8Threads) *qdst(r, c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
+    for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
   }
 }
 

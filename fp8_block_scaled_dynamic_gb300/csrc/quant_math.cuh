@@ -35,12 +35,6 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sign bits of the two bf16 in `w`, moved to bits 3 and 7 of a byte (the sign
-// bits of the two E2M1 nibbles).
-__device__ __forceinline__ uint32_t nibble_signs(uint32_t w) {
-  return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
-}
-
 // Sign bits of the two bf16 in `w`, moved to bits 7 and 15 (the sign bits
 // of the two E4M3 bytes).
 __device__ __forceinline__ uint32_t byte_signs(uint32_t w) {
@@ -68,17 +62,13 @@ __device__ __forceinline__ size_t tiled_offset(int r, int b, int kc_per_row, int
 
 // Weight panel layout: rows in panels of 256; per panel and 128-byte column
 // kc one block of panel_bytes holding the codes of the panel's two 128-row
-// halves (16 KiB each, laid out as a tile above), then -- MXFP4 -- the
-// scale atoms of the two halves (1 KiB each: the column's two 512-byte atoms
-// of the 128x4-tile scale layout).  Byte b of row r's codes:
-__device__ __forceinline__ size_t panel_code_offset(int r, int b, int kc_per_row, int panel_bytes) {
-  const int j = (b >> 4) & 7;
-  return ((size_t)(r >> 8) * kc_per_row + (b >> 7)) * (size_t)panel_bytes +
-         (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u + (size_t)((j ^ (r & 7)) << 4) +
-         (b & 15);
-}
-// ... and the 4-byte scale word of groups g..g+3 (g % 4 == 0) of row r
-// (MXFP4: 8 groups per column, panel_bytes = 34816).
+// halves (16 KiB each, laid out as a tile above: byte b of row r at
+// ((r / 256) * KC + b / 128) * panel_bytes + ((r / 128) % 2) * 16384 +
+// (r % 128) * 128 + (((b / 16) % 8) ^ (r % 8)) * 16 + b % 16), then -- MXFP4
+// -- the scale atoms of the two halves (1 KiB each: the column's two 512-byte
+// atoms of the 128x4-tile scale layout).  The 4-byte scale word of groups
+// g..g+3 (g % 4 == 0) of row r (MXFP4: 8 groups per column, panel_bytes =
+// 34816) sits at:
 __device__ __forceinline__ size_t panel_sf_offset(int r, int g, int kc_per_row) {
   return ((size_t)(r >> 8) * kc_per_row + (g >> 3)) * 34816u + 32768u + (size_t)((r >> 7) & 1) * 1024u +
          (size_t)((g >> 2) & 1) * 512u + (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u;
@@ -109,8 +99,10 @@ __device__ __forceinline__ uint32_t mx_encode_chunk(const uint4 &w, uint32_t &sc
                     (e2m1x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 8) |
                     (e2m1x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) << 16) |
                     (e2m1x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 24);
-  packed |= nibble_signs(w.x) | (nibble_signs(w.y) << 8) | (nibble_signs(w.z) << 16) |
-            (nibble_signs(w.w) << 24);
+  // the sign of value i (bit 15 or 31 of its word) onto bit 4i + 3
+  packed |= ((w.x >> 12) & 0x8u) | ((w.x >> 24) & 0x80u) | ((w.y >> 4) & 0x800u) |
+            ((w.y >> 16) & 0x8000u) | ((w.z << 4) & 0x80000u) | ((w.z >> 8) & 0x800000u) |
+            ((w.w << 12) & 0x8000000u) | (w.w & 0x80000000u);
   return packed;
 }
 
