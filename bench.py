@@ -426,6 +426,22 @@ def kernel_sources_hash():
     return h.hexdigest()
 
 
+def max_over_ranks(vals, device, world):
+    """Each value's maximum over all ranks: the slowest replica sets the time
+    (one process per GPU; NCCL on the GPUs, gloo in the CPU test)."""
+    if world <= 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_rate(units_per_rank, ms, world):
+    """Whole-job throughput: every rank processes units_per_rank per step
+    (weak scaling), a step takes ms on the slowest rank; units per second."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import fp8_block_scaled_dynamic_gb300 as mx
     import synth
@@ -509,10 +525,7 @@ def run_ours(args, rank, world, local_rank):
             stream.synchronize()
             kern_ms.extend(a.elapsed_ms(b) for a, b in ev_pairs)
     kms = statistics.mean(kern_ms)
-    if world > 1:
-        t = torch.tensor([ms, kms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, kms = float(t[0]), float(t[1])
+    ms, kms = max_over_ranks([ms, kms], dev, world)
 
     # end to end through the public API: pinned host inputs in, results out,
     # every step; the calls captured once in a CUDA graph (copies + library
@@ -541,15 +554,12 @@ def run_ours(args, rank, world, local_rank):
         return statistics.mean(ts)
     e2e = time_e2e(graph_e.replay)
     e2e_eager = time_e2e(wl.e2e_step)
-    if world > 1:
-        t = torch.tensor([e2e, e2e_eager], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e, e2e_eager = float(t[0]), float(t[1])
+    e2e, e2e_eager = max_over_ranks([e2e, e2e_eager], dev, world)
 
     if rank != 0:
         return
     hbm, bf16, peak_src = load_peaks()
-    gbs = world * wl.bytes_per_step / (ms * 1e-3) / 1e9
+    gbs = job_rate(wl.bytes_per_step, ms, world) / 1e9
     achieved_gbs = wl.kernel_bytes / (kms * 1e-3) / 1e9
     achieved_tf = wl.kernel_flops / (kms * 1e-3) / 1e12
     if wl.bound == "hbm":
@@ -585,15 +595,15 @@ def run_ours(args, rank, world, local_rank):
                    "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
                    "weights": f"{WEIGHTS} layout, resident in HBM",
                    "dispatch": {k: wl.plan[k] for k in ("variant", "bn", "ctas", "seg_max")}},
-        "tflops": round(world * wl.flops_per_step / (ms * 1e-3) / 1e12, 2),
+        "tflops": round(job_rate(wl.flops_per_step, ms, world) / 1e12, 2),
         "roofline": roof,
-        "e2e": {"value": round(world * wl.bytes_per_step / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(job_rate(wl.bytes_per_step, e2e, world) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
                 "path": "public API (Python binding -> C ABI) captured in a CUDA graph with the pinned "
                         "host<->device copies of every step, uploads and downloads on two more streams so that "
                         "each layer waits only for its own input and results leave while later layers run",
                 "eager_ms_per_step": round(e2e_eager, 4),
-                "eager_value": round(world * wl.bytes_per_step / (e2e_eager * 1e-3) / 1e9, 1)},
+                "eager_value": round(job_rate(wl.bytes_per_step, e2e_eager, world) / 1e9, 1)},
         "gpu_launches": K * len(launches),
         "clocks": sampler.summary(t0, t1),
     }
