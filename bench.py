@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -416,13 +417,24 @@ def traffic_record(workload: str):
         return None
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank lines: a change to a comment
+    does not change the kernel the counters were taken on.  (No string
+    literal in these sources contains a comment marker.)"""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_hash():
+    """Hash of the device code (every csrc source but the host-side api.cu),
+    comments excluded."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")) and f != "api.cu":
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -10,19 +10,24 @@
 //
 // One kernel template serves both variants the dispatcher chooses from:
 //   full tile  (swap = 0): MMA-A = 128 token rows, MMA-B = 256 weight rows,
-//              each CTA owns whole tiles and all of K (persistent, strided).
+//              each CTA owns whole tiles and all of K (persistent, strided;
+//              in bands of token tiles when the operands exceed L2).
 //   split-K    (swap = 1): MMA-A = 128 weight rows, MMA-B = the (padded)
 //              token rows; the (tile, K-block) units are cut evenly over the
 //              CTAs (stream-K); a CTA that ends a tile part-way writes an
-//              fp32 partial tile, and the last CTA to finish a tile (arrival
-//              counter) sums the partials in slot order -- a fixed order, so
-//              results are deterministic -- and writes y.
+//              fp32 partial tile.  The partials are summed in slot order -- a
+//              fixed order, so results are deterministic -- by the reduce
+//              kernel launched after the GEMM (default), by every CTA after a
+//              grid barrier, by the last CTA to finish the tile, or, for CTA
+//              pairs in a 2-CTA cluster, by the first CTA of the pair from its
+//              partner's partial in its shared memory.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (operand tiles with the
-// 128-byte swizzle, scale-factor tiles with plain bulk copies); warp 1 =
-// TMEM allocator and the single MMA-issuing thread (tcgen05.cp of the scale
-// tiles into TMEM, then the MMAs); warps 2-5 = epilogue (tcgen05.ld of their
-// 32-lane quarter).  All hand-offs are mbarriers; every wait is bounded.
+// Warp roles (192 threads): warp 0 = producer (bulk copies of operand tiles
+// and weight panels, tensor-map boxes for row-major operands, scale tiles);
+// warp 1 = TMEM allocator and the single MMA-issuing thread; warps 2-5 =
+// epilogue (tcgen05.ld of their 32-lane quarter; for the full-tile A4W4 they
+// also move each stage's scale factors into TMEM, and store y by TMA).  All
+// hand-offs are mbarriers; every wait is bounded.
 #include <cstdint>
 #include <cuda_runtime.h>
 
