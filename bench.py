@@ -427,12 +427,12 @@ def _code_only(text: str) -> str:
 
 
 def kernel_sources_hash():
-    """Hash of the device code (every csrc source but the host-side api.cu),
-    comments excluded."""
+    """Hash of the GEMM kernel's device code (gemm.cu and the headers it
+    includes), comments excluded: the code the traffic records were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")) and f != "api.cu":
+        if f.endswith((".cuh", ".h")) or f == "gemm.cu":
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
