@@ -154,9 +154,23 @@ def test_fp8_special_rows():
     check_fp8(bits_to_bf16(np.stack(rows)), "special rows")
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (64, 7168), (64, 18432), (5, 30720)])
+# rows from one to 30720 values, across the multiples of the 2048-value
+# stride of the quantizer's 256 threads
+@pytest.mark.parametrize("M,K", [(1, 128), (64, 7168), (3, 8192), (3, 8320), (64, 18432),
+                                 (2, 24576), (2, 24704), (5, 30720)])
 def test_fp8_act_shapes(M, K):
     check_fp8(synth.activation(M, K, seed=M * 7 + K), f"act {M}x{K}")
+
+
+@pytest.mark.parametrize("K", [8320, 30720])
+def test_fp8_special_rows_long(K):
+    """NaN / Inf rows, zero rows and all -0 rows in long rows."""
+    base = synth.activation(6, K, seed=K).view(torch.int16).numpy().view(np.uint16).copy()
+    base[1, :] = 0
+    base[2, 17] = 0x7FC0          # NaN
+    base[3, K - 1] = 0xFF80       # -Inf
+    base[4, :] = 0x8000           # all -0
+    check_fp8(bits_to_bf16(base), f"special rows K={K}")
 
 
 def test_fp8_gate_up_weight_full_size_sampled_rows():
