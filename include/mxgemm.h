@@ -253,7 +253,10 @@ mxg_status mx_quantize_act(const void *x_bf16, int M, int K, int ldx,
  *   a_codes == NULL and x_bf16 (M, K) with leading dimension ldx: the
  *   activations are quantized inside the call (codes and scales identical to
  *   mx_quantize_act) into the workspace.
- *   w_codes (N, K/2), w_sf (swizzled): the weight.
+ *   w_codes (N, K/2), w_sf (swizzled): the weight, row-major codes, or the
+ *   codes in the layout opts->weights_tiled names (MXG_TILED tiles, or
+ *   MXG_PANEL panels whose scales sit inside them: w_sf is then unused).
+ *   a_codes in the activation tile layout when opts->act_tile_rows != 0.
  *   y: (M, N) with leading dimension ldy elements, bf16 or fp32. */
 mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf,
                         const void *x_bf16, int ldx,
@@ -299,7 +302,10 @@ mxg_status fp8_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int
 
 /* FP8 PTPC A8W8 GEMM: y[m][n] = (acc[m][n] * sa[m]) * sw[n] with
  * acc = sum_k v(qa[m,k]) v(qw[n,k]) accumulated in fp32.
- *   qa (M, K), sa (M); qw (N, K), sw (N); y (M, N), leading dimension ldy. */
+ *   qa (M, K), sa (M); qw (N, K), sw (N); y (M, N), leading dimension ldy.
+ *   qw row-major, or in the layout opts->weights_tiled names (MXG_TILED /
+ *   MXG_PANEL); qa in the activation tile layout when opts->act_tile_rows
+ *   != 0. */
 mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
                          const uint8_t *qw, const float *sw,
                          int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
