@@ -385,18 +385,52 @@ class MlpFp8(Workload):
                                                        ws=self.ws, weights_static=True, weights_tiled=self.wt,
                                                        act_tile_rows=self.Td, k=self.I))]
 
+    E2E_CHUNK = 2048  # as OprojChain: prefill-sized batches go in row chunks
+
+    @property
+    def e2e_note(self):
+        if self.M >= 2 * self.E2E_CHUNK:
+            return f"; the {self.M}-token batch in {self.E2E_CHUNK}-token row chunks (one call per GEMM each)"
+        return ""
+
     def e2e_step(self):
-        ln = [fn for _, fn in self.launches()]
+        mx = self.mx
+        if self.M < 2 * self.E2E_CHUNK:
+            ln = [fn for _, fn in self.launches()]
 
-        def gate_up():
-            ln[0]()
-            ln[1]()
+            def gate_up():
+                ln[0]()
+                ln[1]()
 
-        def down():
-            ln[2]()
-            ln[3]()
-        self.e2e_pipelined([([(self.xg, self.xg_host)], gate_up, [(self.yg_host, self.yg)]),
-                            ([(self.xd, self.xd_host)], down, [(self.yd_host, self.yd)])])
+            def down():
+                ln[2]()
+                ln[3]()
+            self.e2e_pipelined([([(self.xg, self.xg_host)], gate_up, [(self.yg_host, self.yg)]),
+                                ([(self.xd, self.xd_host)], down, [(self.yd_host, self.yd)])])
+            return
+        rows = self.E2E_CHUNK
+        sm = torch.cuda.get_device_properties(self.dev).multi_processor_count
+
+        def chunk_part(x, x_host, qa, T, sa, qw, sw, y, y_host, K, r0, r1):
+            # a chunk's activations in the tile layout are a contiguous run of
+            # its token tiles (the full batch's tiles are T rows too)
+            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, y.shape[1], K, sm)) == T
+            tb = (K // 128) * T * 128  # bytes of one token tile
+            q = qa[(r0 // T) * tb:(r1 // T) * tb]
+
+            def run():
+                mx.fp8_quantize_act_tiled(x[r0:r1], T, q=q, scale=sa[r0:r1])
+                mx.fp8_gemm_ptpc(q, sa[r0:r1], qw, sw, out=y[r0:r1], ws=self.ws, weights_static=True,
+                                 weights_tiled=self.wt, act_tile_rows=T, k=K)
+            return ([(x[r0:r1], x_host[r0:r1])], run, [(y_host[r0:r1], y[r0:r1])])
+        parts = []
+        for r0 in range(0, self.M, rows):
+            r1 = min(self.M, r0 + rows)
+            parts.append(chunk_part(self.xg, self.xg_host, self.qa_g, self.Tg, self.sa_g, self.qg, self.sg,
+                                    self.yg, self.yg_host, self.H, r0, r1))
+            parts.append(chunk_part(self.xd, self.xd_host, self.qa_d, self.Td, self.sa_d, self.qd, self.sd,
+                                    self.yd, self.yd_host, self.I, r0, r1))
+        self.e2e_pipelined(parts)
 
 
 def make_workload(name, mx, synth, dev):
