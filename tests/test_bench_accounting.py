@@ -1,0 +1,50 @@
+"""The algorithmic bytes bench.py divides by (roofline 'achieved' and the
+value of every line), checked on the CPU against the library's own size
+queries and the oracle's output shapes: one unit of work moves exactly its
+operands once and its result once."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import fp8_block_scaled_dynamic_gb300 as mx
+import oracle
+
+
+def test_oproj_decode_bytes_per_launch():
+    # o_proj at M = 64: 29,360,128 weight code bytes + 1,835,008 scale bytes
+    # + 262,144 activation code bytes + 16,384 activation scale bytes + 917,504 output bytes
+    assert bench.a4w4_gemm_bytes(64, 7168, 8192) == 32_391_168
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 7168, 8192), (8, 7168, 8192), (8192, 7168, 8192), (300, 1024, 512)])
+def test_a4w4_bytes_match_size_queries(M, N, K):
+    want = (mx.mxg_weight_bytes(mx.KIND_A4W4, N, K, mx.SF_ROWMAJOR) + mx.mxg_sf_bytes(N, K, mx.SF_ROWMAJOR)
+            + mx.mxg_weight_bytes(mx.KIND_A4W4, M, K, mx.SF_ROWMAJOR) + mx.mxg_sf_bytes(M, K, mx.SF_ROWMAJOR)
+            + 2 * M * N)
+    assert bench.a4w4_gemm_bytes(M, N, K) == want
+    # bf16 activations in instead of codes and scales
+    assert bench.a4w4_fused_bytes(M, N, K) == want - M * K // 2 - M * K // 32 + 2 * M * K
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 36864, 7168), (8192, 7168, 18432)])
+def test_ptpc_bytes_match_size_queries(M, N, K):
+    want = (mx.mxg_weight_bytes(mx.KIND_PTPC, N, K, mx.SF_ROWMAJOR) + 4 * N
+            + mx.mxg_weight_bytes(mx.KIND_PTPC, M, K, mx.SF_ROWMAJOR) + 4 * M + 2 * M * N)
+    assert bench.ptpc_gemm_bytes(M, N, K) == want
+
+
+def test_quantizer_bytes_match_oracle_outputs():
+    M, K = 6, 512
+    x = torch.zeros(M, K, dtype=torch.bfloat16)
+    codes, sf = oracle.mx_quantize_rows(x)
+    assert bench.mx_quant_bytes(M, K) == x.numel() * 2 + np.asarray(codes).nbytes + np.asarray(sf).nbytes
+    q, s = oracle.fp8_quantize_rows(x)
+    assert bench.fp8_quant_bytes(M, K) == x.numel() * 2 + np.asarray(q).nbytes + np.asarray(s, np.float32).nbytes
+
+
+def test_act_tile_rows_follow_the_plan():
+    split = mx.mxg_plan_gemm(mx.KIND_A4W4, 64, 7168, 8192, 152)
+    full = mx.mxg_plan_gemm(mx.KIND_A4W4, 8192, 7168, 8192, 152)
+    assert split["variant"] == 2 and bench.act_tile_rows(split) == split["bn"] == 64
+    assert full["variant"] == 1 and bench.act_tile_rows(full) == 128
