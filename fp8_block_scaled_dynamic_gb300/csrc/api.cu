@@ -391,6 +391,7 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
     return MXG_ERR_INVALID_ARG;
   if (opts && (opts->splitk_reduce < MXG_REDUCE_DEFAULT || opts->splitk_reduce > MXG_REDUCE_PAIR))
     return MXG_ERR_INVALID_ARG;
+  if (opts && (opts->weights_tiled < 0 || opts->weights_tiled > 2)) return MXG_ERR_INVALID_ARG;
   if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
     return MXG_ERR_INVALID_ARG;
   return MXG_OK;

@@ -97,6 +97,33 @@ def test_gemm_argument_errors_before_launch():
     # bad variant
     o.variant = 9
     assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, FAKE, 8, 256, 256, FAKE, 256, 0, ctypes.byref(o), None) == 1
+    o.variant = 0
+    # bad weight layout / split-K reduction
+    o.weights_tiled = 3
+    assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, FAKE, 8, 256, 256, FAKE, 256, 0, ctypes.byref(o), None) == 1
+    o.weights_tiled = 0
+    o.splitk_reduce = 5
+    assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, 0, ctypes.byref(o), None) == 1
+    o.splitk_reduce = 0
+    # w_sf may be NULL only for weight panels
+    assert L.mx_gemm_a4w4(FAKE, FAKE, None, 0, FAKE, None, 8, 256, 256, FAKE, 256, 0, ctypes.byref(o), None) == 1
+
+
+def test_weight_quantizer_layout_errors_before_launch():
+    L = mx.lib()
+    L.mx_quantize_weight.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    # unknown layout
+    assert L.mx_quantize_weight(FAKE, 128, 256, 256, FAKE, FAKE, 4, None) == 1
+    # MXFP4 panels and tiles need K % 256 == 0; tiles also N % 128 == 0
+    assert L.mx_quantize_weight(FAKE, 128, 384, 384, FAKE, None, mx.PANEL, None) == 2
+    assert L.mx_quantize_weight(FAKE, 128, 384, 384, FAKE, FAKE, mx.TILED, None) == 2
+    assert L.mx_quantize_weight(FAKE, 200, 256, 256, FAKE, FAKE, mx.TILED, None) == 2
+    # scales are required except in panels, whose scales sit inside them
+    assert L.mx_quantize_weight(FAKE, 128, 256, 256, FAKE, None, mx.SF_SWIZZLED, None) == 1
+    # FP8 weights: no MXFP4 row-major-scales-only layout
+    assert L.fp8_quantize_weight(FAKE, 128, 256, 256, FAKE, FAKE, mx.SF_SWIZZLED, None) == 1
+    assert L.fp8_quantize_weight(FAKE, 200, 256, 256, FAKE, FAKE, mx.TILED, None) == 2
 
 
 def owner_sim(U, G):
