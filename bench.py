@@ -163,6 +163,12 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workloads
+def gemm_kernels(plan: dict) -> int:
+    """Kernels one GEMM call launches under the default split-K reduction: the
+    GEMM, plus the reduce kernel when a split-K tile has several partials."""
+    return 1 + (1 if plan["variant"] == 2 and plan["seg_max"] > 1 and not plan.get("pair") else 0)
+
+
 def act_tile_rows(plan: dict) -> int:
     """Token-tile height of the activation tile layout a GEMM plan reads:
     the MMA-N tile in split-K (tokens are the MMA-B operand), else 128."""
@@ -184,6 +190,10 @@ class Workload:
     kernel_desc = ""
 
     def launches(self):
+        raise NotImplementedError
+
+    def kernels_per_step(self):
+        """Library kernels one step launches (a GEMM call may launch two)."""
         raise NotImplementedError
 
     def e2e_step(self):
@@ -282,6 +292,10 @@ class OprojChain(Workload):
         self.h2d = layers * M * K * 2
         self.d2h = layers * M * N * 2
 
+    def kernels_per_step(self):
+        # fused: one cooperative kernel per layer; else quantizer + GEMM (+ reduce)
+        return self.n_layers * (1 if self.fused else 1 + gemm_kernels(self.plan))
+
     def launches(self):
         mx = self.mx
         out = []
@@ -347,7 +361,8 @@ class MlpFp8(Workload):
         sm = torch.cuda.get_device_properties(dev).multi_processor_count
         # activations in the tile layout of each GEMM's plan
         self.Tg = act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm))
-        self.Td = act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm))
+        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm)
+        self.Td = act_tile_rows(self.plan_d)
         self.qa_g = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, H, self.Tg), dtype=torch.uint8, device=dev)
         self.sa_g = torch.empty(M, dtype=torch.float32, device=dev)
         self.qa_d = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, synth.MLP_I, self.Td), dtype=torch.uint8,
@@ -373,6 +388,9 @@ class MlpFp8(Workload):
         self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
         self.h2d = 2 * M * H + 2 * M * synth.MLP_I
         self.d2h = 2 * M * I2 + 2 * M * H
+
+    def kernels_per_step(self):
+        return 2 + gemm_kernels(self.plan) + gemm_kernels(self.plan_d)
 
     def launches(self):
         mx = self.mx
@@ -669,7 +687,7 @@ def run_ours(args, rank, world, local_rank):
                         + getattr(wl, "e2e_note", ""),
                 "eager_ms_per_step": round(e2e_eager, 4),
                 "eager_value": round(job_rate(wl.bytes_per_step, e2e_eager, world) / 1e9, 1)},
-        "gpu_launches": K * len(launches),
+        "gpu_launches": K * wl.kernels_per_step(),
         "clocks": sampler.summary(t0, t1),
     }
     if args.cpu_baseline and world == 1:
