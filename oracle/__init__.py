@@ -26,6 +26,12 @@ test_oracle_quant.py, test_oracle_gemm.py, test_oracle_mutants.py):
   fp8_quantize_rows       -- pinned (amax = 448 row, power-of-two invariance)
   gemm_a4w4 / gemm_ptpc   -- pinned (exact rational brute force, integer
                              matmul special case)
+  exp_f32 / silu_mul_f32  -- pinned (libm exp error bound over a dense scan,
+                             scipy expit, the closed-form minimum of silu
+                             via Lambert W, the identity silu(g) - silu(-g)
+                             = g, saturation silu(g) = g for large g)
+  swiglu_rows             -- pinned (gate/up order and bf16 rounding against
+                             closed forms and torch's bf16 cast)
   sf_swizzle              -- bijection only; its placement is pinned on the
                              GPU by one-hot GEMMs (not from the pages)
 """
@@ -107,6 +113,14 @@ def lib():
                                     ctypes.c_int, ctypes.c_int, i32p,
                                     ctypes.c_int, f64p, f64p]
         L.orc_gemm_ptpc.restype = None
+        L.orc_exp_f32.argtypes = [ctypes.c_float]
+        L.orc_exp_f32.restype = ctypes.c_float
+        L.orc_silu_mul_f32.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.orc_silu_mul_f32.restype = ctypes.c_float
+        L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+        L.orc_f32_to_bf16.restype = ctypes.c_uint16
+        L.orc_swiglu_rows.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_longlong, u16p]
+        L.orc_swiglu_rows.restype = None
         L.orc_num_threads.argtypes = []
         L.orc_num_threads.restype = ctypes.c_int
         _lib = L
@@ -265,6 +279,41 @@ def gemm_ptpc(qa, sa, qw, sw, rows=None):
                         M, N, K, None if idx is None else _ptr(idx, ctypes.c_int),
                         nrows, _ptr(ref, ctypes.c_double), _ptr(bound, ctypes.c_double))
     return ref, bound
+
+
+# ---- SwiGLU between gate_up and down --------------------------------------
+def exp_f32(t: float) -> float:
+    """e^t in binary32 by the Cody-Waite method the SwiGLU uses (R17)."""
+    return lib().orc_exp_f32(t)
+
+
+def silu_mul_f32(g: float, u: float) -> float:
+    """silu(g) * u in binary32, one IEEE operation at a time (R14, R17)."""
+    return lib().orc_silu_mul_f32(g, u)
+
+
+def f32_to_bf16(f: float) -> int:
+    return lib().orc_f32_to_bf16(f)
+
+
+def swiglu_rows(gu):
+    """gu: (rows, 2I) bf16 gate_up output [gate | up] -> h (rows, I) as uint16
+    bf16 bits, h = bf16(silu(gate) * up) (R14-R17)."""
+    gb = _as_bf16_bits(gu)
+    rows, I2 = gb.shape
+    assert I2 % 2 == 0
+    I = I2 // 2
+    h = np.zeros((rows, I), np.uint16)
+    lib().orc_swiglu_rows(_ptr(gb, ctypes.c_uint16), rows, I, I2, _ptr(h, ctypes.c_uint16))
+    return h
+
+
+def swiglu_fp8_quantize_rows(gu):
+    """The fused step between gate_up and down: h = swiglu_rows(gu), then the
+    per-token FP8 quantization of h.  Returns (h bits, q, s)."""
+    h = swiglu_rows(gu)
+    q, s = fp8_quantize_rows(h)
+    return h, q, s
 
 
 def num_threads() -> int:

@@ -391,6 +391,102 @@ void orc_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw,
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* SwiGLU between the packed gate_up projection and the down projection.     */
+/* [P2] packs gate_proj and up_proj into one runtime gate_up_proj; the      */
+/* pages do not name the activation between it and down_proj.  Readings:    */
+/*  R14 the activation is SwiGLU: h = silu(gate) * up, silu(g) = g/(1+e^-g). */
+/*  R15 a gate_up output row is [gate (I values) | up (I values)]: the two   */
+/*      projections concatenated along the output axis, gate first.          */
+/*  R16 h is rounded to bf16 (round to nearest even), the dtype in which     */
+/*      the draft layers pass activations between linears, and the down     */
+/*      projection's input is then quantized per token exactly as any other  */
+/*      activation (orc_fp8_quantize_rows).                                  */
+/*  R17 silu and the product are formed in binary32, one IEEE operation at   */
+/*      a time, in the order written below, so that any IEEE machine gets    */
+/*      the same h (and therefore the same FP8 codes).  e^t comes from the   */
+/*      method of W. J. Cody and W. Waite (Software Manual for the           */
+/*      Elementary Functions, 1980): n = nearest integer to t / ln2;         */
+/*      r = (t - n*L1) - n*L2 with ln2 = L1 + L2 split so that n*L1 is exact */
+/*      (L1 has 15 significant bits, |n| <= 128); e^r from its Taylor series */
+/*      through r^7/7! (|r| <= ln2/2, the first dropped term is below 1e-8   */
+/*      relative), summed by Horner's rule; then the exact scaling by 2^n.   */
+/* ------------------------------------------------------------------------ */
+static float f32_from_bits(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* e^t in binary32 for the SwiGLU (R17).  Below t = -87.3 the result would
+ * be subnormal and is returned as 0; above ln(FLT_MAX) it is +inf. */
+float orc_exp_f32(float t)
+{
+    const float log2e = 0x1.715476p+0f;   /* 1/ln2 rounded to binary32 */
+    const float L1 = 0x1.62e4p-1f;        /* 0.693145751953125: 15 significant bits */
+    const float L2 = 0x1.7f7d1cp-20f;     /* ln2 - L1 rounded to binary32 */
+    const float c2 = 0.5f, c3 = 0x1.555556p-3f, c4 = 0x1.555556p-5f, c5 = 0x1.111112p-7f,
+                c6 = 0x1.6c16c2p-10f, c7 = 0x1.a01a02p-13f; /* 1/k! rounded to binary32 */
+    float nf, r, p;
+    int n;
+    if (t != t)
+        return t;
+    if (t > 88.72283f)
+        return INFINITY;
+    if (t < -87.3f)
+        return 0.0f;
+    nf = rintf(t * log2e);
+    n = (int)nf;
+    r = t - nf * L1;
+    r = r - nf * L2;
+    p = c7;
+    p = p * r + c6;
+    p = p * r + c5;
+    p = p * r + c4;
+    p = p * r + c3;
+    p = p * r + c2;
+    p = p * r + 1.0f;
+    p = p * r + 1.0f;
+    if (n > 127)
+        return (p * f32_from_bits((uint32_t)(127 + 127) << 23)) * 2.0f;
+    return p * f32_from_bits((uint32_t)(n + 127) << 23);
+}
+
+/* silu(g) * u in binary32 (R14, R17): e = e^-g, d = 1 + e, s = g / d, s * u. */
+float orc_silu_mul_f32(float g, float u)
+{
+    float e = orc_exp_f32(-g);
+    float d = 1.0f + e;
+    float s = g / d;
+    return s * u;
+}
+
+/* binary32 -> bf16 bits, round to nearest even (a NaN stays a NaN). */
+uint16_t orc_f32_to_bf16(float f)
+{
+    uint32_t u = f32_bits(f);
+    if ((u & 0x7FFFFFFFu) > 0x7F800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* h (rows x I bf16 bits) = bf16(silu(gate) * up) for every row of the
+ * gate_up output gu (rows x 2I bf16, leading dimension ldgu, R15, R16). */
+void orc_swiglu_rows(const uint16_t *gu, int rows, int I, long long ldgu, uint16_t *h)
+{
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t *row = gu + (size_t)r * (size_t)ldgu;
+        for (int j = 0; j < I; ++j) {
+            float g = orc_bf16_to_f32(row[j]);
+            float u = orc_bf16_to_f32(row[I + j]);
+            h[(size_t)r * I + j] = orc_f32_to_bf16(orc_silu_mul_f32(g, u));
+        }
+    }
+}
+
 /* Threads OpenMP will use (1 when built without OpenMP). */
 int orc_num_threads(void)
 {

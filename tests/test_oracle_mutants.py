@@ -12,7 +12,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "mxoracle.c")
-PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_quant.py", "tests/test_oracle_gemm.py"]
+PINS = ["tests/test_oracle_formats.py", "tests/test_oracle_quant.py", "tests/test_oracle_gemm.py",
+        "tests/test_oracle_swiglu.py"]
 
 MUTANTS = {
     "e2m1_table_entry": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 4.0, 6.0}"),
@@ -29,6 +30,13 @@ MUTANTS = {
     "a4w4_wrong_weight_scale_row": ("orc_e8m0_value(w_sf[(size_t)n * G + g]);", "orc_e8m0_value(w_sf[(size_t)n * G + (G - 1 - g)]);"),
     "ptpc_channel_scale_dropped": ("acc * (double)sa[m] * (double)sw[n];", "acc * (double)sa[m];"),
     "ptpc_bound_signed": ("accabs += fabs(p);", "accabs += p;"),
+    "swiglu_gate_up_swapped": ("float g = orc_bf16_to_f32(row[j]);\n            float u = orc_bf16_to_f32(row[I + j]);",
+                               "float g = orc_bf16_to_f32(row[I + j]);\n            float u = orc_bf16_to_f32(row[j]);"),
+    "silu_exp_sign": ("float e = orc_exp_f32(-g);", "float e = orc_exp_f32(g);"),
+    "silu_one_dropped": ("float d = 1.0f + e;", "float d = 0.5f + e;"),
+    "exp_taylor_term_dropped": ("p = p * r + c6;", "p = p * r + 0.0f * c6;"),
+    "exp_reduction_low_part_sign": ("r = r - nf * L2;", "r = r + nf * L2;"),
+    "bf16_round_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u * ((u >> 16) & 1u);"),
 }
 
 
