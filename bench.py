@@ -10,10 +10,22 @@ and fed to the block-scaled A4W4 GEMM, bf16 out.  Inputs are synthetic
 flushed between timed steps (256 MiB written, then read back, so that no
 dirty line is written back inside the timed interval).
 
-Other workloads (--workload): oproj_m8 (one layer, M = 8), oproj_prefill
-(M = 8192, standalone quantization + full-tile GEMM), mlp_fp8_m64 /
-mlp_fp8_m8192 (FP8 PTPC gate_up + down), sweep (mixed-precision draft layer
-over M; one line per M).
+The default line also carries, under "extra", the other single-GPU
+workloads, each timed the same way with its own clock sample: oproj_prefill
+(M = 8192, standalone quantization + full-tile GEMM), oproj_m8 (one layer,
+M = 8) and the FP8 PTPC MLP chain at M = 64 and M = 8192 (per-token
+quantization, gate_up, fused SwiGLU + per-token quantization, down).
+--workload picks another main workload; `sweep` prints the mixed-precision
+draft layer over M, one line per M.
+
+Every GEMM call gets a device status word; after the timed steps it is read
+back, and a set bit (a bounded device wait that ran out) fails the run.
+The per-launch time of the dominant kernel comes from global-timer stamps
+the kernel writes at its first CTA's entry and its last CTA's exit, taken
+in a replay of the same step graph (event nodes around one kernel would cut
+the programmatic-launch overlap the step relies on).  On rank 0 at one GPU
+the CPU leg times the oracle on the same workload and checks the outputs
+the timed graph left behind against it.
 
 Prints ONE JSON line on rank 0 (plus one per M for the sweep).  N > 1: one
 process per GPU (torchrun), every rank runs its own replica of the workload
@@ -23,9 +35,9 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import re
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -36,12 +48,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "MXFP4 A4W4 / FP8 A8W8 GEMM TFLOPS & HBM GB/s vs GB300 roofline by M"
 FLUSH_BYTES = 256 << 20
 NOMINAL_HBM_GBS = 7900.0               # GB300 HBM3e, nominal
 DATASHEET_TFLOPS = {0: 13500.0, 1: 4500.0}  # GB300 dense FP4 / FP8 tensor, nominal
+TRACE_POINTS = 40                      # uint64 trace slots per CTA (include/mxgemm.h)
+GEMM_REL_TOL = 1e-5                    # |y - ref| <= 1e-5 * sum_k |a_k w_k| before the bf16 cast
+EXTRA_WORKLOADS = ("oproj_prefill", "oproj_m8", "mlp_fp8_m64", "mlp_fp8_m8192")
 
 
 def flush_l2(buf: torch.Tensor):
@@ -85,23 +101,20 @@ def fp8_quant_bytes(M, K):
     return 2 * M * K + M * K + 4 * M
 
 
-# ----------------------------------------------------------------- timing helpers
-class GraphEvent:
-    """A timing event that becomes an event-record node inside a CUDA graph."""
-
-    def __init__(self):
-        try:
-            self.ev = torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:  # torch without external events: plain events, eager use only
-            self.ev = torch.cuda.Event(enable_timing=True)
-
-    def record(self, stream=None):
-        self.ev.record(stream)
-
-    def elapsed_ms(self, other: "GraphEvent") -> float:
-        return self.ev.elapsed_time(other.ev)
+def swiglu_quant_bytes(M, I):
+    """Fused SwiGLU + per-token FP8 quantization: the bf16 gate_up output
+    (M, 2I) in, E4M3 codes (M, I) and one fp32 scale per token out."""
+    return 2 * M * 2 * I + M * I + 4 * M
 
 
+def mlp_chain_bytes(M, H, I):
+    """The FP8 MLP chain: x quantization, gate_up GEMM, fused SwiGLU +
+    quantization, down GEMM; each moves its operands once and its result once."""
+    return (fp8_quant_bytes(M, H) + ptpc_gemm_bytes(M, 2 * I, H) + swiglu_quant_bytes(M, I)
+            + ptpc_gemm_bytes(M, H, I))
+
+
+# ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock/throttle samples (100 ms) while the bench runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -177,8 +190,13 @@ def act_tile_rows(plan: dict) -> int:
 
 class Workload:
     """Builds resident device operands and exposes one step as a list of
-    (label, fn) launches; `timed_label` marks the dominant kernel."""
+    (label, fn) launches; `timed_label` marks the dominant kernel.
+
+    Every GEMM call passes the workload's device status word.  While the
+    traced copy of the step is captured, `trace_bufs` holds one buffer per
+    GEMM launch (in launch order) and each GEMM call takes the next one."""
     name = ""
+    key = ""
     n_layers = 1
     timed_label = ""
     kernel_bytes = 0       # algorithmic bytes of one launch of the dominant kernel
@@ -188,6 +206,27 @@ class Workload:
     dtype = ""
     bound = "hbm"
     kernel_desc = ""
+    kind = 0
+
+    def init_common(self, dev):
+        self.dev = dev
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.trace_bufs = None
+        self.trace_labels = []
+        self._tn = 0
+
+    def tr(self, label):
+        """The trace buffer of this GEMM launch (None outside the traced capture)."""
+        if self.trace_bufs is None:
+            return None
+        self.trace_labels.append(label)
+        t = self.trace_bufs[self._tn]
+        self._tn += 1
+        return t
+
+    def gemm_plans(self):
+        """(label, plan) of every GEMM launch of one step, in launch order."""
+        raise NotImplementedError
 
     def launches(self):
         raise NotImplementedError
@@ -197,6 +236,10 @@ class Workload:
         raise NotImplementedError
 
     def e2e_step(self):
+        raise NotImplementedError
+
+    def outputs(self):
+        """The step's results (device tensors) the CPU leg checks."""
         raise NotImplementedError
 
     def e2e_pipelined(self, parts):
@@ -243,15 +286,20 @@ def weight_layout(mx):
 
 
 class OprojChain(Workload):
-    """A4W4 o_proj layers: fused dynamic MXFP4 activation quantization +
-    block-scaled GEMM per layer."""
+    """A4W4 o_proj layers: dynamic MXFP4 activation quantization + block-scaled
+    GEMM per layer, the layers in sequence on one stream."""
 
-    def __init__(self, mx, synth, dev, M, layers, w_seeds, cfg, row_scale=False, name="", fused=False):
-        self.mx, self.dev = mx, dev
+    def __init__(self, mx, synth, dev, M, layers, w_seeds, cfg, row_scale=False, name="", key="",
+                 out_f32=False):
+        self.init_common(dev)
+        self.mx = mx
         N, K = synth.OPROJ_N, synth.OPROJ_K
         self.M, self.N, self.K = M, N, K
         self.n_layers = layers
-        self.name = name
+        self.name, self.key = name, key
+        self.cfg, self.row_scale, self.w_seeds = cfg, row_scale, tuple(w_seeds)
+        self.out_f32 = out_f32
+        self.kind = 0
         self.w = []
         layout, self.wt = weight_layout(mx)
         for s in w_seeds:
@@ -263,9 +311,11 @@ class OprojChain(Workload):
         self.x_host = torch.stack([synth.activation(M, K, seed=synth.act_seed(cfg, l, 0), row_scale=row_scale)
                                    for l in range(layers)]).pin_memory()
         self.x = self.x_host.to(dev)
-        self.y = torch.empty(layers, M, N, dtype=torch.bfloat16, device=dev)
-        self.y_host = torch.empty(layers, M, N, dtype=torch.bfloat16).pin_memory()
-        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count)
+        ydt = torch.float32 if out_f32 else torch.bfloat16
+        self.y = torch.empty(layers, M, N, dtype=ydt, device=dev)
+        self.y_host = torch.empty(layers, M, N, dtype=ydt).pin_memory()
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, sm)
         # activation codes in the tile layout the GEMM fetches by bulk copy
         self.T = act_tile_rows(self.plan)
         self.ac = [torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_A4W4, M, K, self.T), dtype=torch.uint8, device=dev)
@@ -273,12 +323,8 @@ class OprojChain(Workload):
         self.asf = [torch.empty(mx.mxg_sf_bytes(M, K), dtype=torch.uint8, device=dev) for _ in range(layers)]
         self.ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(mx.KIND_A4W4, True, M, N, K)),
                               dtype=torch.uint8, device=dev)
-        # fused: one launch per layer -- the GEMM's CTAs quantize x themselves
-        # (split-K plans only; slower than the three-kernel chain, kept for
-        # comparison); else the standalone quantizer, then the GEMM
-        self.fused = fused and self.plan["variant"] == 2 and K % 256 == 0
-        self.timed_label = "a4w4_fused" if self.fused else "a4w4_gemm"
-        self.kernel_bytes = a4w4_fused_bytes(M, N, K) if self.fused else a4w4_gemm_bytes(M, N, K)
+        self.timed_label = "a4w4_gemm"
+        self.kernel_bytes = a4w4_gemm_bytes(M, N, K)
         self.kernel_flops = 2 * M * N * K
         self.bytes_per_step = layers * a4w4_fused_bytes(M, N, K)
         self.flops_per_step = layers * 2 * M * N * K
@@ -286,32 +332,31 @@ class OprojChain(Workload):
         self.bound = "hbm" if M <= 512 else "tensor"
         v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
         self.kernel_desc = f"gemm_kernel<A4W4, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
-        if self.fused:
-            self.kernel_desc += (", one cooperative launch: activation quantization, grid barrier, "
-                                 "GEMM, grid barrier, split-K reduction")
         self.h2d = layers * M * K * 2
-        self.d2h = layers * M * N * 2
+        self.d2h = layers * M * N * ydt.itemsize
+
+    def gemm_plans(self):
+        return [("a4w4_gemm", self.plan)] * self.n_layers
 
     def kernels_per_step(self):
-        # fused: one cooperative kernel per layer; else quantizer + GEMM (+ reduce)
-        return self.n_layers * (1 if self.fused else 1 + gemm_kernels(self.plan))
+        # quantizer + GEMM (+ reduce) per layer
+        return self.n_layers * (1 + gemm_kernels(self.plan))
 
     def launches(self):
         mx = self.mx
         out = []
         for l in range(self.n_layers):
             wc, wsf = self.w[l]
-            if self.fused:
-                out.append(("a4w4_fused", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
-                    wc, wsf, x=self.x[l], out=self.y[l], ws=self.ws, weights_static=True, weights_tiled=self.wt,
-                    n=self.N, k=self.K, splitk_reduce="grid")))
-                continue
             out.append(("mx_quant", lambda l=l: mx.mx_quantize_act_tiled(self.x[l], self.T, codes=self.ac[l],
                                                                          sf=self.asf[l])))
             out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
-                wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], ws=self.ws,
-                weights_static=True, weights_tiled=self.wt, act_tile_rows=self.T, m=self.M, n=self.N, k=self.K)))
+                wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], out_f32=self.out_f32, ws=self.ws,
+                weights_static=True, weights_tiled=self.wt, act_tile_rows=self.T, m=self.M, n=self.N, k=self.K,
+                dev_status=self.status, trace=self.tr("a4w4_gemm"))))
         return out
+
+    def outputs(self):
+        return {"y": self.y}
 
     # prefill-sized batches go end to end in row chunks of this many tokens
     # (rows are independent), so that the upload of one chunk, the GEMM of the
@@ -330,8 +375,9 @@ class OprojChain(Workload):
 
         def gemm(l, r0, r1):
             wc, wsf = self.w[l]
-            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l][r0:r1], out=self.y[l][r0:r1], ws=self.ws,
-                            weights_tiled=self.wt, weights_static=True, n=self.N, k=self.K)
+            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l][r0:r1], out=self.y[l][r0:r1], out_f32=self.out_f32, ws=self.ws,
+                            weights_tiled=self.wt, weights_static=True, n=self.N, k=self.K,
+                            dev_status=self.status)
         parts = []
         for l in range(self.n_layers):
             for r0 in range(0, self.M, rows):
@@ -343,24 +389,31 @@ class OprojChain(Workload):
 
 
 class MlpFp8(Workload):
-    """FP8 PTPC gate_up (7168 -> 2 x 18432) + down (18432 -> 7168)."""
+    """The FP8 PTPC MLP chain: per-token FP8 quantization of x, gate_up
+    (7168 -> 2 x 18432, bf16 out), SwiGLU fused with the per-token FP8
+    quantization of its output, down (18432 -> 7168).  x, w_gu, w_down
+    (bf16 CPU tensors) replace the seeded inputs when given."""
 
-    def __init__(self, mx, synth, dev, M, name):
-        self.mx, self.dev, self.M = mx, dev, M
-        self.name = name
+    def __init__(self, mx, synth, dev, M, name, key="", out_f32=False, x=None, w_gu=None, w_down=None):
+        self.init_common(dev)
+        self.mx, self.M = mx, M
+        self.name, self.key = name, key
+        self.out_f32 = out_f32
+        self.kind = 1
         I2, H = 2 * synth.MLP_I, 7168
         self.H, self.I = H, synth.MLP_I
         layout, self.wt = weight_layout(mx)
-        self.qg, self.sg = mx.fp8_quantize_weight(synth.weight(I2, H, seed=synth.SEED_CFG3_GATE_UP).to(dev),
-                                                  layout=layout)
-        self.qd, self.sd = mx.fp8_quantize_weight(synth.weight(H, synth.MLP_I, seed=synth.SEED_CFG3_DOWN).to(dev),
-                                                  layout=layout)
-        self.xg_host = synth.activation(M, H, seed=synth.act_seed(3, 0, 0)).pin_memory()
-        self.xd_host = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1)).pin_memory()
-        self.xg, self.xd = self.xg_host.to(dev), self.xd_host.to(dev)
+        w_gu = synth.weight(I2, H, seed=synth.SEED_CFG3_GATE_UP) if w_gu is None else w_gu
+        w_down = synth.weight(H, synth.MLP_I, seed=synth.SEED_CFG3_DOWN) if w_down is None else w_down
+        self.qg, self.sg = mx.fp8_quantize_weight(w_gu.to(dev), layout=layout)
+        self.qd, self.sd = mx.fp8_quantize_weight(w_down.to(dev), layout=layout)
+        x = synth.activation(M, H, seed=synth.act_seed(3, 0, 0)) if x is None else x
+        self.x_host = x.contiguous().pin_memory()
+        self.x = self.x_host.to(dev)
         sm = torch.cuda.get_device_properties(dev).multi_processor_count
         # activations in the tile layout of each GEMM's plan
-        self.Tg = act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm))
+        self.plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm)
+        self.Tg = act_tile_rows(self.plan)
         self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm)
         self.Td = act_tile_rows(self.plan_d)
         self.qa_g = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, H, self.Tg), dtype=torch.uint8, device=dev)
@@ -368,103 +421,312 @@ class MlpFp8(Workload):
         self.qa_d = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, synth.MLP_I, self.Td), dtype=torch.uint8,
                                 device=dev)
         self.sa_d = torch.empty(M, dtype=torch.float32, device=dev)
+        # the gate_up output is the SwiGLU's bf16 input in either output mode
         self.yg = torch.empty(M, I2, dtype=torch.bfloat16, device=dev)
-        self.yd = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-        self.yg_host = torch.empty(M, I2, dtype=torch.bfloat16).pin_memory()
-        self.yd_host = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+        ydt = torch.float32 if out_f32 else torch.bfloat16
+        self.yd = torch.empty(M, H, dtype=ydt, device=dev)
+        self.yd_host = torch.empty(M, H, dtype=ydt).pin_memory()
         wsb = max(mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, I2, H),
                   mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, H, synth.MLP_I), 1 << 20)
         self.ws = torch.zeros(wsb, dtype=torch.uint8, device=dev)
-        self.plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm)
         self.timed_label = "ptpc_gate_up"
         self.kernel_bytes = ptpc_gemm_bytes(M, I2, H)
         self.kernel_flops = 2 * M * I2 * H
-        self.bytes_per_step = (fp8_quant_bytes(M, H) + ptpc_gemm_bytes(M, I2, H) +
-                               fp8_quant_bytes(M, synth.MLP_I) + ptpc_gemm_bytes(M, H, synth.MLP_I))
+        self.bytes_per_step = mlp_chain_bytes(M, H, synth.MLP_I)
         self.flops_per_step = 2 * M * I2 * H + 2 * M * H * synth.MLP_I
         self.dtype = "e4m3 x e4m3 -> f32 (bf16 out)"
         self.bound = "hbm" if M <= 256 else "tensor"
         v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
         self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
-        self.h2d = 2 * M * H + 2 * M * synth.MLP_I
-        self.d2h = 2 * M * I2 + 2 * M * H
+        self.h2d = 2 * M * H
+        self.d2h = M * H * ydt.itemsize
+
+    def gemm_plans(self):
+        return [("ptpc_gate_up", self.plan), ("ptpc_down", self.plan_d)]
 
     def kernels_per_step(self):
+        # x quantizer, gate_up (+ reduce), SwiGLU + quantizer, down (+ reduce)
         return 2 + gemm_kernels(self.plan) + gemm_kernels(self.plan_d)
 
-    def launches(self):
+    def chain(self, r0, r1, qa_g, qa_d, trace=False):
+        """The launches of token rows [r0, r1) (qa_g / qa_d: their token tiles)."""
         mx = self.mx
-        return [("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xg, self.Tg, q=self.qa_g, scale=self.sa_g)),
-                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(self.qa_g, self.sa_g, self.qg, self.sg, out=self.yg,
-                                                          ws=self.ws, weights_static=True, weights_tiled=self.wt,
-                                                          act_tile_rows=self.Tg, k=self.H)),
-                ("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.xd, self.Td, q=self.qa_d, scale=self.sa_d)),
-                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(self.qa_d, self.sa_d, self.qd, self.sd, out=self.yd,
-                                                       ws=self.ws, weights_static=True, weights_tiled=self.wt,
-                                                       act_tile_rows=self.Td, k=self.I))]
+        sl = slice(r0, r1)
+        return [("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.x[sl], self.Tg, q=qa_g, scale=self.sa_g[sl])),
+                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(
+                    qa_g, self.sa_g[sl], self.qg, self.sg, out=self.yg[sl], ws=self.ws,
+                    weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Tg, k=self.H,
+                    dev_status=self.status, trace=self.tr("ptpc_gate_up") if trace else None)),
+                ("swiglu_fp8", lambda: mx.swiglu_fp8_quantize(self.yg[sl], self.Td, q=qa_d, scale=self.sa_d[sl])),
+                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(
+                    qa_d, self.sa_d[sl], self.qd, self.sd, out=self.yd[sl], out_f32=self.out_f32, ws=self.ws,
+                    weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Td, k=self.I,
+                    dev_status=self.status, trace=self.tr("ptpc_down") if trace else None))]
+
+    def launches(self):
+        return self.chain(0, self.M, self.qa_g, self.qa_d, trace=True)
+
+    def outputs(self):
+        return {"yg": self.yg, "yd": self.yd, "qh": self.qa_d, "sh": self.sa_d}
 
     E2E_CHUNK = 2048  # as OprojChain: prefill-sized batches go in row chunks
 
     @property
     def e2e_note(self):
         if self.M >= 2 * self.E2E_CHUNK:
-            return f"; the {self.M}-token batch in {self.E2E_CHUNK}-token row chunks (one call per GEMM each)"
+            return f"; the {self.M}-token batch in {self.E2E_CHUNK}-token row chunks (one chain each)"
         return ""
 
     def e2e_step(self):
-        mx = self.mx
-        if self.M < 2 * self.E2E_CHUNK:
-            ln = [fn for _, fn in self.launches()]
-
-            def gate_up():
-                ln[0]()
-                ln[1]()
-
-            def down():
-                ln[2]()
-                ln[3]()
-            self.e2e_pipelined([([(self.xg, self.xg_host)], gate_up, [(self.yg_host, self.yg)]),
-                                ([(self.xd, self.xd_host)], down, [(self.yd_host, self.yd)])])
-            return
-        rows = self.E2E_CHUNK
+        rows = self.E2E_CHUNK if self.M >= 2 * self.E2E_CHUNK else self.M
         sm = torch.cuda.get_device_properties(self.dev).multi_processor_count
-
-        def chunk_part(x, x_host, qa, T, sa, qw, sw, y, y_host, K, r0, r1):
-            # a chunk's activations in the tile layout are a contiguous run of
-            # its token tiles (the full batch's tiles are T rows too)
-            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, y.shape[1], K, sm)) == T
-            tb = (K // 128) * T * 128  # bytes of one token tile
-            q = qa[(r0 // T) * tb:(r1 // T) * tb]
-
-            def run():
-                mx.fp8_quantize_act_tiled(x[r0:r1], T, q=q, scale=sa[r0:r1])
-                mx.fp8_gemm_ptpc(q, sa[r0:r1], qw, sw, out=y[r0:r1], ws=self.ws, weights_static=True,
-                                 weights_tiled=self.wt, act_tile_rows=T, k=K)
-            return ([(x[r0:r1], x_host[r0:r1])], run, [(y_host[r0:r1], y[r0:r1])])
+        mx = self.mx
         parts = []
         for r0 in range(0, self.M, rows):
             r1 = min(self.M, r0 + rows)
-            parts.append(chunk_part(self.xg, self.xg_host, self.qa_g, self.Tg, self.sa_g, self.qg, self.sg,
-                                    self.yg, self.yg_host, self.H, r0, r1))
-            parts.append(chunk_part(self.xd, self.xd_host, self.qa_d, self.Td, self.sa_d, self.qd, self.sd,
-                                    self.yd, self.yd_host, self.I, r0, r1))
+            # a chunk's activations in the tile layout are a contiguous run of
+            # its token tiles (the full batch's tiles have the same height)
+            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, 2 * self.I, self.H, sm)) == self.Tg
+            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, self.H, self.I, sm)) == self.Td
+            tg = (self.H // 128) * self.Tg * 128
+            td = (self.I // 128) * self.Td * 128
+            qa_g = self.qa_g[(r0 // self.Tg) * tg:-(-r1 // self.Tg) * tg]
+            qa_d = self.qa_d[(r0 // self.Td) * td:-(-r1 // self.Td) * td]
+            ln = [fn for _, fn in self.chain(r0, r1, qa_g, qa_d)]
+            parts.append(([(self.x[r0:r1], self.x_host[r0:r1])], lambda ln=ln: [f() for f in ln],
+                          [(self.yd_host[r0:r1], self.yd[r0:r1])]))
         self.e2e_pipelined(parts)
 
 
-def make_workload(name, mx, synth, dev):
-    if name == "oproj_decode":
-        return OprojChain(mx, synth, dev, 64, 5, synth.SEEDS_CFG1_W, 1,
-                          name="A4W4 o_proj decode chain: M=64 (conc 8 x 8 tokens), N=7168, K=8192, 5 layers")
-    if name == "oproj_m8":
-        return OprojChain(mx, synth, dev, 8, 1, (synth.SEED_CFG0_W,), 0,
-                          name="A4W4 o_proj single layer: M=8 (1 verified + 7 drafted), N=7168, K=8192")
-    if name == "oproj_prefill":
-        return OprojChain(mx, synth, dev, 8192, 1, (synth.SEED_CFG2_W,), 2, row_scale=True,
-                          name="A4W4 o_proj prefill: M=8192 (8 x 1024 tokens), N=7168, K=8192")
-    if name in ("mlp_fp8_m64", "mlp_fp8_m8192"):
-        M = 64 if name.endswith("m64") else 8192
-        return MlpFp8(mx, synth, dev, M, name=f"FP8 PTPC MLP pair: M={M}, gate_up 7168->36864, down 18432->7168")
-    raise SystemExit(f"unknown workload {name}")
+WORKLOAD_NAMES = {
+    "oproj_decode": "A4W4 o_proj decode chain: M=64 (conc 8 x 8 tokens), N=7168, K=8192, 5 layers",
+    "oproj_m8": "A4W4 o_proj single layer: M=8 (1 verified + 7 drafted), N=7168, K=8192",
+    "oproj_prefill": "A4W4 o_proj prefill: M=8192 (8 x 1024 tokens), N=7168, K=8192",
+    "mlp_fp8_m64": "FP8 PTPC MLP chain: M=64, quant, gate_up 7168->36864, SwiGLU+quant, down 18432->7168",
+    "mlp_fp8_m8192": "FP8 PTPC MLP chain: M=8192, quant, gate_up 7168->36864, SwiGLU+quant, down 18432->7168",
+}
+
+
+def make_workload(key, mx, synth, dev, out_f32=False):
+    name = WORKLOAD_NAMES.get(key)
+    if key == "oproj_decode":
+        return OprojChain(mx, synth, dev, 64, 5, synth.SEEDS_CFG1_W, 1, name=name, key=key, out_f32=out_f32)
+    if key == "oproj_m8":
+        return OprojChain(mx, synth, dev, 8, 1, (synth.SEED_CFG0_W,), 0, name=name, key=key, out_f32=out_f32)
+    if key == "oproj_prefill":
+        return OprojChain(mx, synth, dev, 8192, 1, (synth.SEED_CFG2_W,), 2, row_scale=True, name=name, key=key,
+                          out_f32=out_f32)
+    if key in ("mlp_fp8_m64", "mlp_fp8_m8192"):
+        M = 64 if key.endswith("m64") else 8192
+        return MlpFp8(mx, synth, dev, M, name=name, key=key, out_f32=out_f32)
+    raise SystemExit(f"unknown workload {key}")
+
+
+def workload_config(key, world=1):
+    """The config dict of a workload line (the same for both arms)."""
+    return {"workload": WORKLOAD_NAMES[key], "key": key,
+            "l2": "flushed between steps (256 MiB write + read back, outside the timed interval)",
+            "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
+            "weights": f"{WEIGHTS} layout, resident in HBM"}
+
+
+# ----------------------------------------------------------------- step graphs
+def capture_step(wl, stream, traced=False):
+    """One step of `wl` as a CUDA graph (kernels only, so that consecutive
+    kernels overlap through programmatic dependent launch).  traced: every
+    GEMM launch records its CTAs' global-timer stamps into a buffer of its own
+    (wl.trace_bufs, zero-filled before each replay by the caller)."""
+    if traced:
+        plans = wl.gemm_plans()
+        wl.trace_bufs = [torch.zeros(p["ctas"] * TRACE_POINTS, dtype=torch.int64, device=wl.dev)
+                         for _, p in plans]
+        wl.trace_labels = []
+        wl._tn = 0
+    launches = wl.launches()
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            for _, fn in launches:
+                fn()
+    finally:
+        bufs = wl.trace_bufs
+        wl.trace_bufs = None
+    return graph, (bufs if traced else None)
+
+
+def read_spans(bufs, labels):
+    """Per GEMM launch of one replay: (label, span ms = first CTA entry to last
+    CTA exit, after-wait ms = first return from the dependency wait to last
+    exit, reduce span ms or None, first entry ns, last exit ns)."""
+    out = []
+    for b, lab in zip(bufs, labels):
+        t = b.view(-1, TRACE_POINTS).cpu().numpy()
+        entry, exit_, waited = t[:, 16], t[:, 17], t[:, 20]
+        e0, e1 = int(entry.min()), int(exit_.max())
+        w0 = int(waited[waited > 0].min()) if (waited > 0).any() else e0
+        red = None
+        if t[0, 22] != 0:
+            r0 = int(np.uint64(t[0, 22]) ^ np.uint64(0xFFFFFFFFFFFFFFFF))
+            red = (int(t[0, 23]) - r0) / 1e6
+            e1r = int(t[0, 23])
+        else:
+            e1r = e1
+        out.append((lab, (e1 - e0) / 1e6, (e1 - w0) / 1e6, red, e0, e1r))
+    return out
+
+
+def measure(wl, stream, flush, steps, warmup, min_warmup_s, device_index, world=1, e2e=True):
+    """Time one workload: plain graph (the number), traced graph (per-kernel
+    spans), status word, clocks, and optionally the end-to-end path."""
+    mx = wl.mx
+    launches = wl.launches()
+    with torch.cuda.stream(stream):  # eager warm-up (sets kernel attributes)
+        for _, fn in launches:
+            fn()
+    stream.synchronize()
+    graph, _ = capture_step(wl, stream)
+    graph_t, bufs = capture_step(wl, stream, traced=True)
+    labels = list(wl.trace_labels)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(device_index)
+    sampler.start()
+    t_w = time.time()
+    i = 0
+    with torch.cuda.stream(stream):
+        while i < warmup or time.time() - t_w < min_warmup_s:
+            flush_l2(flush)
+            graph.replay()
+            i += 1
+            if i % 50 == 0:
+                stream.synchronize()
+    stream.synchronize()
+
+    st_s = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    st_e = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_l2(flush)
+            st_s[i].record(stream)
+            graph.replay()
+            st_e[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in zip(st_s, st_e))
+    status = mx.mxg_query_status(wl.status, stream)
+    # the results of the last timed replay, for the CPU leg
+    outs = {k: v.detach().cpu() for k, v in wl.outputs().items()}
+
+    # per-launch spans from the traced copy of the same graph
+    spans = []
+    step_t = []
+    with torch.cuda.stream(stream):
+        for r in range(max(3, min(steps, 30))):
+            for b in bufs:
+                b.zero_()
+            flush_l2(flush)
+            a = torch.cuda.Event(enable_timing=True)
+            b_ = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph_t.replay()
+            b_.record(stream)
+            stream.synchronize()
+            step_t.append(a.elapsed_time(b_))
+            spans.append(read_spans(bufs, labels))
+    status_t = mx.mxg_query_status(wl.status, stream)
+
+    res = {"ms": ms, "clocks": clocks, "status": status, "status_traced": status_t, "outputs": outs,
+           "steps": steps}
+    lab_span = {}
+    for rep in spans:
+        for lab, sp, aw, red, _, _ in rep:
+            d = lab_span.setdefault(lab, {"span": [], "after_wait": [], "reduce": []})
+            d["span"].append(sp)
+            d["after_wait"].append(aw)
+            if red is not None:
+                d["reduce"].append(red)
+    res["kernel_spans"] = {lab: {"span_ms": round(statistics.mean(d["span"]), 5),
+                                 "after_wait_ms": round(statistics.mean(d["after_wait"]), 5),
+                                 "reduce_span_ms": round(statistics.mean(d["reduce"]), 5) if d["reduce"] else None,
+                                 "launches_per_step": sum(1 for l in labels if l == lab)}
+                           for lab, d in lab_span.items()}
+    # A GEMM launch's CTAs become resident only once the GEMM before it has
+    # left the SMs, so the GEMM spans of one step are disjoint: their sum must
+    # fit inside the step (the reduce and quantizer kernels overlap them)
+    per_step_sum = [sum(sp for (_, sp, _, _, _, _) in rep) for rep in spans]
+    res["trace_step_ms"] = statistics.mean(step_t)
+    res["trace_span_sum_ms"] = statistics.mean(per_step_sum)
+    res["kernel_ms"] = res["kernel_spans"][wl.timed_label]["span_ms"]
+
+    if e2e:
+        ke = max(3, min(steps, 50))
+        with torch.cuda.stream(stream):
+            wl.e2e_step()
+        stream.synchronize()
+        graph_e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_e, stream=stream):
+            wl.e2e_step()
+
+        def time_e2e(run):
+            ts = []
+            with torch.cuda.stream(stream):
+                for i in range(ke + 2):
+                    flush_l2(flush)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    run()
+                    b.record(stream)
+                    stream.synchronize()
+                    if i >= 2:
+                        ts.append(a.elapsed_time(b))
+            return statistics.mean(ts)
+        res["e2e_ms"] = time_e2e(graph_e.replay)
+        res["e2e_eager_ms"] = time_e2e(wl.e2e_step)
+        res["status_e2e"] = mx.mxg_query_status(wl.status, stream)
+        del graph_e
+    del graph, graph_t
+    return res
+
+
+def roofline(wl, res, hbm, bf16, peak_src, kernel_ms=None):
+    """Roofline of the dominant kernel: its algorithmic bytes (or FLOPs) per
+    launch over its traced span (first CTA entry to last CTA exit, inside the
+    step graph)."""
+    kms = res["kernel_ms"] if kernel_ms is None else kernel_ms
+    achieved_gbs = wl.kernel_bytes / (kms * 1e-3) / 1e9
+    achieved_tf = wl.kernel_flops / (kms * 1e-3) / 1e12
+    if wl.bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4), "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_of_nominal": round(achieved_gbs / NOMINAL_HBM_GBS, 4)}
+    else:
+        # FP4/FP8 dense tensor peak: the measured bf16 cuBLAS peak x the nominal ratio
+        ratio = 6.0 if wl.kind == 0 else 2.0
+        pk = bf16 * ratio
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": round(pk, 1),
+                "unit": "TFLOP/s", "frac": round(achieved_tf / pk, 4),
+                "peak_note": f"{peak_src} bf16 {bf16} TFLOP/s x nominal {'fp4' if ratio == 6 else 'fp8'}/bf16 "
+                             f"ratio {ratio}",
+                "datasheet_peak": DATASHEET_TFLOPS[wl.kind],
+                "frac_of_datasheet": round(achieved_tf / DATASHEET_TFLOPS[wl.kind], 4)}
+    roof["kernel"] = wl.kernel_desc
+    roof["kernel_ms"] = round(kms, 5)
+    roof["kernel_timing"] = ("global-timer span of each launch (first CTA entry to last CTA exit), "
+                             "from replays of the step graph with the kernel's trace stamps on; "
+                             "mean over launches and replays")
+    roof["algorithmic_bytes_per_launch"] = wl.kernel_bytes
+    roof["algorithmic_flops_per_launch"] = wl.kernel_flops
+    roof["peak_source"] = peak_src
+    return roof
 
 
 # ----------------------------------------------------------------- our arm
@@ -524,6 +786,42 @@ def job_rate(units_per_rank, ms, world):
     return world * units_per_rank / (ms * 1e-3)
 
 
+def span_check(res):
+    """The traced spans of one step's kernels fit inside the traced step."""
+    return bool(res["trace_span_sum_ms"] <= res["trace_step_ms"] * 1.02 + 0.002)
+
+
+def workload_summary(wl, res, hbm, bf16, peak_src, world):
+    """The measured figures of one workload (also the 'extra' entries)."""
+    ms = res["ms"]
+    d = {"ms_per_step": round(ms, 5),
+         "value": round(job_rate(wl.bytes_per_step, ms, world) / 1e9, 1), "unit": "GB/s",
+         "tflops": round(job_rate(wl.flops_per_step, ms, world) / 1e12, 2),
+         "dtype": wl.dtype,
+         "roofline": roofline(wl, res, hbm, bf16, peak_src),
+         "kernel_spans": res["kernel_spans"],
+         "trace_step_ms": round(res["trace_step_ms"], 5),
+         "trace_span_sum_ms": round(res["trace_span_sum_ms"], 5),
+         "spans_fit_step": span_check(res),
+         "step_frac_of_hbm": round(wl.bytes_per_step / (ms * 1e-3) / 1e9 / hbm, 4),
+         "dispatch": {lab: {k: p[k] for k in ("variant", "bn", "ctas", "seg_max")}
+                      for lab, p in dict(wl.gemm_plans()).items()},
+         "gpu_launches": res["steps"] * wl.kernels_per_step(),
+         "status_ok": res["status"] == 0 and res["status_traced"] == 0 and res.get("status_e2e", 0) == 0,
+         "clocks": res["clocks"]}
+    if "e2e_ms" in res:
+        d["e2e"] = {"value": round(job_rate(wl.bytes_per_step, res["e2e_ms"], world) / 1e9, 1), "unit": "GB/s",
+                    "ms_per_step": round(res["e2e_ms"], 4), "h2d_bytes_per_step": wl.h2d,
+                    "d2h_bytes_per_step": wl.d2h,
+                    "path": "public API (Python binding -> C ABI) captured in a CUDA graph with the pinned "
+                            "host<->device copies of every step, uploads and downloads on two more streams so that "
+                            "each layer waits only for its own input and results leave while later layers run"
+                            + getattr(wl, "e2e_note", ""),
+                    "eager_ms_per_step": round(res["e2e_eager_ms"], 4),
+                    "eager_value": round(job_rate(wl.bytes_per_step, res["e2e_eager_ms"], world) / 1e9, 1)}
+    return d
+
+
 def run_ours(args, rank, world, local_rank):
     import fp8_block_scaled_dynamic_gb300 as mx
     import synth
@@ -531,225 +829,219 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     mx.lib()
-    wl = make_workload(args.workload, mx, synth, dev)
+    hbm, bf16, peak_src = load_peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    launches = wl.launches()
-    n_timed = sum(1 for lab, _ in launches if lab == wl.timed_label)
 
-    # eager warm-up (sets kernel attributes), then capture one step as a graph
-    with torch.cuda.stream(stream):
-        for _, fn in launches:
-            fn()
-    stream.synchronize()
-    # One step as a CUDA graph (kernels only, so that consecutive kernels can
-    # overlap through programmatic dependent launch) ...
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for _, fn in launches:
-            fn()
-    # ... and an instrumented copy with event-record nodes around each launch
-    # of the dominant kernel, for its per-launch duration (roofline).
-    ev_pairs = [(GraphEvent(), GraphEvent()) for _ in range(n_timed)]
-    graph_k = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_k, stream=stream):
-        k = 0
-        for lab, fn in launches:
-            if lab == wl.timed_label:
-                ev_pairs[k][0].record()
-                fn()
-                ev_pairs[k][1].record()
-                k += 1
-            else:
-                fn()
-    torch.cuda.synchronize()
+    wl = make_workload(args.workload, mx, synth, dev)
+    res = measure(wl, stream, flush, args.steps, args.warmup, args.min_warmup_s, local_rank, world)
+    ms, kms, e2e, e2e_eager = max_over_ranks([res["ms"], res["kernel_ms"], res["e2e_ms"], res["e2e_eager_ms"]],
+                                             dev, world)
+    res["ms"], res["kernel_ms"], res["e2e_ms"], res["e2e_eager_ms"] = ms, kms, e2e, e2e_eager
+    main = workload_summary(wl, res, hbm, bf16, peak_src, world)
+    main["roofline"]["traffic"] = traffic_record(args.workload)
+    if wl.bound == "tensor":
+        loop = mx.mxg_mma_peak(wl.kind, 256)
+        main["roofline"]["mma_loop_peak"] = round(loop, 1)
+        main["roofline"]["frac_of_mma_loop"] = round(main["roofline"]["achieved"] / loop, 4)
+    outputs = {args.workload: res["outputs"]}
+    del wl, res
+    torch.cuda.empty_cache()
 
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    # warm-up: at least W steps and ~0.5 s of load so clocks settle
-    t_w = time.time()
-    i = 0
-    with torch.cuda.stream(stream):
-        while i < args.warmup or time.time() - t_w < args.min_warmup_s:
-            flush_l2(flush)
-            graph.replay()
-            i += 1
-            if i % 50 == 0:
-                stream.synchronize()
-    stream.synchronize()
-
-    K = args.steps
-    st_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    st_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = time.time()
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            flush_l2(flush)
-            st_s[i].record(stream)
-            graph.replay()
-            st_e[i].record(stream)
-    torch.cuda.synchronize()
-    t1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
-    sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b in zip(st_s, st_e)]
-    ms = statistics.mean(step_ms)
-    # per-launch duration of the dominant kernel (instrumented graph)
-    kern_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(max(3, min(K, 50))):
-            flush_l2(flush)
-            graph_k.replay()
-            stream.synchronize()
-            kern_ms.extend(a.elapsed_ms(b) for a, b in ev_pairs)
-    kms = statistics.mean(kern_ms)
-    ms, kms = max_over_ranks([ms, kms], dev, world)
-
-    # end to end through the public API: pinned host inputs in, results out,
-    # every step; the calls captured once in a CUDA graph (copies + library
-    # calls), as a serving loop runs them, and also launched eagerly
-    ke = max(3, min(K, 50))
-    with torch.cuda.stream(stream):
-        wl.e2e_step()
-    stream.synchronize()
-    graph_e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_e, stream=stream):
-        wl.e2e_step()
-
-    def time_e2e(run):
-        ts = []
-        with torch.cuda.stream(stream):
-            for i in range(ke + 2):
-                flush_l2(flush)
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                run()
-                b.record(stream)
-                stream.synchronize()
-                if i >= 2:
-                    ts.append(a.elapsed_time(b))
-        return statistics.mean(ts)
-    e2e = time_e2e(graph_e.replay)
-    e2e_eager = time_e2e(wl.e2e_step)
-    e2e, e2e_eager = max_over_ranks([e2e, e2e_eager], dev, world)
+    extras = {}
+    if args.extras:
+        for key in EXTRA_WORKLOADS:
+            if key == args.workload:
+                continue
+            w2 = make_workload(key, mx, synth, dev)
+            steps = max(5, min(args.steps, 50))
+            r2 = measure(w2, stream, flush, steps, args.warmup, 0.2, local_rank, world, e2e=False)
+            r2["ms"], r2["kernel_ms"] = max_over_ranks([r2["ms"], r2["kernel_ms"]], dev, world)
+            e = workload_summary(w2, r2, hbm, bf16, peak_src, world)
+            e["steps"] = steps
+            e["workload"] = w2.name
+            extras[key] = e
+            outputs[key] = r2["outputs"]
+            del w2, r2
+            torch.cuda.empty_cache()
 
     if rank != 0:
-        return
-    hbm, bf16, peak_src = load_peaks()
-    gbs = job_rate(wl.bytes_per_step, ms, world) / 1e9
-    achieved_gbs = wl.kernel_bytes / (kms * 1e-3) / 1e9
-    achieved_tf = wl.kernel_flops / (kms * 1e-3) / 1e12
-    if wl.bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved_gbs / hbm, 4)}
-    else:
-        # FP4/FP8 dense tensor peak: the measured bf16 cuBLAS peak x the nominal ratio
-        ratio = 6.0 if "e2m1" in wl.dtype else 2.0
-        pk = bf16 * ratio
-        roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": round(pk, 1),
-                "unit": "TFLOP/s", "frac": round(achieved_tf / pk, 4),
-                "peak_note": f"{peak_src} bf16 {bf16} TFLOP/s x nominal {'fp4' if ratio == 6 else 'fp8'}/bf16 ratio {ratio}"}
-    if wl.bound == "hbm":
-        roof["nominal_peak"] = NOMINAL_HBM_GBS
-        roof["frac_of_nominal"] = round(achieved_gbs / NOMINAL_HBM_GBS, 4)
-    else:
-        kind = 0 if "e2m1" in wl.dtype else 1
-        loop = mx.mxg_mma_peak(kind, 256)
-        roof["mma_loop_peak"] = round(loop, 1)
-        roof["frac_of_mma_loop"] = round(achieved_tf / loop, 4)
-        roof["datasheet_peak"] = DATASHEET_TFLOPS[kind]
-        roof["frac_of_datasheet"] = round(achieved_tf / DATASHEET_TFLOPS[kind], 4)
-    roof["traffic"] = traffic_record(args.workload)
-    roof["kernel"] = wl.kernel_desc
-    roof["kernel_ms"] = round(kms, 5)
-    roof["peak_source"] = peak_src
+        return 0
+    status_ok = main["status_ok"] and all(e["status_ok"] for e in extras.values())
     line = {
-        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "metric": METRIC, "value": main["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": main["dtype"],
         "data": "synthetic (seeded bf16 N(0,1) activations with 0.1% x50 outliers, N(0,0.02) weights)",
-        "config": {"workload": wl.name, "key": args.workload, "l2": "flushed between steps (256 MiB write + read back, outside the timed interval)",
-                   "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
-                   "weights": f"{WEIGHTS} layout, resident in HBM",
-                   "dispatch": {k: wl.plan[k] for k in ("variant", "bn", "ctas", "seg_max")}},
-        "tflops": round(job_rate(wl.flops_per_step, ms, world) / 1e12, 2),
-        "roofline": roof,
-        "e2e": {"value": round(job_rate(wl.bytes_per_step, e2e, world) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": wl.h2d, "d2h_bytes_per_step": wl.d2h,
-                "path": "public API (Python binding -> C ABI) captured in a CUDA graph with the pinned "
-                        "host<->device copies of every step, uploads and downloads on two more streams so that "
-                        "each layer waits only for its own input and results leave while later layers run"
-                        + getattr(wl, "e2e_note", ""),
-                "eager_ms_per_step": round(e2e_eager, 4),
-                "eager_value": round(job_rate(wl.bytes_per_step, e2e_eager, world) / 1e9, 1)},
-        "gpu_launches": K * wl.kernels_per_step(),
-        "clocks": sampler.summary(t0, t1),
+        "config": workload_config(args.workload, world),
+        "dispatch": main["dispatch"],
+        "tflops": main["tflops"],
+        "roofline": main["roofline"],
+        "kernel_spans": main["kernel_spans"],
+        "trace_step_ms": main["trace_step_ms"], "trace_span_sum_ms": main["trace_span_sum_ms"],
+        "spans_fit_step": main["spans_fit_step"], "step_frac_of_hbm": main["step_frac_of_hbm"],
+        "e2e": main["e2e"],
+        "gpu_launches": main["gpu_launches"],
+        "clocks": main["clocks"],
+        "status_ok": status_ok,
+        "extra": extras,
     }
+    parity_ok = True
     if args.cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+        line["cpu_baseline"], parity = cpu_leg(args.workload, outputs, budget_s=args.cpu_budget)
+        line["parity"] = parity
+        parity_ok = all(p.get("ok", False) for p in parity.values())
+    else:
+        line["parity"] = None
+    line["parity_ok"] = parity_ok if line["parity"] is not None else None
     print(json.dumps(line), flush=True)
+    if not status_ok:
+        print("bench: a device status word was set (a bounded wait ran out); the numbers above are invalid",
+              file=sys.stderr)
+        return 3
+    if not parity_ok:
+        print("bench: the timed graph's outputs differ from the oracle; the numbers above are invalid",
+              file=sys.stderr)
+        return 4
+    return 0
 
 
-# ----------------------------------------------------------------- CPU oracle legs
+# ----------------------------------------------------------------- CPU leg (oracle)
+# Everything below this line that imports `oracle` runs only in the CPU leg
+# (cpu_leg, on rank 0 at one GPU) and in the reference arm.
 _ORACLE_CACHE = {}
 
 
-def _oracle_operands(workload: str):
-    """Quantized weights (offline conversion, not timed) and bf16 activations
-    of one layer of the workload, prepared once."""
+def oproj_spec(workload):
+    """(M, layers, cfg, weight seeds, row_scale) of an o_proj workload."""
+    import synth
+    return {"oproj_decode": (64, 5, 1, synth.SEEDS_CFG1_W, False),
+            "oproj_m8": (8, 1, 0, (synth.SEED_CFG0_W,), False),
+            "oproj_prefill": (8192, 1, 2, (synth.SEED_CFG2_W,), True)}[workload]
+
+
+def _oracle_weights(workload):
+    """Quantized weights of the workload (offline conversion, not timed)."""
     if workload in _ORACLE_CACHE:
         return _ORACLE_CACHE[workload]
     import oracle
     import synth
     if workload.startswith("oproj"):
-        M, layers, cfg, seed = {"oproj_decode": (64, 5, 1, synth.SEEDS_CFG1_W[0]),
-                                "oproj_m8": (8, 1, 0, synth.SEED_CFG0_W),
-                                "oproj_prefill": (8192, 1, 2, synth.SEED_CFG2_W)}[workload]
-        wq = oracle.mx_quantize_rows(synth.weight(synth.OPROJ_N, synth.OPROJ_K, seed=seed))
-        x = synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(cfg, 0, 0), row_scale=(cfg == 2))
-        ops = ("a4w4", M, layers, wq, x)
+        M, layers, cfg, seeds, rs = oproj_spec(workload)
+        w = [oracle.mx_quantize_rows(synth.weight(synth.OPROJ_N, synth.OPROJ_K, seed=s)) for s in seeds]
+    else:
+        w = (oracle.fp8_quantize_rows(synth.weight(2 * synth.MLP_I, 7168, seed=synth.SEED_CFG3_GATE_UP)),
+             oracle.fp8_quantize_rows(synth.weight(7168, synth.MLP_I, seed=synth.SEED_CFG3_DOWN)))
+    _ORACLE_CACHE[workload] = w
+    return w
+
+
+def _activations(workload):
+    key = ("x", workload)
+    if key in _ORACLE_CACHE:
+        return _ORACLE_CACHE[key]
+    import synth
+    if workload.startswith("oproj"):
+        M, layers, cfg, seeds, rs = oproj_spec(workload)
+        xs = [synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(cfg, l, 0), row_scale=rs)
+              for l in range(layers)]
     else:
         M = 64 if workload.endswith("m64") else 8192
-        qg = oracle.fp8_quantize_rows(synth.weight(2 * synth.MLP_I, 7168, seed=synth.SEED_CFG3_GATE_UP))
-        qd = oracle.fp8_quantize_rows(synth.weight(7168, synth.MLP_I, seed=synth.SEED_CFG3_DOWN))
-        xg = synth.activation(M, 7168, seed=synth.act_seed(3, 0, 0))
-        xd = synth.activation(M, synth.MLP_I, seed=synth.act_seed(3, 0, 1))
-        ops = ("ptpc", M, 1, (qg, qd), (xg, xd))
-    _ORACLE_CACHE[workload] = ops
-    return ops
+        xs = synth.activation(M, 7168, seed=synth.act_seed(3, 0, 0))
+    _ORACLE_CACHE[key] = xs
+    return xs
 
 
-def oracle_sample(workload: str, rows: int):
-    """Time the oracle (activation quantization + reference GEMM, all output
-    channels) on `rows` token rows of one layer.  Returns (raw seconds,
-    factor that scales it to one full step -- linear in rows and layers --,
-    description)."""
+def workload_rows(workload):
+    if workload.startswith("oproj"):
+        return oproj_spec(workload)[0]
+    return 64 if workload.endswith("m64") else 8192
+
+
+# The down projection's input depends on the bf16 rounding of the gate_up
+# output, which the GEMM tolerance leaves open by one bf16 step; through the
+# SwiGLU that can move the row's FP8 scale by one step of its amax (2^-8
+# relative) and single codes by one E4M3 step.  The down output of the chain
+# is therefore held to 2^-7 * sum_k |a_k w_k| against the oracle's chain (the
+# chain itself is checked bit for bit on exactly representable data in the
+# tests).
+CHAIN_REL_TOL = 2.0 ** -7
+
+
+def oracle_step(workload: str, rows: np.ndarray):
+    """The oracle's version of one step of `workload`, restricted to the
+    token rows `rows` (every layer, all output channels).  Returns (seconds,
+    [(output name, layer or None, ref, bound, rule)]) with ref/bound float64
+    (len(rows), N); rule "gemm" (GEMM_REL_TOL) or "chain" (CHAIN_REL_TOL)."""
     import oracle
-    kind, M, layers, w, x = _oracle_operands(workload)
-    rows = max(1, min(rows, M))
-    if kind == "a4w4":
-        xs = x[:rows].contiguous()
-        t = time.perf_counter()
-        ac, asf = oracle.mx_quantize_rows(xs)
-        oracle.gemm_a4w4(ac, asf, w[0], w[1])
-        dt = time.perf_counter() - t
-        f = (M / rows) * layers
-        return dt, f, f"1 layer, {rows} of {M} token rows, all 7168 outputs; time x{f:g} (rows, layers)"
-    (qg, sg), (qd, sd) = w
-    xg, xd = x[0][:rows].contiguous(), x[1][:rows].contiguous()
+    w = _oracle_weights(workload)
+    xs = _activations(workload)
+    refs = []
+    idx = torch.from_numpy(rows)
     t = time.perf_counter()
-    qa, sa = oracle.fp8_quantize_rows(xg)
-    oracle.gemm_ptpc(qa, sa, qg, sg)
-    qa, sa = oracle.fp8_quantize_rows(xd)
-    oracle.gemm_ptpc(qa, sa, qd, sd)
-    dt = time.perf_counter() - t
-    f = M / rows
-    return dt, f, f"gate_up + down, {rows} of {M} token rows, all outputs; time x{f:g} (rows)"
+    if workload.startswith("oproj"):
+        for l, x in enumerate(xs):
+            ac, asf = oracle.mx_quantize_rows(x[idx].contiguous())
+            refs.append(("y", l, *oracle.gemm_a4w4(ac, asf, w[l][0], w[l][1]), "gemm"))
+    else:
+        (qg, sg), (qd, sd) = w
+        qa, sa = oracle.fp8_quantize_rows(xs[idx].contiguous())
+        ref_g, bound_g = oracle.gemm_ptpc(qa, sa, qg, sg)
+        refs.append(("yg", None, ref_g, bound_g, "gemm"))
+        # the gate_up output as the bf16 tensor the chain passes on
+        g16 = torch.from_numpy(ref_g.astype(np.float32)).to(torch.bfloat16)
+        _, qh, sh = oracle.swiglu_fp8_quantize_rows(g16)
+        refs.append(("yd", None, *oracle.gemm_ptpc(qh, sh, qd, sd), "chain"))
+    return time.perf_counter() - t, refs
+
+
+def bf16_interval_check(y_bf16: torch.Tensor, ref: np.ndarray, bound: np.ndarray, rel_tol=GEMM_REL_TOL):
+    """A bf16 output is correct when it is the round-to-nearest-even of some
+    fp32 value within rel_tol * bound of the reference; rounding is
+    monotone, so it must lie in [rne(ref - tol), rne(ref + tol)] (NaN where
+    the reference is NaN).  Returns (ok, largest |y - ref| / (tol + half a bf16
+    step at |ref|))."""
+    y = y_bf16.float().numpy().astype(np.float64)
+    tol = rel_tol * bound
+    lo = torch.from_numpy((ref - tol).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    hi = torch.from_numpy((ref + tol).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    nan = np.isnan(ref)
+    ok = np.where(nan, np.isnan(y), (y >= lo) & (y <= hi))
+    step = np.abs(ref) * 2.0 ** -8
+    r = np.where(nan, 0.0, np.abs(y - ref) / (tol + step / 2 + 1e-300))
+    return bool(ok.all()), float(np.nanmax(r)) if r.size else 0.0
+
+
+def check_outputs(workload, gpu_out, rows, refs):
+    ok, worst, n, tight, n_chain = True, 0.0, 0, 0, 0
+    idx = torch.from_numpy(rows)
+    for name, layer, ref, bound, rule in refs:
+        y = gpu_out[name]
+        y = (y[layer] if layer is not None else y)[idx]
+        tol = GEMM_REL_TOL if rule == "gemm" else CHAIN_REL_TOL
+        o, w = bf16_interval_check(y, ref, bound, tol)
+        ok &= o
+        n += ref.size
+        if rule == "gemm":
+            worst = max(worst, w)
+        else:
+            n_chain += ref.size
+            tight += int((np.abs(y.float().numpy() - ref) <= GEMM_REL_TOL * bound
+                          + np.abs(ref) * 2.0 ** -9).sum())
+    d = {"ok": ok, "rows": int(len(rows)), "outputs_checked": int(n), "worst_err_over_tol": round(worst, 4),
+         "rule": "bf16 y within [rne(ref - t), rne(ref + t)] per element, t = 1e-5 * sum|a w|"}
+    if n_chain:
+        d["chain_rule"] = ("down output of the MLP chain: t = 2^-7 * sum|a w| (its input depends on the "
+                           "bf16 rounding of the gate_up output)")
+        d["chain_frac_within_gemm_tol"] = round(tight / n_chain, 6)
+    return d
+
+
+def sample_rows(M, n, seed=12345):
+    if n >= M:
+        return np.arange(M, dtype=np.int64)
+    g = np.random.default_rng(seed)
+    return np.sort(g.choice(M, size=n, replace=False)).astype(np.int64)
 
 
 def step_bytes(workload: str):
@@ -761,63 +1053,84 @@ def step_bytes(workload: str):
     if workload == "oproj_prefill":
         return a4w4_fused_bytes(8192, N, K)
     M = 64 if workload.endswith("m64") else 8192
-    return (fp8_quant_bytes(M, 7168) + ptpc_gemm_bytes(M, 36864, 7168) +
-            fp8_quant_bytes(M, 18432) + ptpc_gemm_bytes(M, 7168, 18432))
+    return mlp_chain_bytes(M, 7168, 18432)
 
 
-def cpu_baseline(workload: str, budget_s: float = 20.0):
-    """The oracle as it stands, on this host's cores, on a bounded sample
-    (about budget_s of CPU work) of the benchmarked workload."""
+def cpu_leg(main_workload, outputs, budget_s=20.0):
+    """The oracle as it stands, on this host's cores: (1) timed on a bounded
+    sample of the main workload (the whole step when it fits the budget),
+    (2) the outputs the timed GPU graph left behind checked against the
+    oracle -- every row for decode-sized workloads, seeded sampled rows for
+    the prefill-sized ones."""
     import oracle
-    M = _oracle_operands(workload)[1]
-    dt1, _, _ = oracle_sample(workload, 1)  # calibration on one row
-    rows = max(1, min(M, int(budget_s / max(dt1, 1e-6))))
-    dt, f, desc = oracle_sample(workload, rows)
-    t_full = dt * f
-    return {"value": round(step_bytes(workload) / t_full / 1e9, 5), "unit": "GB/s",
-            "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
-            "sample_s": round(dt, 3), "s_per_step_extrapolated": round(t_full, 3)}
+    oracle.build()
+    parity = {}
+    cpu = None
+    for key, gpu_out in outputs.items():
+        M = workload_rows(key)
+        if key == main_workload:
+            t1, _ = oracle_step(key, np.arange(1, dtype=np.int64))  # calibration on one row
+            n = max(1, min(M, int(budget_s / max(t1, 1e-6))))
+            rows = sample_rows(M, n)
+            dt, refs = oracle_step(key, rows)
+            f = M / len(rows)
+            cpu = {"value": round(step_bytes(key) / (dt * f) / 1e9, 5), "unit": "GB/s",
+                   "cores": oracle.num_threads(), "kind": "oracle",
+                   "sample": (f"the whole step ({M} token rows, every layer, all outputs)" if f == 1 else
+                              f"{len(rows)} of {M} token rows, every layer, all outputs; time x{f:g} (rows)"),
+                   "sample_s": round(dt, 3), "extrapolation_factor": round(f, 4)}
+        else:
+            rows = sample_rows(M, 64)
+            _, refs = oracle_step(key, rows)
+        parity[key] = check_outputs(key, gpu_out, rows, refs)
+    return cpu, parity
 
 
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle as it stands, on this machine's host
-    cores, each step a bounded sample of the same workload."""
+    cores, each step the main workload's step (or, where that would not fit
+    the run, a seeded row sample of it, extrapolated by rows)."""
     if rank != 0:
-        return
+        return 0
     if args.workload == "sweep":
         print(json.dumps({"impl": "reference", "unavailable": "the sweep reports per-GEMM GPU rates only; "
                           "the oracle arm times the single workloads"}), flush=True)
-        return
+        return 0
     import oracle
     oracle.build()
+    M = workload_rows(args.workload)
     # rows per step: as many as keep the whole run (warm-up + steps) near two minutes
-    M = _oracle_operands(args.workload)[1]
     per_step = 120.0 / (args.steps + args.warmup)
-    rows = 1
+    rows = sample_rows(M, 1)
     for r in (M, 256, 64, 16, 4):
         if r <= M:
-            dt, _, _ = oracle_sample(args.workload, r)
+            cand = sample_rows(M, r)
+            dt, _ = oracle_step(args.workload, cand)
             if dt <= per_step:
-                rows = r
+                rows = cand
                 break
     for _ in range(max(0, args.warmup)):
-        oracle_sample(args.workload, rows)
+        oracle_step(args.workload, rows)
     ts = []
-    descs = None
     for _ in range(args.steps):
-        dt, f, descs = oracle_sample(args.workload, rows)
-        ts.append(dt * f)
+        dt, _ = oracle_step(args.workload, rows)
+        ts.append(dt)
     s = statistics.mean(ts)
-    v = step_bytes(args.workload) / s / 1e9
+    f = M / len(rows)
+    v = step_bytes(args.workload) / (s * f) / 1e9
+    desc = (f"the whole step ({M} token rows, every layer, all outputs)" if f == 1 else
+            f"{len(rows)} of {M} token rows, every layer, all outputs per step; rate extrapolated x{f:g} (rows)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3),
+        "extrapolation_factor": round(f, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload},
+        "data": "synthetic", "config": workload_config(args.workload, world),
         "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": descs},
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+    return 0
 
 
 # ----------------------------------------------------------------- sweep
@@ -839,6 +1152,7 @@ def run_sweep(args, rank, world, local_rank):
     hbm, bf16, peak_src = load_peaks()
     H, I2, I, N_O, K_O = 7168, 2 * synth.MLP_I, synth.MLP_I, synth.OPROJ_N, synth.OPROJ_K
     L = 5
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     # resident weights (panel or tile layout); bf16 originals freed after conversion
     layout, wt = weight_layout(mx)
     w = {"gate_up": [], "down": [], "o_proj": []}
@@ -859,6 +1173,7 @@ def run_sweep(args, rank, world, local_rank):
     stream = torch.cuda.Stream(device=dev)
     reps = max(3, min(args.steps, 20))
     loop_peak = {k: mx.mxg_mma_peak(k, 256) for k in (0, 1)}
+    bad = 0
     for M in SWEEP_M:
         per = {}
         total_ms = 0.0
@@ -877,7 +1192,7 @@ def run_sweep(args, rank, world, local_rank):
                     mx.fp8_quantize_act_tiled(x, T, q=qa, scale=sa)
                     qw, sw = w[g][l]
                     mx.fp8_gemm_ptpc(qa, sa, qw, sw, out=y, ws=ws, weights_static=True,
-                                     weights_tiled=wt, act_tile_rows=T, k=K)
+                                     weights_tiled=wt, act_tile_rows=T, k=K, dev_status=status)
                 gbytes = ptpc_gemm_bytes(M, N, K) + fp8_quant_bytes(M, K)
             else:
                 ac = torch.empty(mx.mxg_act_tiled_bytes(0, M, K, T), dtype=torch.uint8, device=dev)
@@ -887,7 +1202,7 @@ def run_sweep(args, rank, world, local_rank):
                     mx.mx_quantize_act_tiled(x, T, codes=ac, sf=asf)
                     wc, wsf = w[g][l]
                     mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out=y, ws=ws, weights_static=True,
-                                    weights_tiled=wt, act_tile_rows=T, m=M, n=N, k=K)
+                                    weights_tiled=wt, act_tile_rows=T, m=M, n=N, k=K, dev_status=status)
                 gbytes = a4w4_gemm_bytes(M, N, K) + mx_quant_bytes(M, K)
             with torch.cuda.stream(stream):
                 for l in range(L):
@@ -909,6 +1224,8 @@ def run_sweep(args, rank, world, local_rank):
                     stream.synchronize()
                     if r >= 2:
                         ts.append(a.elapsed_time(b))
+            st = mx.mxg_query_status(status, stream)
+            bad += st != 0
             ms = statistics.median(ts) / L  # one layer's quantizer + GEMM
             total_ms += ms
             flops = 2.0 * M * N * K
@@ -927,7 +1244,7 @@ def run_sweep(args, rank, world, local_rank):
                         "frac_of_mma_loop": round(tf / loop_peak[kind], 4)}
             per[g] = {"dtype": "e2m1 x e2m1" if kind == 0 else "e4m3 x e4m3", "N": N, "K": K,
                       "us": round(ms * 1e3, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
-                      "roofline": roof,
+                      "roofline": roof, "status_ok": st == 0,
                       "dispatch": {k: plan[k] for k in ("variant", "bn", "ctas", "seg_max")}}
             del graph
         layer_flops = sum(2.0 * M * n * k for n, k, _ in shapes.values())
@@ -940,6 +1257,7 @@ def run_sweep(args, rank, world, local_rank):
                 "data": "synthetic (seeded bf16 N(0,1) activations with 0.1% x50 outliers, N(0,0.02) weights)"}
         if rank == 0:
             print(json.dumps(line), flush=True)
+    return 3 if bad else 0
 
 
 def main():
@@ -953,6 +1271,8 @@ def main():
                              "sweep"])
     ap.add_argument("--weights", default="panel", choices=["panel", "tiled"],
                     help="resident weight layout: 256-row panels (scales inside) or 128-row tiles")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="time the main workload only (no 'extra' entries)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--min-warmup-s", type=float, default=0.5,
@@ -966,20 +1286,18 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
+        return run_reference(args, rank, world)
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     try:
         if args.workload == "sweep":
-            run_sweep(args, rank, world, local_rank)
-        else:
-            run_ours(args, rank, world, local_rank)
+            return run_sweep(args, rank, world, local_rank)
+        return run_ours(args, rank, world, local_rank)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
             L.mx_quantize_act_tiled.restype = i
             L.fp8_quantize_act_tiled.argtypes = [vp, i, i, i, i, vp, vp, vp]
             L.fp8_quantize_act_tiled.restype = i
+            L.swiglu_fp8_quantize.argtypes = [vp, i, i, i, i, vp, vp, vp, i, vp]
+            L.swiglu_fp8_quantize.restype = i
             L.fp8_gemm_ptpc.argtypes = [vp, vp, vp, vp, i, i, i, vp, i, i,
                                         ctypes.POINTER(GemmOpts), vp]
             L.fp8_gemm_ptpc.restype = i
@@ -281,6 +283,27 @@ def fp8_quantize_act(x: torch.Tensor, q=None, scale=None, stream=None):
         scale = torch.empty(M, dtype=torch.float32, device=x.device)
     _check("fp8_quantize_act", lib().fp8_quantize_act(
         _ptr(x), M, K, x.stride(0), _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def swiglu_fp8_quantize(gu: torch.Tensor, tile_rows: int = 0, q=None, scale=None, h=None, stream=None):
+    """The step between gate_up and down: gu (M, 2I) bf16 [gate | up] ->
+    (q, scale) = per-token FP8 of h = bf16(silu(gate) * up); q row-major
+    (M, I) or, with tile_rows, flat in the activation tile layout.  Pass
+    h (M, I) bf16 to also receive h."""
+    _need(gu.is_cuda and gu.dtype == torch.bfloat16 and gu.dim() == 2 and gu.stride(1) == 1
+          and gu.shape[1] % 2 == 0, "gu must be a CUDA bf16 (M, 2I) tensor with unit inner stride")
+    M, I = gu.shape[0], gu.shape[1] // 2
+    if q is None:
+        q = (torch.empty(mxg_act_tiled_bytes(KIND_PTPC, M, I, tile_rows), dtype=torch.uint8, device=gu.device)
+             if tile_rows else torch.empty(M, I, dtype=torch.uint8, device=gu.device))
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=gu.device)
+    if h is not None:
+        _need(h.dtype == torch.bfloat16 and h.stride(1) == 1 and tuple(h.shape) == (M, I), "h must be (M, I) bf16")
+    _check("swiglu_fp8_quantize", lib().swiglu_fp8_quantize(
+        _ptr(gu), M, I, gu.stride(0), int(tile_rows), _ptr(q), _ptr(scale), _ptr(h),
+        h.stride(0) if h is not None else 0, _stream(stream)))
     return q, scale
 
 

@@ -322,6 +322,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.timeout_ns = (unsigned long long)tmo * 1000000ull;
   p.debug_stall = opts ? opts->debug_stall : 0;
   p.early_w = (opts && opts->weights_static) ? 1 : 0;
+
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
   p.kc_per_row = (int)((row_bytes + 127) / 128);  // the last column may be half (TMA pads it)
   if (!swap) {
@@ -362,7 +363,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
     p.fuse_quant = 1;
   }
   ReduceMode mode = requested_reduce(opts);
-  if (op.x) mode = ReduceMode::kGrid;
+  if (op.x && mode != ReduceMode::kLastCta) mode = ReduceMode::kGrid;
   if (pl.pair && !op.x) {
     p.pair_reduce = 1;
   } else {
@@ -516,6 +517,23 @@ mxg_status fp8_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 
+mxg_status swiglu_fp8_quantize(const void *gu_bf16, int M, int I, int ldgu, int tile_rows, uint8_t *q,
+                               float *scale, void *h_bf16, int ldh, mxg_stream_t stream) {
+  if (!gu_bf16 || M < 1 || I < 1 || ldgu < 2 * I || !q || !scale) return MXG_ERR_INVALID_ARG;
+  if (tile_rows != 0 && !valid_tile_rows(tile_rows)) return MXG_ERR_INVALID_ARG;
+  if (h_bf16 && ldh < I) return MXG_ERR_INVALID_ARG;
+  if (I % 128 != 0 || I > mxg::kSwigluMaxI) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(gu_bf16) || (ldgu % 8) != 0 || !aligned16(q) || !aligned16(scale) ||
+      (h_bf16 && (!aligned16(h_bf16) || (ldh % 8) != 0)))
+    return MXG_ERR_MISALIGNED;
+  int sm = 0;
+  mxg_status st = check_device(&sm);
+  if (st != MXG_OK) return st;
+  cudaError_t e = mxg::launch_swiglu_fp8(gu_bf16, ldgu, M, I, tile_rows, h_bf16, ldh, q, scale, sm,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
 mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_t *q, float *scale,
                                mxg_sf_layout layout, mxg_stream_t stream) {
   mxg_status st = check_rows_arg(w_bf16, N, K, ldw);
@@ -532,17 +550,18 @@ mxg_status fp8_quantize_weight(const void *w_bf16, int N, int K, int ldw, uint8_
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
 
-mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void *x_bf16, int ldx,
-                        const uint8_t *w_codes, const uint8_t *w_sf, int M, int N, int K, void *y,
-                        int ldy, mxg_out_dtype out_dtype, const mxg_gemm_opts *opts,
-                        mxg_stream_t stream) {
+namespace {
+// The operand checks of mx_gemm_a4w4 (everything it can reject on the host
+// before touching the device).
+mxg_status check_a4w4_args(const uint8_t *a_codes, const uint8_t *a_sf, const void *x_bf16, int ldx,
+                           const uint8_t *w_codes, const uint8_t *w_sf, int M, int N, int K,
+                           const void *y, int ldy, mxg_out_dtype out_dtype, const mxg_gemm_opts *opts) {
   mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, opts);
   if (st != MXG_OK) return st;
   // weight panels carry their scales; w_sf is then unused (may be NULL)
   const bool w_panels = opts && opts->weights_tiled == 2;
   if (!w_codes || (!w_sf && !w_panels)) return MXG_ERR_INVALID_ARG;
-  const bool fused = a_codes == nullptr;
-  if (fused) {
+  if (a_codes == nullptr) {
     if (!x_bf16 || a_sf) return MXG_ERR_INVALID_ARG;
     if ((st = check_rows_arg(x_bf16, M, K, ldx)) != MXG_OK) return st;
   } else if (!a_sf) {
@@ -550,6 +569,17 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
   }
   if (!aligned16(w_codes) || (w_sf && !aligned16(w_sf)) || (a_codes && (!aligned16(a_codes) || !aligned16(a_sf))))
     return MXG_ERR_MISALIGNED;
+  return MXG_OK;
+}
+}  // namespace
+
+mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void *x_bf16, int ldx,
+                        const uint8_t *w_codes, const uint8_t *w_sf, int M, int N, int K, void *y,
+                        int ldy, mxg_out_dtype out_dtype, const mxg_gemm_opts *opts,
+                        mxg_stream_t stream) {
+  mxg_status st = check_a4w4_args(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype, opts);
+  if (st != MXG_OK) return st;
+  const bool fused = a_codes == nullptr;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -575,7 +605,7 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
     a_sf = sf;
     part_off += need;
     if (pl.variant == MXG_VARIANT_SPLITK && act_tile_rows && opts &&
-        opts->splitk_reduce == MXG_REDUCE_GRID) {
+        (opts->splitk_reduce == MXG_REDUCE_GRID || opts->splitk_reduce == MXG_REDUCE_LAST_CTA)) {
       // one kernel: its CTAs quantize x into the token tiles themselves
       GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr, x_bf16, ldx};
       return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off,
@@ -698,13 +728,20 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, con
                                 int ldx, const uint8_t *w_codes, const uint8_t *w_sf, int M, int N,
                                 int K, void *y, int ldy, mxg_out_dtype out_dtype, int weights_tiled,
                                 mxg_stream_t stream) {
-  mxg_status st = check_gemm_common(M, N, K, y, ldy, out_dtype, nullptr);
+  mxg_gemm_opts opts;
+  std::memset(&opts, 0, sizeof(opts));
+  opts.variant = MXG_VARIANT_AUTO;
+  opts.weights_tiled = weights_tiled;
+  // every operand check first: a rejected call touches no device memory
+  // (in particular not the shared scratch another stream may be using)
+  mxg_status st = check_a4w4_args(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype,
+                                  &opts);
   if (st != MXG_OK) return st;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
   // the scratch this call needs, exactly as mx_gemm_a4w4 would ask for it
   mxg_plan pl;
-  if ((st = plan_impl(0, M, N, K, sm, nullptr, &pl)) != MXG_OK) return st;
+  if ((st = plan_impl(0, M, N, K, sm, &opts, &pl)) != MXG_OK) return st;
   const bool fused = a_codes == nullptr;
   const size_t act =
       fused ? fused_act_bytes(M, K, K % 256 == 0 ? plan_act_tile_rows(pl) : 0) : 0;
@@ -716,12 +753,8 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, con
   // previous call (on any stream) left in it
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, kCounterBytes, s) != cudaSuccess) return MXG_ERR_CUDA;
-  mxg_gemm_opts opts;
-  std::memset(&opts, 0, sizeof(opts));
-  opts.variant = MXG_VARIANT_AUTO;
   opts.workspace = scratch;
   opts.ws_bytes = MXG_NOALLOC_SCRATCH_BYTES;
-  opts.weights_tiled = weights_tiled;
   return mx_gemm_a4w4(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype, &opts,
                       stream);
 }

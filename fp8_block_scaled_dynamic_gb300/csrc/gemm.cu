@@ -29,6 +29,8 @@
 // also move each stage's scale factors into TMEM, and store y by TMA).  All
 // hand-offs are mbarriers; every wait is bounded.
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -462,13 +464,18 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   // each stage's scale factors into TMEM with tcgen05.st, off the tensor
   // pipe; a tcgen05.cp there would hold up the MMAs behind it and, through
   // them, the release of the stage.
-  constexpr bool kEpiScales = KIND == 0 && KS == 1;
+  constexpr bool kEpiScales = KIND == 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     trace_mark(p, kTrEntry);
     trace_set(p, kTrEntryNs, global_timer_ns());
+    if (p.trace) {
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      trace_set(p, kTrSmid, smid);
+    }
   }
   // The next kernel may launch now: it touches no memory this one writes or
   // reads before its own griddepcontrol.wait, which returns only when this
@@ -663,8 +670,55 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           ++pre;
         }
       }
+      // With the weights already in flight, what remains of the first stages
+      // after the wait is the activation operand: when it is in the tile
+      // layout, every one of those copies (dst, src, bytes) is worked out
+      // now, and lane j issues copy j right after the wait -- one converged
+      // instruction for all of them, instead of one stage after another.
+      const bool act_tiles = p.swap ? (p.b_tiles && p.b_tile_rows == BN) : (p.a_tiles != nullptr);
+      const int n_act = 1 + (KIND == 0 ? (p.swap ? C::kSfBlocksB : 1) : 0);  // copies per stage (at most)
+      const bool fast_first = p.early_w && act_tiles && pre * n_act <= 32;
+      uint32_t fc_dst = 0, fc_bytes = 0, fc_bar = 0;
+      const uint8_t *fc_src = nullptr;
+      if (fast_first && lane < pre * n_act) {
+        const int k = lane / n_act, j = lane % n_act;
+        Item itk;
+        int kbk = 0;
+        stage_of(k, itk, kbk);
+        const int nc = ncol_of(kbk);
+        fc_bar = full_bar(k);
+        if (j == 0) {
+          if (p.swap) {
+            fc_dst = b_smem(k);
+            fc_src = p.b_tiles + ((size_t)itk.tb * p.kc_per_row + (size_t)kbk * KS) * (size_t)C::kBColBytes;
+            fc_bytes = (uint32_t)nc * C::kBColBytes;
+          } else {
+            fc_dst = a_smem(k);
+            fc_src = p.a_tiles + ((size_t)itk.ta * p.kc_per_row + (size_t)kbk * KS) * (size_t)C::kAColBytes;
+            fc_bytes = (uint32_t)nc * C::kAColBytes;
+          }
+        } else if (KIND == 0) {
+          const int na = natoms_of(kbk);
+          if (p.swap) {
+            const int rb0 = (itk.tb * BN) / 128;
+            const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+            if (j - 1 < nblk) {
+              fc_dst = sfb_smem(k) + (uint32_t)(j - 1) * (1024 * KS);
+              fc_src = p.sfB + ((size_t)(rb0 + j - 1) * p.G4 + 2 * KS * kbk) * 512u;
+              fc_bytes = (uint32_t)na * 512u;
+            }
+          } else {
+            fc_dst = sfa_smem(k);
+            fc_src = p.sfA + ((size_t)itk.ta * p.G4 + 2 * KS * kbk) * 512u;
+            fc_bytes = (uint32_t)na * 512u;
+          }
+        }
+      }
       pdl_wait();
-      if (lane == 0) trace_mark(p, kTrWaited);
+      if (lane == 0) {
+        trace_mark(p, kTrWaited);
+        trace_set(p, kTrWaitedNs, global_timer_ns());
+      }
       bool ok = true;
       if (p.fuse_quant) {
         // the token tiles are written by every CTA of this grid; the epilogue
@@ -676,7 +730,10 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       // the rest of the first stages -- also when the fused phase failed:
       // every armed stage must land before the CTA exits (contents are then
       // irrelevant; every address stays in bounds)
-      for (int k = 0; k < pre; ++k) {
+      if (fast_first) {
+        if (fc_bytes) bulk_load(fc_dst, fc_src, fc_bytes, fc_bar, p.swap ? polB : polA);
+      }
+      for (int k = 0; k < pre && !fast_first; ++k) {
         Item itk;
         int kbk = 0;
         stage_of(k, itk, kbk);
@@ -850,7 +907,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             fed = false;
             break;
           }
-          const int natoms = min(2, p.G4 - 2 * kb);
+          if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
+          const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
           const int rb0 = (it.tb * BN) / 128;
           const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
           const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -861,11 +919,12 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           for (int j = 0; j < nblk; ++j)
             for (int a = 0; a < natoms; ++a)
               tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
-                       ld_shared_v4(sfb_smem(st) + j * 1024 + a * 512 + lane * 16));
+                       ld_shared_v4(sfb_smem(st) + j * (1024 * KS) + a * 512 + lane * 16));
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(sf_ready(st));
+          if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
         }
         if (!fed) break;
       }
@@ -1202,12 +1261,17 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 
 // The split-K reduction as its own kernel, launched right after the GEMM.
 template <int KIND>
-__global__ void __launch_bounds__(kRedThreads) splitk_reduce_kernel(const GemmParams p, int bn,
-                                                                    unsigned gemm_ctas) {
+__global__ void __maxnreg__(48)  // 128-thread CTAs, 3 of them beside a GEMM CTA and a quantizer CTA
+    splitk_reduce_kernel(const GemmParams p, int bn, unsigned gemm_ctas) {
   pdl_trigger();  // touches nothing before the wait below
+  if (p.trace && threadIdx.x == 0)
+    atomicMax(p.trace + kTrRedEntryInv, ~(unsigned long long)global_timer_ns());
   pdl_wait();     // the GEMM that wrote the partial slots has completed
-  reduce_share<KIND>(p, bn, gemm_ctas, blockIdx.x * kRedThreads + threadIdx.x,
-                     gridDim.x * kRedThreads);
+  reduce_share<KIND>(p, bn, gemm_ctas, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+  if (p.trace) {  // (uniform over the grid)
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(p.trace + kTrRedExitNs, (unsigned long long)global_timer_ns());
+  }
 }
 
 template <int KIND, int BN, int KS>
@@ -1369,8 +1433,9 @@ cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm
                                  int sm_count, cudaStream_t stream) {
   const long long total = (long long)p.tilesA * p.tilesB * bn * (kTileA / 4);
   long long blocks = (total + kRedThreads * kRedJ - 1) / (kRedThreads * kRedJ);
-  // launched early (programmatic launch), every reduce CTA must fit beside a
-  // resident GEMM CTA: 3 small CTAs per SM at most
+  // Launched early (programmatic launch), the reduce CTAs sit beside the
+  // GEMM CTAs of a layer chain: 3 per SM at most (48 registers a thread),
+  // so that a GEMM CTA (26K registers) and a quantizer CTA still fit.
   const long long cap = (long long)(sm_count > 0 ? sm_count : 152) * 3;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;

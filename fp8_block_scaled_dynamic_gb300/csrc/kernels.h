@@ -91,6 +91,13 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
                              float *scale, int tile_rows, bool act, int sm_count,
                              cudaStream_t stream);
 
+// SwiGLU of a [gate | up] row (I values each) fused with the per-token FP8
+// quantization of h = bf16(silu(gate) * up); q in the layout tile_rows names
+// (0 = row-major, else token tiles), h_out (nullable) receives h.
+cudaError_t launch_swiglu_fp8(const void *gu, long long ldgu, int rows, int I, int tile_rows, void *h_out,
+                              long long ldh, uint8_t *q, float *scale, int sm_count, cudaStream_t stream);
+constexpr int kSwigluMaxI = 102400;  // h of one row lives in shared memory (2 bytes a value)
+
 // Everything one GEMM launch needs besides the two tensor maps.
 struct GemmParams {
   const uint8_t *sfA;  // A4W4: scale factors of the MMA-A / MMA-B operands,
@@ -142,13 +149,21 @@ struct GemmParams {
                        //   [64] / [96] of barrier 2 (zero-initialised, 128 bytes apart)
 };
 
-// Timeline trace points (index into a CTA's 16 slots): SM clock64 values.
+// Timeline trace points (index into a CTA's kTracePoints slots): SM clock64
+// values, except the *Ns slots (global timer, ns).  Row 0 also holds the span
+// of the split-K reduce kernel that follows the GEMM: kTrRedEntryInv = the
+// bitwise NOT of its first CTA's entry time (so that an atomic max finds the
+// earliest), kTrRedExitNs = its last CTA's exit time.
 enum TracePoint {
   kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrLastLoad = 3, kTrFirstFull = 4,
   kTrLastCommit = 5, kTrAcc0 = 6, kTrItem0Done = 7, kTrAcc1 = 8, kTrItem1Done = 9,
   kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12, kTrDecision = 13, kTrReduced = 14,
   kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18, kTrQuantDone = 19,
-  kTracePoints = 20  // fused path: kTrDecision = second grid barrier passed
+  kTrWaitedNs = 20, kTrSmid = 21, kTrRedEntryInv = 22, kTrRedExitNs = 23,
+  // A4W4, per pipeline stage k < 8 of the CTA's sequence, seen by the first
+  // epilogue warp: the stage's data landed / its scales are in TMEM
+  kTrStageLanded = 24, kTrStageFed = 32,
+  kTracePoints = 40  // fused path: kTrDecision = second grid barrier passed
 };
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.

@@ -15,6 +15,7 @@
 // the sign of x; FP8 s = amax / 448 (1 for an all-zero row), q =
 // E4M3_RNE_sat(x / s).  Built without fast-math: x * 2^-e is an exact fp32
 // product (subnormal inputs included) and x / s is IEEE division.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -142,6 +143,50 @@ __device__ __forceinline__ uint32_t amax_bf16x8(const uint4 &w) {
   return max(m2 & 0xFFFFu, m2 >> 16);
 }
 
+// 8 bf16 values -> 8 E4M3 bytes: q = E4M3_RNE_sat(x / s) (IEEE division),
+// the sign of x kept on codes that round to zero.
+__device__ __forceinline__ uint2 fp8_quant8(const uint4 &w, float s) {
+  uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w.x), s), __fdiv_rn(bf16_hi(w.x), s)) |
+                (e4m3x2(__fdiv_rn(bf16_lo(w.y), s), __fdiv_rn(bf16_hi(w.y), s)) << 16);
+  uint32_t hi = e4m3x2(__fdiv_rn(bf16_lo(w.z), s), __fdiv_rn(bf16_hi(w.z), s)) |
+                (e4m3x2(__fdiv_rn(bf16_lo(w.w), s), __fdiv_rn(bf16_hi(w.w), s)) << 16);
+  lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
+  hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
+  return make_uint2(lo, hi);
+}
+
+// Where row r of a per-row FP8 output of K bytes goes: 128-byte column c of
+// the row at base + c * col_stride, its 16-byte unit j at ((j ^ rsw) * 16).
+// tile_rows: 0 = row-major, kPanelLayout = weight panels, else token tiles.
+struct Fp8RowDest {
+  size_t base, col_stride;
+  int rsw;
+  __device__ __forceinline__ Fp8RowDest(int r, int K, int tile_rows) {
+    const int KC = K >> 7;  // 128-byte columns per row
+    if (tile_rows == kPanelLayout) {
+      base = (size_t)(r >> 8) * KC * kF8PanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
+      col_stride = kF8PanelBytes;
+      rsw = r & 7;
+    } else if (tile_rows > 0) {
+      const int t_shift = __ffs(tile_rows) - 1;  // tile_rows is a power of 2
+      const int rr = r & (tile_rows - 1);
+      base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
+      col_stride = (size_t)tile_rows * 128u;
+      rsw = rr & 7;
+    } else {
+      base = (size_t)r * K;
+      col_stride = 128;
+      rsw = 0;
+    }
+  }
+  // the 8 bytes of 8-value chunk c
+  __device__ __forceinline__ uint2 *chunk(uint8_t *q, int c) const {
+    const int b = c * 8;
+    return reinterpret_cast<uint2 *>(q + base + (size_t)(b >> 7) * col_stride +
+                                     (size_t)((((b >> 4) & 7) ^ rsw) << 4) + (b & 15));
+  }
+};
+
 // One CTA per row (grid-stride over rows), two passes over the row: the
 // amax, then the codes (the row is re-read from L1).  Few registers, so the
 // CTAs fit beside a resident GEMM CTA.  tile_rows: 0 = row-major q,
@@ -164,37 +209,10 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
       prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
   }
   pdl_wait();
-  const int KC = K >> 7;  // 128-byte columns per row
-  const int t_shift = (tile_rows > 0) ? __ffs(tile_rows) - 1 : 0;  // tile_rows is a power of 2
-  // destination of the 8 bytes of chunk c of row r: column c / 16 at
-  // row_base + column * col_stride, 16-byte unit j at ((j ^ rsw) * 16)
-  size_t row_base = 0, col_stride = 128;
-  int rsw = 0;
-  auto set_row = [&](int r) {
-    if (tile_rows == kPanelLayout) {
-      row_base = (size_t)(r >> 8) * KC * kF8PanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
-      col_stride = kF8PanelBytes;
-      rsw = r & 7;
-    } else if (tile_rows > 0) {
-      const int rr = r & (tile_rows - 1);
-      row_base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
-      col_stride = (size_t)tile_rows * 128u;
-      rsw = rr & 7;
-    } else {
-      row_base = (size_t)r * K;
-      col_stride = 128;
-      rsw = 0;
-    }
-  };
-  auto qdst = [&](int c) -> uint2 * {
-    const int b = c * 8;
-    return reinterpret_cast<uint2 *>(q + row_base + (size_t)(b >> 7) * col_stride +
-                                     (size_t)((((b >> 4) & 7) ^ rsw) << 4) + (b & 15));
-  };
   for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
-    set_row(r);
+    const Fp8RowDest dst(r, K, tile_rows);
     if (r >= rows) {  // panel padding (uniform over the CTA)
-      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
       continue;
     }
     const uint16_t *xr = x + (size_t)r * ldx;
@@ -219,22 +237,111 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
 
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
-      for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = make_uint2(0u, 0u);
+      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
       continue;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
-    auto quant8 = [&](const uint4 &w) {
-      uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w.x), s), __fdiv_rn(bf16_hi(w.x), s)) |
-                    (e4m3x2(__fdiv_rn(bf16_lo(w.y), s), __fdiv_rn(bf16_hi(w.y), s)) << 16);
-      uint32_t hi = e4m3x2(__fdiv_rn(bf16_lo(w.z), s), __fdiv_rn(bf16_hi(w.z), s)) |
-                    (e4m3x2(__fdiv_rn(bf16_lo(w.w), s), __fdiv_rn(bf16_hi(w.w), s)) << 16);
-      // keep the sign of x on codes that round to zero
-      lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
-      hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
-      return make_uint2(lo, hi);
-    };
-    for (int c = tid; c < cpr; c += kF8Threads) *qdst(c) = quant8(ld_keep_v4(xr + (size_t)c * 8));
+    for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = fp8_quant8(ld_keep_v4(xr + (size_t)c * 8), s);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU between the packed gate_up projection and the down projection, fused
+// with the per-token FP8 quantization of its output ("Kimi-K3-DSpark-FP8-PTPC",
+// "Phase 1 FP8 PTPC Quantization": gate_proj and up_proj packed into one
+// gate_up_proj; the activation is the SwiGLU reading).  A gate_up output row
+// is [gate (I) | up (I)]; h = bf16(silu(gate) * up) with
+//   silu(g) * u = (g / (1 + e^-g)) * u
+// formed in binary32 one IEEE operation at a time (no contraction), and e^t
+// by the method of Cody and Waite (Software Manual for the Elementary
+// Functions, 1980): n = rint(t / ln2), r = (t - n L1) - n L2 with ln2 split
+// so that n L1 is exact, e^r by its Taylor series through r^7/7! (Horner),
+// times 2^n.  h is then quantized per row exactly as fp8_quant_kernel does.
+__device__ __forceinline__ float cw_exp(float t) {
+  if (t != t) return t;
+  if (t > 88.72283f) return __int_as_float(0x7F800000);
+  if (t < -87.3f) return 0.0f;
+  const float log2e = 0x1.715476p+0f;   // 1/ln2 rounded to binary32
+  const float L1 = 0x1.62e4p-1f;        // 15 significant bits: n * L1 exact for |n| <= 128
+  const float L2 = 0x1.7f7d1cp-20f;     // ln2 - L1 rounded to binary32
+  const float nf = rintf(__fmul_rn(t, log2e));
+  const int n = (int)nf;
+  float r = __fsub_rn(t, __fmul_rn(nf, L1));
+  r = __fsub_rn(r, __fmul_rn(nf, L2));
+  float p = 0x1.a01a02p-13f;                       // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);  // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);   // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);   // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);   // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  if (n > 127) return __fmul_rn(__fmul_rn(p, __uint_as_float(254u << 23)), 2.0f);
+  return __fmul_rn(p, __uint_as_float((uint32_t)(n + 127) << 23));
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  const float d = __fadd_rn(1.0f, cw_exp(-g));
+  return __fmul_rn(__fdiv_rn(g, d), u);
+}
+
+// two bf16 gate values and the matching up values -> two bf16 h values
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
+  return pack_bf16x2(silu_mul(bf16_lo(g), bf16_lo(u)), silu_mul(bf16_hi(g), bf16_hi(u)));
+}
+
+constexpr int kSwThreads = 256;
+
+// One CTA per row (grid-stride over rows): pass 1 forms h for the row into
+// shared memory (I bf16) and takes its amax; pass 2 quantizes h from shared
+// memory into q (row-major or the down GEMM's token tiles) and writes the
+// row's scale.  h_out (optional) receives h itself.
+__global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *__restrict__ gu,
+                                                                long long ldgu, int rows, int I,
+                                                                int tile_rows, uint16_t *__restrict__ h_out,
+                                                                long long ldh, uint8_t *__restrict__ q,
+                                                                float *__restrict__ scale) {
+  extern __shared__ uint4 hrow[];  // I / 8 chunks of 8 bf16
+  __shared__ uint32_t red[kSwThreads / 32];
+  const int tid = threadIdx.x;
+  const int cpr = I >> 3;
+  pdl_trigger();  // an activation step: the next kernel may launch now
+  if (tid == 0 && (int)blockIdx.x < rows) {  // warm L2 with the first row
+    const uint16_t *g = gu + (size_t)blockIdx.x * ldgu;
+    for (int c = 0; c < 2 * cpr; c += 1024)
+      prefetch_l2_bulk(g + (size_t)c * 8, (uint32_t)min(1024, 2 * cpr - c) * 16u);
+  }
+  pdl_wait();  // gu comes from the kernel ahead (the gate_up GEMM)
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t *gr = gu + (size_t)r * ldgu;
+    const uint16_t *ur = gr + I;
+    uint32_t amax = 0;
+    for (int c = tid; c < cpr; c += kSwThreads) {
+      const uint4 g = ld_stream_v4(gr + (size_t)c * 8);
+      const uint4 u = ld_stream_v4(ur + (size_t)c * 8);
+      const uint4 h = make_uint4(swiglu2(g.x, u.x), swiglu2(g.y, u.y), swiglu2(g.z, u.z), swiglu2(g.w, u.w));
+      hrow[c] = h;
+      if (h_out) *reinterpret_cast<uint4 *>(h_out + (size_t)r * ldh + (size_t)c * 8) = h;
+      amax = max(amax, amax_bf16x8(h));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();  // also: hrow complete
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kSwThreads / 32; ++i) amax = max(amax, red[i]);
+    const Fp8RowDest dst(r, I, tile_rows);
+    if (amax >= 0x7F80u) {  // Inf or NaN in h
+      if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
+      for (int c = tid; c < cpr; c += kSwThreads) *dst.chunk(q, c) = make_uint2(0u, 0u);
+    } else {
+      const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
+      if (tid == 0) scale[r] = s;
+      for (int c = tid; c < cpr; c += kSwThreads) *dst.chunk(q, c) = fp8_quant8(hrow[c], s);
+    }
+    __syncthreads();  // red[] and hrow are reused by the next row
   }
 }
 
@@ -249,9 +356,13 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   const int rows_iter = tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows
                         : swizzled                   ? ((rows + 127) / 128) * 128
                                                      : rows;
-  // enough CTAs for ~8 resident per SM, rows beyond that are grid-strided
+  // enough CTAs for ~8 resident per SM, rows beyond that are grid-strided;
+  // for a decode-sized activation (a few hundred rows at most) one CTA per
+  // SM: launched early beside the GEMMs of a layer chain, a second
+  // quantizer CTA on an SM would leave no registers for the next GEMM CTA
   int gy = rows_iter;
-  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
+  const int sms = sm_count > 0 ? sm_count : 152;
+  const int cap = (act && rows <= 512) ? sms : sms * 8;
   if (gy * gx > cap) gy = (cap + gx - 1) / gx;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
@@ -284,6 +395,32 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows,
                             rows_iter, K, tile_rows, act ? 1 : 0, q, scale);
+}
+
+cudaError_t launch_swiglu_fp8(const void *gu, long long ldgu, int rows, int I, int tile_rows, void *h_out,
+                              long long ldh, uint8_t *q, float *scale, int sm_count, cudaStream_t stream) {
+  const size_t smem = (size_t)I * 2u;
+  int g = rows;
+  const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (200u * 1024u) / std::max<size_t>(smem, 1)));
+  const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
+  if (g > cap) g = cap;
+  static DeviceOnce once;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!once.done(dev)) {
+    e = cudaFuncSetAttribute(swiglu_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(swiglu_fp8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    once.set(dev);
+  }
+  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kSwThreads), smem, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, swiglu_fp8_kernel, static_cast<const uint16_t *>(gu), ldgu, rows, I, tile_rows,
+                            static_cast<uint16_t *>(h_out), ldh, q, scale);
 }
 
 }  // namespace mxg

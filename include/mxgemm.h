@@ -153,14 +153,18 @@ typedef struct {
                              must equal the plan's MMA-N tile (mxg_plan_gemm().bn) for the
                              SPLITK variant and 128 for the FULL variant.  (The fused A4W4
                              path picks its own layout and ignores this field.) */
-    void *trace;          /* optional device buffer of ctas x 20 uint64, zero-filled: each
+    void *trace;          /* optional device buffer of ctas x 40 uint64, zero-filled: each
                              CTA records SM clock64 stamps of its timeline (entry, setup,
                              first/last load, first stage ready, last MMA commit, epilogue
                              items, split-K hand-off, exit; slot 15 = items; slots 16/17 =
                              global timer ns at entry/exit; slot 18 = the producer's
-                             dependency wait returned; fused path: slot 19 = activation
-                             share quantized, slot 12 = first and slot 13 = second grid
-                             barrier passed).
+                             dependency wait returned, slot 20 = the same in global timer
+                             ns; fused path: slot 19 = activation share quantized, slot 12
+                             = first and slot 13 = second grid barrier passed).  Slots 22
+                             and 23 of CTA 0's row: the split-K reduce kernel of the same
+                             call, ~(first entry ns) and last exit ns.  Slot 21: the SM.
+                             A4W4, slots 24+k / 32+k: the CTA's k-th pipeline stage
+                             (k < 8) landed in shared memory / its scales are in TMEM.
                              NULL = off. */
     int splitk_reduce;    /* how SPLITK partial tiles are summed when the activations come
                              pre-quantized: MXG_REDUCE_DEFAULT (= MXG_REDUCE_KERNEL),
@@ -300,6 +304,28 @@ mxg_status mx_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int 
 mxg_status fp8_quantize_act_tiled(const void *x_bf16, int M, int K, int ldx, int tile_rows,
                                   uint8_t *q, float *scale, mxg_stream_t stream);
 
+/* The step between the packed gate_up projection and the down projection of
+ * the FP8 MLP ("Phase 1 FP8 PTPC Quantization": gate_proj and up_proj are
+ * packed into one gate_up_proj), fused with the down projection's dynamic
+ * per-token FP8 quantization.  The pages do not name the activation; the
+ * library takes SwiGLU:
+ *   h[m][j] = bf16(silu(g) * u),  g = gu[m][j], u = gu[m][I + j],
+ *   silu(g) * u = (g / (1 + e^-g)) * u in binary32, one IEEE operation at a
+ *   time, e^t by the Cody-Waite method (t = n ln2 + r, Taylor series of e^r
+ *   through r^7/7!), so the result is the same on any IEEE machine;
+ * then q, scale = fp8_quantize_act(h) (per row: s = amax/448, q = E4M3(h/s)).
+ *   gu_bf16: (M, 2I) bf16, a row [gate (I) | up (I)], leading dimension ldgu
+ *            (>= 2I elements).  I % 128 == 0, I <= 102400.
+ *   q:       E4M3 codes of h, row-major (M, I) for tile_rows == 0, else in
+ *            the activation tile layout with tiles of tile_rows rows (as
+ *            fp8_quantize_act_tiled writes; what fp8_gemm_ptpc reads with
+ *            opts->act_tile_rows = tile_rows).  scale: M floats.
+ *   h_bf16:  optional (NULL = not written) (M, I) bf16 output of h itself,
+ *            leading dimension ldh. */
+mxg_status swiglu_fp8_quantize(const void *gu_bf16, int M, int I, int ldgu, int tile_rows,
+                               uint8_t *q, float *scale, void *h_bf16, int ldh,
+                               mxg_stream_t stream);
+
 /* FP8 PTPC A8W8 GEMM: y[m][n] = (acc[m][n] * sa[m]) * sw[n] with
  * acc = sum_k v(qa[m,k]) v(qw[n,k]) accumulated in fp32.
  *   qa (M, K), sa (M); qw (N, K), sw (N); y (M, N), leading dimension ldy.
@@ -335,7 +361,12 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
  *     `stream`), then runs the GEMM.  All calls share the one array, which
  *     keeps the last call's contents: calls that overlap on the GPU (other
  *     streams, other threads) race on it and must be serialised by the
- *     caller. */
+ *     caller.
+ *   - Every operand is checked before the scratch is touched: a call that
+ *     returns an error has written nothing.
+ *   - It has no device status word: a bounded device wait that runs out
+ *     ends the kernel early (y then partly written) without being reported.
+ *     Callers that need that report use mx_gemm_a4w4 with opts->dev_status. */
 mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf,
                                 const void *x_bf16, int ldx,
                                 const uint8_t *w_codes, const uint8_t *w_sf,

@@ -201,3 +201,19 @@ def test_dispatcher_rule(kind, M, N, K, want):
     a full wave of 128 x 256 tiles -> full tile; otherwise split-K for M <= 128,
     and up to M = 256 when K exceeds 64 128-byte columns."""
     assert mx.mxg_plan_gemm(kind, M, N, K, 152)["variant"] == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((FAKE, 8, 100, 200, 0, FAKE, FAKE, None, 0), 2),      # I % 128
+    ((FAKE, 8, 204800, 409600, 0, FAKE, FAKE, None, 0), 2),  # h of a row beyond shared memory
+    ((None, 8, 128, 256, 0, FAKE, FAKE, None, 0), 1),       # null input
+    ((FAKE, 0, 128, 256, 0, FAKE, FAKE, None, 0), 1),       # M = 0
+    ((FAKE, 8, 128, 200, 0, FAKE, FAKE, None, 0), 1),       # ldgu < 2I
+    ((FAKE, 8, 128, 256, 48, FAKE, FAKE, None, 0), 1),      # tile height not a power of two in 16..256
+    ((FAKE, 8, 128, 256, 0, FAKE, FAKE, FAKE, 64), 1),      # ldh < I
+    ((FAKE + 2, 8, 128, 256, 0, FAKE, FAKE, None, 0), 3),   # misaligned gate_up
+    ((FAKE, 8, 128, 260, 0, FAKE, FAKE, None, 0), 3),       # ldgu * 2 not a multiple of 16
+    ((FAKE, 8, 128, 256, 0, FAKE, FAKE + 4, None, 0), 3),   # misaligned scale
+])
+def test_swiglu_argument_errors_before_launch(args, want):
+    assert mx.lib().swiglu_fp8_quantize(*args, None) == want

@@ -48,3 +48,18 @@ def test_act_tile_rows_follow_the_plan():
     full = mx.mxg_plan_gemm(mx.KIND_A4W4, 8192, 7168, 8192, 152)
     assert split["variant"] == 2 and bench.act_tile_rows(split) == split["bn"] == 64
     assert full["variant"] == 1 and bench.act_tile_rows(full) == 128
+
+
+def test_bench_interval_check_catches_a_wrong_value():
+    """The bf16 check the bench applies to its timed outputs rejects a value
+    one bf16 step off when the tolerance is far below a step."""
+    ref = np.array([[1.0, -3.0, 100.0]])
+    bound = np.array([[1.0, 1.0, 1.0]])
+    good = torch.tensor(ref, dtype=torch.float32).to(torch.bfloat16)
+    assert bench.bf16_interval_check(good, ref, bound)[0]
+    bad = good.clone()
+    bad.view(torch.int16)[0, 2] += 1
+    assert not bench.bf16_interval_check(bad, ref, bound)[0]
+    nan_ref = np.array([[np.nan]])
+    assert bench.bf16_interval_check(torch.tensor([[float("nan")]]).to(torch.bfloat16), nan_ref, bound[:, :1])[0]
+    assert not bench.bf16_interval_check(torch.tensor([[0.0]]).to(torch.bfloat16), nan_ref, bound[:, :1])[0]

@@ -273,3 +273,29 @@ def test_ptpc_full_tile_banded_raster():
     rows = np.array([0, 127, 128, 1023, 1024, 1151, 2047, 2048, 2200, 2559])
     ref, bound = oracle_ptpc(x, w, rows=rows)
     assert_gemm_close(y32[rows], ref, bound, f"ptpc full banded {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("variant", ["full", "splitk"])
+@pytest.mark.parametrize("kind", [0, 1])
+def test_nonfinite_activation_rows_through_the_gemm(kind, variant):
+    """A block (MXFP4) or a row (FP8) that holds a NaN or an infinity gets a
+    NaN scale and zero codes (the OCP MX rule that a NaN scale makes the
+    whole block NaN; the same reading for the per-token FP8 scale).  Its
+    output row is then NaN in every column, and every other row is as usual:
+    the NaN pattern and the finite values must match the oracle."""
+    M, N, K = 40, 512, 1024
+    x, w = quant_pair(M, N, K, seed=91)
+    x = x.clone()
+    x[3, 100] = float("nan")
+    x[17, K - 1] = float("inf")
+    x[30, 0] = float("-inf")
+    if kind == 0:
+        ref, bound = oracle_a4w4(x, w)
+        for fused in (True, False):
+            y = run_a4w4(x, w, variant, fused=fused).cpu().numpy()
+            assert_gemm_close(y, ref, bound, f"a4w4 {variant} fused={fused} non-finite rows")
+    else:
+        ref, bound = oracle_ptpc(x, w)
+        y = run_ptpc(x, w, variant).cpu().numpy()
+        assert_gemm_close(y, ref, bound, f"ptpc {variant} non-finite rows")
+    assert np.isnan(ref[[3, 17, 30]]).all() and not np.isnan(np.delete(ref, [3, 17, 30], axis=0)).any()

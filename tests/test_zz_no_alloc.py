@@ -5,10 +5,12 @@ memory up front and must not allocate on its hot path).  Its scratch is a
 device array owned by the library, so the caller passes no workspace.
 
 Checked through the C ABI against the existing entry point (mx_gemm_a4w4
-with a caller workspace): two calls in a row must agree with it within the
-GEMM tolerance of the other tests (|dy| <= 1e-5 * sum_k |a_k w_k|).  This
-file sorts last so that a stop-at-first-failure run has already run every
-other test; it needs no state from them.
+with a caller workspace) and against the oracle's reference: on two calls
+in a row the output must agree with both within the GEMM tolerance of the
+other tests (|dy| <= 1e-5 * sum_k |a_k w_k|).  A call rejected for a bad
+operand must write nothing.  This file sorts last so that a
+stop-at-first-failure run has already run every other test; it needs no
+state from them.
 """
 import ctypes
 
@@ -56,7 +58,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(M, fused, tiled):
     y_ref = y_ref.cpu().numpy()
     a_c, a_s = oracle.mx_quantize_rows(x)
     w_c, w_s = oracle.mx_quantize_rows(w)
-    _, bound = oracle.gemm_a4w4(a_c, a_s, w_c, w_s)
+    ref, bound = oracle.gemm_a4w4(a_c, a_s, w_c, w_s)
+    assert_gemm_close(y_ref, ref, bound, "mx_gemm_a4w4 with a caller workspace")
 
     f = noalloc_entry()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -70,6 +73,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(M, fused, tiled):
         assert not np.isnan(got).any(), f"call {call}: output not fully written"
         err = np.abs(got.astype(np.float64) - y_ref.astype(np.float64))
         assert (err <= GEMM_REL_TOL * bound).all(), f"call {call}: max err/bound {float((err / np.maximum(bound, 1e-300)).max())}"
+        assert_gemm_close(got, ref, bound, f"mx_gemm_a4w4_noalloc call {call} vs the oracle")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
@@ -84,3 +88,22 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = noalloc_entry()(None, None, ptr(x), K, ptr(wc), ptr(wsf), M, N, K, ptr(y), N, mx.OUT_BF16, 0,
                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 7  # MXG_ERR_WORKSPACE, before any launch
+
+
+def test_noalloc_rejected_call_writes_nothing():
+    """Bad operands are refused before anything is launched: the output
+    buffer keeps its contents (the shared scratch is not touched either,
+    which is what lets a refused call run beside one in flight)."""
+    d = dev()
+    M, N, K = 8, 256, 512
+    x = torch.zeros(M, K, dtype=torch.bfloat16, device=d)
+    wc = torch.zeros(N, K // 2, dtype=torch.uint8, device=d)
+    y = torch.full((M, N), 7.0, dtype=torch.float32, device=d)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    f = noalloc_entry()
+    st = f(None, None, ptr(x), K, ptr(wc), None, M, N, K, ptr(y), N, mx.OUT_F32, 0, stream)  # w_sf missing
+    assert st == 1  # MXG_ERR_INVALID_ARG
+    st = f(None, None, ptr(x), K, ptr(wc), ptr(wc), M, N, K, ptr(y), N, mx.OUT_F32, 5, stream)  # bad layout
+    assert st == 1
+    torch.cuda.synchronize()
+    assert (y == 7.0).all()
