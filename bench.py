@@ -179,7 +179,7 @@ class ClockSampler:
 def gemm_kernels(plan: dict) -> int:
     """Kernels one GEMM call launches under the default split-K reduction: the
     GEMM, plus the reduce kernel when a split-K tile has several partials."""
-    return 1 + (1 if plan["variant"] == 2 and plan["seg_max"] > 1 and not plan.get("pair") else 0)
+    return 1 + (1 if plan["variant"] == 2 and plan["seg_max"] > 1 else 0)
 
 
 def act_tile_rows(plan: dict) -> int:

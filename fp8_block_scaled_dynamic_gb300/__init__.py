@@ -53,13 +53,13 @@ class GemmOpts(ctypes.Structure):
                 ("trace", ctypes.c_void_p), ("splitk_reduce", ctypes.c_int)]
 
 
-REDUCE = {"default": 0, "kernel": 1, "grid": 2, "lastcta": 3, "pair": 4}
+REDUCE = {"default": 0, "kernel": 1}
 
 
 class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("kblocks", ctypes.c_int),
-                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t), ("pair", ctypes.c_int)]
+                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t), ("reserved", ctypes.c_int)]
 
 
 _lib = None
@@ -165,8 +165,8 @@ _ws_cache: dict = {}
 
 def workspace(nbytes: int, device=None) -> torch.Tensor | None:
     """A zero-filled device workspace of at least nbytes, cached per device.
-    Completed calls leave its counters zero, so it is reused across calls on
-    one stream; give concurrent streams their own workspace."""
+    It is reused across calls on one stream; give concurrent streams their
+    own workspace."""
     if nbytes <= 0:
         return None
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)

@@ -17,15 +17,9 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-// Workspace layout, fixed for every call so that no call's data can land in
-// another call's counters: [0, 64 KiB) split-K arrival counters (zero before
-// the first call, left zero by every completed call), then the quantized
-// activations of the fused A4W4 path, then the split-K partial tiles.
-constexpr size_t kCounterBytes = 64 * 1024;
-// the last 512 bytes of the counter region hold the grid barrier words
-// (one 128-byte line each)
-constexpr size_t kGridBarrierOff = kCounterBytes - 512;
-constexpr long long kMaxSplitTiles = kGridBarrierOff / sizeof(int);
+// Workspace layout: the quantized activations of the fused A4W4 path (when
+// the call quantizes x itself), then the split-K partial tiles.  Nothing in
+// it needs to start at any particular value.
 
 struct DevInfo {
   bool init = false;
@@ -98,36 +92,6 @@ mxg_status make_output_map(CUtensorMap *m, void *y, int M, int N, int ldy) {
   return r == CUDA_SUCCESS ? MXG_OK : MXG_ERR_CUDA;
 }
 
-// How split-K partial tiles are summed on the two-kernel path:
-//   kernel (default): a reduce kernel launched right after the GEMM;
-//   grid: by every CTA of the GEMM after a grid barrier (one launch);
-//   lastcta: by the last CTA to finish each tile (arrival counter).
-// MXG_SPLITK_REDUCE=kernel|grid|lastcta selects it (MXG_SPLITK_INKERNEL=1 =
-// lastcta).  The single-kernel fused A4W4 path always sums in-grid.
-enum class ReduceMode { kKernel, kGrid, kLastCta, kPair };
-ReduceMode reduce_mode() {
-  static const ReduceMode m = [] {
-    const char *e = std::getenv("MXG_SPLITK_REDUCE");
-    if (e && std::strcmp(e, "grid") == 0) return ReduceMode::kGrid;
-    if (e && std::strcmp(e, "lastcta") == 0) return ReduceMode::kLastCta;
-    if (e && std::strcmp(e, "pair") == 0) return ReduceMode::kPair;
-    const char *f = std::getenv("MXG_SPLITK_INKERNEL");
-    if (f && f[0] == '1') return ReduceMode::kLastCta;
-    return ReduceMode::kKernel;
-  }();
-  return m;
-}
-// The split-K reduction a call asks for: opts->splitk_reduce, else the
-// MXG_SPLITK_REDUCE environment default.
-ReduceMode requested_reduce(const mxg_gemm_opts *opts) {
-  ReduceMode mode = reduce_mode();
-  if (opts && opts->splitk_reduce == MXG_REDUCE_KERNEL) mode = ReduceMode::kKernel;
-  if (opts && opts->splitk_reduce == MXG_REDUCE_GRID) mode = ReduceMode::kGrid;
-  if (opts && opts->splitk_reduce == MXG_REDUCE_LAST_CTA) mode = ReduceMode::kLastCta;
-  if (opts && opts->splitk_reduce == MXG_REDUCE_PAIR) mode = ReduceMode::kPair;
-  return mode;
-}
-
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
@@ -183,20 +147,9 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
     pl->bn = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
     const long long tilesA = N / 128, tilesB = (M + pl->bn - 1) / pl->bn;
     const long long tiles = tilesA * tilesB;
-    if (requested_reduce(opts) == ReduceMode::kPair && KB >= 2 && 2 * tiles <= sm_count &&
-        !(opts && opts->ctas > 0)) {
-      // CTA pairs: the stream-K split with G = 2 x tiles gives CTAs 2t and
-      // 2t + 1 the two halves of tile t's K range
-      pl->tiles = (int)tiles;
-      pl->ctas = (int)(2 * tiles);
-      pl->seg_max = 2;
-      pl->ws_bytes = 0;
-      pl->pair = 1;
-      return MXG_OK;
-    }
     const long long U = tiles * KB;
     if (U > (1LL << 40) / 4) return MXG_ERR_UNSUPPORTED_SHAPE;
-    // persistent: at most one CTA per SM (grid barriers need them all resident)
+    // persistent: at most one CTA per SM
     long long G = (opts && opts->ctas > 0 && opts->ctas < sm_count) ? opts->ctas : sm_count;
     if (G > U) G = U;
     int seg_max = 1;
@@ -204,15 +157,12 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
       const long long n = owner_of(t * KB + KB - 1, U, G) - owner_of(t * KB, U, G) + 1;
       if (n > seg_max) seg_max = (int)n;
     }
-    if (seg_max > 1 && tiles > kMaxSplitTiles) return MXG_ERR_UNSUPPORTED_SHAPE;
     // the kernel walks its stream-K range in 32-bit arithmetic
     if ((U + 1) * G >= (1LL << 32)) return MXG_ERR_UNSUPPORTED_SHAPE;
     pl->tiles = (int)tiles;
     pl->ctas = (int)G;
     pl->seg_max = seg_max;
-    pl->ws_bytes = seg_max > 1 ? kCounterBytes +
-                                     (size_t)tiles * seg_max * pl->bn * 128 * sizeof(float)
-                               : 0;
+    pl->ws_bytes = seg_max > 1 ? (size_t)tiles * seg_max * pl->bn * 128 * sizeof(float) : 0;
   }
   return MXG_OK;
 }
@@ -249,12 +199,10 @@ bool valid_tile_rows(int t) { return t == 16 || t == 32 || t == 64 || t == 128 |
 struct GemmOperands {
   const uint8_t *a, *a_sf, *w, *w_sf;  // codes (A4W4) or E4M3 bytes (PTPC)
   const float *sa, *sw;                // PTPC scales
-  const void *x;                       // single-kernel fused A4W4: bf16 activations that the
-  long long ldx;                       //   GEMM quantizes into a / a_sf itself
 };
 
 // ws: the caller's workspace base; part_off: where the partial tiles start
-// (after the counters and, on the fused path, the quantized activations).
+// (after the quantized activations on the fused path).
 // act_tile_rows: 0 = activations row-major, else in the tile layout with
 // tiles of that many rows (must match the plan: plan_act_tile_rows).
 mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void *y, int ldy,
@@ -265,7 +213,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   mxg_status st = plan_impl(kind, M, N, K, sm_count, opts, &pl);
   if (st != MXG_OK) return st;
   if (pl.ws_bytes > 0) {
-    if (!ws || ws_bytes < part_off + (pl.ws_bytes - kCounterBytes)) return MXG_ERR_WORKSPACE;
+    if (!ws || ws_bytes < part_off + pl.ws_bytes) return MXG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
   }
 
@@ -312,10 +260,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.G4 = K / 128;
   p.splitk = swap ? 1 : 0;
   p.units = (long long)p.tilesA * p.tilesB * p.kblocks;
-  if (pl.ws_bytes > 0) {
-    p.counters = static_cast<int *>(ws);
-    p.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + part_off);
-  }
+  if (pl.ws_bytes > 0) p.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + part_off);
   p.seg_max = pl.seg_max;
   p.status = opts ? opts->dev_status : nullptr;
   const uint32_t tmo = (opts && opts->timeout_ms) ? opts->timeout_ms : 1000u;
@@ -356,27 +301,8 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
       p.a_tiles = op.a;
     }
   }
-  if (op.x) {
-    // single kernel: quantize x into the token tiles, grid barrier, GEMM
-    p.x = static_cast<const uint16_t *>(op.x);
-    p.ldx = op.ldx;
-    p.fuse_quant = 1;
-  }
-  ReduceMode mode = requested_reduce(opts);
-  if (op.x && mode != ReduceMode::kLastCta) mode = ReduceMode::kGrid;
-  if (pl.pair && !op.x) {
-    p.pair_reduce = 1;
-  } else {
-    if (mode == ReduceMode::kPair) mode = ReduceMode::kKernel;  // the plan found no room for pairs
-    p.grid_reduce = (pl.seg_max > 1 && mode == ReduceMode::kGrid) ? 1 : 0;
-    p.defer_reduce = (pl.seg_max > 1 && mode == ReduceMode::kKernel) ? 1 : 0;
-  }
-  if (p.fuse_quant || p.grid_reduce) {
-    if (!ws) return MXG_ERR_WORKSPACE;
-    p.gbar = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + kGridBarrierOff);
-  }
   cudaError_t e = mxg::launch_gemm(kind, pl.bn, tmA, tmB, tmY, p, pl.ctas, stream);
-  if (e == cudaSuccess && p.defer_reduce)
+  if (e == cudaSuccess && swap && pl.seg_max > 1)
     e = mxg::launch_splitk_reduce(kind, pl.bn, p, pl.ctas, sm_count, stream);
   return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
 }
@@ -390,7 +316,7 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
     return MXG_ERR_MISALIGNED;
   if (opts && (opts->variant < 0 || opts->variant > 2 || opts->ctas < 0))
     return MXG_ERR_INVALID_ARG;
-  if (opts && (opts->splitk_reduce < MXG_REDUCE_DEFAULT || opts->splitk_reduce > MXG_REDUCE_PAIR))
+  if (opts && opts->splitk_reduce != MXG_REDUCE_DEFAULT && opts->splitk_reduce != MXG_REDUCE_KERNEL)
     return MXG_ERR_INVALID_ARG;
   if (opts && (opts->weights_tiled < 0 || opts->weights_tiled > 2)) return MXG_ERR_INVALID_ARG;
   if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
@@ -435,8 +361,7 @@ size_t mxg_gemm_workspace_bytes(int kind, int fused, int M, int N, int K,
   mxg_plan pl;
   if (plan_impl(kind, M, N, K, sm, opts, &pl) != MXG_OK) return 0;
   const size_t act = (kind == 0 && fused) ? fused_act_bytes(M, K, plan_act_tile_rows(pl)) : 0;
-  if (pl.ws_bytes == 0 && act == 0) return 0;
-  return kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
+  return act + pl.ws_bytes;
 }
 
 namespace {
@@ -585,7 +510,7 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *ws = opts ? static_cast<uint8_t *>(opts->workspace) : nullptr;
   size_t ws_bytes = opts ? opts->ws_bytes : 0;
-  size_t part_off = kCounterBytes;
+  size_t part_off = 0;
   int act_tile_rows = opts ? opts->act_tile_rows : 0;
   if (fused) {
     // plan first: the activations are quantized straight into the tile
@@ -595,26 +520,17 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
     if ((st = plan_impl(0, M, N, K, sm, opts, &pl)) != MXG_OK) return st;
     act_tile_rows = K % 256 == 0 ? plan_act_tile_rows(pl) : 0;
     const size_t need = fused_act_bytes(M, K, act_tile_rows);
-    if (!ws || ws_bytes < kCounterBytes + need) return MXG_ERR_WORKSPACE;
+    if (!ws || ws_bytes < need + pl.ws_bytes) return MXG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
-    if (pl.ws_bytes > 0 && ws_bytes < kCounterBytes + need + (pl.ws_bytes - kCounterBytes))
-      return MXG_ERR_WORKSPACE;
-    uint8_t *codes = ws + kCounterBytes;
+    uint8_t *codes = ws;
     uint8_t *sf = codes + align256(act_code_bytes(M, (size_t)K / 2, act_tile_rows));
     a_codes = codes;
     a_sf = sf;
     part_off += need;
-    if (pl.variant == MXG_VARIANT_SPLITK && act_tile_rows && opts &&
-        (opts->splitk_reduce == MXG_REDUCE_GRID || opts->splitk_reduce == MXG_REDUCE_LAST_CTA)) {
-      // one kernel: its CTAs quantize x into the token tiles themselves
-      GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr, x_bf16, ldx};
-      return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off,
-                      act_tile_rows, sm, s);
-    }
     cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s);
     if (e != cudaSuccess) return MXG_ERR_CUDA;
   }
-  GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr, nullptr, 0};
+  GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
   return run_gemm(0, op, M, N, K, y, ldy, out_dtype, opts, ws, ws_bytes, part_off, act_tile_rows,
                   sm, s);
 }
@@ -630,9 +546,9 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, 
     return MXG_ERR_MISALIGNED;
   int sm = 0;
   if ((st = check_device(&sm)) != MXG_OK) return st;
-  GemmOperands op{qa, nullptr, qw, nullptr, sa, sw, nullptr, 0};
+  GemmOperands op{qa, nullptr, qw, nullptr, sa, sw};
   return run_gemm(1, op, M, N, K, y, ldy, out_dtype, opts, opts ? opts->workspace : nullptr,
-                  opts ? opts->ws_bytes : 0, kCounterBytes, opts ? opts->act_tile_rows : 0, sm,
+                  opts ? opts->ws_bytes : 0, 0, opts ? opts->act_tile_rows : 0, sm,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -695,8 +611,8 @@ const char *mxg_status_string(mxg_status s) {
 
 // ---------------------------------------------------------------------------
 // mx_gemm_a4w4_noalloc: the A4W4 GEMM for callers that cannot allocate device
-// memory.  Its scratch (split-K arrival counters, fused activations, partial
-// tiles -- the same layout as the caller workspace of mx_gemm_a4w4) lives in
+// memory.  Its scratch (fused activations, partial tiles -- the same layout
+// as the caller workspace of mx_gemm_a4w4) lives in
 // this file-scope device array, which every GPU that loads the library holds
 // until the process exits.  Host code must not use the array's name as a
 // device address: the address comes from cudaGetSymbolAddress, once per
@@ -745,14 +661,12 @@ mxg_status mx_gemm_a4w4_noalloc(const uint8_t *a_codes, const uint8_t *a_sf, con
   const bool fused = a_codes == nullptr;
   const size_t act =
       fused ? fused_act_bytes(M, K, K % 256 == 0 ? plan_act_tile_rows(pl) : 0) : 0;
-  const size_t need = kCounterBytes + act + (pl.ws_bytes > 0 ? pl.ws_bytes - kCounterBytes : 0);
+  const size_t need = act + pl.ws_bytes;
   if (need > (size_t)MXG_NOALLOC_SCRATCH_BYTES) return MXG_ERR_WORKSPACE;
   void *scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != MXG_OK) return st;
-  // the arrival counters must start at zero; the array keeps whatever the
-  // previous call (on any stream) left in it
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(scratch, 0, kCounterBytes, s) != cudaSuccess) return MXG_ERR_CUDA;
+  // every byte of scratch a call reads, that call has written first, so
+  // whatever the previous call left in the array is never used
   opts.workspace = scratch;
   opts.ws_bytes = MXG_NOALLOC_SCRATCH_BYTES;
   return mx_gemm_a4w4(a_codes, a_sf, x_bf16, ldx, w_codes, w_sf, M, N, K, y, ldy, out_dtype, &opts,

@@ -15,18 +15,15 @@
 //   split-K    (swap = 1): MMA-A = 128 weight rows, MMA-B = the (padded)
 //              token rows; the (tile, K-block) units are cut evenly over the
 //              CTAs (stream-K); a CTA that ends a tile part-way writes an
-//              fp32 partial tile.  The partials are summed in slot order -- a
-//              fixed order, so results are deterministic -- by the reduce
-//              kernel launched after the GEMM (default), by every CTA after a
-//              grid barrier, by the last CTA to finish the tile, or, for CTA
-//              pairs in a 2-CTA cluster, by the first CTA of the pair from its
-//              partner's partial in its shared memory.
+//              fp32 partial tile, and the reduce kernel launched right after
+//              the GEMM sums the partials of each tile in slot order -- a
+//              fixed order, so results are deterministic.
 //
 // Warp roles (192 threads): warp 0 = producer (bulk copies of operand tiles
 // and weight panels, tensor-map boxes for row-major operands, scale tiles);
 // warp 1 = TMEM allocator and the single MMA-issuing thread; warps 2-5 =
-// epilogue (tcgen05.ld of their 32-lane quarter; for the full-tile A4W4 they
-// also move each stage's scale factors into TMEM, and store y by TMA).  All
+// epilogue (tcgen05.ld of their 32-lane quarter; for A4W4 they also move each
+// stage's scale factors into TMEM, and in the full tile store y by TMA).  All
 // hand-offs are mbarriers; every wait is bounded.
 #include <cstdint>
 #include <cstdlib>
@@ -73,6 +70,10 @@ struct Cfg {
   // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
   static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
+  // TMEM accumulators: two where the columns allow (FP8: all 512; A4W4: the
+  // 256 below the scale factors), so that the epilogue of one item runs
+  // beside the MMAs of the next
+  static constexpr int kAccBufs = 2 * BN <= (KIND == 0 ? (int)kSfCol : (int)kTmemCols) ? 2 : 1;
   static constexpr int kChunk = BN >= 32 ? 32 : 16;  // epilogue TMEM columns per load
   static constexpr int kSteps = 4 * KS;              // MMAs (K = 64 / 32) per stage
   static constexpr uint32_t kSfColsA = 8u * KS;      // 4 TMEM columns per scale atom
@@ -194,148 +195,65 @@ __device__ __forceinline__ void store_out(const GemmParams &p, int m, int n, flo
         static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
 }
 
-// Sum the nseg partial tiles of one output tile in slot order and write y.
-// Each slot is [column][128 rows] fp32; the 128 epilogue threads take float4
-// groups (4 consecutive rows of one column) so that loads and stores are
-// coalesced, with the loads of up to 4 slots x kU groups in flight at once
-// (one round of L2 latency per 128 * kU groups).
-template <int KIND>
-__device__ __forceinline__ void reduce_partials(const GemmParams &p, const float *tile_ws,
-                                                size_t slot_elems, int nseg, int ncols, int row0,
-                                                int col0, int tid) {
-  constexpr int kU = 8;
-  const int ngrp = ncols * (kTileA / 4);
-  const float4 *base = reinterpret_cast<const float4 *>(tile_ws);
-  const size_t slot4 = slot_elems / 4;
-#pragma unroll 1
-  for (int g0 = tid; g0 < ngrp; g0 += 128 * kU) {
-    float4 acc[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 v[4][kU];
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int g = g0 + 128 * u;
-        v[s][u] = (s < nseg && g < ngrp) ? __ldcg(base + s * slot4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        acc[u].x += v[s][u].x;
-        acc[u].y += v[s][u].y;
-        acc[u].z += v[s][u].z;
-        acc[u].w += v[s][u].w;
-      }
-#pragma unroll 1
-    for (int s = 4; s < nseg; ++s)
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int g = g0 + 128 * u;
-        if (g < ngrp) {
-          const float4 t = __ldcg(base + s * slot4 + g);
-          acc[u].x += t.x;
-          acc[u].y += t.y;
-          acc[u].z += t.z;
-          acc[u].w += t.w;
-        }
-      }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int g = g0 + 128 * u;
-      if (g >= ngrp) continue;
-      const int c = g / (kTileA / 4);
-      const int r = (g % (kTileA / 4)) * 4;
-      const int m = col0 + c;  // token
-      const int n = row0 + r;  // output channel (N % 128 == 0: always in range)
-      float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
-      if (KIND == 1) {
-        const float sa = p.tok_scale[m];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
-      }
-      if (p.out_f32) {
-        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
-            make_float4(f[0], f[1], f[2], f[3]);
-      } else {
-        *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
-            make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-      }
-    }
-  }
-}
-
-// Split-K reduction: for every tile that more than one CTA touched, y = sum
-// of the partial slots in slot order (fixed order: deterministic), then the
-// PTPC scales, then bf16 (or fp32).  One thread per float4 group of a slot
-// ([column][128 rows]), kRedJ groups per thread with all their loads issued
-// before the first sum (one round of L2 latency); threads first, first +
-// stride, ... so that every SM pulls a share.
+// Split-K reduction: the work is cut into (tile, chunk) items, a chunk being
+// kRedThreads x kRedJ float4 groups (4 consecutive rows of one column) of
+// the tile's [column][128 rows] slots.  An item sums the slots in slot order
+// (a fixed order: deterministic), applies the PTPC scales and writes y; all
+// loads of a thread go out before its first sum (one round of L2 latency).
 constexpr int kRedThreads = 128;
 constexpr int kRedJ = 2;
 
 template <int KIND>
-__device__ __forceinline__ void reduce_share(const GemmParams &p, int bn, unsigned gemm_ctas,
-                                             int first, int stride) {
+__device__ __forceinline__ void reduce_items(const GemmParams &p, int bn, unsigned gemm_ctas) {
   const unsigned U = (unsigned)p.units, KB = (unsigned)p.kblocks;
   const int per_col = kTileA / 4;
   const int per_tile = bn * per_col;
-  const int total = p.tilesA * p.tilesB * per_tile;
+  const int chunk = kRedThreads * kRedJ;
+  const int chunks = (per_tile + chunk - 1) / chunk;
+  const int items = p.tilesA * p.tilesB * chunks;
   const size_t slot4 = (size_t)bn * kTileA / 4;
-  for (int e0 = first; e0 < total; e0 += stride * kRedJ) {
-    int nseg[kRedJ];
-    const float4 *src[kRedJ];
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int t = item / chunks, c = item - t * chunks;
+    const unsigned first_u = (unsigned)t * KB;
+    const unsigned o0 = owner_of(first_u, U, gemm_ctas);
+    const int nseg = (int)(owner_of(first_u + KB - 1, U, gemm_ctas) - o0 + 1);
+    if (nseg <= 1) continue;  // one CTA owned the whole tile and wrote y itself
+    const int tb = t - (t / p.tilesB) * p.tilesB;
+    const int ta = t / p.tilesB;
+    const int valid_cols = min(bn, p.rowsB - tb * bn);
+    const float4 *base = reinterpret_cast<const float4 *>(p.ws) + (size_t)t * p.seg_max * slot4;
+    int g[kRedJ];
     float4 v[kRedJ][4];
 #pragma unroll
     for (int j = 0; j < kRedJ; ++j) {
-      const int e = e0 + j * stride;
-      nseg[j] = 0;
-      src[j] = nullptr;
-      if (e < total) {
-        const int t = e / per_tile;
-        const int g = e - t * per_tile;
-        const unsigned first_u = (unsigned)t * KB;
-        const unsigned o0 = owner_of(first_u, U, gemm_ctas);
-        const int ns = (int)(owner_of(first_u + KB - 1, U, gemm_ctas) - o0 + 1);
-        const int tb = t - (t / p.tilesB) * p.tilesB;
-        const int c = g / per_col;
-        // one CTA owned the whole tile and wrote y itself; padding columns
-        if (ns > 1 && c < min(bn, p.rowsB - tb * bn)) {
-          nseg[j] = ns;
-          src[j] = reinterpret_cast<const float4 *>(p.ws) + (size_t)t * p.seg_max * slot4 + g;
-        }
-      }
+      g[j] = c * chunk + j * kRedThreads + threadIdx.x;
+      const bool in = g[j] < per_tile && g[j] / per_col < valid_cols;
+      if (!in) g[j] = -1;
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        v[j][s] = s < nseg[j] ? __ldcg(src[j] + s * slot4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sg = 0; sg < 4; ++sg)
+        v[j][sg] = (in && sg < nseg) ? __ldcg(base + sg * slot4 + g[j]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int j = 0; j < kRedJ; ++j) {
-      if (nseg[j] == 0) continue;
+      if (g[j] < 0) continue;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        acc.x += v[j][s].x;
-        acc.y += v[j][s].y;
-        acc.z += v[j][s].z;
-        acc.w += v[j][s].w;
+      for (int sg = 0; sg < 4; ++sg) {
+        acc.x += v[j][sg].x;
+        acc.y += v[j][sg].y;
+        acc.z += v[j][sg].z;
+        acc.w += v[j][sg].w;
       }
-      for (int s = 4; s < nseg[j]; ++s) {
-        const float4 w = __ldcg(src[j] + s * slot4);
+      for (int sg = 4; sg < nseg; ++sg) {
+        const float4 w = __ldcg(base + sg * slot4 + g[j]);
         acc.x += w.x;
         acc.y += w.y;
         acc.z += w.z;
         acc.w += w.w;
       }
-      const int e = e0 + j * stride;
-      const int t = e / per_tile;
-      const int g = e - t * per_tile;
-      const int ta = t / p.tilesB, tb = t - ta * p.tilesB;
-      const int c = g / per_col, r = (g - c * per_col) * 4;
-      const int m = tb * bn + c;      // token
-      const int n = ta * kTileA + r;  // output channel
+      const int col = g[j] / per_col, r = (g[j] - col * per_col) * 4;
+      const int m = tb * bn + col;      // token
+      const int n = ta * kTileA + r;    // output channel
       float f[4] = {acc.x, acc.y, acc.z, acc.w};
       if (KIND == 1) {
         const float sa = p.tok_scale[m];
@@ -349,62 +267,6 @@ __device__ __forceinline__ void reduce_share(const GemmParams &p, int bn, unsign
         *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
             make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
     }
-  }
-}
-
-// Fused activation phase (A4W4 split-K): the M x K/128 units (one row, 128
-// values = 16 chunks of 8) are cut evenly over the CTAs; 128 threads = 8
-// half-warps take one unit each per round, two rounds' loads in flight.
-// Codes go to the token tiles (T = BN rows, 128-byte columns), scales to the
-// 128x4-tile layout; padding rows stay unwritten (their columns of the
-// accumulator are never stored).  Every lane of a warp runs every round:
-// the block amax is a 4-lane shuffle.
-__device__ __forceinline__ void quant_share(const GemmParams &p, int T, int tid) {
-  const int upr = p.K >> 7;
-  const long long W = (long long)p.M * upr;
-  const long long u0 = (long long)blockIdx.x * W / gridDim.x;
-  const long long u1 = (long long)(blockIdx.x + 1) * W / gridDim.x;
-  const int hw = tid >> 4, hl = tid & 15;
-  const int kc = p.K >> 8;  // 128-byte code columns per row
-  const int G = p.K >> 5;   // MX blocks per row
-  uint8_t *codes = const_cast<uint8_t *>(p.b_tiles);
-  uint8_t *sf = const_cast<uint8_t *>(p.sfB);
-  for (long long base = u0; base < u1; base += 16) {
-    uint4 v[2];
-    int r[2], ch[2];
-    bool ok[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const long long u = base + hw + 8 * j;
-      ok[j] = u < u1;
-      r[j] = ok[j] ? (int)(u / upr) : 0;
-      ch[j] = ok[j] ? (int)(u - (long long)r[j] * upr) * 16 + hl : 0;
-      v[j] = ok[j] ? ld_stream_v4(p.x + (size_t)r[j] * p.ldx + (size_t)ch[j] * 8)
-                   : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint32_t scode;
-      const uint32_t packed = mx_encode_chunk(v[j], scode);
-      if (ok[j]) *reinterpret_cast<uint32_t *>(codes + tiled_offset(r[j], ch[j] * 4, kc, T)) = packed;
-      const uint32_t word = mx_scale_word(scode);
-      if (ok[j] && hl == 0)
-        *reinterpret_cast<uint32_t *>(sf + sf_swizzled_offset(r[j], ch[j] >> 2, G)) = word;
-    }
-  }
-}
-
-// L2 prefetch of this CTA's share of x (contiguous runs within a row).
-__device__ __forceinline__ void prefetch_x_share(const GemmParams &p) {
-  const int upr = p.K >> 7;
-  const long long W = (long long)p.M * upr;
-  long long u = (long long)blockIdx.x * W / gridDim.x;
-  const long long u1 = (long long)(blockIdx.x + 1) * W / gridDim.x;
-  while (u < u1) {
-    const long long r = u / upr;
-    const long long hi = min(u1, (r + 1) * upr);
-    prefetch_l2_bulk(p.x + (size_t)r * p.ldx + (size_t)(u - r * upr) * 128, (uint32_t)(hi - u) * 256u);
-    u = hi;
   }
 }
 
@@ -429,45 +291,33 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   auto sfa_smem = [&](int st) { return sfb_smem(st) + C::kSfbBytes; };
   const uint32_t sEpi = sA + S * C::kStageBytes;
   const uint32_t bars = sEpi + C::kEpiBytes;
-  const uint32_t acc_full = bars + 8 * (2 * S);
-  const uint32_t acc_empty = acc_full + 8;
-  const uint32_t part_bar = acc_full + 16;
-  const uint32_t dec_bar = acc_full + 24;
-  const uint32_t stall_bar = acc_full + 32;
-  const uint32_t mma_done = acc_full + 40;
-  const uint32_t acts_ready = acc_full + 48;  // fused path: token tiles of every CTA written
-  const uint32_t sf_bars = acc_full + 56;     // full tile: a stage's scales are in TMEM
-  const uint32_t pull_bar = sf_bars + 8 * S;  // last-CTA split-K: the partial tiles are in smem
-  // CTA-pair split-K: rank 0's pair_bar completes once rank 1's partial tile
-  // is in rank 0's shared memory; rank 1's ready_bar once rank 0's pipeline
-  // shared memory is free to receive it
-  const uint32_t pair_bar = pull_bar + 8;
-  const uint32_t ready_bar = pull_bar + 16;
-  // FP8 full tile: two accumulators (TMEM columns [0, 256) and [256, 512)),
-  // so that the epilogue of one tile overlaps the MMAs of the next; A4W4
-  // needs TMEM columns for its scale factors and keeps one
-  constexpr int kAccBufs = (KIND == 1 && KS == 1) ? 2 : 1;
-  static_assert(kAccCol + kAccBufs * BN <= (KIND == 0 ? kSfCol : kTmemCols), "TMEM accumulators");
-  const uint32_t acc_full1 = pull_bar + 24;
-  const uint32_t acc_empty1 = pull_bar + 32;
-  auto accf = [&](int b) { return b ? acc_full1 : acc_full; };
-  auto acce = [&](int b) { return b ? acc_empty1 : acc_empty; };
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 12);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
-  volatile int *decision = reinterpret_cast<volatile int *>(misc + 8);
-  volatile int *reduce_go = reinterpret_cast<volatile int *>(misc + 12);
+  // mbarriers: per stage full / empty / scales in TMEM (A4W4), then per
+  // accumulator full / empty, the debug stall and the MMA drain
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
-  auto sf_ready = [&](int s) { return sf_bars + 8u * s; };
-  // Full-tile A4W4: the epilogue warps (idle during a tile's main loop) move
-  // each stage's scale factors into TMEM with tcgen05.st, off the tensor
-  // pipe; a tcgen05.cp there would hold up the MMAs behind it and, through
-  // them, the release of the stage.
+  auto sf_ready = [&](int s) { return bars + 8u * (2 * S + s); };
+  const uint32_t acc_bars = bars + 8u * (3 * S);
+  auto accf = [&](int b) { return acc_bars + 8u * (uint32_t)b; };
+  auto acce = [&](int b) { return acc_bars + 16u + 8u * (uint32_t)b; };
+  const uint32_t stall_bar = acc_bars + 32;
+  const uint32_t mma_done = acc_bars + 40;
+  constexpr int kAccBufs = C::kAccBufs;
+  static_assert(kAccCol + kAccBufs * BN <= (KIND == 0 ? kSfCol : kTmemCols), "TMEM accumulators");
+  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 6);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
+  // A4W4: the epilogue warps (idle during an item's main loop) move each
+  // stage's scale factors into TMEM with tcgen05.st, off the tensor pipe; a
+  // tcgen05.cp there would hold up the MMAs behind it in the in-order tensor
+  // pipe and, through them, the release of the stage.
   constexpr bool kEpiScales = KIND == 0;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The next kernel may launch now: it touches no memory this one writes or
+  // reads before its own griddepcontrol.wait, which returns only when this
+  // grid has completed.  Its CTAs take an SM as this kernel's leave it.
+  pdl_trigger();
   if (threadIdx.x == 0) {
     trace_mark(p, kTrEntry);
     trace_set(p, kTrEntryNs, global_timer_ns());
@@ -477,32 +327,19 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       trace_set(p, kTrSmid, smid);
     }
   }
-  // The next kernel may launch now: it touches no memory this one writes or
-  // reads before its own griddepcontrol.wait, which returns only when this
-  // grid has completed.  Its CTAs take an SM as this kernel's leave it.
-  pdl_trigger();
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
-    mbar_init(part_bar, 128);
-    mbar_init(dec_bar, 1);
+    for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf(b), 1);
+      mbar_init(acce(b), 4);
+    }
     mbar_init(stall_bar, 1);
     mbar_init(mma_done, 1);
-    mbar_init(acts_ready, 1);
-    for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
-    mbar_init(pull_bar, 1);
-    mbar_init(pair_bar, 128);
-    mbar_init(ready_bar, 1);
-    mbar_init(acc_full1, 1);
-    mbar_init(acc_empty1, 4);
     *abort_flag = 0;
-    *decision = 0;
-    *reduce_go = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -515,9 +352,6 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   }
   tc_fence_before();
   __syncthreads();
-  // the peer CTA arrives on this CTA's barriers later: their init must be
-  // visible across the cluster first
-  if (p.pair_reduce) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
@@ -720,16 +554,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         trace_set(p, kTrWaitedNs, global_timer_ns());
       }
       bool ok = true;
-      if (p.fuse_quant) {
-        // the token tiles are written by every CTA of this grid; the epilogue
-        // warps signal once the grid barrier after that phase has passed
-        ok = mbar_wait(acts_ready, 0, ctl) && !*abort_flag;
-        ok = __all_sync(0xFFFFFFFFu, ok);
-        fence_proxy_async_global();
-      }
-      // the rest of the first stages -- also when the fused phase failed:
-      // every armed stage must land before the CTA exits (contents are then
-      // irrelevant; every address stays in bounds)
+      // the rest of the first stages
       if (fast_first) {
         if (fc_bytes) bulk_load(fc_dst, fc_src, fc_bytes, fc_bar, p.swap ? polB : polA);
       }
@@ -874,66 +699,47 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r_in = q * 32 + lane;    // row of the MMA-A tile
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + kAccCol;
-    if (p.fuse_quant && threadIdx.x == 64) prefetch_x_share(p);  // L2 only: safe before the wait
-    pdl_wait();  // x, scales, counters and partial tiles may come from the previous kernel
-    if (p.fuse_quant) {
-      quant_share(p, BN, threadIdx.x - 64);
-      fence_proxy_async_global();  // these generic stores are read by other CTAs' bulk copies
-      named_barrier(1, 128);
-      if (threadIdx.x == 64) {
-        trace_mark(p, kTrQuantDone);
-        grid_barrier(p.gbar, p.gbar + 32, gridDim.x, ctl);  // raises the abort flag on failure
-        trace_mark(p, kTrPartStored);  // (fused path: the first grid barrier passed)
-        fence_proxy_async_global();
-        mbar_arrive(acts_ready);
-      }
-      __syncwarp();
-    }
-    uint32_t cur = first_cursor(p);
-    Item it;
-    int i = 0;
-    uint32_t part_phase = 0;
+    pdl_wait();  // scales and partial tiles may come from the kernel ahead
     long long q_sf = 0;  // stage sequence number (kEpiScales)
-    while (next_item(p, cur, it)) {
-      if (kEpiScales) {
-        // The item's stages in order: once the stage's data is in, its scale
-        // atoms go smem -> registers -> this warp's TMEM lane quarter, in the
-        // layout tcgen05.cp 32x128b.warpx4 makes (lane 32q+i, columns c..c+3
-        // = the atom's 16-byte row i, in every quarter q).
-        bool fed = true;
-        for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
-          const int st = (int)(q_sf % S);
-          if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) {
-            fed = false;
-            break;
-          }
-          if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
-          const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
-          const int rb0 = (it.tb * BN) / 128;
-          const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-          const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-          const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
-          const uint32_t sfb_col = sfa_col + C::kSfColsA;
+    // A4W4: the item's stages in order; once a stage's data is in, its scale
+    // atoms go smem -> registers -> this warp's TMEM lane quarter, in the
+    // layout tcgen05.cp 32x128b.warpx4 makes (lane 32q+i, columns c..c+3 =
+    // the atom's 16-byte row i, in every quarter q).
+    auto feed = [&](const Item &it) -> bool {
+      for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
+        const int st = (int)(q_sf % S);
+        if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) return false;
+        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
+        const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
+        const int rb0 = (it.tb * BN) / 128;
+        const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
+        const uint32_t sfb_col = sfa_col + C::kSfColsA;
+        for (int a = 0; a < natoms; ++a)
+          tmem_st4(sfa_col + 4 * a, ld_shared_v4(sfa_smem(st) + a * 512 + lane * 16));
+        for (int j = 0; j < nblk; ++j)
           for (int a = 0; a < natoms; ++a)
-            tmem_st4(sfa_col + 4 * a, ld_shared_v4(sfa_smem(st) + a * 512 + lane * 16));
-          for (int j = 0; j < nblk; ++j)
-            for (int a = 0; a < natoms; ++a)
-              tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
-                       ld_shared_v4(sfb_smem(st) + j * (1024 * KS) + a * 512 + lane * 16));
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(sf_ready(st));
-          if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
-        }
-        if (!fed) break;
+            tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
+                     ld_shared_v4(sfb_smem(st) + j * (1024 * KS) + a * 512 + lane * 16));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sf_ready(st));
+        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
       }
+      return true;
+    };
+    // Read out the accumulator of item i and store it: y (the item covers
+    // all of K) or this CTA's fp32 partial tile (part of K; the reduce
+    // kernel sums the partials).  Hands the accumulator back to the MMA warp.
+    auto finish = [&](const Item &it, int i) -> bool {
       if (p.debug_stall && i == 0) {
         // test hook: a barrier nothing arrives at; the bounded wait gives up
-        if (!warp_wait(stall_bar, 0, ctl)) break;
+        if (!warp_wait(stall_bar, 0, ctl)) return false;
       }
       const int acc_b = i % kAccBufs, acc_use = i / kAccBufs;
-      if (!warp_wait(accf(acc_b), (uint32_t)(acc_use & 1), ctl)) break;
+      if (!warp_wait(accf(acc_b), (uint32_t)(acc_use & 1), ctl)) return false;
       const uint32_t t_acc = t_row + (uint32_t)(acc_b * BN);  // this item's accumulator
       if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrAcc0 : kTrAcc1);
       tc_fence_after();
@@ -941,32 +747,6 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       const int cb0 = it.tb * BN;            // first MMA-B row of the tile
       const int ncols = min(BN, p.rowsB - cb0);
       const bool whole = (it.kb0 == 0 && it.kb1 == p.kblocks);
-      bool ok = true;
-      bool released = false;
-      // write this CTA's fp32 partial of the tile ([column][128 rows]) into
-      // its slot of the workspace; returns the tile's first slot
-      auto publish_partial = [&]() -> float * {
-        const size_t slot_elems = (size_t)BN * kTileA;
-        float *tile_ws = p.ws + (size_t)it.t * p.seg_max * slot_elems;
-        float *mine = tile_ws + (size_t)it.seg * slot_elems;
-#pragma unroll 1
-        for (int c = 0; c < BN / CH; ++c) {
-          uint32_t v[CH];
-          tmem_ld_chunk<CH>(t_acc + c * CH, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < CH; ++j)
-            if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
-        }
-        return tile_ws;
-      };
-      // hand the accumulator back to the MMA warp once its TMEM reads are done
-      auto release_acc = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acce(acc_b));
-        released = true;
-      };
       if (whole && !p.swap && KS == 1 && p.y_tma) {
         // rows = tokens, columns = output channels; per 32-column chunk the
         // warp's 32 x 32 bf16 box goes registers -> smem -> one TMA store
@@ -1063,187 +843,58 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             }
           }
         }
-      } else if (p.pair_reduce) {
-        // A CTA pair (one cluster) shares the tile: rank 0 holds the first
-        // part of K, rank 1 the rest.  Rank 1 pushes its fp32 partial into
-        // rank 0's pipeline shared memory (idle once rank 0's MMAs are done:
-        // each CTA of a pair has this one item); rank 0 adds it to its own,
-        // (partial 0 + partial 1, as the reduce kernel sums the slots) and
-        // writes y.  Row r's 16-byte chunk k sits at r * BN * 4 +
-        // ((k ^ (r % 8)) * 16), so that 8 consecutive rows cover all banks.
-        constexpr int kChunks = BN / 4;
-        constexpr int kSw = kChunks >= 8 ? 7 : kChunks - 1;
-        auto pofs = [&](int r, int k) -> uint32_t {
-          return (uint32_t)r * (uint32_t)(BN * 4) + (uint32_t)((k ^ (r & kSw)) << 4);
-        };
-        if (it.seg == 1) {
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(ready_bar, 0, ctl));
-          if (ok) {
-            const uint32_t dst = mapa_shared(sA, 0);
+      } else {
+        // swapped, part of K: this CTA's fp32 partial tile ([column][128
+        // rows]) into its slot of the workspace; the reduce kernel sums them
+        float *mine = p.ws + ((size_t)it.t * p.seg_max + (size_t)it.seg) * ((size_t)BN * kTileA);
 #pragma unroll 1
-            for (int c = 0; c < BN / CH; ++c) {
-              uint32_t v[CH];
-              tmem_ld_chunk<CH>(t_acc + c * CH, v);
-              tmem_ld_wait();
+        for (int c = 0; c < BN / CH; ++c) {
+          uint32_t v[CH];
+          tmem_ld_chunk<CH>(t_acc + c * CH, v);
+          tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < CH / 4; ++j)
-                st_cluster_v4(dst + pofs(r_in, c * (CH / 4) + j), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                              v[4 * j + 3]);
-            }
-          }
-          release_acc();
-          if (ok) mbar_arrive_remote(mapa_shared(pair_bar, 0));
-        } else {
-          if (threadIdx.x == 64) mbar_arrive_remote(mapa_shared(ready_bar, 1));
-          ok = __all_sync(0xFFFFFFFFu, mbar_wait_cluster(pair_bar, 0, ctl));
-          if (ok) {
-            const int n = ra;
-            const float sw = (KIND == 1 && n < p.N) ? p.chan_scale[n] : 1.0f;
-#pragma unroll 1
-            for (int c = 0; c < BN / CH; ++c) {
-              uint32_t v[CH];
-              tmem_ld_chunk<CH>(t_acc + c * CH, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < CH / 4; ++j) {
-                const uint4 u = ld_shared_v4(sA + pofs(r_in, c * (CH / 4) + j));
-                const uint32_t o[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int m = cb0 + c * CH + 4 * j + e;
-                  if (m < p.M && n < p.N) {
-                    float f = 0.0f;
-                    f += __uint_as_float(v[4 * j + e]);
-                    f += __uint_as_float(o[e]);
-                    if (KIND == 1) f = (f * p.tok_scale[m]) * sw;
-                    store_out(p, m, n, f);
-                  }
-                }
-              }
-            }
-          }
+          for (int j = 0; j < CH; ++j)
+            if (c * CH + j < ncols) mine[(size_t)(c * CH + j) * kTileA + r_in] = __uint_as_float(v[j]);
         }
-      } else if (p.defer_reduce || p.grid_reduce) {
-        // swapped, part of K: publish this CTA's fp32 partial tile into its
-        // slot; the split-K reduce kernel that follows (or every CTA of this
-        // grid, after a grid barrier) sums the slots
-        publish_partial();
-        release_acc();  // the MMA may start the next item during the hand-off
-        if (threadIdx.x == 64 && !p.fuse_quant && p.trace &&
+        if (threadIdx.x == 64 && p.trace &&
             p.trace[(size_t)blockIdx.x * kTracePoints + kTrPartStored] == 0)
           trace_mark(p, kTrPartStored);
-      } else if (!whole) {
-        // (in-kernel variant) the last CTA of the tile reduces the partials
-        const size_t slot_elems = (size_t)BN * kTileA;
-        float *tile_ws = publish_partial();
-        fence_proxy_async_global();  // the last CTA may read them with bulk copies
-        release_acc();
-        // the arrive (release, CTA scope) orders this thread's partial stores
-        // before the leader's acquire-release counter increment (GPU scope)
-        mbar_arrive(part_bar);
-        if (warp == 2 && lane == 0) {
-          const bool okp = mbar_wait(part_bar, part_phase, ctl);
-          int last = 0;
-          if (okp) {
-            // one acquire-release increment both publishes this CTA's partial
-            // (the part_bar arrivals order the other threads' stores before
-            // it) and, for the last arriver, makes the other partials visible
-            const unsigned old =
-                atom_add_acq_rel_gpu(reinterpret_cast<unsigned *>(p.counters) + it.t, 1u);
-            last = (old == (unsigned)(it.nseg - 1)) ? 1 : 0;
-            if (last) p.counters[it.t] = 0;  // every segment arrived: left zero for the next call
-          }
-          *decision = okp ? last : -1;
-          if (p.trace && p.trace[(size_t)blockIdx.x * kTracePoints + kTrDecision] == 0)
-            trace_mark(p, kTrDecision);
-          mbar_arrive(dec_bar);
-        }
-        ok = warp_wait(dec_bar, part_phase, ctl);
-        part_phase ^= 1u;
-        const int dec = ok ? *decision : -1;
-        if (dec < 0) {
-          ok = false;
-        } else if (dec == 1) {
-          // The tile's last item in this CTA's range and nothing after it: the
-          // pipeline's shared memory is idle (the MMAs behind acc_full have
-          // consumed every stage), so the partial slots come in by bulk copies,
-          // one lane per slot, and are summed from smem.
-          uint32_t cur2 = cur;
-          Item nxt;
-          const bool more = next_item(p, cur2, nxt);
-          const uint32_t slot_bytes = (uint32_t)(slot_elems * sizeof(float));
-          if (!more && (size_t)it.nseg * slot_bytes <= (size_t)S * C::kStageBytes) {
-            if (warp == 2) {
-              fence_proxy_async_global();  // the slots were stored by other CTAs' generic stores
-              if (lane == 0) mbar_arrive_expect_tx(pull_bar, (uint32_t)it.nseg * slot_bytes);
-              __syncwarp();
-              if (lane < it.nseg)
-                bulk_load(sA + (uint32_t)lane * slot_bytes,
-                          reinterpret_cast<const uint8_t *>(tile_ws + (size_t)lane * slot_elems), slot_bytes,
-                          pull_bar, policy_evict_first());
-            }
-            ok = warp_wait(pull_bar, 0, ctl);
-            if (ok) {
-              const int tid = threadIdx.x - 64;
-              const int ngrp = ncols * (kTileA / 4);
-              const int row0 = it.ta * kTileA;
-              for (int g = tid; g < ngrp; g += 128) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int sgi = 0; sgi < it.nseg; ++sgi) {
-                  const uint32_t a = sA + (uint32_t)sgi * slot_bytes + (uint32_t)g * 16u;
-                  const uint4 u = ld_shared_v4(a);
-                  acc.x += __uint_as_float(u.x);
-                  acc.y += __uint_as_float(u.y);
-                  acc.z += __uint_as_float(u.z);
-                  acc.w += __uint_as_float(u.w);
-                }
-                const int c = g / (kTileA / 4);
-                const int r = (g % (kTileA / 4)) * 4;
-                const int m = cb0 + c;    // token
-                const int n = row0 + r;   // output channel
-                float f[4] = {acc.x, acc.y, acc.z, acc.w};
-                if (KIND == 1) {
-                  const float sa = p.tok_scale[m];
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) f[j] = (f[j] * sa) * p.chan_scale[n + j];
-                }
-                if (p.out_f32)
-                  *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + (size_t)m * p.ldy + n) =
-                      make_float4(f[0], f[1], f[2], f[3]);
-                else
-                  *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(p.y) + (size_t)m * p.ldy + n) =
-                      make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-              }
-            }
-          } else {
-            reduce_partials<KIND>(p, tile_ws, slot_elems, it.nseg, ncols, it.ta * kTileA, cb0,
-                                  threadIdx.x - 64);
-          }
-          if (threadIdx.x == 64) trace_mark(p, kTrReduced);
-        }
       }
-      if (!released) release_acc();
+      // hand the accumulator back to the MMA warp once its TMEM reads are done
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce(acc_b));
       if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrItem0Done : kTrItem1Done);
-      if (!ok) break;
-      ++i;
+      return true;
+    };
+    // Feed ahead: with two accumulators, the scales of item i+1 go into TMEM
+    // before item i is read out, so that the MMAs of item i+1 run while the
+    // epilogue stores item i.
+    uint32_t cur = first_cursor(p);
+    Item it, held;  // held: fed, not yet finished (two accumulators only)
+    bool holding = false;
+    int i_fin = 0;
+    bool ok = true;
+    while (ok && next_item(p, cur, it)) {
+      if (kEpiScales && !feed(it)) {
+        ok = false;
+        break;
+      }
+      if (kAccBufs == 1) {
+        ok = finish(it, i_fin++);
+      } else if (holding) {
+        ok = finish(held, i_fin++);
+        held = it;
+      } else {
+        held = it;
+        holding = true;
+      }
     }
+    if (ok && holding) ok = finish(held, i_fin++);
     if (KS == 1 && p.y_tma && lane == 0) bulk_wait_group_all();  // y stores complete
     if (threadIdx.x == 64) {
       trace_mark(p, kTrEpiDone);
-      trace_set(p, kTrItems, (unsigned long long)i);
-    }
-    if (p.grid_reduce) {
-      // every CTA's partial slots are stored: sum a share of all of them
-      named_barrier(1, 128);
-      if (threadIdx.x == 64) {
-        *reduce_go = (!*abort_flag && grid_barrier(p.gbar + 64, p.gbar + 96, gridDim.x, ctl)) ? 1 : 0;
-        trace_mark(p, kTrDecision);
-      }
-      named_barrier(1, 128);
-      if (*reduce_go) {
-        reduce_share<KIND>(p, BN, gridDim.x, blockIdx.x * 128 + (threadIdx.x - 64), gridDim.x * 128);
-        if (threadIdx.x == 64) trace_mark(p, kTrReduced);
-      }
+      trace_set(p, kTrItems, (unsigned long long)i_fin);
     }
   }
 
@@ -1261,13 +912,13 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 
 // The split-K reduction as its own kernel, launched right after the GEMM.
 template <int KIND>
-__global__ void __maxnreg__(48)  // 128-thread CTAs, 3 of them beside a GEMM CTA and a quantizer CTA
+__global__ void __maxnreg__(64)  // 128-thread CTAs, 3 of them beside a GEMM CTA and a quantizer CTA
     splitk_reduce_kernel(const GemmParams p, int bn, unsigned gemm_ctas) {
   pdl_trigger();  // touches nothing before the wait below
   if (p.trace && threadIdx.x == 0)
     atomicMax(p.trace + kTrRedEntryInv, ~(unsigned long long)global_timer_ns());
   pdl_wait();     // the GEMM that wrote the partial slots has completed
-  reduce_share<KIND>(p, bn, gemm_ctas, blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x);
+  reduce_items<KIND>(p, bn, gemm_ctas);
   if (p.trace) {  // (uniform over the grid)
     __syncthreads();
     if (threadIdx.x == 0) atomicMax(p.trace + kTrRedExitNs, (unsigned long long)global_timer_ns());
@@ -1289,29 +940,8 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUten
     once.set(dev);
   }
   cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
-  if (p.pair_reduce) {
-    // CTA pairs (2j, 2j + 1) share a tile and exchange partials through
-    // distributed shared memory
-    if (ctas % 2 != 0) return cudaErrorInvalidValue;
-    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-    attr[cfg.numAttrs].val.clusterDim.x = 2;
-    attr[cfg.numAttrs].val.clusterDim.y = 1;
-    attr[cfg.numAttrs].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs += 1;
-  }
-  if (p.fuse_quant || p.grid_reduce) {
-    // grid barriers: every CTA must be resident at once, also when other
-    // streams run kernels of their own (a cooperative launch guarantees it)
-    if (cooperative_enabled()) {
-      attr[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
-      attr[cfg.numAttrs].val.cooperative = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs += 1;
-    }
-  }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
 }
 
@@ -1431,11 +1061,13 @@ cudaError_t launch_mma_peak(int kind, int bn, int iters, int sm_count, int *stat
 
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream) {
-  const long long total = (long long)p.tilesA * p.tilesB * bn * (kTileA / 4);
-  long long blocks = (total + kRedThreads * kRedJ - 1) / (kRedThreads * kRedJ);
+  const int per_tile = bn * (kTileA / 4);
+  const long long chunks = (per_tile + kRedThreads * kRedJ - 1) / (kRedThreads * kRedJ);
+  long long blocks = (long long)p.tilesA * p.tilesB * chunks;
   // Launched early (programmatic launch), the reduce CTAs sit beside the
-  // GEMM CTAs of a layer chain: 3 per SM at most (48 registers a thread),
-  // so that a GEMM CTA (26K registers) and a quantizer CTA still fit.
+  // GEMM CTAs: 3 per SM at most (64 registers a thread, 8K a CTA), so that
+  // the next GEMM CTA (at most 26K registers) and a quantizer CTA (10K)
+  // still fit on the SM.
   const long long cap = (long long)(sm_count > 0 ? sm_count : 152) * 3;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;

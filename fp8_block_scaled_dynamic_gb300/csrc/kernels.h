@@ -115,8 +115,7 @@ struct GemmParams {
   int G4;              // K / 128: 512-byte scale tiles per 128-row block
   int splitk;          // 1: stream-K over (tile, K-block) units
   long long units;     // tilesA * tilesB * kblocks
-  float *ws;           // split-K partial tiles
-  int *counters;       // split-K arrival counters, one per tile
+  float *ws;           // split-K partial tiles: [tile][slot][BN columns][128 rows] fp32
   int seg_max;         // partial slots per tile
   int *status;         // optional device status word
   unsigned long long timeout_ns;
@@ -130,23 +129,9 @@ struct GemmParams {
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int raster_group;        // full tile: 0 = tiles in row order (token tile slowest), else
                            //   bands of this many token tiles, the token tile fastest
-  int defer_reduce;        // split-K: partial tiles are summed by launch_splitk_reduce, not by
-                           //          the last CTA of each tile
-  int pair_reduce;         // split-K over CTA pairs (2-CTA clusters, grid = 2 x tiles): rank 1
-                           //          pushes its partial into rank 0's shared memory
   int early_w;         // 1: no kernel still in flight writes the weights, so their first
                        //    stages may load before griddepcontrol.wait
-  // Single-kernel split-K (swap) path: the CTAs first quantize the bf16
-  // activations x into the token tiles (b_tiles, T = BN rows) and their
-  // 128x4-tile scales (sfB), then a grid barrier, then the GEMM; partial
-  // tiles are summed after a second grid barrier by all CTAs (grid_reduce).
   int y_tma;           // full tile, bf16 out: the epilogue stores y through tensor map tmY
-  const uint16_t *x;
-  long long ldx;
-  int fuse_quant;
-  int grid_reduce;
-  unsigned *gbar;      // grid barrier words: [0] / [32] count / generation of barrier 1,
-                       //   [64] / [96] of barrier 2 (zero-initialised, 128 bytes apart)
 };
 
 // Timeline trace points (index into a CTA's kTracePoints slots): SM clock64
@@ -157,20 +142,20 @@ struct GemmParams {
 enum TracePoint {
   kTrEntry = 0, kTrSetup = 1, kTrFirstLoad = 2, kTrLastLoad = 3, kTrFirstFull = 4,
   kTrLastCommit = 5, kTrAcc0 = 6, kTrItem0Done = 7, kTrAcc1 = 8, kTrItem1Done = 9,
-  kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12, kTrDecision = 13, kTrReduced = 14,
-  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18, kTrQuantDone = 19,
+  kTrEpiDone = 10, kTrExit = 11, kTrPartStored = 12,  // 13, 14: unused
+  kTrItems = 15, kTrEntryNs = 16, kTrExitNs = 17, kTrWaited = 18,  // 19: unused
   kTrWaitedNs = 20, kTrSmid = 21, kTrRedEntryInv = 22, kTrRedExitNs = 23,
   // A4W4, per pipeline stage k < 8 of the CTA's sequence, seen by the first
   // epilogue warp: the stage's data landed / its scales are in TMEM
   kTrStageLanded = 24, kTrStageFed = 32,
-  kTracePoints = 40  // fused path: kTrDecision = second grid barrier passed
+  kTracePoints = 40
 };
 
 // kind 0 = A4W4 (kind::mxf4), 1 = PTPC (kind::f8f6f4); bn = MMA-B tile rows.
 cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                         const CUtensorMap &tmY, const GemmParams &p, int ctas, cudaStream_t stream);
 
-// Split-K reduction of a GEMM launched with p.defer_reduce = 1 (the same
+// Split-K reduction of a GEMM whose tiles have several partials (the same
 // params, its grid size gemm_ctas); launched right after it on the stream.
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream);

@@ -19,8 +19,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -72,116 +70,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
       return false;
     }
   }
-}
-
-// ---------------------------------------------------------------- grid barrier
-// ---- thread-block clusters: a CTA pair exchanging a partial tile through
-// distributed shared memory
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The shared::cluster address of this CTA's shared address saddr in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(caddr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-// Arrive on an mbarrier of a CTA of this cluster; release at cluster scope:
-// this thread's earlier stores (shared::cluster ones included) are visible
-// to a thread that sees the phase complete with an acquire.cluster wait.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-// (test_wait, which never suspends the thread: a phase completed by another
-// CTA's arrive need not wake a thread suspended in try_wait)
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// mbar_wait whose completion also acquires stores released at cluster scope.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*ctl.abort_flag) return false;
-    if (global_timer_ns() - t0 > ctl.timeout_ns) {
-      *ctl.abort_flag = 1;
-      if (ctl.status) atomicOr(ctl.status, 0x1 /* MXG_DEV_TIMEOUT */);
-      return false;
-    }
-  }
-}
-// Every thread of both CTAs of the cluster; used once after barrier init
-// (the CTAs of a cluster are launched together, so this wait is short).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Orders this thread's generic-proxy global accesses with its async-proxy
-// (bulk copy / TMA) ones: the writer side and the reader side of data that
-// one CTA stores with st.global and another loads with cp.async.bulk.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Barrier of all G CTAs of a launch, taken by one thread per CTA once the
-// CTA's own writes are ordered before it (bar.sync among the writers).
-// `cnt` and `gen` are zero-initialised words of the caller's workspace;
-// completed barriers leave `cnt` at zero, `gen` only ever advances.  Every
-// CTA must be resident at the same time (the persistent grid is at most one
-// CTA per SM); the wait is bounded like every other one.
-__device__ __forceinline__ bool grid_barrier(unsigned *cnt, unsigned *gen, unsigned G,
-                                             const WaitCtl &ctl) {
-  // The generation cannot move before this CTA has arrived.
-  const unsigned g0 = ld_acquire_gpu(gen);
-  __threadfence();
-  const unsigned old = atomicAdd(cnt, 1u);
-  if (old == G - 1) {  // last to arrive: reset the count, open the barrier
-    atomicExch(cnt, 0u);
-    __threadfence();
-    atomicAdd(gen, 1u);
-    return true;
-  }
-  const uint64_t t0 = global_timer_ns();
-  while (ld_acquire_gpu(gen) == g0) {
-    __nanosleep(32);  // fewer polls of the line the arrivals update
-    if (*ctl.abort_flag) return false;
-    if (global_timer_ns() - t0 > ctl.timeout_ns) {
-      *ctl.abort_flag = 1;
-      if (ctl.status) atomicOr(ctl.status, 0x1 /* MXG_DEV_TIMEOUT */);
-      return false;
-    }
-  }
-  return true;
-}
-
-// Named barrier among `n` threads (whole warps) of the CTA; id 0 is __syncthreads.
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA
@@ -404,21 +292,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
-}
-
-// Atomic add with acquire-release semantics at GPU scope: publishes every
-// write ordered before it (cumulatively, including the writes of other
-// threads synchronised with this one) and orders the reads after it.
-__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ float ld_cg_f32(const float *p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
 }
 
 }  // namespace mxg

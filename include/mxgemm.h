@@ -126,10 +126,9 @@ typedef struct {
     int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over; 0 or more
                              than the SM count = the SM count (one persistent CTA per SM) */
     void *workspace;      /* device scratch of >= mxg_gemm_workspace_bytes() bytes,
-                             256-byte aligned.  Its first 64 KiB hold split-K arrival
-                             counters: zero them before the first call; every completed
-                             call leaves them zero again (after MXG_ERR_TIMEOUT, zero them
-                             again).  Calls that overlap on the GPU need separate
+                             256-byte aligned: the fused path's quantized activations, then
+                             the split-K partial tiles.  Its contents on entry do not
+                             matter.  Calls that overlap on the GPU need separate
                              workspaces.  NULL only when the call needs none. */
     size_t ws_bytes;      /* size of workspace */
     int *dev_status;      /* optional device int; kernels OR MXG_DEV_* bits into it */
@@ -156,41 +155,26 @@ typedef struct {
     void *trace;          /* optional device buffer of ctas x 40 uint64, zero-filled: each
                              CTA records SM clock64 stamps of its timeline (entry, setup,
                              first/last load, first stage ready, last MMA commit, epilogue
-                             items, split-K hand-off, exit; slot 15 = items; slots 16/17 =
-                             global timer ns at entry/exit; slot 18 = the producer's
-                             dependency wait returned, slot 20 = the same in global timer
-                             ns; fused path: slot 19 = activation share quantized, slot 12
-                             = first and slot 13 = second grid barrier passed).  Slots 22
+                             items, split-K partial stored, exit; slot 15 = items; slots
+                             16/17 = global timer ns at entry/exit; slot 18 = the
+                             producer's dependency wait returned, slot 20 = the same in
+                             global timer ns).  Slots 22
                              and 23 of CTA 0's row: the split-K reduce kernel of the same
                              call, ~(first entry ns) and last exit ns.  Slot 21: the SM.
                              A4W4, slots 24+k / 32+k: the CTA's k-th pipeline stage
                              (k < 8) landed in shared memory / its scales are in TMEM.
                              NULL = off. */
-    int splitk_reduce;    /* how SPLITK partial tiles are summed when the activations come
-                             pre-quantized: MXG_REDUCE_DEFAULT (= MXG_REDUCE_KERNEL),
-                             MXG_REDUCE_KERNEL (a reduce kernel launched right after the
-                             GEMM), MXG_REDUCE_GRID (every CTA of the GEMM, after a grid
-                             barrier: one launch; the grid is launched cooperatively),
-                             MXG_REDUCE_LAST_CTA (the last CTA to finish each tile),
-                             MXG_REDUCE_PAIR (when 2 x tiles <= SM count: two CTAs per
-                             tile, launched as a 2-CTA cluster, each taking half of K; the
-                             second pushes its partial into the first one's shared memory,
-                             which adds it and writes y -- no workspace partials and no
-                             second kernel; otherwise as MXG_REDUCE_KERNEL).  On
-                             the fused A4W4 path (x given, K % 256 == 0) MXG_REDUCE_GRID
-                             runs everything as one cooperative kernel: quantize, grid
-                             barrier, GEMM, grid barrier, reduce; otherwise the fused path
-                             is the quantizer kernel, the GEMM and the reduce kernel,
-                             chained by programmatic dependent launch (faster on GB300:
-                             a grid barrier costs more than a kernel boundary). */
+    int splitk_reduce;    /* MXG_REDUCE_DEFAULT or MXG_REDUCE_KERNEL (the same): SPLITK
+                             partial tiles are summed, in slot order, by a reduce kernel
+                             launched right after the GEMM.  Any other value is
+                             MXG_ERR_INVALID_ARG.  On the fused A4W4 path (x given) the
+                             call launches the activation quantizer, the GEMM and the
+                             reduce kernel, chained by programmatic dependent launch. */
 } mxg_gemm_opts;
 
 enum {
     MXG_REDUCE_DEFAULT = 0,
-    MXG_REDUCE_KERNEL = 1,
-    MXG_REDUCE_GRID = 2,
-    MXG_REDUCE_LAST_CTA = 3,
-    MXG_REDUCE_PAIR = 4
+    MXG_REDUCE_KERNEL = 1
 };
 
 typedef struct {
@@ -202,8 +186,8 @@ typedef struct {
                           for A4W4, 128 K for PTPC), one per stage for FULL, two for
                           SPLITK */
     int seg_max;       /* SPLITK: most CTAs contributing to one tile */
-    size_t ws_bytes;   /* workspace this plan needs */
-    int pair;          /* SPLITK: 1 = CTA pairs (MXG_REDUCE_PAIR), ctas = 2 x tiles */
+    size_t ws_bytes;   /* workspace this plan needs (partial tiles) */
+    int reserved;      /* always 0 */
 } mxg_plan;
 
 /* Bytes of a scale-factor array for `rows` rows of K elements (K/32 groups).
@@ -357,11 +341,11 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
  *     before any stream capture.
  *   - Shapes whose scratch would exceed the array (see
  *     mxg_gemm_workspace_bytes) return MXG_ERR_WORKSPACE before any launch.
- *   - Each call clears the array's arrival counters (a 64 KiB memset on
- *     `stream`), then runs the GEMM.  All calls share the one array, which
- *     keeps the last call's contents: calls that overlap on the GPU (other
- *     streams, other threads) race on it and must be serialised by the
- *     caller.
+ *   - Every byte of the array a call reads, that call has written first, so
+ *     nothing needs clearing between calls.  All calls share the one array,
+ *     which keeps the last call's contents: calls that overlap on the GPU
+ *     (other streams, other threads) race on it and must be serialised by
+ *     the caller.
  *   - Every operand is checked before the scratch is touched: a call that
  *     returns an error has written nothing.
  *   - It has no device status word: a bounded device wait that runs out

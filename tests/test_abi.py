@@ -172,19 +172,16 @@ def test_plan_errors():
         mx.mxg_plan_gemm(2, 8, 7168, 8192, 152)  # kind
 
 
-@pytest.mark.parametrize("kind,M,N,K,sm", [(0, 64, 7168, 8192, 152), (0, 8, 7168, 8192, 148),
-                                          (1, 64, 7168, 18432, 152), (1, 64, 36864, 7168, 152),
-                                          (0, 200, 1024, 1024, 16)])
-def test_plan_pair(kind, M, N, K, sm):
-    """CTA pairs: two CTAs per tile when 2 x tiles fits the SMs, else the stream-K plan."""
-    p = mx.mxg_plan_gemm(kind, M, N, K, sm, variant="splitk", splitk_reduce="pair")
-    base = mx.mxg_plan_gemm(kind, M, N, K, sm, variant="splitk", splitk_reduce="kernel")
-    assert p["tiles"] == base["tiles"] and p["bn"] == base["bn"] and p["kblocks"] == base["kblocks"]
-    if 2 * base["tiles"] <= sm:
-        assert (p["pair"], p["ctas"], p["seg_max"], p["ws_bytes"]) == (1, 2 * base["tiles"], 2, 0)
-    else:
-        assert p["pair"] == 0 and p["ctas"] == base["ctas"] and p["ws_bytes"] == base["ws_bytes"]
-    assert base["pair"] == 0
+def test_only_the_reduce_kernel_is_a_split_k_reduction():
+    """The split-K partials are summed by the reduce kernel; other values of
+    splitk_reduce are refused before anything is launched."""
+    L = mx.lib()
+    o = mx.GemmOpts()
+    for v in (2, 3, 4, -1):
+        o.splitk_reduce = v
+        assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, 0, ctypes.byref(o), None) == 1
+    p = mx.mxg_plan_gemm(0, 64, 7168, 8192, 152, variant="splitk")
+    assert p["reserved"] == 0 and p["ws_bytes"] == p["tiles"] * p["seg_max"] * p["bn"] * 128 * 4
 
 
 @pytest.mark.parametrize("kind,M,N,K,want", [

@@ -15,11 +15,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("kind,variant,reduce", [(0, "full", "default"), (0, "splitk", "default"),
-                                                 (1, "splitk", "default"), (1, "full", "default"),
-                                                 (0, "splitk", "pair"), (1, "splitk", "pair")])
+                                                 (1, "splitk", "default"), (1, "full", "default")])
 def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
-    """Also for the 2-CTA-cluster split-K (pair): every CTA of the pair gives
-    up before any exchange with its partner starts."""
     d = dev()
     M, N, K = 16, 512, 1024
     x = synth.activation(M, K, seed=50)
@@ -44,7 +41,6 @@ def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
     run(dev_status=status, timeout_ms=20, debug_stall=1)
     assert mx.mxg_query_status(status) == 6  # MXG_ERR_TIMEOUT
     assert int(status.item()) == 0           # cleared by the query
-    ws.zero_()                               # a timed-out call may leave counters behind
     y = run(dev_status=status)
     assert mx.mxg_query_status(status) == 0
     assert_gemm_close(y.cpu().numpy(), ref, bound, "after timeout")

@@ -90,19 +90,20 @@ def test_ptpc_panel_weights_bit_identical(M, N, K, variant):
     assert (y0.view(np.uint32) == y1.view(np.uint32)).all()
 
 
-@pytest.mark.parametrize("reduce", ["kernel", "grid", "lastcta"])
-def test_a4w4_panel_splitk_reduce_modes(reduce):
+@pytest.mark.parametrize("ctas", [0, 3])
+def test_a4w4_panel_splitk_fused(ctas):
     """The split-K path takes one 128-row half of a panel as its weight tile;
-    every reduction mode, the one-kernel fused form (grid) included."""
+    on the fused path (x quantized inside the call) panels and weight tiles
+    give the same bits."""
     d = dev()
     M, N, K = 64, 1536, 4096
     x = synth.activation(M, K, seed=91).to(d)
     w = synth.weight(N, K, seed=92).to(d)
     wt, wtsf = mx.mx_quantize_weight(w, layout=mx.TILED)
     wp, _ = mx.mx_quantize_weight(w, layout=mx.PANEL)
-    y0 = mx.mx_gemm_a4w4(wt, wtsf, x=x, out_f32=True, weights_tiled=mx.W_TILED, splitk_reduce=reduce)
-    y1 = mx.mx_gemm_a4w4(wp, None, x=x, out_f32=True, weights_tiled=mx.W_PANEL, n=N, k=K,
-                         splitk_reduce=reduce)
+    y0 = mx.mx_gemm_a4w4(wt, wtsf, x=x, out_f32=True, weights_tiled=mx.W_TILED, variant="splitk", ctas=ctas)
+    y1 = mx.mx_gemm_a4w4(wp, None, x=x, out_f32=True, weights_tiled=mx.W_PANEL, n=N, k=K, variant="splitk",
+                         ctas=ctas)
     assert (y0.cpu().numpy().view(np.uint32) == y1.cpu().numpy().view(np.uint32)).all()
 
 
