@@ -32,6 +32,8 @@ test_oracle_quant.py, test_oracle_gemm.py, test_oracle_mutants.py):
                              = g, saturation silu(g) = g for large g)
   swiglu_rows             -- pinned (gate/up order and bf16 rounding against
                              closed forms and torch's bf16 cast)
+  gemm_a4w4_grouped       -- pinned (one-hot rows that only their own expert
+                             can light, empty groups, one group = gemm_a4w4)
   sf_swizzle              -- bijection only; its placement is pinned on the
                              GPU by one-hot GEMMs (not from the pages)
 """
@@ -278,6 +280,31 @@ def gemm_ptpc(qa, sa, qw, sw, rows=None):
                         _ptr(qw, ctypes.c_uint8), _ptr(sw, ctypes.c_float),
                         M, N, K, None if idx is None else _ptr(idx, ctypes.c_int),
                         nrows, _ptr(ref, ctypes.c_double), _ptr(bound, ctypes.c_double))
+    return ref, bound
+
+
+def gemm_a4w4_grouped(a_codes, a_sf, w_codes, w_sf, row_off):
+    """Grouped (MoE) A4W4: the token rows arrive grouped by expert (rows
+    row_off[e] .. row_off[e+1]-1 were routed to expert e; a group may be
+    empty), and each group goes through its own expert's MXFP4 weight:
+    y[rows of e] = x[rows of e] . W_e^T ("Kimi-K3-Quark-MXFP4-AttnFP8", "Model
+    Overview": the experts are OCP MXFP4).  w_codes / w_sf: one (N, K/2) /
+    (N, K/32) array per expert.  Returns (ref, bound) (M, N) float64.  The
+    routing and the token permutation that produce the grouping are a
+    dispatch step of their own, not part of the GEMM."""
+    a_codes = np.ascontiguousarray(a_codes, np.uint8)
+    a_sf = np.ascontiguousarray(a_sf, np.uint8)
+    off = [int(v) for v in row_off]
+    E = len(off) - 1
+    assert len(w_codes) == E and len(w_sf) == E and off[0] == 0 and off[-1] == a_codes.shape[0]
+    assert all(off[e] <= off[e + 1] for e in range(E))
+    N = np.asarray(w_codes[0]).shape[0]
+    ref = np.zeros((a_codes.shape[0], N), np.float64)
+    bound = np.zeros((a_codes.shape[0], N), np.float64)
+    for e in range(E):
+        r0, r1 = off[e], off[e + 1]
+        if r1 > r0:
+            ref[r0:r1], bound[r0:r1] = gemm_a4w4(a_codes[r0:r1], a_sf[r0:r1], w_codes[e], w_sf[e])
     return ref, bound
 
 
