@@ -57,7 +57,7 @@ NOMINAL_HBM_GBS = 7900.0               # GB300 HBM3e, nominal
 DATASHEET_TFLOPS = {0: 13500.0, 1: 4500.0}  # GB300 dense FP4 / FP8 tensor, nominal
 TRACE_POINTS = 40                      # uint64 trace slots per CTA (include/mxgemm.h)
 GEMM_REL_TOL = 1e-5                    # |y - ref| <= 1e-5 * sum_k |a_k w_k| before the bf16 cast
-EXTRA_WORKLOADS = ("oproj_prefill", "oproj_m8", "mlp_fp8_m64", "mlp_fp8_m8192")
+EXTRA_WORKLOADS = ("oproj_prefill", "oproj_m8", "mlp_fp8_m64", "mlp_fp8_m8192", "moe_grouped")
 
 
 def flush_l2(buf: torch.Tensor):
@@ -498,12 +498,77 @@ class MlpFp8(Workload):
         self.e2e_pipelined(parts)
 
 
+class MoeGrouped(Workload):
+    """Grouped (MoE) A4W4: 8 synthetic experts of gate_up shape (N = 2 x 2048,
+    K = 7168), 8192 routed token rows in seeded uneven groups; one call
+    quantizes the grouped activations and runs the grouped GEMM."""
+
+    def __init__(self, mx, synth, dev, name, key="", out_f32=False):
+        self.init_common(dev)
+        self.mx, self.name, self.key, self.out_f32 = mx, name, key, out_f32
+        self.kind = 0
+        E, N, K, M = synth.MOE_EXPERTS, synth.MOE_N, synth.MOE_K, synth.MOE_ROWS
+        self.E, self.N, self.K, self.M = E, N, K, M
+        self.sizes = synth.group_sizes(M, E, synth.SEED_MOE_ROUTE)
+        off = [0]
+        for c in self.sizes:
+            off.append(off[-1] + c)
+        self.row_off_host = off
+        self.row_off = torch.tensor(off, dtype=torch.int32, device=dev)
+        self.panels = torch.cat([mx.mx_quantize_weight(synth.weight(N, K, seed=synth.SEED_MOE_W + e).to(dev),
+                                                       layout=mx.PANEL)[0] for e in range(E)])
+        self.x_host = synth.activation(M, K, seed=synth.act_seed(5, 0, 0)).pin_memory()
+        self.x = self.x_host.to(dev)
+        ydt = torch.float32 if out_f32 else torch.bfloat16
+        self.y = torch.empty(M, N, dtype=ydt, device=dev)
+        self.y_host = torch.empty(M, N, dtype=ydt).pin_memory()
+        self.ws = torch.zeros(mx.mxg_grouped_workspace_bytes(M, K, E), dtype=torch.uint8, device=dev)
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        tiles = (-(-M // 128) + E) * (N // 256)
+        self.plan = {"variant": 1, "bn": 256, "ctas": min(tiles, sm), "seg_max": 1, "tiles": tiles}
+        self.timed_label = "a4w4_grouped"
+        wbytes = E * (N * K // 2 + N * K // 32)
+        self.kernel_bytes = wbytes + M * K // 2 + M * K // 32 + 2 * M * N
+        self.kernel_flops = 2 * M * N * K
+        self.bytes_per_step = wbytes + 2 * M * K + 2 * M * N
+        self.flops_per_step = 2 * M * N * K
+        self.dtype = "e2m1 x e2m1 -> f32 (bf16 out)"
+        self.bound = "tensor"
+        self.kernel_desc = (f"gemm_kernel<A4W4, BN=256> grouped full tile, {E} experts, {self.plan['ctas']} CTAs "
+                            f"(grouped activation quantizer ahead of it, same call)")
+        self.h2d = 2 * M * K
+        self.d2h = M * N * ydt.itemsize
+
+    def gemm_plans(self):
+        return [("a4w4_grouped", self.plan)]
+
+    def kernels_per_step(self):
+        return 2  # grouped quantizer + grouped GEMM
+
+    def launches(self):
+        mx = self.mx
+        return [("a4w4_grouped", lambda: mx.mx_gemm_a4w4_grouped(
+            self.x, self.row_off, self.panels, n=self.N, out=self.y, out_f32=self.out_f32, ws=self.ws,
+            dev_status=self.status, weights_static=True, trace=self.tr("a4w4_grouped")))]
+
+    def outputs(self):
+        return {"y": self.y}
+
+    def e2e_step(self):
+        mx = self.mx
+        self.e2e_pipelined([([(self.x, self.x_host)], lambda: mx.mx_gemm_a4w4_grouped(
+            self.x, self.row_off, self.panels, n=self.N, out=self.y, out_f32=self.out_f32, ws=self.ws,
+            dev_status=self.status, weights_static=True), [(self.y_host, self.y)])])
+
+
 WORKLOAD_NAMES = {
     "oproj_decode": "A4W4 o_proj decode chain: M=64 (conc 8 x 8 tokens), N=7168, K=8192, 5 layers",
     "oproj_m8": "A4W4 o_proj single layer: M=8 (1 verified + 7 drafted), N=7168, K=8192",
     "oproj_prefill": "A4W4 o_proj prefill: M=8192 (8 x 1024 tokens), N=7168, K=8192",
     "mlp_fp8_m64": "FP8 PTPC MLP chain: M=64, quant, gate_up 7168->36864, SwiGLU+quant, down 18432->7168",
     "mlp_fp8_m8192": "FP8 PTPC MLP chain: M=8192, quant, gate_up 7168->36864, SwiGLU+quant, down 18432->7168",
+    "moe_grouped": "grouped (MoE) A4W4: 8 experts of gate_up 7168->4096, 8192 routed token rows in seeded "
+                   "uneven groups",
 }
 
 
@@ -519,6 +584,8 @@ def make_workload(key, mx, synth, dev, out_f32=False):
     if key in ("mlp_fp8_m64", "mlp_fp8_m8192"):
         M = 64 if key.endswith("m64") else 8192
         return MlpFp8(mx, synth, dev, M, name=name, key=key, out_f32=out_f32)
+    if key == "moe_grouped":
+        return MoeGrouped(mx, synth, dev, name=name, key=key, out_f32=out_f32)
     raise SystemExit(f"unknown workload {key}")
 
 
@@ -926,7 +993,10 @@ def _oracle_weights(workload):
         return _ORACLE_CACHE[workload]
     import oracle
     import synth
-    if workload.startswith("oproj"):
+    if workload == "moe_grouped":
+        w = [oracle.mx_quantize_rows(synth.weight(synth.MOE_N, synth.MOE_K, seed=synth.SEED_MOE_W + e))
+             for e in range(synth.MOE_EXPERTS)]
+    elif workload.startswith("oproj"):
         M, layers, cfg, seeds, rs = oproj_spec(workload)
         w = [oracle.mx_quantize_rows(synth.weight(synth.OPROJ_N, synth.OPROJ_K, seed=s)) for s in seeds]
     else:
@@ -941,7 +1011,9 @@ def _activations(workload):
     if key in _ORACLE_CACHE:
         return _ORACLE_CACHE[key]
     import synth
-    if workload.startswith("oproj"):
+    if workload == "moe_grouped":
+        xs = synth.activation(synth.MOE_ROWS, synth.MOE_K, seed=synth.act_seed(5, 0, 0))
+    elif workload.startswith("oproj"):
         M, layers, cfg, seeds, rs = oproj_spec(workload)
         xs = [synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(cfg, l, 0), row_scale=rs)
               for l in range(layers)]
@@ -953,6 +1025,9 @@ def _activations(workload):
 
 
 def workload_rows(workload):
+    if workload == "moe_grouped":
+        import synth
+        return synth.MOE_ROWS
     if workload.startswith("oproj"):
         return oproj_spec(workload)[0]
     return 64 if workload.endswith("m64") else 8192
@@ -979,7 +1054,20 @@ def oracle_step(workload: str, rows: np.ndarray):
     refs = []
     idx = torch.from_numpy(rows)
     t = time.perf_counter()
-    if workload.startswith("oproj"):
+    if workload == "moe_grouped":
+        # each sampled row through the weight of the expert whose group holds it
+        import synth
+        sizes = synth.group_sizes(synth.MOE_ROWS, synth.MOE_EXPERTS, synth.SEED_MOE_ROUTE)
+        off = np.concatenate([[0], np.cumsum(sizes)])
+        expert = np.searchsorted(off, rows, side="right") - 1
+        ref = np.zeros((len(rows), synth.MOE_N))
+        bound = np.zeros_like(ref)
+        for e in np.unique(expert):
+            sel = np.nonzero(expert == e)[0]
+            ac, asf = oracle.mx_quantize_rows(xs[torch.from_numpy(rows[sel])].contiguous())
+            ref[sel], bound[sel] = oracle.gemm_a4w4(ac, asf, w[e][0], w[e][1])
+        refs.append(("y", None, ref, bound, "gemm"))
+    elif workload.startswith("oproj"):
         for l, x in enumerate(xs):
             ac, asf = oracle.mx_quantize_rows(x[idx].contiguous())
             refs.append(("y", l, *oracle.gemm_a4w4(ac, asf, w[l][0], w[l][1]), "gemm"))
@@ -1052,6 +1140,10 @@ def step_bytes(workload: str):
         return a4w4_fused_bytes(8, N, K)
     if workload == "oproj_prefill":
         return a4w4_fused_bytes(8192, N, K)
+    if workload == "moe_grouped":
+        import synth
+        E, Nm, Km, M = synth.MOE_EXPERTS, synth.MOE_N, synth.MOE_K, synth.MOE_ROWS
+        return E * (Nm * Km // 2 + Nm * Km // 32) + 2 * M * Km + 2 * M * Nm
     M = 64 if workload.endswith("m64") else 8192
     return mlp_chain_bytes(M, 7168, 18432)
 
@@ -1268,7 +1360,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="oproj_decode",
                     choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192",
-                             "sweep"])
+                             "moe_grouped", "sweep"])
     ap.add_argument("--weights", default="panel", choices=["panel", "tiled"],
                     help="resident weight layout: 256-row panels (scales inside) or 128-row tiles")
     ap.add_argument("--no-extras", dest="extras", action="store_false",

@@ -107,6 +107,11 @@ def lib() -> ctypes.CDLL:
             L.fp8_gemm_ptpc.argtypes = [vp, vp, vp, vp, i, i, i, vp, i, i,
                                         ctypes.POINTER(GemmOpts), vp]
             L.fp8_gemm_ptpc.restype = i
+            L.mxg_grouped_workspace_bytes.argtypes = [i, i, i]
+            L.mxg_grouped_workspace_bytes.restype = sz
+            L.mx_gemm_a4w4_grouped.argtypes = [vp, i, vp, i, vp, i, i, i, vp, i, i,
+                                               ctypes.POINTER(GemmOpts), vp]
+            L.mx_gemm_a4w4_grouped.restype = i
             L.mxg_mma_peak.argtypes = [i, i, i, ctypes.POINTER(ctypes.c_double), vp]
             L.mxg_mma_peak.restype = i
             L.mxg_query_status.argtypes = [vp, vp]
@@ -390,6 +395,33 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
               weights_tiled, act_tile_rows, splitk_reduce)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
+        OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
+    return out
+
+
+def mxg_grouped_workspace_bytes(M_total: int, K: int, E: int) -> int:
+    return int(lib().mxg_grouped_workspace_bytes(M_total, K, E))
+
+
+def mx_gemm_a4w4_grouped(x: torch.Tensor, row_off: torch.Tensor, w_panels: torch.Tensor, *, n: int,
+                         out=None, out_f32: bool = False, ws=None, dev_status=None, timeout_ms: int = 0,
+                         weights_static: bool = False, trace=None, stream=None):
+    """Grouped (MoE) A4W4: x (M_total, K) bf16 with the tokens sorted by
+    expert, row_off (E + 1,) int32 on the device (expert e owns rows
+    row_off[e] .. row_off[e+1]-1), w_panels flat: E panel sets of
+    mxg_weight_bytes(KIND_A4W4, n, K, PANEL) bytes each.  Returns y (M_total, n)."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1,
+          "x must be a CUDA bf16 (M, K) tensor with unit inner stride")
+    _need(row_off.is_cuda and row_off.dtype == torch.int32 and row_off.dim() == 1 and row_off.is_contiguous(),
+          "row_off must be a contiguous CUDA int32 vector")
+    M, K = x.shape
+    E = row_off.numel() - 1
+    out = _out(out, M, n, out_f32, x.device)
+    if ws is None:
+        ws = workspace(mxg_grouped_workspace_bytes(M, K, E), x.device)
+    o = _opts("auto", 0, ws, dev_status, timeout_ms, 0, weights_static, trace)
+    _check("mx_gemm_a4w4_grouped", lib().mx_gemm_a4w4_grouped(
+        _ptr(x), x.stride(0), _ptr(row_off), E, _ptr(w_panels), M, n, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
     return out
 

@@ -535,6 +535,106 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
                   sm, s);
 }
 
+namespace {
+// Grouped A4W4: a bound on the 128-row token tiles when each of E groups
+// starts a new tile, and the workspace layout [tile offsets][codes][scales].
+long long grouped_tiles(int M_total, int E) { return (long long)(M_total + 127) / 128 + E; }
+struct GroupedWs {
+  size_t tile_off, codes, sf, total;
+};
+GroupedWs grouped_ws(int M_total, int K, int E) {
+  GroupedWs w;
+  const size_t rows = (size_t)grouped_tiles(M_total, E) * 128;
+  w.tile_off = 0;
+  w.codes = align256((size_t)(E + 1) * sizeof(int));
+  w.sf = w.codes + align256(rows * (size_t)K / 2);
+  w.total = w.sf + align256(rows * (size_t)K / 32);
+  return w;
+}
+}  // namespace
+
+size_t mxg_grouped_workspace_bytes(int M_total, int K, int E) {
+  if (M_total < 0 || K < 256 || E < 1 || E > mxg::kMaxGroups) return 0;
+  return grouped_ws(M_total, K, E).total;
+}
+
+mxg_status mx_gemm_a4w4_grouped(const void *x_bf16, int ldx, const int *row_off, int E,
+                                const uint8_t *w_panels, int M_total, int N, int K, void *y, int ldy,
+                                mxg_out_dtype out_dtype, const mxg_gemm_opts *opts, mxg_stream_t stream) {
+  // with no token routed, x and y may be empty (null) tensors
+  if ((M_total > 0 && (!x_bf16 || !y)) || !row_off || !w_panels || E < 1 || E > mxg::kMaxGroups ||
+      M_total < 0 || N < 1 || K < 1 || ldx < K || ldy < N)
+    return MXG_ERR_INVALID_ARG;
+  if (out_dtype != MXG_OUT_BF16 && out_dtype != MXG_OUT_F32) return MXG_ERR_INVALID_ARG;
+  if (opts && ((opts->variant != MXG_VARIANT_AUTO && opts->variant != MXG_VARIANT_FULL) ||
+               (opts->weights_tiled != 0 && opts->weights_tiled != 2) || opts->act_tile_rows != 0 ||
+               (opts->splitk_reduce != MXG_REDUCE_DEFAULT && opts->splitk_reduce != MXG_REDUCE_KERNEL)))
+    return MXG_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
+  if ((x_bf16 && !aligned16(x_bf16)) || (ldx % 8) != 0 || !aligned16(w_panels) || (y && !aligned16(y)) ||
+      ((size_t)ldy * (out_dtype == MXG_OUT_F32 ? 4 : 2)) % 16 != 0 || (reinterpret_cast<uintptr_t>(row_off) & 3u))
+    return MXG_ERR_MISALIGNED;
+  const GroupedWs wl = grouped_ws(M_total, K, E);
+  uint8_t *ws = opts ? static_cast<uint8_t *>(opts->workspace) : nullptr;
+  if (!ws || opts->ws_bytes < wl.total) return MXG_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXG_ERR_MISALIGNED;
+  const long long TA = grouped_tiles(M_total, E);
+  const long long tilesB = (N + 255) / 256;
+  if (TA * tilesB >= (1LL << 31)) return MXG_ERR_UNSUPPORTED_SHAPE;
+  int sm = 0;
+  mxg_status st = check_device(&sm);
+  if (st != MXG_OK) return st;
+  if (M_total == 0) return MXG_OK;  // no token was routed: nothing to compute
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int *tile_off = reinterpret_cast<int *>(ws + wl.tile_off);
+  uint8_t *codes = ws + wl.codes, *sf = ws + wl.sf;
+  cudaError_t e = mxg::launch_mx_quant_grouped(x_bf16, ldx, M_total, K, row_off, E, tile_off, codes, sf, sm, s);
+  if (e != cudaSuccess) return MXG_ERR_CUDA;
+
+  const uint64_t row_bytes = (uint64_t)K / 2;
+  CUtensorMap tmA, tmB, tmY;
+  std::memset(&tmY, 0, sizeof(tmY));
+  if ((st = make_operand_map(&tmA, codes, row_bytes, (uint64_t)TA * 128, 128)) != MXG_OK) return st;
+  if ((st = make_operand_map(&tmB, w_panels, row_bytes, (uint64_t)N, 256)) != MXG_OK) return st;
+  mxg::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.sfA = sf;
+  p.y = y;
+  p.ldy = ldy;
+  p.out_f32 = out_dtype == MXG_OUT_F32 ? 1 : 0;
+  p.M = M_total;
+  p.N = N;
+  p.K = K;
+  p.swap = 0;
+  p.rowsA = (int)(TA * 128);
+  p.rowsB = N;
+  p.tilesA = (int)TA;
+  p.tilesB = (int)tilesB;
+  p.kblocks = K / 256;  // one 128-byte code column (256 values) per stage
+  p.G4 = K / 128;
+  p.splitk = 0;
+  p.units = TA * tilesB * p.kblocks;
+  p.seg_max = 1;
+  p.status = opts->dev_status;
+  const uint32_t tmo = opts->timeout_ms ? opts->timeout_ms : 1000u;
+  p.timeout_ns = (unsigned long long)tmo * 1000000ull;
+  p.debug_stall = opts->debug_stall;
+  p.early_w = opts->weights_static ? 1 : 0;
+  p.trace = static_cast<unsigned long long *>(opts->trace);
+  p.a_tiles = codes;
+  p.b_tiles = w_panels;
+  p.b_tile_rows = mxg::kPanelRows;
+  p.w_panels = 1;
+  p.kc_per_row = (int)(row_bytes / 128);
+  p.groups = E;
+  p.g_tile_off = tile_off;
+  p.g_row_off = row_off;
+  p.w_group_bytes = mxg_weight_bytes(0, N, K, MXG_PANEL);
+  const long long ctas = std::min<long long>(TA * tilesB, sm);
+  e = mxg::launch_gemm(0, mxg::kPanelRows, tmA, tmB, tmY, p, (int)ctas, s);
+  return e == cudaSuccess ? MXG_OK : MXG_ERR_CUDA;
+}
+
 mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw, const float *sw,
                          int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
                          const mxg_gemm_opts *opts, mxg_stream_t stream) {

@@ -86,7 +86,22 @@ struct Cfg {
 
 struct Item {
   int t, ta, tb, kb0, kb1, seg, nseg;
+  // grouped GEMM: the expert of token tile ta, its first token tile, its
+  // first token row and its number of token rows
+  int e, tile0, row0, rows;
 };
+
+// Grouped GEMM: the expert whose token tiles include global token tile ta
+// (the largest e with tile_off[e] <= ta), by binary search over E + 1 offsets.
+__device__ __forceinline__ int group_of_tile(const int *tile_off, int E, int ta) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(tile_off + mid) <= ta) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
 
 // CTA that owns stream-K unit u when U units are cut into G equal ranges
 // [c*U/G, (c+1)*U/G): the largest c with c*U < (u+1)*G.  The host checks
@@ -103,6 +118,30 @@ __device__ __forceinline__ uint32_t first_cursor(const GemmParams &p) {
 // The work items of this CTA, in order; every role walks the same list.
 __device__ __forceinline__ bool next_item(const GemmParams &p, uint32_t &cur, Item &it) {
   const uint32_t G = gridDim.x;
+  it.e = 0;
+  if (p.groups) {
+    // grouped (full tile): item i = (weight tile i / tilesA, token tile i %
+    // tilesA), token tiles fastest so that the CTAs running at one time
+    // share a weight tile of one expert; tilesA is the host's bound on the
+    // token tiles, the items past the groups' last tile are skipped
+    const int valid = __ldg(p.g_tile_off + p.groups);
+    const uint32_t total = (uint32_t)(p.tilesA * p.tilesB);
+    while (cur < total && (int)(cur % (uint32_t)p.tilesA) >= valid) cur += G;
+    if (cur >= total) return false;
+    it.t = (int)cur;
+    it.ta = (int)(cur % (uint32_t)p.tilesA);
+    it.tb = (int)(cur / (uint32_t)p.tilesA);
+    it.kb0 = 0;
+    it.kb1 = p.kblocks;
+    it.seg = 0;
+    it.nseg = 1;
+    cur += G;
+    it.e = group_of_tile(p.g_tile_off, p.groups, it.ta);
+    it.tile0 = __ldg(p.g_tile_off + it.e);
+    it.row0 = __ldg(p.g_row_off + it.e);
+    it.rows = __ldg(p.g_row_off + it.e + 1) - it.row0;
+    return true;
+  }
   if (!p.splitk) {
     if (cur >= (uint32_t)(p.tilesA * p.tilesB)) return false;
     it.t = (int)cur;
@@ -442,7 +481,8 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (want_b && b_pan) {  // BN == 256, one column per stage
           if (i == 0)
             bulk_load(b_smem(stage),
-                      p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes,
+                      p.b_tiles + (size_t)it.e * p.w_group_bytes +
+                          ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes,
                       (uint32_t)C::kPanelBytes, fb, polB);
         } else if (want_b) {
           const bool tok = p.b_tiles && p.b_tile_rows == BN;
@@ -488,6 +528,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         }
         return false;
       };
+      // A grouped GEMM's tiles follow the token-tile offsets the quantizer
+      // ahead of it writes: walk them only after the wait.
+      if (p.groups) pdl_wait();
       // The first S stages (fewer if the CTA has fewer): weights that no
       // kernel still in flight writes stream in before griddepcontrol.wait;
       // the activation operand follows the wait.
@@ -785,9 +828,18 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           }
         }
       } else if (whole && !p.swap) {
-        // rows = tokens, columns = output channels: each thread writes a row run
-        const bool mvalid = ra < p.M;
-        const float sa = (KIND == 1 && mvalid) ? p.tok_scale[ra] : 1.0f;
+        // rows = tokens, columns = output channels: each thread writes a row
+        // run (grouped: the tile's rows are the expert's rows from
+        // (ta - tile0) * 128 on, stored at row0 + that, rows past the
+        // expert's last token skipped)
+        int yr = ra;
+        bool mvalid = ra < p.M;
+        if (p.groups) {
+          const int lr = (it.ta - it.tile0) * kTileA + r_in;
+          yr = it.row0 + lr;
+          mvalid = lr < it.rows;
+        }
+        const float sa = (KIND == 1 && mvalid) ? p.tok_scale[yr] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < BN / CH; ++c) {
           uint32_t v[CH];
@@ -804,13 +856,13 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           if (n0 + CH <= p.N) {
             if (p.out_f32) {
               float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) +
-                                                       (size_t)ra * p.ldy + n0);
+                                                       (size_t)yr * p.ldy + n0);
 #pragma unroll
               for (int j = 0; j < CH / 4; ++j)
                 dst[j] = make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
             } else {
               uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) +
-                                                     (size_t)ra * p.ldy + n0);
+                                                     (size_t)yr * p.ldy + n0);
 #pragma unroll
               for (int j = 0; j < CH / 8; ++j)
                 dst[j] = make_uint4(pack_bf16x2(f[8 * j], f[8 * j + 1]),
@@ -821,7 +873,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           } else {
 #pragma unroll
             for (int j = 0; j < CH; ++j)
-              if (n0 + j < p.N) store_out(p, ra, n0 + j, f[j]);
+              if (n0 + j < p.N) store_out(p, yr, n0 + j, f[j]);
           }
         }
       } else if (whole) {

@@ -132,6 +132,15 @@ struct GemmParams {
   int early_w;         // 1: no kernel still in flight writes the weights, so their first
                        //    stages may load before griddepcontrol.wait
   int y_tma;           // full tile, bf16 out: the epilogue stores y through tensor map tmY
+  // Grouped (MoE) full tile, A4W4: groups = number of experts E (0 = a plain
+  // GEMM).  The MMA-A operand is token tiles (a_tiles) in which each
+  // expert's rows start a new 128-row tile; g_tile_off / g_row_off (device,
+  // E + 1 each) give each expert's first token tile and first token row
+  // (y row); the MMA-B operand is E weight panel sets, w_group_bytes apart.
+  int groups;
+  const int *g_tile_off;
+  const int *g_row_off;
+  size_t w_group_bytes;
 };
 
 // Timeline trace points (index into a CTA's kTracePoints slots): SM clock64
@@ -159,6 +168,16 @@ cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensor
 // params, its grid size gemm_ctas); launched right after it on the stream.
 cudaError_t launch_splitk_reduce(int kind, int bn, const GemmParams &p, int gemm_ctas,
                                  int sm_count, cudaStream_t stream);
+
+// Grouped MXFP4 activation quantizer: x (M_total rows sorted by expert,
+// row_off: E + 1 device offsets) -> codes in 128-row token tiles where each
+// expert's rows start a new tile, scales in the 128x4 layout over those
+// padded rows; every CTA forms the tile offsets from row_off, and the first
+// one also writes them to tile_off (E + 1 ints) for the GEMM.
+cudaError_t launch_mx_quant_grouped(const void *x, long long ldx, int M_total, int K, const int *row_off,
+                                    int E, int *tile_off, uint8_t *codes, uint8_t *sf, int sm_count,
+                                    cudaStream_t stream);
+constexpr int kMaxGroups = 1024;
 
 // The tensor-pipe rate probe behind mxg_mma_peak: sm_count CTAs, one per SM.
 cudaError_t launch_mma_peak(int kind, int bn, int iters, int sm_count, int *status,

@@ -126,6 +126,67 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   }
 }
 
+// Grouped activations (MoE experts): the rows of x arrive sorted by expert,
+// expert e owning rows row_off[e] .. row_off[e+1]-1.  Each expert's rows
+// start a new 128-row token tile: compact row r of expert e goes to padded
+// row 128 tile_off[e] + (r - row_off[e]), tile_off the running sum of
+// ceil(rows_e / 128).  Every CTA forms tile_off in shared memory; the first
+// also writes it out for the GEMM.  Codes go to 128-row token tiles, scales
+// to the 128x4 layout over the padded rows; the padding rows of an expert's
+// last tile are left unwritten (they only feed output rows that are never
+// stored).  A half-warp covers 16 chunks (4 blocks) of one row, as in
+// mx_quant_kernel.
+__global__ void __launch_bounds__(kMxThreads) mx_quant_grouped_kernel(const uint16_t *__restrict__ x,
+                                                                      long long ldx, int M_total, int K,
+                                                                      const int *__restrict__ row_off,
+                                                                      int E, int *__restrict__ tile_off_out,
+                                                                      uint8_t *__restrict__ codes,
+                                                                      uint8_t *__restrict__ sf) {
+  __shared__ int s_row[kMaxGroups + 1];
+  __shared__ int s_tile[kMaxGroups + 1];
+  const int lane = threadIdx.x & 31;
+  pdl_trigger();  // an activation step: the next kernel may launch now
+  pdl_wait();     // x and row_off may come from the kernel ahead
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_row[e] = row_off[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_tile[e] = acc;
+      acc += (s_row[e + 1] - s_row[e] + 127) >> 7;
+    }
+    s_tile[E] = acc;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) tile_off_out[e] = s_tile[e];
+  const int cpr = K >> 3;  // 16-byte chunks per row, a multiple of 16
+  const int G = K >> 5;
+  const int KC = K >> 8;   // 128-byte code columns per row
+  for (int r = blockIdx.x; r < M_total; r += gridDim.x) {
+    int lo = 0, hi = E - 1;  // the expert of row r: the largest e with row_off[e] <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_row[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int pr = (s_tile[lo] << 7) + (r - s_row[lo]);  // padded row
+    for (int c0 = 0; c0 < cpr; c0 += kMxThreads) {
+      const int c = c0 + (int)threadIdx.x;
+      const bool in_row = c < cpr;  // uniform over a half-warp (cpr % 16 == 0)
+      const uint4 v = in_row ? ld_stream_v4(x + (size_t)r * ldx + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t scode;
+      const uint32_t packed = mx_encode_chunk(v, scode);
+      const uint32_t word = mx_scale_word(scode);
+      if (in_row) {
+        *reinterpret_cast<uint32_t *>(codes + tiled_offset(pr, c * 4, KC, 128)) = packed;
+        if ((lane & 15) == 0)
+          *reinterpret_cast<uint32_t *>(sf + sf_swizzled_offset(pr, c >> 2, G)) = word;
+      }
+    }
+  }
+}
+
 constexpr int kF8Threads = 256;
 
 // Read-only 16-byte load that stays in L1: the second pass over a row finds it there.
@@ -395,6 +456,21 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows,
                             rows_iter, K, tile_rows, act ? 1 : 0, q, scale);
+}
+
+cudaError_t launch_mx_quant_grouped(const void *x, long long ldx, int M_total, int K, const int *row_off,
+                                    int E, int *tile_off, uint8_t *codes, uint8_t *sf, int sm_count,
+                                    cudaStream_t stream) {
+  int g = M_total < 1 ? 1 : M_total;
+  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
+  if (g > cap) g = cap;
+  cudaError_t e = prefer_shared_carveout(mx_quant_grouped_kernel);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kMxThreads), 0, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
+  return cudaLaunchKernelEx(&cfg, mx_quant_grouped_kernel, static_cast<const uint16_t *>(x), ldx, M_total, K,
+                            row_off, E, tile_off, codes, sf);
 }
 
 cudaError_t launch_swiglu_fp8(const void *gu, long long ldgu, int rows, int I, int tile_rows, void *h_out,

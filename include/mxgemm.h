@@ -321,6 +321,38 @@ mxg_status fp8_gemm_ptpc(const uint8_t *qa, const float *sa,
                          int M, int N, int K, void *y, int ldy, mxg_out_dtype out_dtype,
                          const mxg_gemm_opts *opts, mxg_stream_t stream);
 
+/* Grouped (MoE) A4W4 GEMM for the experts of a mixture-of-experts layer
+ * (page "Kimi-K3-Quark-MXFP4-AttnFP8", section "Model Overview": the experts
+ * are OCP MXFP4): the token rows arrive grouped by expert, and each group goes
+ * through its own expert's MXFP4 weight,
+ *   y[row_off[e] + i][n] = sum_k x_q[row_off[e] + i][k] * W_e_q[n][k]
+ * for i < row_off[e+1] - row_off[e], with x quantized inside the call (dynamic
+ * MXFP4, codes and scales as mx_quantize_act) and fp32 accumulation.  The
+ * routing and the token permutation that produce the grouping are not part of
+ * this call.
+ *   x_bf16:   (M_total, K) bf16, the tokens sorted by expert, leading dimension
+ *             ldx elements.
+ *   row_off:  DEVICE array of E + 1 ints: expert e owns rows row_off[e] ..
+ *             row_off[e+1] - 1; row_off[0] = 0, row_off[E] = M_total, non-
+ *             decreasing (empty groups allowed).  1 <= E <= 1024.
+ *   w_panels: E weight panel sets (MXG_PANEL, as mx_quantize_weight writes),
+ *             expert e at byte e * mxg_weight_bytes(0, N, K, MXG_PANEL).
+ *   y:        (M_total, N) bf16 or fp32, leading dimension ldy, rows in x's
+ *             order.
+ *   opts:     required; workspace of >= mxg_grouped_workspace_bytes(M_total, K,
+ *             E) bytes (256-byte aligned; its contents on entry do not matter);
+ *             variant AUTO or FULL (the full-tile kernel: 128-token x 256-
+ *             channel tiles, each expert's tokens starting a new tile);
+ *             dev_status, timeout_ms, weights_static and trace as for
+ *             mx_gemm_a4w4.
+ *   K % 256 == 0, N % 128 == 0.  M_total == 0 launches nothing (x and y may
+ *   then be NULL). */
+size_t mxg_grouped_workspace_bytes(int M_total, int K, int E);
+mxg_status mx_gemm_a4w4_grouped(const void *x_bf16, int ldx, const int *row_off, int E,
+                                const uint8_t *w_panels, int M_total, int N, int K,
+                                void *y, int ldy, mxg_out_dtype out_dtype,
+                                const mxg_gemm_opts *opts, mxg_stream_t stream);
+
 /* Size of the library-owned scratch array used by mx_gemm_a4w4_noalloc. */
 #define MXG_NOALLOC_SCRATCH_BYTES (16u << 20)
 

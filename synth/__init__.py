@@ -78,6 +78,24 @@ def seed_cfg4(kind: str, layer: int) -> int:
     return {"o_proj": 20, "gate_up": 30, "down": 40}[kind] + layer
 
 
+# Synthetic expert layer (the pages give no expert shapes): gate_up of a
+# 2048-wide expert over the 7168-wide hidden state, 8 experts, 8192 routed
+# token rows (e.g. 1024 tokens x top-8), seed 60 + e for expert e's weight.
+MOE_EXPERTS, MOE_N, MOE_K, MOE_ROWS = 8, 4096, 7168, 8192
+SEED_MOE_W, SEED_MOE_ROUTE = 60, 61
+
+
+def group_sizes(rows: int, groups: int, seed: int) -> list:
+    """Uneven seeded group sizes summing to `rows`: each row goes to a group
+    drawn from a seeded Dirichlet(3)-weighted categorical distribution."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    # Dirichlet(3) weights from the generator: normalised sums of 3 exponentials
+    e = -torch.log(torch.rand(groups, 3, generator=g, dtype=torch.float64)).sum(dim=1)
+    p = e / e.sum()
+    pick = torch.multinomial(p, rows, replacement=True, generator=g)
+    return torch.bincount(pick, minlength=groups).tolist()
+
+
 def special_values_bf16() -> torch.Tensor:
     """A row of edge-case bf16 bit patterns for quantizer edge tests: +-0,
     the smallest/largest subnormals and normals, the E2M1 rounding midpoints

@@ -214,3 +214,22 @@ def test_dispatcher_rule(kind, M, N, K, want):
 ])
 def test_swiglu_argument_errors_before_launch(args, want):
     assert mx.lib().swiglu_fp8_quantize(*args, None) == want
+
+
+def test_grouped_argument_errors_before_launch():
+    L = mx.lib()
+    o = mx.GemmOpts()
+    f = L.mx_gemm_a4w4_grouped
+    # x, ldx, row_off, E, w, M, N, K, y, ldy, dtype, opts, stream
+    assert f(None, 512, FAKE, 4, FAKE, 64, 256, 512, FAKE, 256, 0, ctypes.byref(o), None) == 1  # no x
+    assert f(FAKE, 512, FAKE, 0, FAKE, 64, 256, 512, FAKE, 256, 0, ctypes.byref(o), None) == 1  # E = 0
+    assert f(FAKE, 256, FAKE, 4, FAKE, 64, 256, 512, FAKE, 256, 0, ctypes.byref(o), None) == 1  # ldx < K
+    assert f(FAKE, 384, FAKE, 4, FAKE, 64, 256, 384, FAKE, 256, 0, ctypes.byref(o), None) == 2  # K % 256
+    assert f(FAKE, 512, FAKE, 4, FAKE, 64, 200, 512, FAKE, 256, 0, ctypes.byref(o), None) == 2  # N % 128
+    assert f(FAKE, 512, FAKE, 4, FAKE, 64, 256, 512, FAKE, 256, 0, ctypes.byref(o), None) == 7  # no workspace
+    assert f(FAKE, 512, FAKE, 4, FAKE, 64, 256, 512, FAKE, 256, 0, None, None) == 7
+    o.variant = 2  # split-K is not a grouped variant
+    assert f(FAKE, 512, FAKE, 4, FAKE, 64, 256, 512, FAKE, 256, 0, ctypes.byref(o), None) == 1
+    # workspace: token tiles for ceil(M / 128) + E tiles, plus the tile offsets
+    assert mx.mxg_grouped_workspace_bytes(300, 1024, 4) >= (3 + 4) * 128 * (1024 // 2 + 1024 // 32)
+    assert mx.mxg_grouped_workspace_bytes(300, 1024, 0) == 0

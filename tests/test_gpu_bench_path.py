@@ -74,7 +74,8 @@ def run_graph(key, out_f32):
     return a
 
 
-@pytest.mark.parametrize("key", ["oproj_decode", "oproj_m8", "mlp_fp8_m64", "oproj_prefill", "mlp_fp8_m8192"])
+@pytest.mark.parametrize("key", ["oproj_decode", "oproj_m8", "mlp_fp8_m64", "oproj_prefill", "mlp_fp8_m8192",
+                                 "moe_grouped"])
 def test_benched_step_graph_matches_oracle(key):
     """Every output of the benched step against the oracle's version of the
     same step.  The FP8 MLP is the chain quantize -> gate_up -> SwiGLU +
