@@ -57,7 +57,8 @@ NOMINAL_HBM_GBS = 7900.0               # GB300 HBM3e, nominal
 DATASHEET_TFLOPS = {0: 13500.0, 1: 4500.0}  # GB300 dense FP4 / FP8 tensor, nominal
 TRACE_POINTS = 40                      # uint64 trace slots per CTA (include/mxgemm.h)
 GEMM_REL_TOL = 1e-5                    # |y - ref| <= 1e-5 * sum_k |a_k w_k| before the bf16 cast
-EXTRA_WORKLOADS = ("oproj_prefill", "oproj_m8", "mlp_fp8_m64", "mlp_fp8_m8192", "moe_grouped")
+EXTRA_WORKLOADS = ("oproj_prefill", "oproj_m8", "mlp_fp8_m64", "mlp_fp8_m8192", "moe_grouped", "mla_fp8_m64",
+                   "mla_fp8_m8192", "draft_m64")
 
 
 def flush_l2(buf: torch.Tensor):
@@ -498,6 +499,175 @@ class MlpFp8(Workload):
         self.e2e_pipelined(parts)
 
 
+class DraftLayers(Workload):
+    """The GEMM path of the mixed-precision draft layer, five layers chained in
+    one graph: per layer the A4W4 o_proj (dynamic MXFP4 quantization of the
+    attention output, 8192 -> 7168), then the FP8 PTPC MLP on the o_proj
+    output (per-token quantization, gate_up 7168 -> 2 x 18432, SwiGLU fused
+    with the quantization of its output, down 18432 -> 7168).  The attention
+    output of every layer is a seeded input (attention is not on the path);
+    the MLP consumes the o_proj output as it is (the residual add and norm
+    between them are not on the path either)."""
+
+    def __init__(self, mx, synth, dev, M, layers, name, key="", out_f32=False):
+        self.init_common(dev)
+        self.mx, self.M, self.n_layers, self.name, self.key = mx, M, layers, name, key
+        self.out_f32 = out_f32
+        self.kind = 1
+        H, I, KO = 7168, synth.MLP_I, synth.OPROJ_K
+        self.H, self.I, self.KO = H, I, KO
+        layout, self.wt = weight_layout(mx)
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.plan_o = mx.mxg_plan_gemm(mx.KIND_A4W4, M, H, KO, sm)
+        self.plan_g = mx.mxg_plan_gemm(mx.KIND_PTPC, M, 2 * I, H, sm)
+        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, I, sm)
+        self.plan = self.plan_g
+        self.To, self.Tg, self.Td = act_tile_rows(self.plan_o), act_tile_rows(self.plan_g), act_tile_rows(self.plan_d)
+        ydt = torch.float32 if out_f32 else torch.bfloat16
+        self.L = []
+        for l in range(layers):
+            wo, wos = mx.mx_quantize_weight(synth.weight(H, KO, seed=synth.seed_cfg4("o_proj", l)).to(dev),
+                                            layout=layout)
+            qg, sg = mx.fp8_quantize_weight(synth.weight(2 * I, H, seed=synth.seed_cfg4("gate_up", l)).to(dev),
+                                            layout=layout)
+            qd, sd = mx.fp8_quantize_weight(synth.weight(H, I, seed=synth.seed_cfg4("down", l)).to(dev),
+                                            layout=layout)
+            x_host = synth.activation(M, KO, seed=synth.act_seed(4, l, 9)).pin_memory()
+            self.L.append(dict(
+                wo=wo, wos=wos, qg=qg, sg=sg, qd=qd, sd=sd, x_host=x_host, x=x_host.to(dev),
+                ac=torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_A4W4, M, KO, self.To), dtype=torch.uint8, device=dev),
+                asf=torch.empty(mx.mxg_sf_bytes(M, KO), dtype=torch.uint8, device=dev),
+                yo=torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+                qa_g=torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, H, self.Tg), dtype=torch.uint8, device=dev),
+                sa_g=torch.empty(M, dtype=torch.float32, device=dev),
+                yg=torch.empty(M, 2 * I, dtype=torch.bfloat16, device=dev),
+                qa_d=torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, I, self.Td), dtype=torch.uint8, device=dev),
+                sa_d=torch.empty(M, dtype=torch.float32, device=dev),
+                yd=torch.empty(M, H, dtype=ydt, device=dev),
+                yd_host=torch.empty(M, H, dtype=ydt).pin_memory()))
+        self.ws = torch.zeros(max(1 << 20, mx.mxg_gemm_workspace_bytes(mx.KIND_A4W4, False, M, H, KO),
+                                  mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, 2 * I, H),
+                                  mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, H, I)),
+                              dtype=torch.uint8, device=dev)
+        self.timed_label = "ptpc_gate_up"
+        self.kernel_bytes = ptpc_gemm_bytes(M, 2 * I, H)
+        self.kernel_flops = 2 * M * 2 * I * H
+        self.bytes_per_step = layers * (a4w4_fused_bytes(M, H, KO) + mlp_chain_bytes(M, H, I))
+        self.flops_per_step = layers * (2 * M * H * KO + 2 * M * 2 * I * H + 2 * M * H * I)
+        self.dtype = "e2m1 x e2m1 (o_proj), e4m3 x e4m3 (MLP) -> f32 (bf16 out)"
+        self.bound = "hbm" if M <= 256 else "tensor"
+        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan_g["variant"]]
+        self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan_g['bn']}> {v}, {self.plan_g['ctas']} CTAs (gate_up)"
+        self.h2d = layers * 2 * M * KO
+        self.d2h = layers * M * H * ydt.itemsize
+
+    def gemm_plans(self):
+        return [p for _ in range(self.n_layers)
+                for p in (("a4w4_o_proj", self.plan_o), ("ptpc_gate_up", self.plan_g), ("ptpc_down", self.plan_d))]
+
+    def kernels_per_step(self):
+        return self.n_layers * (1 + gemm_kernels(self.plan_o) + 2 + gemm_kernels(self.plan_g)
+                                + gemm_kernels(self.plan_d))
+
+    def layer_launches(self, l):
+        mx, L, M = self.mx, self.L[l], self.M
+        return [
+            ("mx_quant", lambda: mx.mx_quantize_act_tiled(L["x"], self.To, codes=L["ac"], sf=L["asf"])),
+            ("a4w4_o_proj", lambda: mx.mx_gemm_a4w4(
+                L["wo"], L["wos"], a_codes=L["ac"], a_sf=L["asf"], out=L["yo"], ws=self.ws, weights_static=True,
+                weights_tiled=self.wt, act_tile_rows=self.To, m=M, n=self.H, k=self.KO, dev_status=self.status,
+                trace=self.tr("a4w4_o_proj"))),
+            ("fp8_quant", lambda: mx.fp8_quantize_act_tiled(L["yo"], self.Tg, q=L["qa_g"], scale=L["sa_g"])),
+            ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(
+                L["qa_g"], L["sa_g"], L["qg"], L["sg"], out=L["yg"], ws=self.ws, weights_static=True,
+                weights_tiled=self.wt, act_tile_rows=self.Tg, k=self.H, dev_status=self.status,
+                trace=self.tr("ptpc_gate_up"))),
+            ("swiglu_fp8", lambda: mx.swiglu_fp8_quantize(L["yg"], self.Td, q=L["qa_d"], scale=L["sa_d"])),
+            ("ptpc_down", lambda: mx.fp8_gemm_ptpc(
+                L["qa_d"], L["sa_d"], L["qd"], L["sd"], out=L["yd"], out_f32=self.out_f32, ws=self.ws,
+                weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Td, k=self.I,
+                dev_status=self.status, trace=self.tr("ptpc_down")))]
+
+    def launches(self):
+        return [ln for l in range(self.n_layers) for ln in self.layer_launches(l)]
+
+    def outputs(self):
+        return {"yo": torch.stack([L["yo"] for L in self.L]), "yg": torch.stack([L["yg"] for L in self.L]),
+                "yd": torch.stack([L["yd"] for L in self.L])}
+
+    def e2e_step(self):
+        parts = []
+        for l, L in enumerate(self.L):
+            ln = [fn for _, fn in self.layer_launches(l)]
+            parts.append(([(L["x"], L["x_host"])], lambda ln=ln: [f() for f in ln], [(L["yd_host"], L["yd"])]))
+        self.e2e_pipelined(parts)
+
+
+class MlaFp8(Workload):
+    """FP8 PTPC at the MLA up-projection shapes: q_b (1536 -> 12288) and kv_b
+    (512 -> 16384), each its per-token quantizer + GEMM, on their own seeded
+    inputs (the attention between them is not on the path)."""
+
+    def __init__(self, mx, synth, dev, M, name, key="", out_f32=False):
+        self.init_common(dev)
+        self.mx, self.M, self.name, self.key, self.out_f32 = mx, M, name, key, out_f32
+        self.kind = 1
+        layout, self.wt = weight_layout(mx)
+        sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        ydt = torch.float32 if out_f32 else torch.bfloat16
+        self.g = []
+        for gi, ((N, K), seed) in enumerate(((synth.MLA_QB, synth.SEED_MLA_QB), (synth.MLA_KVB, synth.SEED_MLA_KVB))):
+            qw, sw = mx.fp8_quantize_weight(synth.weight(N, K, seed=seed).to(dev), layout=layout)
+            plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, N, K, sm)
+            T = act_tile_rows(plan)
+            x_host = synth.activation(M, K, seed=synth.act_seed(6, 0, gi)).pin_memory()
+            self.g.append(dict(N=N, K=K, qw=qw, sw=sw, plan=plan, T=T, x_host=x_host, x=x_host.to(dev),
+                               qa=torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, K, T), dtype=torch.uint8,
+                                              device=dev),
+                               sa=torch.empty(M, dtype=torch.float32, device=dev),
+                               y=torch.empty(M, N, dtype=ydt, device=dev),
+                               y_host=torch.empty(M, N, dtype=ydt).pin_memory()))
+        self.ws = torch.zeros(max(1 << 20, *(mx.mxg_gemm_workspace_bytes(mx.KIND_PTPC, False, M, g["N"], g["K"])
+                                            for g in self.g)), dtype=torch.uint8, device=dev)
+        self.timed_label = "ptpc_kv_b"
+        g1 = self.g[1]
+        self.kernel_bytes = ptpc_gemm_bytes(M, g1["N"], g1["K"])
+        self.kernel_flops = 2 * M * g1["N"] * g1["K"]
+        self.bytes_per_step = sum(fp8_quant_bytes(M, g["K"]) + ptpc_gemm_bytes(M, g["N"], g["K"]) for g in self.g)
+        self.flops_per_step = sum(2 * M * g["N"] * g["K"] for g in self.g)
+        self.dtype = "e4m3 x e4m3 -> f32 (bf16 out)"
+        self.bound = "hbm" if M <= 256 else "tensor"
+        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[g1["plan"]["variant"]]
+        self.kernel_desc = f"gemm_kernel<PTPC, BN={g1['plan']['bn']}> {v}, {g1['plan']['ctas']} CTAs (kv_b)"
+        self.h2d = sum(2 * M * g["K"] for g in self.g)
+        self.d2h = sum(M * g["N"] * ydt.itemsize for g in self.g)
+
+    def gemm_plans(self):
+        return [("ptpc_q_b", self.g[0]["plan"]), ("ptpc_kv_b", self.g[1]["plan"])]
+
+    def kernels_per_step(self):
+        return sum(1 + gemm_kernels(g["plan"]) for g in self.g)
+
+    def launches(self):
+        mx = self.mx
+        out = []
+        for g, lab in zip(self.g, ("ptpc_q_b", "ptpc_kv_b")):
+            out.append(("fp8_quant", lambda g=g: mx.fp8_quantize_act_tiled(g["x"], g["T"], q=g["qa"], scale=g["sa"])))
+            out.append((lab, lambda g=g, lab=lab: mx.fp8_gemm_ptpc(
+                g["qa"], g["sa"], g["qw"], g["sw"], out=g["y"], out_f32=self.out_f32, ws=self.ws,
+                weights_static=True, weights_tiled=self.wt, act_tile_rows=g["T"], k=g["K"],
+                dev_status=self.status, trace=self.tr(lab))))
+        return out
+
+    def outputs(self):
+        return {"y_q_b": self.g[0]["y"], "y_kv_b": self.g[1]["y"]}
+
+    def e2e_step(self):
+        ln = [fn for _, fn in self.launches()]
+        self.e2e_pipelined([([(g["x"], g["x_host"])], (lambda a=ln[2 * i], b=ln[2 * i + 1]: (a(), b())),
+                             [(g["y_host"], g["y"])]) for i, g in enumerate(self.g)])
+
+
 class MoeGrouped(Workload):
     """Grouped (MoE) A4W4: 8 synthetic experts of gate_up shape (N = 2 x 2048,
     K = 7168), 8192 routed token rows in seeded uneven groups; one call
@@ -569,6 +739,10 @@ WORKLOAD_NAMES = {
     "mlp_fp8_m8192": "FP8 PTPC MLP chain: M=8192, quant, gate_up 7168->36864, SwiGLU+quant, down 18432->7168",
     "moe_grouped": "grouped (MoE) A4W4: 8 experts of gate_up 7168->4096, 8192 routed token rows in seeded "
                    "uneven groups",
+    "mla_fp8_m64": "FP8 PTPC MLA up-projections: M=64, q_b 1536->12288 and kv_b 512->16384",
+    "draft_m64": "draft-layer GEMM chain, 5 layers: M=64, A4W4 o_proj 8192->7168 then FP8 MLP chain on its output",
+    "draft_m8192": "draft-layer GEMM chain, 5 layers: M=8192, A4W4 o_proj 8192->7168 then FP8 MLP chain on its output",
+    "mla_fp8_m8192": "FP8 PTPC MLA up-projections: M=8192, q_b 1536->12288 and kv_b 512->16384",
 }
 
 
@@ -586,6 +760,11 @@ def make_workload(key, mx, synth, dev, out_f32=False):
         return MlpFp8(mx, synth, dev, M, name=name, key=key, out_f32=out_f32)
     if key == "moe_grouped":
         return MoeGrouped(mx, synth, dev, name=name, key=key, out_f32=out_f32)
+    if key in ("draft_m64", "draft_m8192"):
+        return DraftLayers(mx, synth, dev, 64 if key.endswith("m64") else 8192, 5, name=name, key=key,
+                           out_f32=out_f32)
+    if key in ("mla_fp8_m64", "mla_fp8_m8192"):
+        return MlaFp8(mx, synth, dev, 64 if key.endswith("m64") else 8192, name=name, key=key, out_f32=out_f32)
     raise SystemExit(f"unknown workload {key}")
 
 
@@ -996,6 +1175,14 @@ def _oracle_weights(workload):
     if workload == "moe_grouped":
         w = [oracle.mx_quantize_rows(synth.weight(synth.MOE_N, synth.MOE_K, seed=synth.SEED_MOE_W + e))
              for e in range(synth.MOE_EXPERTS)]
+    elif workload.startswith("draft"):
+        w = [(oracle.mx_quantize_rows(synth.weight(7168, synth.OPROJ_K, seed=synth.seed_cfg4("o_proj", l))),
+              oracle.fp8_quantize_rows(synth.weight(2 * synth.MLP_I, 7168, seed=synth.seed_cfg4("gate_up", l))),
+              oracle.fp8_quantize_rows(synth.weight(7168, synth.MLP_I, seed=synth.seed_cfg4("down", l))))
+             for l in range(5)]
+    elif workload.startswith("mla"):
+        w = [oracle.fp8_quantize_rows(synth.weight(*synth.MLA_QB, seed=synth.SEED_MLA_QB)),
+             oracle.fp8_quantize_rows(synth.weight(*synth.MLA_KVB, seed=synth.SEED_MLA_KVB))]
     elif workload.startswith("oproj"):
         M, layers, cfg, seeds, rs = oproj_spec(workload)
         w = [oracle.mx_quantize_rows(synth.weight(synth.OPROJ_N, synth.OPROJ_K, seed=s)) for s in seeds]
@@ -1013,6 +1200,13 @@ def _activations(workload):
     import synth
     if workload == "moe_grouped":
         xs = synth.activation(synth.MOE_ROWS, synth.MOE_K, seed=synth.act_seed(5, 0, 0))
+    elif workload.startswith("draft"):
+        M = 64 if workload.endswith("m64") else 8192
+        xs = [synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(4, l, 9)) for l in range(5)]
+    elif workload.startswith("mla"):
+        M = 64 if workload.endswith("m64") else 8192
+        xs = [synth.activation(M, K, seed=synth.act_seed(6, 0, gi))
+              for gi, (_, K) in enumerate((synth.MLA_QB, synth.MLA_KVB))]
     elif workload.startswith("oproj"):
         M, layers, cfg, seeds, rs = oproj_spec(workload)
         xs = [synth.activation(M, synth.OPROJ_K, seed=synth.act_seed(cfg, l, 0), row_scale=rs)
@@ -1028,6 +1222,8 @@ def workload_rows(workload):
     if workload == "moe_grouped":
         import synth
         return synth.MOE_ROWS
+    if workload.startswith("mla") or workload.startswith("draft"):
+        return 64 if workload.endswith("m64") else 8192
     if workload.startswith("oproj"):
         return oproj_spec(workload)[0]
     return 64 if workload.endswith("m64") else 8192
@@ -1067,6 +1263,23 @@ def oracle_step(workload: str, rows: np.ndarray):
             ac, asf = oracle.mx_quantize_rows(xs[torch.from_numpy(rows[sel])].contiguous())
             ref[sel], bound[sel] = oracle.gemm_a4w4(ac, asf, w[e][0], w[e][1])
         refs.append(("y", None, ref, bound, "gemm"))
+    elif workload.startswith("draft"):
+        for l, ((wo, wos), (qg, sg), (qd, sd)) in enumerate(w):
+            ac, asf = oracle.mx_quantize_rows(xs[l][idx].contiguous())
+            ref_o, bound_o = oracle.gemm_a4w4(ac, asf, wo, wos)
+            refs.append(("yo", l, ref_o, bound_o, "gemm"))
+            # the o_proj output as the bf16 tensor the chain passes on
+            yo16 = torch.from_numpy(ref_o.astype(np.float32)).to(torch.bfloat16)
+            qa, sa = oracle.fp8_quantize_rows(yo16)
+            ref_g, bound_g = oracle.gemm_ptpc(qa, sa, qg, sg)
+            refs.append(("yg", l, ref_g, bound_g, "chain"))
+            g16 = torch.from_numpy(ref_g.astype(np.float32)).to(torch.bfloat16)
+            _, qh, sh = oracle.swiglu_fp8_quantize_rows(g16)
+            refs.append(("yd", l, *oracle.gemm_ptpc(qh, sh, qd, sd), "chain"))
+    elif workload.startswith("mla"):
+        for name, (qw, sw), x in zip(("y_q_b", "y_kv_b"), w, xs):
+            qa, sa = oracle.fp8_quantize_rows(x[idx].contiguous())
+            refs.append((name, None, *oracle.gemm_ptpc(qa, sa, qw, sw), "gemm"))
     elif workload.startswith("oproj"):
         for l, x in enumerate(xs):
             ac, asf = oracle.mx_quantize_rows(x[idx].contiguous())
@@ -1144,6 +1357,13 @@ def step_bytes(workload: str):
         import synth
         E, Nm, Km, M = synth.MOE_EXPERTS, synth.MOE_N, synth.MOE_K, synth.MOE_ROWS
         return E * (Nm * Km // 2 + Nm * Km // 32) + 2 * M * Km + 2 * M * Nm
+    if workload.startswith("draft"):
+        M = 64 if workload.endswith("m64") else 8192
+        return 5 * (a4w4_fused_bytes(M, N, K) + mlp_chain_bytes(M, 7168, 18432))
+    if workload.startswith("mla"):
+        import synth
+        M = 64 if workload.endswith("m64") else 8192
+        return sum(fp8_quant_bytes(M, K) + ptpc_gemm_bytes(M, N, K) for N, K in (synth.MLA_QB, synth.MLA_KVB))
     M = 64 if workload.endswith("m64") else 8192
     return mlp_chain_bytes(M, 7168, 18432)
 
@@ -1360,7 +1580,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="oproj_decode",
                     choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192",
-                             "moe_grouped", "sweep"])
+                             "moe_grouped", "mla_fp8_m64", "mla_fp8_m8192", "draft_m64", "draft_m8192", "sweep"])
     ap.add_argument("--weights", default="panel", choices=["panel", "tiled"],
                     help="resident weight layout: 256-row panels (scales inside) or 128-row tiles")
     ap.add_argument("--no-extras", dest="extras", action="store_false",

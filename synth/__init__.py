@@ -78,6 +78,13 @@ def seed_cfg4(kind: str, layer: int) -> int:
     return {"o_proj": 20, "gate_up": 30, "down": 40}[kind] + layer
 
 
+# MLA up-projections of the draft layer, FP8 PTPC (the pages list q_b_proj
+# and kv_b_proj among the FP8 weights but give no shapes; synthetic, from the
+# usual MLA layout with 64 heads): (N, K) = (64 x (128 + 64), 1536) and
+# (64 x (128 + 128), 512); weight seeds 70 and 71.
+MLA_QB, MLA_KVB = (12288, 1536), (16384, 512)
+SEED_MLA_QB, SEED_MLA_KVB = 70, 71
+
 # Synthetic expert layer (the pages give no expert shapes): gate_up of a
 # 2048-wide expert over the 7168-wide hidden state, 8 experts, 8192 routed
 # token rows (e.g. 1024 tokens x top-8), seed 60 + e for expert e's weight.

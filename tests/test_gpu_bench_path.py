@@ -75,7 +75,7 @@ def run_graph(key, out_f32):
 
 
 @pytest.mark.parametrize("key", ["oproj_decode", "oproj_m8", "mlp_fp8_m64", "oproj_prefill", "mlp_fp8_m8192",
-                                 "moe_grouped"])
+                                 "moe_grouped", "mla_fp8_m64", "mla_fp8_m8192", "draft_m64"])
 def test_benched_step_graph_matches_oracle(key):
     """Every output of the benched step against the oracle's version of the
     same step.  The FP8 MLP is the chain quantize -> gate_up -> SwiGLU +
