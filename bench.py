@@ -189,6 +189,15 @@ def act_tile_rows(plan: dict) -> int:
     return plan["bn"] if plan["variant"] == 2 else 128
 
 
+def variant_desc(plan):
+    """How the dispatcher runs a GEMM, for the bench line."""
+    if plan["variant"] == 2:
+        return f"split-K (swapped, stream-K), {plan['ctas']} CTAs"
+    if plan["cta_pair"]:
+        return f"full-tile, CTA pairs (2-SM MMA, 256 x 256 tiles), {plan['ctas']} CTAs"
+    return f"full-tile, {plan['ctas']} CTAs"
+
+
 class Workload:
     """Builds resident device operands and exposes one step as a list of
     (label, fn) launches; `timed_label` marks the dominant kernel.
@@ -281,6 +290,18 @@ class Workload:
 WEIGHTS = "panel"
 
 
+# --cta-pair: full-tile GEMMs of M > 128 on CTA pairs (2-SM MMAs)
+CTA_PAIR = False
+
+
+def gemm_a4w4(mx, *args, **kw):
+    return mx.mx_gemm_a4w4(*args, cta_pair=CTA_PAIR, **kw)
+
+
+def gemm_ptpc(mx, *args, **kw):
+    return mx.fp8_gemm_ptpc(*args, cta_pair=CTA_PAIR, **kw)
+
+
 def weight_layout(mx):
     """(quantizer layout, GEMM weights_tiled value) of the chosen layout."""
     return (mx.PANEL, mx.W_PANEL) if WEIGHTS == "panel" else (mx.TILED, mx.W_TILED)
@@ -316,7 +337,7 @@ class OprojChain(Workload):
         self.y = torch.empty(layers, M, N, dtype=ydt, device=dev)
         self.y_host = torch.empty(layers, M, N, dtype=ydt).pin_memory()
         sm = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, sm)
+        self.plan = mx.mxg_plan_gemm(mx.KIND_A4W4, M, N, K, sm, cta_pair=CTA_PAIR)
         # activation codes in the tile layout the GEMM fetches by bulk copy
         self.T = act_tile_rows(self.plan)
         self.ac = [torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_A4W4, M, K, self.T), dtype=torch.uint8, device=dev)
@@ -331,8 +352,7 @@ class OprojChain(Workload):
         self.flops_per_step = layers * 2 * M * N * K
         self.dtype = "e2m1 x e2m1 -> f32 (bf16 out)"
         self.bound = "hbm" if M <= 512 else "tensor"
-        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
-        self.kernel_desc = f"gemm_kernel<A4W4, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
+        self.kernel_desc = f"gemm_kernel<A4W4, BN={self.plan['bn']}> {variant_desc(self.plan)}"
         self.h2d = layers * M * K * 2
         self.d2h = layers * M * N * ydt.itemsize
 
@@ -350,7 +370,7 @@ class OprojChain(Workload):
             wc, wsf = self.w[l]
             out.append(("mx_quant", lambda l=l: mx.mx_quantize_act_tiled(self.x[l], self.T, codes=self.ac[l],
                                                                          sf=self.asf[l])))
-            out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: mx.mx_gemm_a4w4(
+            out.append(("a4w4_gemm", lambda l=l, wc=wc, wsf=wsf: gemm_a4w4(mx, 
                 wc, wsf, a_codes=self.ac[l], a_sf=self.asf[l], out=self.y[l], out_f32=self.out_f32, ws=self.ws,
                 weights_static=True, weights_tiled=self.wt, act_tile_rows=self.T, m=self.M, n=self.N, k=self.K,
                 dev_status=self.status, trace=self.tr("a4w4_gemm"))))
@@ -376,7 +396,7 @@ class OprojChain(Workload):
 
         def gemm(l, r0, r1):
             wc, wsf = self.w[l]
-            mx.mx_gemm_a4w4(wc, wsf, x=self.x[l][r0:r1], out=self.y[l][r0:r1], out_f32=self.out_f32, ws=self.ws,
+            gemm_a4w4(mx, wc, wsf, x=self.x[l][r0:r1], out=self.y[l][r0:r1], out_f32=self.out_f32, ws=self.ws,
                             weights_tiled=self.wt, weights_static=True, n=self.N, k=self.K,
                             dev_status=self.status)
         parts = []
@@ -413,9 +433,9 @@ class MlpFp8(Workload):
         self.x = self.x_host.to(dev)
         sm = torch.cuda.get_device_properties(dev).multi_processor_count
         # activations in the tile layout of each GEMM's plan
-        self.plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm)
+        self.plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, I2, H, sm, cta_pair=CTA_PAIR)
         self.Tg = act_tile_rows(self.plan)
-        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm)
+        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, synth.MLP_I, sm, cta_pair=CTA_PAIR)
         self.Td = act_tile_rows(self.plan_d)
         self.qa_g = torch.empty(mx.mxg_act_tiled_bytes(mx.KIND_PTPC, M, H, self.Tg), dtype=torch.uint8, device=dev)
         self.sa_g = torch.empty(M, dtype=torch.float32, device=dev)
@@ -437,8 +457,7 @@ class MlpFp8(Workload):
         self.flops_per_step = 2 * M * I2 * H + 2 * M * H * synth.MLP_I
         self.dtype = "e4m3 x e4m3 -> f32 (bf16 out)"
         self.bound = "hbm" if M <= 256 else "tensor"
-        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan["variant"]]
-        self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan['bn']}> {v}, {self.plan['ctas']} CTAs"
+        self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan['bn']}> {variant_desc(self.plan)}"
         self.h2d = 2 * M * H
         self.d2h = M * H * ydt.itemsize
 
@@ -454,12 +473,12 @@ class MlpFp8(Workload):
         mx = self.mx
         sl = slice(r0, r1)
         return [("fp8_quant", lambda: mx.fp8_quantize_act_tiled(self.x[sl], self.Tg, q=qa_g, scale=self.sa_g[sl])),
-                ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(
+                ("ptpc_gate_up", lambda: gemm_ptpc(mx, 
                     qa_g, self.sa_g[sl], self.qg, self.sg, out=self.yg[sl], ws=self.ws,
                     weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Tg, k=self.H,
                     dev_status=self.status, trace=self.tr("ptpc_gate_up") if trace else None)),
                 ("swiglu_fp8", lambda: mx.swiglu_fp8_quantize(self.yg[sl], self.Td, q=qa_d, scale=self.sa_d[sl])),
-                ("ptpc_down", lambda: mx.fp8_gemm_ptpc(
+                ("ptpc_down", lambda: gemm_ptpc(mx, 
                     qa_d, self.sa_d[sl], self.qd, self.sd, out=self.yd[sl], out_f32=self.out_f32, ws=self.ws,
                     weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Td, k=self.I,
                     dev_status=self.status, trace=self.tr("ptpc_down") if trace else None))]
@@ -487,8 +506,8 @@ class MlpFp8(Workload):
             r1 = min(self.M, r0 + rows)
             # a chunk's activations in the tile layout are a contiguous run of
             # its token tiles (the full batch's tiles have the same height)
-            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, 2 * self.I, self.H, sm)) == self.Tg
-            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, self.H, self.I, sm)) == self.Td
+            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, 2 * self.I, self.H, sm, cta_pair=CTA_PAIR)) == self.Tg
+            assert act_tile_rows(mx.mxg_plan_gemm(mx.KIND_PTPC, r1 - r0, self.H, self.I, sm, cta_pair=CTA_PAIR)) == self.Td
             tg = (self.H // 128) * self.Tg * 128
             td = (self.I // 128) * self.Td * 128
             qa_g = self.qa_g[(r0 // self.Tg) * tg:-(-r1 // self.Tg) * tg]
@@ -518,9 +537,9 @@ class DraftLayers(Workload):
         self.H, self.I, self.KO = H, I, KO
         layout, self.wt = weight_layout(mx)
         sm = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.plan_o = mx.mxg_plan_gemm(mx.KIND_A4W4, M, H, KO, sm)
-        self.plan_g = mx.mxg_plan_gemm(mx.KIND_PTPC, M, 2 * I, H, sm)
-        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, I, sm)
+        self.plan_o = mx.mxg_plan_gemm(mx.KIND_A4W4, M, H, KO, sm, cta_pair=CTA_PAIR)
+        self.plan_g = mx.mxg_plan_gemm(mx.KIND_PTPC, M, 2 * I, H, sm, cta_pair=CTA_PAIR)
+        self.plan_d = mx.mxg_plan_gemm(mx.KIND_PTPC, M, H, I, sm, cta_pair=CTA_PAIR)
         self.plan = self.plan_g
         self.To, self.Tg, self.Td = act_tile_rows(self.plan_o), act_tile_rows(self.plan_g), act_tile_rows(self.plan_d)
         ydt = torch.float32 if out_f32 else torch.bfloat16
@@ -573,17 +592,17 @@ class DraftLayers(Workload):
         mx, L, M = self.mx, self.L[l], self.M
         return [
             ("mx_quant", lambda: mx.mx_quantize_act_tiled(L["x"], self.To, codes=L["ac"], sf=L["asf"])),
-            ("a4w4_o_proj", lambda: mx.mx_gemm_a4w4(
+            ("a4w4_o_proj", lambda: gemm_a4w4(mx, 
                 L["wo"], L["wos"], a_codes=L["ac"], a_sf=L["asf"], out=L["yo"], ws=self.ws, weights_static=True,
                 weights_tiled=self.wt, act_tile_rows=self.To, m=M, n=self.H, k=self.KO, dev_status=self.status,
                 trace=self.tr("a4w4_o_proj"))),
             ("fp8_quant", lambda: mx.fp8_quantize_act_tiled(L["yo"], self.Tg, q=L["qa_g"], scale=L["sa_g"])),
-            ("ptpc_gate_up", lambda: mx.fp8_gemm_ptpc(
+            ("ptpc_gate_up", lambda: gemm_ptpc(mx, 
                 L["qa_g"], L["sa_g"], L["qg"], L["sg"], out=L["yg"], ws=self.ws, weights_static=True,
                 weights_tiled=self.wt, act_tile_rows=self.Tg, k=self.H, dev_status=self.status,
                 trace=self.tr("ptpc_gate_up"))),
             ("swiglu_fp8", lambda: mx.swiglu_fp8_quantize(L["yg"], self.Td, q=L["qa_d"], scale=L["sa_d"])),
-            ("ptpc_down", lambda: mx.fp8_gemm_ptpc(
+            ("ptpc_down", lambda: gemm_ptpc(mx, 
                 L["qa_d"], L["sa_d"], L["qd"], L["sd"], out=L["yd"], out_f32=self.out_f32, ws=self.ws,
                 weights_static=True, weights_tiled=self.wt, act_tile_rows=self.Td, k=self.I,
                 dev_status=self.status, trace=self.tr("ptpc_down")))]
@@ -618,7 +637,7 @@ class MlaFp8(Workload):
         self.g = []
         for gi, ((N, K), seed) in enumerate(((synth.MLA_QB, synth.SEED_MLA_QB), (synth.MLA_KVB, synth.SEED_MLA_KVB))):
             qw, sw = mx.fp8_quantize_weight(synth.weight(N, K, seed=seed).to(dev), layout=layout)
-            plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, N, K, sm)
+            plan = mx.mxg_plan_gemm(mx.KIND_PTPC, M, N, K, sm, cta_pair=CTA_PAIR)
             T = act_tile_rows(plan)
             x_host = synth.activation(M, K, seed=synth.act_seed(6, 0, gi)).pin_memory()
             self.g.append(dict(N=N, K=K, qw=qw, sw=sw, plan=plan, T=T, x_host=x_host, x=x_host.to(dev),
@@ -653,7 +672,7 @@ class MlaFp8(Workload):
         out = []
         for g, lab in zip(self.g, ("ptpc_q_b", "ptpc_kv_b")):
             out.append(("fp8_quant", lambda g=g: mx.fp8_quantize_act_tiled(g["x"], g["T"], q=g["qa"], scale=g["sa"])))
-            out.append((lab, lambda g=g, lab=lab: mx.fp8_gemm_ptpc(
+            out.append((lab, lambda g=g, lab=lab: gemm_ptpc(mx, 
                 g["qa"], g["sa"], g["qw"], g["sw"], out=g["y"], out_f32=self.out_f32, ws=self.ws,
                 weights_static=True, weights_tiled=self.wt, act_tile_rows=g["T"], k=g["K"],
                 dev_status=self.status, trace=self.tr(lab))))
@@ -773,7 +792,8 @@ def workload_config(key, world=1):
     return {"workload": WORKLOAD_NAMES[key], "key": key,
             "l2": "flushed between steps (256 MiB write + read back, outside the timed interval)",
             "step": "one CUDA graph replay", "parallelism": f"replicas x{world}",
-            "weights": f"{WEIGHTS} layout, resident in HBM"}
+            "weights": f"{WEIGHTS} layout, resident in HBM",
+            "full_tile": "CTA pairs, 2-SM MMAs (--cta-pair)" if CTA_PAIR else "one CTA per 128 x 256 tile"}
 
 
 # ----------------------------------------------------------------- step graphs
@@ -1490,7 +1510,7 @@ def run_sweep(args, rank, world, local_rank):
         per = {}
         total_ms = 0.0
         for g, (N, K, kind) in shapes.items():
-            plan = mx.mxg_plan_gemm(kind, M, N, K, sm)
+            plan = mx.mxg_plan_gemm(kind, M, N, K, sm, cta_pair=CTA_PAIR)
             T = act_tile_rows(plan)
             x = xs[g][:M]
             y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
@@ -1503,7 +1523,7 @@ def run_sweep(args, rank, world, local_rank):
                 def layer(l, x=x, y=y, ws=ws, qa=qa, sa=sa, T=T, g=g, K=K):
                     mx.fp8_quantize_act_tiled(x, T, q=qa, scale=sa)
                     qw, sw = w[g][l]
-                    mx.fp8_gemm_ptpc(qa, sa, qw, sw, out=y, ws=ws, weights_static=True,
+                    gemm_ptpc(mx, qa, sa, qw, sw, out=y, ws=ws, weights_static=True,
                                      weights_tiled=wt, act_tile_rows=T, k=K, dev_status=status)
                 gbytes = ptpc_gemm_bytes(M, N, K) + fp8_quant_bytes(M, K)
             else:
@@ -1513,7 +1533,7 @@ def run_sweep(args, rank, world, local_rank):
                 def layer(l, x=x, y=y, ws=ws, ac=ac, asf=asf, T=T, M=M, g=g, N=N, K=K):
                     mx.mx_quantize_act_tiled(x, T, codes=ac, sf=asf)
                     wc, wsf = w[g][l]
-                    mx.mx_gemm_a4w4(wc, wsf, a_codes=ac, a_sf=asf, out=y, ws=ws, weights_static=True,
+                    gemm_a4w4(mx, wc, wsf, a_codes=ac, a_sf=asf, out=y, ws=ws, weights_static=True,
                                     weights_tiled=wt, act_tile_rows=T, m=M, n=N, k=K, dev_status=status)
                 gbytes = a4w4_gemm_bytes(M, N, K) + mx_quant_bytes(M, K)
             with torch.cuda.stream(stream):
@@ -1557,7 +1577,7 @@ def run_sweep(args, rank, world, local_rank):
             per[g] = {"dtype": "e2m1 x e2m1" if kind == 0 else "e4m3 x e4m3", "N": N, "K": K,
                       "us": round(ms * 1e3, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
                       "roofline": roof, "status_ok": st == 0,
-                      "dispatch": {k: plan[k] for k in ("variant", "bn", "ctas", "seg_max")}}
+                      "dispatch": {k: plan[k] for k in ("variant", "bm", "bn", "ctas", "seg_max", "cta_pair")}}
             del graph
         layer_flops = sum(2.0 * M * n * k for n, k, _ in shapes.values())
         line = {"metric": METRIC, "workload": "sweep", "M": M, "n_gpus": world,
@@ -1581,6 +1601,8 @@ def main():
     ap.add_argument("--workload", default="oproj_decode",
                     choices=["oproj_decode", "oproj_m8", "oproj_prefill", "mlp_fp8_m64", "mlp_fp8_m8192",
                              "moe_grouped", "mla_fp8_m64", "mla_fp8_m8192", "draft_m64", "draft_m8192", "sweep"])
+    ap.add_argument("--cta-pair", action="store_true",
+                    help="run full-tile GEMMs of M > 128 on CTA pairs (2-SM MMAs)")
     ap.add_argument("--weights", default="panel", choices=["panel", "tiled"],
                     help="resident weight layout: 256-row panels (scales inside) or 128-row tiles")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
@@ -1590,8 +1612,9 @@ def main():
     ap.add_argument("--min-warmup-s", type=float, default=0.5,
                     help="keep warming up at least this long so clocks settle (0 under a profiler)")
     args = ap.parse_args()
-    global WEIGHTS
+    global WEIGHTS, CTA_PAIR
     WEIGHTS = args.weights
+    CTA_PAIR = args.cta_pair
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

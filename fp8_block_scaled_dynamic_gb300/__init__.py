@@ -50,7 +50,7 @@ class GemmOpts(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p), ("timeout_ms", ctypes.c_uint32),
                 ("debug_stall", ctypes.c_int), ("weights_static", ctypes.c_int),
                 ("weights_tiled", ctypes.c_int), ("act_tile_rows", ctypes.c_int),
-                ("trace", ctypes.c_void_p), ("splitk_reduce", ctypes.c_int)]
+                ("trace", ctypes.c_void_p), ("splitk_reduce", ctypes.c_int), ("cta_pair", ctypes.c_int)]
 
 
 REDUCE = {"default": 0, "kernel": 1}
@@ -59,7 +59,7 @@ REDUCE = {"default": 0, "kernel": 1}
 class Plan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bm", ctypes.c_int), ("bn", ctypes.c_int),
                 ("ctas", ctypes.c_int), ("tiles", ctypes.c_int), ("kblocks", ctypes.c_int),
-                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t), ("reserved", ctypes.c_int)]
+                ("seg_max", ctypes.c_int), ("ws_bytes", ctypes.c_size_t), ("cta_pair", ctypes.c_int)]
 
 
 _lib = None
@@ -151,9 +151,10 @@ def mxg_weight_bytes(kind: int, N: int, K: int, layout: int) -> int:
 
 
 def mxg_plan_gemm(kind: int, M: int, N: int, K: int, sm_count: int,
-                  variant: str = "auto", ctas: int = 0, splitk_reduce: str = "default") -> dict:
+                  variant: str = "auto", ctas: int = 0, splitk_reduce: str = "default",
+                  cta_pair: bool = False) -> dict:
     """Pure host dispatcher: the variant/tile/grid/workspace of a GEMM."""
-    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas, splitk_reduce=REDUCE[splitk_reduce])
+    o = GemmOpts(variant=VARIANTS[variant], ctas=ctas, splitk_reduce=REDUCE[splitk_reduce], cta_pair=int(cta_pair))
     p = Plan()
     _check("mxg_plan_gemm", lib().mxg_plan_gemm(kind, M, N, K, sm_count, ctypes.byref(o), ctypes.byref(p)))
     return {f: getattr(p, f) for f, _ in Plan._fields_}
@@ -314,8 +315,10 @@ def swiglu_fp8_quantize(gu: torch.Tensor, tile_rows: int = 0, q=None, scale=None
 
 # ---------------------------------------------------------------- GEMMs
 def _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static=False,
-          trace=None, weights_tiled=False, act_tile_rows=0, splitk_reduce="default") -> GemmOpts:
+          trace=None, weights_tiled=False, act_tile_rows=0, splitk_reduce="default",
+          cta_pair=False) -> GemmOpts:
     return GemmOpts(variant=VARIANTS[variant], ctas=int(ctas), weights_static=int(weights_static),
+                    cta_pair=int(cta_pair),
                     weights_tiled=int(weights_tiled), act_tile_rows=int(act_tile_rows),
                     splitk_reduce=REDUCE[splitk_reduce],
                     trace=0 if trace is None else trace.data_ptr(),
@@ -338,13 +341,14 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf, *, a_codes=None, a_sf=None, x=None
                  ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                  weights_static: bool = False, trace=None, weights_tiled: int = W_ROWMAJOR,
                  act_tile_rows: int = 0, m: int = 0, n: int = 0, k: int = 0,
-                 splitk_reduce: str = "default", stream=None):
+                 splitk_reduce: str = "default", cta_pair: bool = False, stream=None):
     """y (M, N) = MXFP4 A4W4 GEMM.  Either (a_codes, a_sf) pre-quantized or
     x (M, K) bf16 (quantized inside the call).  w_sf must be in the 128x4
     tiles; w_codes row-major, or in weight tiles with weights_tiled=W_TILED
     (or True); with weights_tiled=W_PANEL w_codes is flat in 256-row panels
     (scales inside, w_sf None) and n, k give N, K.  With act_tile_rows,
-    a_codes is flat in the activation tile layout and m gives M."""
+    a_codes is flat in the activation tile layout and m gives M.  cta_pair:
+    run a full-tile GEMM of M > 128 on CTA pairs (2-SM MMAs)."""
     if w_codes.dim() == 1:
         _need(n > 0 and k > 0, "flat weight codes need n and k")
         N, K = n, k
@@ -363,7 +367,7 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf, *, a_codes=None, a_sf=None, x=None
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_A4W4, fused, M, N, K, variant, ctas), w_codes.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled, act_tile_rows, splitk_reduce)
+              weights_tiled, act_tile_rows, splitk_reduce, cta_pair)
     _check("mx_gemm_a4w4", lib().mx_gemm_a4w4(
         _ptr(a_codes), _ptr(a_sf), _ptr(x), ldx, _ptr(w_codes), _ptr(w_sf), M, N, K,
         _ptr(out), out.stride(0), OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))
@@ -374,12 +378,14 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
                   out=None, out_f32: bool = False, variant: str = "auto", ctas: int = 0,
                   ws=None, dev_status=None, timeout_ms: int = 0, debug_stall: int = 0,
                   weights_static: bool = False, trace=None, weights_tiled: int = W_ROWMAJOR,
-                  act_tile_rows: int = 0, k: int = 0, splitk_reduce: str = "default", stream=None):
+                  act_tile_rows: int = 0, k: int = 0, splitk_reduce: str = "default",
+                  cta_pair: bool = False, stream=None):
     """y (M, N) = (sum_k qa qw * sa[m]) * sw[n]: FP8 PTPC A8W8 GEMM; qw
     row-major, or in weight tiles with weights_tiled=W_TILED (or True), or
     flat in 256-row panels with weights_tiled=W_PANEL (k gives K); qa
     row-major, or flat in the activation tile layout with act_tile_rows
-    (M = len(sa), N = len(sw))."""
+    (M = len(sa), N = len(sw)).  cta_pair: run a full-tile GEMM of M > 128
+    on CTA pairs (2-SM MMAs)."""
     M = sa.numel()
     N = sw.numel()
     if qw.dim() == 1:
@@ -392,7 +398,7 @@ def fp8_gemm_ptpc(qa: torch.Tensor, sa: torch.Tensor, qw: torch.Tensor, sw: torc
     if ws is None:
         ws = workspace(mxg_gemm_workspace_bytes(KIND_PTPC, False, M, N, K, variant, ctas), qa.device)
     o = _opts(variant, ctas, ws, dev_status, timeout_ms, debug_stall, weights_static, trace,
-              weights_tiled, act_tile_rows, splitk_reduce)
+              weights_tiled, act_tile_rows, splitk_reduce, cta_pair)
     _check("fp8_gemm_ptpc", lib().fp8_gemm_ptpc(
         _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), M, N, K, _ptr(out), out.stride(0),
         OUT_F32 if out_f32 else OUT_BF16, ctypes.byref(o), _stream(stream)))

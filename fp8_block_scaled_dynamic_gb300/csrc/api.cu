@@ -137,10 +137,22 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
   pl->bm = 128;
   if (variant == MXG_VARIANT_FULL) {
     pl->bn = 256;
-    const long long tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
-    if (tiles + sm_count >= (1LL << 31)) return MXG_ERR_UNSUPPORTED_SHAPE;
-    pl->tiles = (int)tiles;
-    pl->ctas = (int)(tiles < sm_count ? tiles : sm_count);
+    const long long tA = (M + 127) / 128, tB = (N + 255) / 256;
+    if (tA * tB + sm_count >= (1LL << 31)) return MXG_ERR_UNSUPPORTED_SHAPE;
+    if (opts && opts->cta_pair && tA >= 2 && sm_count >= 2) {
+      // on request, with two token tiles or more: CTA pairs with 2-SM MMAs
+      // over 256 x 256 tiles, one pair per two SMs
+      const long long tiles = ((tA + 1) / 2) * tB;
+      const long long pairs = sm_count / 2;
+      pl->bm = 256;
+      pl->cta_pair = 1;
+      pl->tiles = (int)tiles;
+      pl->ctas = (int)(2 * (tiles < pairs ? tiles : pairs));
+    } else {
+      const long long tiles = tA * tB;
+      pl->tiles = (int)tiles;
+      pl->ctas = (int)(tiles < sm_count ? tiles : sm_count);
+    }
     pl->seg_max = 1;
     pl->ws_bytes = 0;
   } else {
@@ -233,7 +245,9 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   const uint8_t *B = swap ? op.a : op.w;
   const int rowsA = swap ? N : M, rowsB = swap ? M : N;
   if ((st = make_operand_map(&tmA, A, row_bytes, rowsA, 128)) != MXG_OK) return st;
-  if ((st = make_operand_map(&tmB, B, row_bytes, rowsB, (uint32_t)pl.bn)) != MXG_OK) return st;
+  // (a CTA pair's CTA holds 128 rows of the BN-row weight tile)
+  if ((st = make_operand_map(&tmB, B, row_bytes, rowsB, (uint32_t)(pl.cta_pair ? 128 : pl.bn))) != MXG_OK)
+    return st;
 
   mxg::GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -259,6 +273,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.kblocks = pl.kblocks;
   p.G4 = K / 128;
   p.splitk = swap ? 1 : 0;
+  p.cta_pair = pl.cta_pair;
   p.units = (long long)p.tilesA * p.tilesB * p.kblocks;
   if (pl.ws_bytes > 0) p.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + part_off);
   p.seg_max = pl.seg_max;
@@ -319,6 +334,7 @@ mxg_status check_gemm_common(int M, int N, int K, const void *y, int ldy, mxg_ou
   if (opts && opts->splitk_reduce != MXG_REDUCE_DEFAULT && opts->splitk_reduce != MXG_REDUCE_KERNEL)
     return MXG_ERR_INVALID_ARG;
   if (opts && (opts->weights_tiled < 0 || opts->weights_tiled > 2)) return MXG_ERR_INVALID_ARG;
+  if (opts && (opts->cta_pair < 0 || opts->cta_pair > 1)) return MXG_ERR_INVALID_ARG;
   if (opts && opts->act_tile_rows && !valid_tile_rows(opts->act_tile_rows))
     return MXG_ERR_INVALID_ARG;
   return MXG_OK;
@@ -568,7 +584,8 @@ mxg_status mx_gemm_a4w4_grouped(const void *x_bf16, int ldx, const int *row_off,
   if (out_dtype != MXG_OUT_BF16 && out_dtype != MXG_OUT_F32) return MXG_ERR_INVALID_ARG;
   if (opts && ((opts->variant != MXG_VARIANT_AUTO && opts->variant != MXG_VARIANT_FULL) ||
                (opts->weights_tiled != 0 && opts->weights_tiled != 2) || opts->act_tile_rows != 0 ||
-               (opts->splitk_reduce != MXG_REDUCE_DEFAULT && opts->splitk_reduce != MXG_REDUCE_KERNEL)))
+               (opts->splitk_reduce != MXG_REDUCE_DEFAULT && opts->splitk_reduce != MXG_REDUCE_KERNEL) ||
+               opts->cta_pair != 0))
     return MXG_ERR_INVALID_ARG;
   if (K % 256 != 0 || N % 128 != 0) return MXG_ERR_UNSUPPORTED_SHAPE;
   if ((x_bf16 && !aligned16(x_bf16)) || (ldx % 8) != 0 || !aligned16(w_panels) || (y && !aligned16(y)) ||

@@ -11,7 +11,12 @@
 // One kernel template serves both variants the dispatcher chooses from:
 //   full tile  (swap = 0): MMA-A = 128 token rows, MMA-B = 256 weight rows,
 //              each CTA owns whole tiles and all of K (persistent, strided;
-//              in bands of token tiles when the operands exceed L2).
+//              in bands of token tiles when the operands exceed L2).  With
+//              CTA pairs (CG = 2, clusters of two) a tile is 256 tokens x 256
+//              channels: each CTA brings 128 token rows and one 128-row half
+//              of the weight tile, and the even CTA issues 2-SM MMAs
+//              (cta_group::2) over both -- 256 instead of 384 operand rows
+//              per 128 x 256 share of output, and stages half as big.
 //   split-K    (swap = 1): MMA-A = 128 weight rows, MMA-B = the (padded)
 //              token rows; the (tile, K-block) units are cut evenly over the
 //              CTAs (stream-K); a CTA that ends a tile part-way writes an
@@ -47,29 +52,36 @@ constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, BN)
 // the copy for the next stage never waits for the MMAs still reading the
 // scales of this one.
 constexpr uint32_t kSfCol = 256;
-constexpr int kSmemBudget = 220 * 1024;
+// Dynamic shared memory of a CTA: the mbarriers and a few words in the first
+// 1024 bytes, then the 1024-byte-aligned pipeline stages and the epilogue's
+// staging boxes, up to the 227 KB a CTA may have.
+constexpr int kSmemMax = 227 * 1024;
+constexpr int kSmemHead = 1024;
 
 // KS: 128-byte K columns per pipeline stage (one column = 256 E2M1 or 128
 // E4M3 values of every row).  Two columns per stage halve the number of bulk
 // copies per byte, which is what bounds the weight-streaming (split-K) rate.
-template <int KIND, int BN, int KS>
+template <int KIND, int BN, int KS, int CG = 1>
 struct Cfg {
   static constexpr int kSfBlocksB = BN >= 128 ? BN / 128 : 1;
+  static constexpr int kBRows = BN / CG;  // MMA-B rows this CTA holds (the MMA's N is BN)
   static constexpr int kAColBytes = kTileA * kRowBytes;  // one column of the A operand
-  static constexpr int kBColBytes = BN * kRowBytes;
+  static constexpr int kBColBytes = kBRows * kRowBytes;
   static constexpr int kABytes = kAColBytes * KS;
   static constexpr int kBBytes = kBColBytes * KS;
   static constexpr int kSfaBytes = KIND == 0 ? 1024 * KS : 0;  // 2 scale atoms per column
+  // the scales of all BN rows of B (a CTA pair: each CTA holds both halves'
+  // scales, since each CTA's MMAs cover all BN columns of its output rows)
   static constexpr int kSfbBytes = KIND == 0 ? 1024 * KS * kSfBlocksB : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   // one column of a 256-row weight panel: codes, then (E2M1) the 2 x 2 scale atoms
   static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
-  static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 8 * (3 * kStages + 12) + 16;
   // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
   static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kStagesRaw = (kSmemMax - kSmemHead - kEpiBytes) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kBarBytes = 8 * (4 * kStages + 6) + 8;  // mbarriers, TMEM base, abort flag
+  static constexpr size_t kSmem = (size_t)kSmemHead + (size_t)kStages * kStageBytes + kEpiBytes;
   // TMEM accumulators: two where the columns allow (FP8: all 512; A4W4: the
   // 256 below the scale factors), so that the epilogue of one item runs
   // beside the MMAs of the next
@@ -79,9 +91,11 @@ struct Cfg {
   static constexpr uint32_t kSfColsA = 8u * KS;      // 4 TMEM columns per scale atom
   static constexpr uint32_t kSfColsPerStage = kSfColsA + 8u * KS * (uint32_t)kSfBlocksB;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(CG == 1 || (KS == 1 && BN == 256), "CTA pairs: full tile only");
   static_assert(kStages >= 2, "pipeline depth");
-  static_assert(KS == 1 || 128 * BN * 4 <= kStages * kStageBytes, "CTA-pair partial tile fits the pipeline");
+  static_assert(kBarBytes <= kSmemHead && kSmem <= (size_t)kSmemMax, "shared memory");
   static_assert(KIND != 0 || kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(kSfColsPerStage % 8 == 0, "scale columns of a stage: whole 8-column stores");
 };
 
 struct Item {
@@ -111,13 +125,17 @@ __device__ __forceinline__ uint32_t owner_of(uint32_t u, uint32_t U, uint32_t G)
   return ((u + 1) * G - 1) / U;
 }
 
+// The first item cursor of this CTA (CG = 2: of its pair; both CTAs of a
+// pair walk the same items).
+template <int CG>
 __device__ __forceinline__ uint32_t first_cursor(const GemmParams &p) {
-  return p.splitk ? (blockIdx.x * (uint32_t)p.units) / gridDim.x : blockIdx.x;
+  return p.splitk ? (blockIdx.x * (uint32_t)p.units) / gridDim.x : blockIdx.x / (uint32_t)CG;
 }
 
 // The work items of this CTA, in order; every role walks the same list.
+template <int CG>
 __device__ __forceinline__ bool next_item(const GemmParams &p, uint32_t &cur, Item &it) {
-  const uint32_t G = gridDim.x;
+  const uint32_t G = gridDim.x / (uint32_t)CG;
   it.e = 0;
   if (p.groups) {
     // grouped (full tile): item i = (weight tile i / tilesA, token tile i %
@@ -143,44 +161,52 @@ __device__ __forceinline__ bool next_item(const GemmParams &p, uint32_t &cur, It
     return true;
   }
   if (!p.splitk) {
-    if (cur >= (uint32_t)(p.tilesA * p.tilesB)) return false;
+    // full tile; a CTA pair's item is a pair of token tiles (the CTA of rank
+    // r takes token tile 2 * pair + r; past the last token tile it loads no
+    // activations and stores nothing)
+    const uint32_t tA = CG == 2 ? ((uint32_t)p.tilesA + 1u) >> 1 : (uint32_t)p.tilesA;
+    const uint32_t tB = (uint32_t)p.tilesB;
+    if (cur >= tA * tB) return false;
     it.t = (int)cur;
     it.kb0 = 0;
     it.kb1 = p.kblocks;
     it.seg = 0;
     it.nseg = 1;
+    const uint32_t t = cur;
     cur += G;
     if (p.raster_group > 0) {
       // bands of raster_group MMA-A (token) tiles: within a band the token
       // tile varies fastest, so the CTAs running at one time share a few
       // weight tiles and the band's activations stay in L2 -- the weights
       // are read from HBM once per band, not once per token tile
-      const uint32_t g = (uint32_t)p.raster_group;
-      const uint32_t band = g * (uint32_t)p.tilesB;
-      const uint32_t bi = (uint32_t)it.t;
-      const uint32_t b0 = bi / band, r = bi - b0 * band;
+      const uint32_t g = max(1u, (uint32_t)p.raster_group / (uint32_t)CG);
+      const uint32_t band = g * tB;
+      const uint32_t b0 = t / band, r = t - b0 * band;
       const uint32_t ta0 = b0 * g;
-      const uint32_t gsz = min(g, (uint32_t)p.tilesA - ta0);
+      const uint32_t gsz = min(g, tA - ta0);
       it.ta = (int)(ta0 + r % gsz);
       it.tb = (int)(r / gsz);
-      return true;
+    } else {
+      it.ta = (int)(t / tB);
+      it.tb = (int)(t - (uint32_t)it.ta * tB);
     }
-  } else {
-    const uint32_t U = (uint32_t)p.units;
-    const uint32_t u1 = ((blockIdx.x + 1) * U) / G;
-    if (cur >= u1) return false;
-    const uint32_t KB = (uint32_t)p.kblocks;
-    const uint32_t t = cur / KB;
-    it.t = (int)t;
-    it.kb0 = (int)(cur - t * KB);
-    const uint32_t room = u1 - cur;
-    it.kb1 = (KB - (uint32_t)it.kb0) < room ? (int)KB : it.kb0 + (int)room;
-    cur += (uint32_t)(it.kb1 - it.kb0);
-    const uint32_t first = t * KB;
-    const uint32_t o0 = owner_of(first, U, G);
-    it.seg = (int)(blockIdx.x - o0);
-    it.nseg = (int)(owner_of(first + KB - 1, U, G) - o0 + 1);
+    if (CG == 2) it.ta = 2 * it.ta + (int)(blockIdx.x & 1u);
+    return true;
   }
+  const uint32_t U = (uint32_t)p.units;
+  const uint32_t u1 = ((blockIdx.x + 1) * U) / G;
+  if (cur >= u1) return false;
+  const uint32_t KB = (uint32_t)p.kblocks;
+  const uint32_t t = cur / KB;
+  it.t = (int)t;
+  it.kb0 = (int)(cur - t * KB);
+  const uint32_t room = u1 - cur;
+  it.kb1 = (KB - (uint32_t)it.kb0) < room ? (int)KB : it.kb0 + (int)room;
+  cur += (uint32_t)(it.kb1 - it.kb0);
+  const uint32_t first = t * KB;
+  const uint32_t o0 = owner_of(first, U, G);
+  it.seg = (int)(blockIdx.x - o0);
+  it.nseg = (int)(owner_of(first + KB - 1, U, G) - o0 + 1);
   it.ta = it.t / p.tilesB;
   it.tb = it.t - it.ta * p.tilesB;
   return true;
@@ -309,17 +335,24 @@ __device__ __forceinline__ void reduce_items(const GemmParams &p, int bn, unsign
   }
 }
 
-template <int KIND, int BN, int KS>
+template <int KIND, int BN, int KS, int CG>
 __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small kernels beside it
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
-  using C = Cfg<KIND, BN, KS>;
+  using C = Cfg<KIND, BN, KS, CG>;
   constexpr int S = C::kStages;
   constexpr int CH = C::kChunk;
 
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
+  // the 128-byte swizzle needs 1024-byte aligned stages: they start at the
+  // first 1024-byte boundary after the barriers
+  const uint32_t base = (raw + (uint32_t)C::kBarBytes + 1023u) & ~1023u;
+  if (base + (uint32_t)(C::kStages * C::kStageBytes + C::kEpiBytes) > raw + (uint32_t)C::kSmem) {
+    // (the same for every CTA of the grid: none of them touches anything)
+    if (threadIdx.x == 0 && p.status) atomicOr(p.status, 0x4 /* MXG_DEV_SMEM_LAYOUT */);
+    return;
+  }
   // Stage s is one block of kStageBytes: A codes, B codes, B scales, A scales
   // (every part 1024-byte aligned; an operand's scales follow its codes so
   // that a weight panel -- codes, then scales -- lands with one copy).
@@ -329,20 +362,24 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   auto sfb_smem = [&](int st) { return b_smem(st) + C::kBBytes; };
   auto sfa_smem = [&](int st) { return sfb_smem(st) + C::kSfbBytes; };
   const uint32_t sEpi = sA + S * C::kStageBytes;
-  const uint32_t bars = sEpi + C::kEpiBytes;
-  // mbarriers: per stage full / empty / scales in TMEM (A4W4), then per
-  // accumulator full / empty, the debug stall and the MMA drain
+  const uint32_t bars = raw;
+  // mbarriers: per stage full / empty / ready for the MMAs (A4W4: scales in
+  // TMEM) / landed in the other CTA of a pair (FP8), then per accumulator
+  // full / empty, the debug stall and the MMA drain.  In a CTA pair the even
+  // CTA's MMA thread waits on its own stage_ready / peer_full / acce, which
+  // both CTAs arrive on; its commits land on empty / accf / mma_done of both.
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
   auto sf_ready = [&](int s) { return bars + 8u * (2 * S + s); };
-  const uint32_t acc_bars = bars + 8u * (3 * S);
+  auto peer_full = [&](int s) { return bars + 8u * (3 * S + s); };
+  const uint32_t acc_bars = bars + 8u * (4 * S);
   auto accf = [&](int b) { return acc_bars + 8u * (uint32_t)b; };
   auto acce = [&](int b) { return acc_bars + 16u + 8u * (uint32_t)b; };
   const uint32_t stall_bar = acc_bars + 32;
   const uint32_t mma_done = acc_bars + 40;
   constexpr int kAccBufs = C::kAccBufs;
   static_assert(kAccCol + kAccBufs * BN <= (KIND == 0 ? kSfCol : kTmemCols), "TMEM accumulators");
-  uint8_t *misc = smem_raw + (bars - raw) + 8 * (3 * S + 6);
+  uint8_t *misc = smem_raw + 8 * (4 * S + 6);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 4);
   // A4W4: the epilogue warps (idle during an item's main loop) move each
@@ -350,6 +387,15 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   // tcgen05.cp there would hold up the MMAs behind it in the in-order tensor
   // pipe and, through them, the release of the stage.
   constexpr bool kEpiScales = KIND == 0;
+  // CTA pair: rank in the cluster; the even CTA issues the MMAs
+  const uint32_t crank = CG == 2 ? cluster_rank() : 0u;
+  // arrival on a barrier the (even CTA's) MMA thread waits on
+  auto arrive_mma = [&](uint32_t bar) {
+    if (CG == 2)
+      mbar_arrive_cluster(mapa_shared(bar, 0));
+    else
+      mbar_arrive(bar);
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -370,11 +416,12 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(peer_full(s), 1);
     }
-    for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4);
+    for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4 * CG);
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf(b), 1);
-      mbar_init(acce(b), 4);
+      mbar_init(acce(b), 4 * CG);
     }
     mbar_init(stall_bar, 1);
     mbar_init(mma_done, 1);
@@ -386,11 +433,12 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if (CG == 2) cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
   const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
@@ -407,15 +455,19 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       auto ncol_of = [&](int kb) { return min(KS, p.kc_per_row - kb * KS); };
       // A4W4 scale atoms (512 bytes: 128 rows x 4 blocks of 32) of stage kb
       auto natoms_of = [&](int kb) { return min(2 * KS, p.G4 - 2 * KS * kb); };
+      // a CTA of a pair whose token tile lies past the last one loads no
+      // activations (its output rows are never stored)
+      auto a_in = [&](const Item &it) { return CG == 1 || it.ta < p.tilesA; };
       // the operand and scale bytes one stage receives
       auto stage_bytes = [&](const Item &it, int kb) {
-        uint32_t bytes = (uint32_t)ncol_of(kb) * (C::kAColBytes + C::kBColBytes);
+        const uint32_t na = a_in(it) ? 1u : 0u;
+        uint32_t bytes = (uint32_t)ncol_of(kb) * (na * C::kAColBytes + C::kBColBytes);
         if (KIND == 0) {
           const int rb0 = (it.tb * BN) / 128;
           const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
           // a weight panel as B brings the scales of both halves, padding included
           const int nblk_in = (p.w_panels && !p.swap) ? C::kSfBlocksB : nblk;
-          bytes += (uint32_t)(natoms_of(kb) * 512 * (1 + nblk_in));
+          bytes += (uint32_t)(natoms_of(kb) * 512) * (na + (uint32_t)nblk_in);
         }
         return bytes;
       };
@@ -424,10 +476,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       // column) at (row tile * KC + column) * tile bytes -- else one 128-byte
       // swizzle box per column), its scales, then the B operand (token tiles:
       // one copy; 128-row weight tiles: one per column and row tile; else one
-      // box per column), its scales (one per 128-row block).  Lane i issues
-      // copy i: copies from one converged instruction run in parallel, while
-      // copies that one thread issues one after another complete one after
-      // another (~0.2-0.4 us each).
+      // box per column), its scales (one per 128-row block).  Copy i of a
+      // stage is issued by one lane (copy_of below), all of a stage's copies
+      // in one converged instruction: they run in parallel.
       auto issue_op = [&](int i, bool want_a, bool want_b, int stage, const Item &it, int kb,
                           uint32_t fb) {
         const int nc = ncol_of(kb);
@@ -459,6 +510,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         } else if (want_a) {
           const int na = p.a_tiles ? 1 : nc;
           if (i < na) {
+            if (!a_in(it)) return;
             if (p.a_tiles)
               bulk_load(a_smem(stage),
                         p.a_tiles + ((size_t)it.ta * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kAColBytes,
@@ -471,39 +523,48 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           i -= na;
           if (KIND == 0) {
             if (i == 0) {
-              bulk_load(sfa_smem(stage), p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
-                        natoms_of(kb) * 512, fb, polA);
+              if (a_in(it))
+                bulk_load(sfa_smem(stage), p.sfA + ((size_t)it.ta * p.G4 + 2 * KS * kb) * 512u,
+                          natoms_of(kb) * 512, fb, polA);
               return;
             }
             i -= 1;
           }
         }
         if (want_b && b_pan) {  // BN == 256, one column per stage
-          if (i == 0)
-            bulk_load(b_smem(stage),
-                      p.b_tiles + (size_t)it.e * p.w_group_bytes +
-                          ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes,
-                      (uint32_t)C::kPanelBytes, fb, polB);
+          const uint8_t *blk = p.b_tiles + (size_t)it.e * p.w_group_bytes +
+                               ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * C::kPanelBytes;
+          if (CG == 1) {
+            if (i == 0) bulk_load(b_smem(stage), blk, (uint32_t)C::kPanelBytes, fb, polB);
+          } else {
+            // this CTA's 128-row half of the panel's codes, then (A4W4) the
+            // scales of both halves
+            if (i == 0)
+              bulk_load(b_smem(stage), blk + crank * 16384u, 16384, fb, polB);
+            else if (KIND == 0 && i == 1)
+              bulk_load(sfb_smem(stage), blk + 32768, 2048, fb, polB);
+          }
         } else if (want_b) {
           const bool tok = p.b_tiles && p.b_tile_rows == BN;
-          const int nb = tok ? 1 : p.b_tiles ? nc * (BN >= 128 ? BN / 128 : 1) : nc;
+          constexpr int kRT = C::kBRows >= 128 ? C::kBRows / 128 : 1;  // 128-row weight tiles per column
+          const int nb = tok ? 1 : p.b_tiles ? nc * kRT : nc;
           if (i < nb) {
             if (tok) {
               bulk_load(b_smem(stage),
                         p.b_tiles + ((size_t)it.tb * p.kc_per_row + (size_t)kb * KS) * (size_t)C::kBColBytes,
                         (uint32_t)nc * C::kBColBytes, fb, polB);
             } else if (p.b_tiles) {  // BN >= 128 here (the dispatcher's weight-tile case)
-              constexpr int kRT = BN >= 128 ? BN / 128 : 1;
               const int j = i / kRT, r = i % kRT;
               // a row tile past the last weight row (N % BN != 0) re-reads the last
               // tile: its rows only feed output columns past N, which are not stored
-              const int rt = min(it.tb * kRT + r, (p.rowsB + 127) / 128 - 1);
+              const int rt = min(it.tb * (BN / 128) + (int)crank * kRT + r, (p.rowsB + 127) / 128 - 1);
               bulk_load(b_smem(stage) + j * C::kBColBytes + r * 16384,
                         p.b_tiles + ((size_t)rt * p.kc_per_row + (size_t)kb * KS + j) * 16384u,
                         16384, fb, polB);
             } else {
+              // (CG = 2: the map's box is the CTA's 128 rows)
               tma_load_2d(b_smem(stage) + i * C::kBColBytes, &tmB, (kb * KS + i) * kRowBytes,
-                          it.tb * BN, fb, polB);
+                          it.tb * BN + (int)crank * C::kBRows, fb, polB);
             }
             return;
           }
@@ -513,12 +574,17 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
                       p.sfB + ((size_t)(rb0 + i) * p.G4 + 2 * KS * kb) * 512u, natoms_of(kb) * 512, fb, polB);
         }
       };
+      // Stage k's copies go to lanes 8 (k % 4) .. 8 (k % 4) + 7 (a stage has at
+      // most 7 copies): the copies one thread issues complete one after
+      // another (~0.4 us each, whatever their size), so giving consecutive
+      // stages to different lanes lets them overlap.
+      auto copy_of = [&](long long k) { return (lane - 8 * (int)(k & 3)) & 31; };
       const bool w_is_a = p.swap != 0;
       // stage k of this CTA's sequence: its item and K-stage
       auto stage_of = [&](int k, Item &it, int &kb) -> bool {
-        uint32_t c = first_cursor(p);
+        uint32_t c = first_cursor<CG>(p);
         int n = 0;
-        while (next_item(p, c, it)) {
+        while (next_item<CG>(p, c, it)) {
           const int len = it.kb1 - it.kb0;
           if (k < n + len) {
             kb = it.kb0 + (k - n);
@@ -542,7 +608,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           if (p.early_w) {
             if (lane == 0) mbar_arrive_expect_tx(full_bar(pre), stage_bytes(itk, kbk));
             __syncwarp();
-            issue_op(lane, w_is_a, !w_is_a, pre, itk, kbk, full_bar(pre));
+            issue_op(copy_of(pre), w_is_a, !w_is_a, pre, itk, kbk, full_bar(pre));
           }
           ++pre;
         }
@@ -564,7 +630,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         stage_of(k, itk, kbk);
         const int nc = ncol_of(kbk);
         fc_bar = full_bar(k);
-        if (j == 0) {
+        if (!p.swap && !a_in(itk)) {
+          // nothing to load
+        } else if (j == 0) {
           if (p.swap) {
             fc_dst = b_smem(k);
             fc_src = p.b_tiles + ((size_t)itk.tb * p.kc_per_row + (size_t)kbk * KS) * (size_t)C::kBColBytes;
@@ -606,22 +674,22 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         int kbk = 0;
         stage_of(k, itk, kbk);
         if (p.early_w) {
-          issue_op(lane, !w_is_a, w_is_a, k, itk, kbk, full_bar(k));
+          issue_op(copy_of(k), !w_is_a, w_is_a, k, itk, kbk, full_bar(k));
         } else {
           if (lane == 0) mbar_arrive_expect_tx(full_bar(k), stage_bytes(itk, kbk));
           __syncwarp();
-          issue_op(lane, true, true, k, itk, kbk, full_bar(k));
+          issue_op(copy_of(k), true, true, k, itk, kbk, full_bar(k));
         }
       }
       if (lane == 0) trace_mark(p, kTrFirstLoad);
       // steady state: the whole warp walks the stages in order; lane 0 waits
       // for a free slot and arms it, then every lane issues its copy
-      uint32_t cur = first_cursor(p);
+      uint32_t cur = first_cursor<CG>(p);
       Item it;
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      while (ok && next_item(p, cur, it)) {
+      while (ok && next_item<CG>(p, cur, it)) {
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (issued >= pre) {
             const uint32_t fb = full_bar(stage);
@@ -634,7 +702,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
               ok = false;
               break;
             }
-            issue_op(lane, true, true, stage, it, kb, fb);
+            issue_op(copy_of(issued), true, true, stage, it, kb, fb);
           }
           ++issued;
           if (++stage == S) {
@@ -658,19 +726,46 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc0 = KIND == 0 ? idesc_mxf4(kTileA, BN) : idesc_f8(kTileA, BN);
+    if (lane == 0 && crank != 0) {
+      // the odd CTA of a pair: tell the even CTA's MMA thread when each FP8
+      // stage has landed here (A4W4: the epilogue warps' scale feed does)
+      pdl_wait();
+      if (KIND == 1) {
+        uint32_t cur = first_cursor<CG>(p);
+        Item it;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        while (ok && next_item<CG>(p, cur, it)) {
+          for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, ctl)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(mapa_shared(peer_full(stage), 0));
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      // the even CTA's last commit: every MMA that reads this CTA's shared
+      // memory or writes its TMEM is done
+      drain_wait(mma_done, 0, p.timeout_ns, p.status);
+    } else if (lane == 0) {
+      const uint32_t idesc0 = KIND == 0 ? idesc_mxf4(kTileA * CG, BN) : idesc_f8(kTileA * CG, BN);
       // the bounded waits below start counting only once the kernels this
       // one depends on have finished
       pdl_wait();
       trace_mark(p, kTrWaited);
-      uint32_t cur = first_cursor(p);
+      uint32_t cur = first_cursor<CG>(p);
       Item it;
       int stage = 0;
       uint32_t phase = 0;
       int i = 0;
       bool ok = true;
-      while (ok && next_item(p, cur, it)) {
+      while (ok && next_item<CG>(p, cur, it)) {
         // accumulator b of item i; its use-th use: wait until the epilogue
         // has read out its previous tile
         const int b = i % kAccBufs, use = i / kAccBufs;
@@ -678,9 +773,13 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         if (use > 0 && !mbar_wait(acce(b), (uint32_t)((use - 1) & 1), ctl)) break;
         tc_fence_after();
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          // full tile A4W4: the epilogue warps signal once the stage's data is
-          // in and its scales are in TMEM
-          if (!mbar_wait(kEpiScales ? sf_ready(stage) : full_bar(stage), phase, ctl)) {
+          // A4W4: the epilogue warps (of both CTAs of a pair) signal once the
+          // stage's data is in and its scales are in TMEM; FP8: the stage's
+          // data is in (here, and in the other CTA of a pair)
+          const bool landed = kEpiScales ? mbar_wait(sf_ready(stage), phase, ctl)
+                                         : (mbar_wait(full_bar(stage), phase, ctl) &&
+                                            (CG == 1 || mbar_wait(peer_full(stage), phase, ctl)));
+          if (!landed) {
             ok = false;
             break;
           }
@@ -695,46 +794,35 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
           auto b_desc = [&](int s) {
             return sdesc_kmajor_sw128(b0 + (uint32_t)(s >> 2) * C::kBColBytes + 32u * (s & 3));
           };
-          if (KIND == 0) {
-            // scale factors: smem -> the TMEM columns of this ring slot
-            const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
-            const int rb0 = (it.tb * BN) / 128;
-            const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+          if constexpr (KIND == 0) {
+            // this ring slot's scale factors, fed into TMEM by the epilogue warps
             const uint32_t sfa_t = tmem + kSfCol + (uint32_t)stage * C::kSfColsPerStage;
             const uint32_t sfb_t = sfa_t + C::kSfColsA;
-            if (!kEpiScales) {
-              for (int a = 0; a < natoms; ++a)
-                tc_cp_sf(sfa_t + 4 * a, sdesc_sf_block(sfa_smem(stage) + a * 512));
-              for (int j = 0; j < nblk; ++j)
-                for (int a = 0; a < natoms; ++a)
-                  tc_cp_sf(sfb_t + 4 * C::kSfBlocksB * a + 4 * j,
-                           sdesc_sf_block(sfb_smem(stage) + j * (1024 * KS) + a * 512));
-            }
             const int nk = min(C::kSteps, (p.K - kb * 256 * KS) / 64);
             for (int s = 0; s < nk; ++s) {
               const uint32_t sel = (uint32_t)(s & 1) * 2u;
-              mma_mxf4(d_acc, a_desc(s), b_desc(s), idesc_sf_ids(idesc0, sel, sel),
-                       sfa_t + 4 * (s >> 1), sfb_t + 4 * C::kSfBlocksB * (s >> 1),
-                       (kb > it.kb0 || s > 0) ? 1u : 0u);
+              mma_mxf4<CG>(d_acc, a_desc(s), b_desc(s), idesc_sf_ids(idesc0, sel, sel),
+                           sfa_t + 4 * (s >> 1), sfb_t + 4 * C::kSfBlocksB * (s >> 1),
+                           (kb > it.kb0 || s > 0) ? 1u : 0u);
             }
           } else {
             const int nk = min(C::kSteps, (p.K - kb * 128 * KS) / 32);
             for (int s = 0; s < nk; ++s)
-              mma_f8(d_acc, a_desc(s), b_desc(s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
+              mma_f8<CG>(d_acc, a_desc(s), b_desc(s), idesc0, (kb > it.kb0 || s > 0) ? 1u : 0u);
           }
-          tc_commit(empty_bar(stage));
+          tc_commit<CG>(empty_bar(stage));
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(accf(b));
+        tc_commit<CG>(accf(b));
         trace_mark(p, kTrLastCommit);
         ++i;
       }
       // every MMA issued so far must finish before TMEM is released
-      tc_commit(mma_done);
+      tc_commit<CG>(mma_done);
       drain_wait(mma_done, 0, p.timeout_ns, p.status);
     }
   } else {
@@ -748,27 +836,61 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     // atoms go smem -> registers -> this warp's TMEM lane quarter, in the
     // layout tcgen05.cp 32x128b.warpx4 makes (lane 32q+i, columns c..c+3 =
     // the atom's 16-byte row i, in every quarter q).
-    auto feed = [&](const Item &it) -> bool {
-      for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
-        const int st = (int)(q_sf % S);
-        if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) return false;
-        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
-        const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
-        const int rb0 = (it.tb * BN) / 128;
-        const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
-        const uint32_t sfb_col = sfa_col + C::kSfColsA;
+    // One stage's scale factors: smem -> registers -> this warp's TMEM lane
+    // quarter.
+    auto feed_stage = [&](const Item &it, int kb, int st) {
+      const int natoms = min(2 * KS, p.G4 - 2 * KS * kb);
+      const int rb0 = (it.tb * BN) / 128;
+      const int nblk = min(C::kSfBlocksB, (p.rowsB + 127) / 128 - rb0);
+      const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+      const uint32_t sfa_col = tmem + lane_base + kSfCol + (uint32_t)st * C::kSfColsPerStage;
+      const uint32_t sfb_col = sfa_col + C::kSfColsA;
+      if (natoms == 2 * KS && nblk == C::kSfBlocksB) {
+        // a whole stage: its columns are contiguous (A atoms, then B atom a
+        // of block j at 4 (blocks a + j)), gathered into registers and
+        // stored with as few wide stores as there are 32 / 16 / 8 columns
+        constexpr int NC = (int)C::kSfColsPerStage;
+        uint32_t v[NC];
+  #pragma unroll
+        for (int a = 0; a < 2 * KS; ++a) {
+          const uint4 w = ld_shared_v4(sfa_smem(st) + a * 512 + lane * 16);
+          v[4 * a] = w.x, v[4 * a + 1] = w.y, v[4 * a + 2] = w.z, v[4 * a + 3] = w.w;
+        }
+  #pragma unroll
+        for (int j = 0; j < C::kSfBlocksB; ++j)
+  #pragma unroll
+          for (int a = 0; a < 2 * KS; ++a) {
+            const uint4 w = ld_shared_v4(sfb_smem(st) + j * (1024 * KS) + a * 512 + lane * 16);
+            const int c = (int)C::kSfColsA + 4 * (C::kSfBlocksB * a + j);
+            v[c] = w.x, v[c + 1] = w.y, v[c + 2] = w.z, v[c + 3] = w.w;
+          }
+        int c = 0;
+  #pragma unroll
+        for (; c + 32 <= NC; c += 32) tmem_st32(sfa_col + c, v + c);
+        if constexpr (NC % 32 >= 16) {
+          tmem_st16(sfa_col + c, v + c);
+          c += 16;
+        }
+        if constexpr (NC % 16 >= 8) tmem_st8(sfa_col + c, v + c);
+      } else {
         for (int a = 0; a < natoms; ++a)
           tmem_st4(sfa_col + 4 * a, ld_shared_v4(sfa_smem(st) + a * 512 + lane * 16));
         for (int j = 0; j < nblk; ++j)
           for (int a = 0; a < natoms; ++a)
             tmem_st4(sfb_col + 4 * C::kSfBlocksB * a + 4 * j,
                      ld_shared_v4(sfb_smem(st) + j * (1024 * KS) + a * 512 + lane * 16));
+      }
+    };
+    auto feed = [&](const Item &it) -> bool {
+      for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
+        const int st = (int)(q_sf % S);
+        if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) return false;
+        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
+        feed_stage(it, kb, st);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(sf_ready(st));
+        if (lane == 0) arrive_mma(sf_ready(st));
         if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
       }
       return true;
@@ -793,11 +915,13 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       if (whole && !p.swap && KS == 1 && p.y_tma) {
         // rows = tokens, columns = output channels; per 32-column chunk the
         // warp's 32 x 32 bf16 box goes registers -> smem -> one TMA store
-        // (rows past M and columns past N are clipped by the tensor map)
+        // (rows past M and columns past N are clipped by the tensor map; a
+        // box wholly past M is not stored)
         const float sa = (KIND == 1 && ra < p.M) ? p.tok_scale[ra] : 1.0f;
         const uint32_t ebuf = sEpi + (uint32_t)(warp - 2) * 4096u;
+        const bool box_in = it.ta * kTileA + q * 32 < p.M;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < (box_in ? BN / 32 : 0); ++c) {
           uint32_t v[32];
           tmem_ld_chunk<32>(t_acc + c * 32, v);
           tmem_ld_wait();
@@ -915,19 +1039,19 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
       // hand the accumulator back to the MMA warp once its TMEM reads are done
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce(acc_b));
+      if (lane == 0) arrive_mma(acce(acc_b));
       if (threadIdx.x == 64 && i < 2) trace_mark(p, i == 0 ? kTrItem0Done : kTrItem1Done);
       return true;
     };
     // Feed ahead: with two accumulators, the scales of item i+1 go into TMEM
     // before item i is read out, so that the MMAs of item i+1 run while the
     // epilogue stores item i.
-    uint32_t cur = first_cursor(p);
+    uint32_t cur = first_cursor<CG>(p);
     Item it, held;  // held: fed, not yet finished (two accumulators only)
     bool holding = false;
     int i_fin = 0;
     bool ok = true;
-    while (ok && next_item(p, cur, it)) {
+    while (ok && next_item<CG>(p, cur, it)) {
       if (kEpiScales && !feed(it)) {
         ok = false;
         break;
@@ -952,13 +1076,17 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
 
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA releases its TMEM or leaves (its shared memory and
+  // barriers are the other's MMA operands and arrival targets) before both
+  // are done
+  if (CG == 2) cluster_sync();
   if (threadIdx.x == 0) {
     trace_mark(p, kTrExit);
     trace_set(p, kTrExitNs, global_timer_ns());
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc<CG>(tmem, kTmemCols);
   }
 }
 
@@ -977,11 +1105,11 @@ __global__ void __maxnreg__(64)  // 128-thread CTAs, 3 of them beside a GEMM CTA
   }
 }
 
-template <int KIND, int BN, int KS>
+template <int KIND, int BN, int KS, int CG = 1>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmY,
                      const GemmParams &p, int ctas, cudaStream_t stream) {
-  using C = Cfg<KIND, BN, KS>;
-  auto kern = gemm_kernel<KIND, BN, KS>;
+  using C = Cfg<KIND, BN, KS, CG>;
+  auto kern = gemm_kernel<KIND, BN, KS, CG>;
   static DeviceOnce once;  // per instantiation and device (a repeat sets the same value)
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -991,9 +1119,18 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUten
     if (e != cudaSuccess) return e;
     once.set(dev);
   }
+  if (CG == 2 && (ctas % 2) != 0) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attach_pdl(cfg, attr);
+  if (CG == 2) {  // clusters of two CTAs (a portable cluster size)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+    attr[cfg.numAttrs].val.clusterDim.x = 2;
+    attr[cfg.numAttrs].val.clusterDim.y = 1;
+    attr[cfg.numAttrs].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
+  }
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmY, p);
 }
 
@@ -1001,8 +1138,11 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUten
 template <int KIND>
 cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmY,
                         const GemmParams &p, int ctas, cudaStream_t stream) {
-  if (!p.splitk)
-    return bn == 256 ? launch_t<KIND, 256, 1>(tmA, tmB, tmY, p, ctas, stream) : cudaErrorInvalidValue;
+  if (!p.splitk) {
+    if (bn != 256) return cudaErrorInvalidValue;
+    return p.cta_pair ? launch_t<KIND, 256, 1, 2>(tmA, tmB, tmY, p, ctas, stream)
+                      : launch_t<KIND, 256, 1, 1>(tmA, tmB, tmY, p, ctas, stream);
+  }
   switch (bn) {
     case 16: return launch_t<KIND, 16, 2>(tmA, tmB, tmY, p, ctas, stream);
     case 32: return launch_t<KIND, 32, 2>(tmA, tmB, tmY, p, ctas, stream);
@@ -1010,32 +1150,6 @@ cudaError_t launch_kind(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, 
     case 128: return launch_t<KIND, 128, 2>(tmA, tmB, tmY, p, ctas, stream);
     case 256: return launch_t<KIND, 256, 2>(tmA, tmB, tmY, p, ctas, stream);
     default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int KIND>
-int stages_kind(int bn, bool splitk) {
-  if (!splitk) return bn == 256 ? Cfg<KIND, 256, 1>::kStages : 0;
-  switch (bn) {
-    case 16: return Cfg<KIND, 16, 2>::kStages;
-    case 32: return Cfg<KIND, 32, 2>::kStages;
-    case 64: return Cfg<KIND, 64, 2>::kStages;
-    case 128: return Cfg<KIND, 128, 2>::kStages;
-    case 256: return Cfg<KIND, 256, 2>::kStages;
-    default: return 0;
-  }
-}
-
-template <int KIND>
-size_t smem_kind(int bn, bool splitk) {
-  if (!splitk) return bn == 256 ? Cfg<KIND, 256, 1>::kSmem : 0;
-  switch (bn) {
-    case 16: return Cfg<KIND, 16, 2>::kSmem;
-    case 32: return Cfg<KIND, 32, 2>::kSmem;
-    case 64: return Cfg<KIND, 64, 2>::kSmem;
-    case 128: return Cfg<KIND, 128, 2>::kSmem;
-    case 256: return Cfg<KIND, 256, 2>::kSmem;
-    default: return 0;
   }
 }
 
@@ -1137,14 +1251,6 @@ cudaError_t launch_gemm(int kind, int bn, const CUtensorMap &tmA, const CUtensor
                         const CUtensorMap &tmY, const GemmParams &p, int ctas, cudaStream_t stream) {
   return kind == 0 ? launch_kind<0>(bn, tmA, tmB, tmY, p, ctas, stream)
                    : launch_kind<1>(bn, tmA, tmB, tmY, p, ctas, stream);
-}
-
-int gemm_stages(int kind, int bn, bool splitk) {
-  return kind == 0 ? stages_kind<0>(bn, splitk) : stages_kind<1>(bn, splitk);
-}
-
-size_t gemm_smem_bytes(int kind, int bn, bool splitk) {
-  return kind == 0 ? smem_kind<0>(bn, splitk) : smem_kind<1>(bn, splitk);
 }
 
 int gemm_cols_per_stage(bool splitk) { return splitk ? 2 : 1; }

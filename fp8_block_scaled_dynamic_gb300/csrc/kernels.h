@@ -36,16 +36,6 @@ inline void attach_pdl(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[N]) 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
 }
-// MXG_NO_COOPERATIVE=1 launches the grid-synchronised GEMM without the
-// cooperative attribute (for A/B timing; co-residency is then only likely).
-inline bool cooperative_enabled() {
-  static const bool on = [] {
-    const char *e = std::getenv("MXG_NO_COOPERATIVE");
-    return !(e && e[0] == '1');
-  }();
-  return on;
-}
-
 // Small kernels (quantizers, split-K reduce) run beside, and just before,
 // GEMM CTAs that need ~210 KB of shared memory.  An SM whose L1/shared split
 // was set for an L1-preferring kernel cannot take a GEMM CTA until it drains,
@@ -129,6 +119,9 @@ struct GemmParams {
   int kc_per_row;          // 128-byte chunks per operand row (tile layout)
   int raster_group;        // full tile: 0 = tiles in row order (token tile slowest), else
                            //   bands of this many token tiles, the token tile fastest
+  int cta_pair;            // full tile: 1 = clusters of two CTAs issuing 2-SM MMAs over
+                           //   256-token x 256-channel tiles (each CTA holds 128 token rows
+                           //   and one 128-row half of the weight tile)
   int early_w;         // 1: no kernel still in flight writes the weights, so their first
                        //    stages may load before griddepcontrol.wait
   int y_tma;           // full tile, bf16 out: the epilogue stores y through tensor map tmY
@@ -186,8 +179,6 @@ cudaError_t launch_mma_peak(int kind, int bn, int iters, int sm_count, int *stat
 // Pipeline stages a (kind, bn, variant) kernel uses, its dynamic shared
 // memory, and the 128-byte K columns one stage covers (p.kblocks counts
 // stages of that many columns).
-int gemm_stages(int kind, int bn, bool splitk);
-size_t gemm_smem_bytes(int kind, int bn, bool splitk);
 int gemm_cols_per_stage(bool splitk);
 
 }  // namespace mxg

@@ -76,6 +76,9 @@ typedef enum {
 /* Bits a kernel ORs into the optional device status word. */
 #define MXG_DEV_TIMEOUT 0x1
 #define MXG_DEV_BAD_INDEX 0x2
+#define MXG_DEV_SMEM_LAYOUT 0x4 /* a GEMM CTA found its dynamic shared memory less aligned than
+                                   its layout needs and did nothing (never seen; reported as
+                                   MXG_ERR_CUDA) */
 
 typedef enum {
     MXG_SF_ROWMAJOR = 0, /* (rows, K/32) bytes, row-major: the stored checkpoint layout */
@@ -170,6 +173,13 @@ typedef struct {
                              MXG_ERR_INVALID_ARG.  On the fused A4W4 path (x given) the
                              call launches the activation quantizer, the GEMM and the
                              reduce kernel, chained by programmatic dependent launch. */
+    int cta_pair;         /* FULL variant, M > 128: 1 = run the tiles on clusters of two CTAs
+                             issuing 2-SM MMAs (tcgen05 cta_group::2) over 256-token x
+                             256-channel tiles, each CTA holding 128 token rows and one
+                             128-row half of the weight tile (a third fewer operand bytes
+                             per flop); 0 (default) = one CTA per 128 x 256 tile, which
+                             measured faster on this part (the MMA issue loop, not operand
+                             bytes, bounds both).  Not for mx_gemm_a4w4_grouped (must be 0). */
 } mxg_gemm_opts;
 
 enum {
@@ -179,7 +189,8 @@ enum {
 
 typedef struct {
     int variant;       /* MXG_VARIANT_FULL or MXG_VARIANT_SPLITK */
-    int bm, bn;        /* MMA tile: bm rows of the 128-row operand, bn of the other */
+    int bm, bn;        /* output tile: bm rows of the MMA-A operand (tokens for FULL,
+                          weight rows for SPLITK), bn of the MMA-B operand */
     int ctas;          /* grid size */
     int tiles;         /* output tiles */
     int kblocks;       /* pipeline stages along K per tile: 128-byte K columns (256 K
@@ -187,7 +198,11 @@ typedef struct {
                           SPLITK */
     int seg_max;       /* SPLITK: most CTAs contributing to one tile */
     size_t ws_bytes;   /* workspace this plan needs (partial tiles) */
-    int reserved;      /* always 0 */
+    int cta_pair;      /* FULL: 1 = clusters of two CTAs issuing 2-SM MMAs (tcgen05
+                          cta_group::2) over 256-token x 256-channel tiles, each CTA holding
+                          128 token rows and one 128-row half of the weight tile (requested
+                          with mxg_gemm_opts.cta_pair and M > 128); 0 = one CTA per
+                          128 x 256 tile */
 } mxg_plan;
 
 /* Bytes of a scale-factor array for `rows` rows of K elements (K/32 groups).

@@ -160,7 +160,7 @@ def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
 def test_plan_full_tile_for_large_m():
     p = mx.mxg_plan_gemm(0, 8192, 7168, 8192, 152)
     assert p["variant"] == 1 and p["bn"] == 256 and p["tiles"] == 64 * 28 and p["ctas"] == 152
-    assert p["ws_bytes"] == 0
+    assert p["ws_bytes"] == 0 and p["cta_pair"] == 0
     p = mx.mxg_plan_gemm(1, 300, 384, 1024, 152, variant="splitk")
     assert p["variant"] == 2 and p["bn"] == 256 and p["tiles"] == 3 * 2
 
@@ -181,7 +181,7 @@ def test_only_the_reduce_kernel_is_a_split_k_reduction():
         o.splitk_reduce = v
         assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, 0, ctypes.byref(o), None) == 1
     p = mx.mxg_plan_gemm(0, 64, 7168, 8192, 152, variant="splitk")
-    assert p["reserved"] == 0 and p["ws_bytes"] == p["tiles"] * p["seg_max"] * p["bn"] * 128 * 4
+    assert p["cta_pair"] == 0 and p["ws_bytes"] == p["tiles"] * p["seg_max"] * p["bn"] * 128 * 4
 
 
 @pytest.mark.parametrize("kind,M,N,K,want", [
@@ -233,3 +233,31 @@ def test_grouped_argument_errors_before_launch():
     # workspace: token tiles for ceil(M / 128) + E tiles, plus the tile offsets
     assert mx.mxg_grouped_workspace_bytes(300, 1024, 4) >= (3 + 4) * 128 * (1024 // 2 + 1024 // 32)
     assert mx.mxg_grouped_workspace_bytes(300, 1024, 0) == 0
+
+
+@pytest.mark.parametrize("kind,M,N,K,pair,tiles,ctas", [
+    # one token tile: one CTA per 128 x 256 tile even when pairs are asked for
+    (1, 64, 36864, 7168, 0, 144, 144), (0, 100, 7168, 8192, 0, 28, 28),
+    # two token tiles or more: CTA pairs over 256 x 256 tiles, one pair per two SMs
+    (0, 192, 7168, 8192, 1, 28, 56), (0, 8192, 7168, 8192, 1, 32 * 28, 152),
+    (1, 8192, 36864, 7168, 1, 32 * 144, 152), (1, 300, 7168, 18432, 1, 2 * 28, 112),
+])
+def test_full_tile_cta_pairs(kind, M, N, K, pair, tiles, ctas):
+    """On request (cta_pair) the full tile runs on CTA pairs (2-SM MMAs,
+    256-token x 256-channel tiles) when there are two token tiles or more;
+    the grid is even and holds at most one pair per two SMs.  Without the
+    request it never does."""
+    p = mx.mxg_plan_gemm(kind, M, N, K, 152, variant="full", cta_pair=True)
+    assert p["variant"] == 1 and p["cta_pair"] == pair and p["tiles"] == tiles and p["ctas"] == ctas
+    assert p["bm"] == (256 if pair else 128) and p["bn"] == 256
+    if pair:
+        assert p["ctas"] % 2 == 0
+    q = mx.mxg_plan_gemm(kind, M, N, K, 152, variant="full")
+    assert q["cta_pair"] == 0 and q["bm"] == 128
+
+
+def test_cta_pair_argument_checked():
+    """cta_pair must be 0 or 1, and 0 for the grouped GEMM; refused before launch."""
+    L = mx.lib()
+    o = mx.GemmOpts(cta_pair=2)
+    assert L.fp8_gemm_ptpc(FAKE, FAKE, FAKE, FAKE, 8, 128, 128, FAKE, 128, 0, ctypes.byref(o), None) == 1
