@@ -42,7 +42,6 @@
 namespace mxg {
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kTileA = 128;      // MMA M: rows of the MMA-A operand per tile
 constexpr int kRowBytes = 128;   // K bytes per row per stage (one 128-byte swizzle row)
 constexpr uint32_t kTmemCols = 512;
@@ -76,8 +75,16 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   // one column of a 256-row weight panel: codes, then (E2M1) the 2 x 2 scale atoms
   static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
-  // full tile: per epilogue warp two 32 x 32 bf16 staging boxes for TMA stores of y
-  static constexpr int kEpiBytes = KS == 1 ? 4 * 2 * 2048 : 0;
+  // Epilogue warps: one set of four (one per TMEM lane quarter), or, for
+  // the A4W4 full tile, two sets that feed alternate stages' scale factors
+  // (a stage's feed waits for its data and for its TMEM stores, so one set
+  // alone paces the MMAs) and read out half of the accumulator's columns
+  // each.  Full tile: per epilogue warp one (two sets) or two 32 x 32 bf16
+  // staging boxes for the TMA stores of y.
+  static constexpr int kEpiSets = (KIND == 0 && KS == 1) ? 2 : 1;
+  static constexpr int kThreads = 64 + 128 * kEpiSets;
+  static constexpr int kEpiBufs = kEpiSets == 2 ? 1 : 2;
+  static constexpr int kEpiBytes = KS == 1 ? 4 * kEpiSets * kEpiBufs * 2048 : 0;
   static constexpr int kStagesRaw = (kSmemMax - kSmemHead - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kBarBytes = 8 * (4 * kStages + 6) + 8;  // mbarriers, TMEM base, abort flag
@@ -421,7 +428,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     for (int st = 0; st < S; ++st) mbar_init(sf_ready(st), 4 * CG);
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf(b), 1);
-      mbar_init(acce(b), 4 * CG);
+      mbar_init(acce(b), 4 * CG * C::kEpiSets);
     }
     mbar_init(stall_bar, 1);
     mbar_init(mma_done, 1);
@@ -828,6 +835,9 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int eset = (warp - 2) >> 2;  // epilogue warp set
+    constexpr int kSetCols = BN / C::kEpiSets;  // accumulator columns this set reads out
+    const int c_lo = eset * kSetCols;
     const int r_in = q * 32 + lane;    // row of the MMA-A tile
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + kAccCol;
     pdl_wait();  // scales and partial tiles may come from the kernel ahead
@@ -883,15 +893,16 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
     };
     auto feed = [&](const Item &it) -> bool {
       for (int kb = it.kb0; kb < it.kb1; ++kb, ++q_sf) {
+        if (C::kEpiSets == 2 && (int)(q_sf & 1) != eset) continue;  // the other set's stage
         const int st = (int)(q_sf % S);
         if (!warp_wait(full_bar(st), (uint32_t)((q_sf / S) & 1), ctl)) return false;
-        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
+        if (p.trace && q == 2 && lane == 0 && q_sf < 8) trace_mark(p, kTrStageLanded + (int)q_sf);
         feed_stage(it, kb, st);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_mma(sf_ready(st));
-        if (p.trace && threadIdx.x == 64 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
+        if (p.trace && q == 2 && lane == 0 && q_sf < 8) trace_mark(p, kTrStageFed + (int)q_sf);
       }
       return true;
     };
@@ -918,10 +929,10 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         // (rows past M and columns past N are clipped by the tensor map; a
         // box wholly past M is not stored)
         const float sa = (KIND == 1 && ra < p.M) ? p.tok_scale[ra] : 1.0f;
-        const uint32_t ebuf = sEpi + (uint32_t)(warp - 2) * 4096u;
+        const uint32_t ebuf = sEpi + (uint32_t)(warp - 2) * (C::kEpiBufs * 2048u);
         const bool box_in = it.ta * kTileA + q * 32 < p.M;
 #pragma unroll 1
-        for (int c = 0; c < (box_in ? BN / 32 : 0); ++c) {
+        for (int c = c_lo / 32; c < (box_in ? (c_lo + kSetCols) / 32 : 0); ++c) {
           uint32_t v[32];
           tmem_ld_chunk<32>(t_acc + c * 32, v);
           tmem_ld_wait();
@@ -936,9 +947,15 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
             }
             w[j] = pack_bf16x2(f0, f1);
           }
-          const uint32_t buf = ebuf + (uint32_t)(c & 1) * 2048u;
-          if (c >= 2) {  // the box written two chunks ago must have been read out
-            if (lane == 0) bulk_wait_group_read<1>();
+          const int j = c - c_lo / 32;  // this warp's chunk count
+          const uint32_t buf = ebuf + (uint32_t)(j % C::kEpiBufs) * 2048u;
+          if (j >= C::kEpiBufs) {  // the box last written here must have been read out
+            if (lane == 0) {
+              if (C::kEpiBufs == 2)
+                bulk_wait_group_read<1>();
+              else
+                bulk_wait_group_read<0>();
+            }
             __syncwarp();
           }
 #pragma unroll
@@ -965,7 +982,7 @@ __global__ void __maxnreg__(136)  // 26K registers a CTA: room for the small ker
         }
         const float sa = (KIND == 1 && mvalid) ? p.tok_scale[yr] : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / CH; ++c) {
+        for (int c = c_lo / CH; c < (c_lo + kSetCols) / CH; ++c) {
           uint32_t v[CH];
           tmem_ld_chunk<CH>(t_acc + c * CH, v);
           tmem_ld_wait();
@@ -1120,7 +1137,7 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUten
     once.set(dev);
   }
   if (CG == 2 && (ctas % 2) != 0) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(kThreads), C::kSmem, stream);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(ctas), dim3(C::kThreads), C::kSmem, stream);
   cudaLaunchAttribute attr[2];
   attach_pdl(cfg, attr);
   if (CG == 2) {  // clusters of two CTAs (a portable cluster size)
