@@ -28,7 +28,6 @@ namespace mxg {
 namespace {
 
 constexpr int kMxThreads = 256;
-constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in flight per thread
 
 // grid: x = chunk groups along the row, y = rows (grid-stride).
 // rows_iter >= rows: rows in [rows, rows_iter) are padding (swizzled layout
@@ -36,7 +35,11 @@ constexpr int kMxChunksPerThread = 2;  // two independent 16-byte loads in fligh
 // tile_rows: 0 = row-major codes, kPanelLayout = weight panels (codes and
 // scales; padding rows get zero codes), else the tile layout with that tile
 // height.
-template <bool kSwizzled>
+// CPT: 16-byte chunks per thread per row, independent loads in flight (4 for
+// large inputs: a CTA covers a whole 8192-value row and its per-row address
+// work is shared by more chunks; 2 for decode-sized inputs, whose latency
+// wants more, smaller CTAs).
+template <bool kSwizzled, int CPT>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
                                                               long long ldx, int rows,
                                                               int rows_iter, int K, int tile_rows,
@@ -54,8 +57,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   // Warm L2 with this CTA's part of its first row while the kernel ahead
   // finishes; the loads below come after the wait.
   if (threadIdx.x == 0 && (int)blockIdx.y < rows) {
-    const int c0 = blockIdx.x * kMxChunksPerThread * kMxThreads;
-    const int nc = min(kMxChunksPerThread * kMxThreads, cpr - c0);
+    const int c0 = blockIdx.x * CPT * kMxThreads;
+    const int nc = min(CPT * kMxThreads, cpr - c0);
     if (nc > 0) prefetch_l2_bulk(x + (size_t)blockIdx.y * ldx + (size_t)c0 * 8, (uint32_t)nc * 16u);
   }
   // x may be the previous kernel's output and codes/sf may still be read by it
@@ -63,22 +66,22 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   const bool panel = tile_rows == kPanelLayout;
   const int KC = K >> 8;  // 128-byte code columns per row
   const int t_shift = (tile_rows > 0) ? __ffs(tile_rows) - 1 : 0;  // tile_rows is a power of 2
-  int cc[kMxChunksPerThread];
+  int cc[CPT];
 #pragma unroll
-  for (int i = 0; i < kMxChunksPerThread; ++i) cc[i] = (blockIdx.x * kMxChunksPerThread + i) * kMxThreads + threadIdx.x;
-  auto load_row = [&](int r, uint4 (&v)[kMxChunksPerThread]) {
+  for (int i = 0; i < CPT; ++i) cc[i] = (blockIdx.x * CPT + i) * kMxThreads + threadIdx.x;
+  auto load_row = [&](int r, uint4 (&v)[CPT]) {
 #pragma unroll
-    for (int i = 0; i < kMxChunksPerThread; ++i) {
+    for (int i = 0; i < CPT; ++i) {
       v[i] = make_uint4(0u, 0u, 0u, 0u);
       if (r < rows && cc[i] < cpr) v[i] = ld_stream_v4(x + (size_t)r * ldx + (size_t)cc[i] * 8);
     }
   };
-  uint4 v[kMxChunksPerThread];
+  uint4 v[CPT];
   int r = blockIdx.y;
   if (r < rows_iter) load_row(r, v);
   for (; r < rows_iter; r += gridDim.y) {
     // the next row's loads go out before this row's arithmetic
-    uint4 vn[kMxChunksPerThread] = {};
+    uint4 vn[CPT] = {};
     if (r + (int)gridDim.y < rows_iter) load_row(r + gridDim.y, vn);
     const bool real_row = r < rows;
     // where this row's codes go: column c of the row at row_base + c *
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       rsw = 0;
     }
 #pragma unroll
-    for (int i = 0; i < kMxChunksPerThread; ++i) {
+    for (int i = 0; i < CPT; ++i) {
       // cpr % 16 == 0: a half-warp is wholly inside the row or wholly past
       // it; past the row it runs on zeros (the shuffles need every lane)
       // and stores nothing.
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       }
     }
 #pragma unroll
-    for (int i = 0; i < kMxChunksPerThread; ++i) v[i] = vn[i];
+    for (int i = 0; i < CPT; ++i) v[i] = vn[i];
   }
 }
 
@@ -204,13 +207,38 @@ __device__ __forceinline__ uint32_t amax_bf16x8(const uint4 &w) {
   return max(m2 & 0xFFFFu, m2 >> 16);
 }
 
-// 8 bf16 values -> 8 E4M3 bytes: q = E4M3_RNE_sat(x / s) (IEEE division),
-// the sign of x kept on codes that round to zero.
-__device__ __forceinline__ uint2 fp8_quant8(const uint4 &w, float s) {
-  uint32_t lo = e4m3x2(__fdiv_rn(bf16_lo(w.x), s), __fdiv_rn(bf16_hi(w.x), s)) |
-                (e4m3x2(__fdiv_rn(bf16_lo(w.y), s), __fdiv_rn(bf16_hi(w.y), s)) << 16);
-  uint32_t hi = e4m3x2(__fdiv_rn(bf16_lo(w.z), s), __fdiv_rn(bf16_hi(w.z), s)) |
-                (e4m3x2(__fdiv_rn(bf16_lo(w.w), s), __fdiv_rn(bf16_hi(w.w), s)) << 16);
+// x / s for the values x of one row and its scale s, rounded as the IEEE
+// division is where it decides a code.  Markstein's correction step (P.
+// Markstein, "IA-64 and Elementary Functions: Speed and Precision", 2000):
+// with r = RN(1/s), q = RN(x r) and the exact residual e = x - q s (one
+// FMA), RN(q + e r) is the correctly rounded quotient -- three operations a
+// value instead of a division.  Checked exhaustively on GB300 over the
+// quantizers' whole domain (every bf16 x with |x| <= amax, every finite bf16
+// amax with s = RN(amax / 448) >= 2^-100): the quotient equals the IEEE one
+// bit for bit wherever |x / s| >= 2^-10 (below, every quotient encodes to
+// +-0), and the E4M3 codes are the same everywhere once the sign of x is
+// set on the code, as fp8_quant8 does.  Rows with a smaller s (the residual
+// would underflow) divide.
+struct RowDivisor {
+  float s, r;
+  bool fast;
+  __device__ __forceinline__ explicit RowDivisor(float s_) {
+    s = s_;
+    r = __fdiv_rn(1.0f, s_);
+    fast = s_ >= 7.8886090522101181e-31f;  // 2^-100
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    if (!fast) return __fdiv_rn(x, s);
+    const float q = __fmul_rn(x, r);
+    return __fmaf_rn(__fmaf_rn(-q, s, x), r, q);
+  }
+};
+
+// 8 bf16 values -> 8 E4M3 bytes: q = E4M3_RNE_sat(x / s), the sign of x kept
+// on codes that round to zero.
+__device__ __forceinline__ uint2 fp8_quant8(const uint4 &w, const RowDivisor &d) {
+  uint32_t lo = e4m3x2(d(bf16_lo(w.x)), d(bf16_hi(w.x))) | (e4m3x2(d(bf16_lo(w.y)), d(bf16_hi(w.y))) << 16);
+  uint32_t hi = e4m3x2(d(bf16_lo(w.z)), d(bf16_hi(w.z))) | (e4m3x2(d(bf16_lo(w.w)), d(bf16_hi(w.w))) << 16);
   lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
   hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
   return make_uint2(lo, hi);
@@ -303,7 +331,68 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
-    for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = fp8_quant8(ld_keep_v4(xr + (size_t)c * 8), s);
+    const RowDivisor dv(s);
+    for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = fp8_quant8(ld_keep_v4(xr + (size_t)c * 8), dv);
+  }
+}
+
+// The same per-row FP8 quantization for large inputs with K <= 8192: one
+// read of the row, held in registers (kF8Hold chunks of 8 values per thread)
+// between its amax and its codes.  (The two-pass kernel above, at 40
+// registers, is kept for decode-sized inputs, whose CTAs sit beside GEMM CTAs
+// of a layer chain.)
+constexpr int kF8Hold = 4;
+
+__global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16_t *__restrict__ x,
+                                                                    long long ldx, int rows, int rows_iter,
+                                                                    int K, int tile_rows, int early_trigger,
+                                                                    uint8_t *__restrict__ q,
+                                                                    float *__restrict__ scale) {
+  __shared__ uint32_t red[2][kF8Threads / 32];
+  const int cpr = K >> 3;  // <= kF8Hold * kF8Threads
+  const int tid = threadIdx.x;
+  if (early_trigger) pdl_trigger();
+  pdl_wait();
+  int parity = 0;
+  for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
+    const Fp8RowDest dst(r, K, tile_rows);
+    if (r >= rows) {  // panel padding (uniform over the CTA)
+      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
+      continue;
+    }
+    const uint16_t *xr = x + (size_t)r * ldx;
+    uint4 v[kF8Hold];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < kF8Hold; ++i) {
+      const int c = tid + i * kF8Threads;
+      v[i] = c < cpr ? ld_stream_v4(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      amax = max(amax, amax_bf16x8(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    // two reduction buffers, alternating over the rows that reduce: one
+    // barrier a row suffices (a buffer is rewritten only after the barrier
+    // of the row between, which every reader of it has passed)
+    if ((tid & 31) == 0) red[parity][tid >> 5] = amax;
+    __syncthreads();
+    amax = red[parity][0];
+#pragma unroll
+    for (int i = 1; i < kF8Threads / 32; ++i) amax = max(amax, red[parity][i]);
+    parity ^= 1;
+    if (amax >= 0x7F80u) {  // Inf or NaN in the row
+      if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
+      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
+      continue;
+    }
+    const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
+    if (tid == 0) scale[r] = s;
+    const RowDivisor dv(s);
+#pragma unroll
+    for (int i = 0; i < kF8Hold; ++i) {
+      const int c = tid + i * kF8Threads;
+      if (c < cpr) *dst.chunk(q, c) = fp8_quant8(v[i], dv);
+    }
   }
 }
 
@@ -400,7 +489,8 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *
     } else {
       const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
       if (tid == 0) scale[r] = s;
-      for (int c = tid; c < cpr; c += kSwThreads) *dst.chunk(q, c) = fp8_quant8(hrow[c], s);
+      const RowDivisor dv(s);
+      for (int c = tid; c < cpr; c += kSwThreads) *dst.chunk(q, c) = fp8_quant8(hrow[c], dv);
     }
     __syncthreads();  // red[] and hrow are reused by the next row
   }
@@ -412,7 +502,8 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
                             uint8_t *sf, bool swizzled, int tile_rows, bool act, int sm_count,
                             cudaStream_t stream) {
   const int cpr = K / 8;
-  const int per_block = kMxThreads * kMxChunksPerThread;
+  const bool big = rows > 512;
+  const int per_block = kMxThreads * (big ? 4 : 2);
   const int gx = (cpr + per_block - 1) / per_block;
   const int rows_iter = tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows
                         : swizzled                   ? ((rows + 127) / 128) * 128
@@ -431,14 +522,11 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
-  cudaError_t e = swizzled ? prefer_shared_carveout(mx_quant_kernel<true>)
-                           : prefer_shared_carveout(mx_quant_kernel<false>);
+  auto kern = swizzled ? (big ? mx_quant_kernel<true, 4> : mx_quant_kernel<true, 2>)
+                       : (big ? mx_quant_kernel<false, 4> : mx_quant_kernel<false, 2>);
+  cudaError_t e = prefer_shared_carveout(kern);
   if (e != cudaSuccess) return e;
-  if (swizzled)
-    return cudaLaunchKernelEx(&cfg, mx_quant_kernel<true>, xp, ldx, rows, rows_iter, K, tile_rows,
-                              act ? 1 : 0, codes, sf);
-  return cudaLaunchKernelEx(&cfg, mx_quant_kernel<false>, xp, ldx, rows, rows_iter, K, tile_rows,
-                            act ? 1 : 0, codes, sf);
+  return cudaLaunchKernelEx(&cfg, kern, xp, ldx, rows, rows_iter, K, tile_rows, act ? 1 : 0, codes, sf);
 }
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
@@ -452,10 +540,12 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
-  cudaError_t e = prefer_shared_carveout(fp8_quant_kernel);
+  // large inputs whose rows fit in the CTA's registers: one read of each row
+  auto kern = (rows > 512 && K / 8 <= kF8Hold * kF8Threads) ? fp8_quant_hold_kernel : fp8_quant_kernel;
+  cudaError_t e = prefer_shared_carveout(kern);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, fp8_quant_kernel, static_cast<const uint16_t *>(x), ldx, rows,
-                            rows_iter, K, tile_rows, act ? 1 : 0, q, scale);
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, tile_rows,
+                            act ? 1 : 0, q, scale);
 }
 
 cudaError_t launch_mx_quant_grouped(const void *x, long long ldx, int M_total, int K, const int *row_off,

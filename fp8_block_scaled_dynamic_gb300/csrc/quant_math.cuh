@@ -95,14 +95,19 @@ __device__ __forceinline__ uint32_t mx_encode_chunk(const uint4 &w, uint32_t &sc
   const int ef = max(static_cast<int>(amax >> 7), 2);
   scode = static_cast<uint32_t>(ef - 2);
   const float inv = __uint_as_float(static_cast<uint32_t>(256 - ef) << 23);  // 2^-e
-  uint32_t packed = e2m1x2(bf16_lo(w.x) * inv, bf16_hi(w.x) * inv) |
-                    (e2m1x2(bf16_lo(w.y) * inv, bf16_hi(w.y) * inv) << 8) |
-                    (e2m1x2(bf16_lo(w.z) * inv, bf16_hi(w.z) * inv) << 16) |
-                    (e2m1x2(bf16_lo(w.w) * inv, bf16_hi(w.w) * inv) << 24);
-  // the sign of value i (bit 15 or 31 of its word) onto bit 4i + 3
-  packed |= ((w.x >> 12) & 0x8u) | ((w.x >> 24) & 0x80u) | ((w.y >> 4) & 0x800u) |
-            ((w.y >> 16) & 0x8000u) | ((w.z << 4) & 0x80000u) | ((w.z >> 8) & 0x800000u) |
-            ((w.w << 12) & 0x8000000u) | (w.w & 0x80000000u);
+  // four conversions of two values each, the four code bytes packed by one
+  // vector move (value 2i in the low nibble of byte i); the conversion keeps
+  // the sign of a value that rounds to zero (-0 -> code 0x8)
+  uint32_t packed;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(packed)
+      : "f"(bf16_lo(w.x) * inv), "f"(bf16_hi(w.x) * inv), "f"(bf16_lo(w.y) * inv), "f"(bf16_hi(w.y) * inv),
+        "f"(bf16_lo(w.z) * inv), "f"(bf16_hi(w.z) * inv), "f"(bf16_lo(w.w) * inv), "f"(bf16_hi(w.w) * inv));
   return packed;
 }
 
