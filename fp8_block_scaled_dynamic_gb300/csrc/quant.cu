@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
 // formed in binary32 one IEEE operation at a time (no contraction), and e^t
 // by the method of Cody and Waite (Software Manual for the Elementary
 // Functions, 1980): n = rint(t / ln2), r = (t - n L1) - n L2 with ln2 split
-// so that n L1 is exact, e^r by its Taylor series through r^7/7! (Horner),
-// times 2^n.  h is then quantized per row exactly as fp8_quant_kernel does.
+// so that n L1 is exact, e^r by its Taylor series through r^7/7! (Horner,
+// each step one fused multiply-add), times 2^n.  h is then quantized per row exactly as fp8_quant_kernel does.
 __device__ __forceinline__ float cw_exp(float t) {
   if (t != t) return t;
   if (t > 88.72283f) return __int_as_float(0x7F800000);
@@ -415,18 +415,22 @@ __device__ __forceinline__ float cw_exp(float t) {
   const float log2e = 0x1.715476p+0f;   // 1/ln2 rounded to binary32
   const float L1 = 0x1.62e4p-1f;        // 15 significant bits: n * L1 exact for |n| <= 128
   const float L2 = 0x1.7f7d1cp-20f;     // ln2 - L1 rounded to binary32
-  const float nf = rintf(__fmul_rn(t, log2e));
-  const int n = (int)nf;
+  // n = rint(t log2e), round half to even: for |t log2e| < 2^22, adding
+  // 1.5 2^23 rounds to an integer in the low mantissa bits and subtracting
+  // it back is exact -- the same n as rintf, and n's bits come for free
+  const float big = __fadd_rn(__fmul_rn(t, log2e), 0x1.8p+23f);
+  const float nf = __fsub_rn(big, 0x1.8p+23f);
+  const int n = (int)(__float_as_uint(big) & 0x7FFFFFu) - 0x400000;
   float r = __fsub_rn(t, __fmul_rn(nf, L1));
   r = __fsub_rn(r, __fmul_rn(nf, L2));
-  float p = 0x1.a01a02p-13f;                       // 1/7!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.6c16c2p-10f);  // 1/6!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.111112p-7f);   // 1/5!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-5f);   // 1/4!
-  p = __fadd_rn(__fmul_rn(p, r), 0x1.555556p-3f);   // 1/3!
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  float p = 0x1.a01a02p-13f;                   // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);         // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);          // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);          // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);          // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
   if (n > 127) return __fmul_rn(__fmul_rn(p, __uint_as_float(254u << 23)), 2.0f);
   return __fmul_rn(p, __uint_as_float((uint32_t)(n + 127) << 23));
 }

@@ -410,7 +410,8 @@ void orc_gemm_ptpc(const uint8_t *qa, const float *sa, const uint8_t *qw,
 /*      r = (t - n*L1) - n*L2 with ln2 = L1 + L2 split so that n*L1 is exact */
 /*      (L1 has 15 significant bits, |n| <= 128); e^r from its Taylor series */
 /*      through r^7/7! (|r| <= ln2/2, the first dropped term is below 1e-8   */
-/*      relative), summed by Horner's rule; then the exact scaling by 2^n.   */
+/*      relative), summed by Horner's rule, each step one fused multiply-   */
+/*      add (an IEEE 754 operation: fmaf); then the exact scaling by 2^n.    */
 /* ------------------------------------------------------------------------ */
 static float f32_from_bits(uint32_t u)
 {
@@ -441,13 +442,13 @@ float orc_exp_f32(float t)
     r = t - nf * L1;
     r = r - nf * L2;
     p = c7;
-    p = p * r + c6;
-    p = p * r + c5;
-    p = p * r + c4;
-    p = p * r + c3;
-    p = p * r + c2;
-    p = p * r + 1.0f;
-    p = p * r + 1.0f;
+    p = fmaf(p, r, c6);
+    p = fmaf(p, r, c5);
+    p = fmaf(p, r, c4);
+    p = fmaf(p, r, c3);
+    p = fmaf(p, r, c2);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
     if (n > 127)
         return (p * f32_from_bits((uint32_t)(127 + 127) << 23)) * 2.0f;
     return p * f32_from_bits((uint32_t)(n + 127) << 23);

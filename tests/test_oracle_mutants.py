@@ -34,7 +34,7 @@ MUTANTS = {
                                "float g = orc_bf16_to_f32(row[I + j]);\n            float u = orc_bf16_to_f32(row[j]);"),
     "silu_exp_sign": ("float e = orc_exp_f32(-g);", "float e = orc_exp_f32(g);"),
     "silu_one_dropped": ("float d = 1.0f + e;", "float d = 0.5f + e;"),
-    "exp_taylor_term_dropped": ("p = p * r + c6;", "p = p * r + 0.0f * c6;"),
+    "exp_taylor_term_dropped": ("p = fmaf(p, r, c6);", "p = fmaf(p, r, 0.0f * c6);"),
     "exp_reduction_low_part_sign": ("r = r - nf * L2;", "r = r + nf * L2;"),
     "bf16_round_truncates": ("u += 0x7FFFu + ((u >> 16) & 1u);", "u += 0u * ((u >> 16) & 1u);"),
 }
