@@ -255,10 +255,17 @@ class Workload:
     def e2e_pipelined(self, parts):
         """One end-to-end step as a serving loop runs it: parts = [(inputs,
         compute, outputs)], inputs / outputs lists of (dst, src) tensor pairs.
-        Every part's pinned host inputs go in on an upload stream at once;
-        part i computes as soon as its own inputs have landed, and its results
-        go out on a download stream while the parts after it compute (uploads
-        and downloads use separate copy engines, so they overlap too)."""
+        The pinned host inputs go in on an upload stream in two groups --
+        part 0, then the rest -- one copy a group where the parts' inputs lie
+        next to each other in memory (a copy has a fixed cost of ~5 us on this
+        link, and every wait of the compute stream on the upload stream breaks
+        the programmatic launch chain of its kernels there): the compute
+        stream waits only at parts 0 and 1, and the first group is small so
+        that computing starts early (measured on the 5-layer decode chain:
+        per-part copies and waits 126 us, one copy 117 us, three groups
+        109 us, two groups 103 us).  Results go out per part on a download stream while the
+        parts after it compute (uploads and downloads use separate copy
+        engines)."""
         if not hasattr(self, "h2d_stream"):
             self.h2d_stream = torch.cuda.Stream(device=self.dev)
             self.d2h_stream = torch.cuda.Stream(device=self.dev)
@@ -268,13 +275,18 @@ class Workload:
         up, down = self.h2d_stream, self.d2h_stream
         up.wait_stream(cur)
         down.wait_stream(cur)
+        n = len(parts)
+        groups = [[0], list(range(1, n))][:min(n, 2)]
         with torch.cuda.stream(up):
-            for i, (ins, _, _) in enumerate(parts):
-                for dst, src in ins:
+            for g in groups:
+                merged = merge_copies([parts[j][0] for j in g])
+                for dst, src in merged:
                     dst.copy_(src, non_blocking=True)
-                self.ev_in[i].record(up)
+                self.ev_in[g[0]].record(up)
+        first = {g[0] for g in groups}
         for i, (_, fn, outs) in enumerate(parts):
-            cur.wait_event(self.ev_in[i])
+            if i in first:
+                cur.wait_event(self.ev_in[i])
             fn()
             self.ev_out[i].record(cur)
             down.wait_event(self.ev_out[i])
@@ -283,6 +295,41 @@ class Workload:
                     dst.copy_(src, non_blocking=True)
         cur.wait_stream(up)
         cur.wait_stream(down)
+
+
+def _bytes_view(t):
+    """A flat uint8 view of a contiguous tensor's bytes."""
+    v = torch.empty(0, dtype=torch.uint8, device=t.device)
+    return v.set_(t.untyped_storage(), t.storage_offset() * t.element_size(), (t.numel() * t.element_size(),))
+
+
+def merge_copies(inputs):
+    """(dst, src) copies of several parts as few copies as possible: the
+    parts' single input pairs merge where each destination and each source
+    directly follows the one before it in the same storage."""
+    pairs = [p for ins in inputs for p in ins]
+    if any(len(ins) != 1 for ins in inputs) or not all(d.is_contiguous() and s.is_contiguous() for d, s in pairs):
+        return pairs
+
+    def follows(a, b):
+        return (a.untyped_storage().data_ptr() == b.untyped_storage().data_ptr() and
+                b.data_ptr() == a.data_ptr() + a.numel() * a.element_size())
+    out = []
+    for d, s in pairs:
+        if out and follows(out[-1][2], d) and follows(out[-1][3], s):
+            out[-1][2], out[-1][3] = d, s
+        else:
+            out.append([d, s, d, s])
+    res = []
+    for d0, s0, d1, s1 in out:
+        if d0 is d1:
+            res.append((d0, s0))
+        else:
+            n = d1.data_ptr() + d1.numel() * d1.element_size() - d0.data_ptr()
+            dv, sv = _bytes_view(d0), _bytes_view(s0)
+            res.append((dv.set_(dv.untyped_storage(), dv.storage_offset(), (n,)),
+                        sv.set_(sv.untyped_storage(), sv.storage_offset(), (n,))))
+    return res
 
 
 # resident weight layout of every workload: "panel" (256-row panels, the
