@@ -75,13 +75,14 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
   // one column of a 256-row weight panel: codes, then (E2M1) the 2 x 2 scale atoms
   static constexpr int kPanelBytes = 256 * kRowBytes + (KIND == 0 ? 2048 : 0);
-  // Epilogue warps: one set of four (one per TMEM lane quarter), or, for
-  // the A4W4 full tile, two sets that feed alternate stages' scale factors
-  // (a stage's feed waits for its data and for its TMEM stores, so one set
-  // alone paces the MMAs) and read out half of the accumulator's columns
-  // each.  Full tile: per epilogue warp one (two sets) or two 32 x 32 bf16
-  // staging boxes for the TMA stores of y.
-  static constexpr int kEpiSets = (KIND == 0 && KS == 1) ? 2 : 1;
+  // Epilogue warps: one set of four (one per TMEM lane quarter) for
+  // split-K, or, for the full tile, two sets that read out half of the
+  // accumulator's columns each (a short-K FP8 tile's read-out outlasts its
+  // MMAs) and, for A4W4, feed alternate stages' scale factors (a stage's
+  // feed waits for its data and for its TMEM stores, so one set alone paces
+  // the MMAs).  Full tile: per epilogue warp one (two sets) or two 32 x 32
+  // bf16 staging boxes for the TMA stores of y.
+  static constexpr int kEpiSets = KS == 1 ? 2 : 1;
   static constexpr int kThreads = 64 + 128 * kEpiSets;
   static constexpr int kEpiBufs = kEpiSets == 2 ? 1 : 2;
   static constexpr int kEpiBytes = KS == 1 ? 4 * kEpiSets * kEpiBufs * 2048 : 0;
