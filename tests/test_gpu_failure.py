@@ -44,3 +44,34 @@ def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
     y = run(dev_status=status)
     assert mx.mxg_query_status(status) == 0
     assert_gemm_close(y.cpu().numpy(), ref, bound, "after timeout")
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_stall_on_cta_pairs_times_out_then_next_call_is_correct(kind):
+    """The same on CTA pairs (2-SM MMAs, clusters of two): both CTAs of a
+    pair give up, meet at the cluster barrier, release their TMEM together
+    and return; the next call on pairs is correct."""
+    d = dev()
+    M, N, K = 256, 512, 1024
+    x = synth.activation(M, K, seed=52)
+    w = synth.weight(N, K, seed=53)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    assert mx.mxg_plan_gemm(kind, M, N, K, 152, variant="full", cta_pair=True)["cta_pair"] == 1
+    if kind == 0:
+        wc, wsf = mx.mx_quantize_weight(w.to(d))
+        run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant="full", cta_pair=True, **kw)
+        ac, asf = oracle.mx_quantize_rows(x)
+        wr, wsr = oracle.mx_quantize_rows(w)
+        ref, bound = oracle.gemm_a4w4(ac, asf, wr, wsr)
+    else:
+        qw, sw = mx.fp8_quantize_act(w.to(d))
+        qa, sa = mx.fp8_quantize_act(x.to(d))
+        run = lambda **kw: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant="full", cta_pair=True, **kw)
+        qar, sar = oracle.fp8_quantize_rows(x)
+        qwr, swr = oracle.fp8_quantize_rows(w)
+        ref, bound = oracle.gemm_ptpc(qar, sar, qwr, swr)
+    run(dev_status=status, timeout_ms=20, debug_stall=1)
+    assert mx.mxg_query_status(status) == 6  # MXG_ERR_TIMEOUT
+    y = run(dev_status=status)
+    assert mx.mxg_query_status(status) == 0
+    assert_gemm_close(y.cpu().numpy(), ref, bound, "after timeout, pairs")
