@@ -1072,12 +1072,13 @@ def _code_only(text: str) -> str:
 
 
 def kernel_sources_hash():
-    """Hash of the GEMM kernel's device code (gemm.cu and the headers it
-    includes), comments excluded: the code the traffic records were taken on."""
+    """Hash of the GEMM kernel's code (gemm.cu, the headers it includes, and
+    api.cu, whose plan sets the tile order and so the DRAM traffic), comments
+    excluded: the code the traffic records were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cuh", ".h")) or f == "gemm.cu":
+        if f.endswith((".cuh", ".h")) or f in ("gemm.cu", "api.cu"):
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(_code_only(fh.read()).encode())
     return h.hexdigest()

@@ -96,10 +96,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
 // Full-tile rasterization: operands above kL2KeepBytes (together) do not stay
-// in the 129 MB L2 across a wave of tiles; a band's activations take up to
-// kL2ActBudget of it.
+// in the 129 MB L2 across a wave of tiles, so the tiles go in bands of token
+// tiles.  Each die's half of the L2 caches what that die's SMs read, and the
+// SMs of both dies read every token tile of a band: a band's activations are
+// held twice, so one copy of them takes at most kL2ActBudget.
 constexpr uint64_t kL2KeepBytes = 96ull << 20;
-constexpr uint64_t kL2ActBudget = 64ull << 20;
+constexpr uint64_t kL2ActBudget = 32ull << 20;
 
 // CTA that owns stream-K unit u (must equal the device-side owner_of).
 long long owner_of(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
@@ -287,14 +289,16 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.kc_per_row = (int)((row_bytes + 127) / 128);  // the last column may be half (TMA pads it)
   if (!swap) {
     // Full tile: when the two operands together exceed what L2 keeps
-    // (129 MB), walk the tiles in bands of token tiles whose activations fit
-    // in half of it, so that every weight tile is read from HBM once per band
-    // (in row order every wave of CTAs would sweep all the weights).
+    // (129 MB), walk the tiles in bands of token tiles (as few bands as keep
+    // each band's activations within kL2ActBudget, of equal size), so that
+    // every weight tile is read from HBM once per band (in row order every
+    // wave of CTAs would sweep all the weights).
     const uint64_t a_tile = 128ull * (row_bytes + (kind == 0 ? row_bytes / 16 : 0));
     const uint64_t total = (uint64_t)(rowsA + rowsB) * row_bytes;
     if (total > kL2KeepBytes) {
-      const uint64_t g = kL2ActBudget / a_tile;
-      p.raster_group = (int)std::max<uint64_t>(1, std::min<uint64_t>(g, (uint64_t)p.tilesA));
+      const uint64_t tiles = (uint64_t)p.tilesA;
+      const uint64_t bands = std::max<uint64_t>(1, (tiles * a_tile + kL2ActBudget - 1) / kL2ActBudget);
+      p.raster_group = (int)((tiles + bands - 1) / bands);
     }
   }
   // operands in the tile layout are fetched by bulk copy (their tensor map

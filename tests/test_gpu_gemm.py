@@ -264,14 +264,15 @@ def test_ptpc_full_tile_several_tiles_per_cta(M, N, K):
 
 
 def test_ptpc_full_tile_banded_raster():
-    """Operands far above L2 (335 MB of activations, 64 MB of weights): the
-    full-tile GEMM walks its tiles in bands of 8 token tiles (their
-    activations fit in half of L2), here 8 + 8 + 4; sampled rows from every
-    band match the oracle."""
-    M, N, K = 2560, 1024, 65536
+    """Operands far above L2 (157 MB of activations, 64 MB of weights): the
+    full-tile GEMM walks its tiles in bands of token tiles whose activations
+    take at most 32 MiB, here 19 token tiles (the last one ragged) in bands of
+    4 + 4 + 4 + 4 + 3; sampled rows from every band, on both sides of each
+    band boundary, match the oracle."""
+    M, N, K = 2400, 1024, 65536
     x, w = quant_pair(M, N, K, seed=77)
     y32 = run_ptpc(x, w, "full").cpu().numpy()
-    rows = np.array([0, 127, 128, 1023, 1024, 1151, 2047, 2048, 2200, 2559])
+    rows = np.array([0, 127, 128, 511, 512, 1023, 1024, 1151, 1535, 1536, 2047, 2048, 2200, 2303, 2304, 2399])
     ref, bound = oracle_ptpc(x, w, rows=rows)
     assert_gemm_close(y32[rows], ref, bound, f"ptpc full banded {M}x{N}x{K}")
 
