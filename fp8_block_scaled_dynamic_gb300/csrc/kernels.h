@@ -3,6 +3,9 @@
 #include <cstddef>
 #include <cstdint>
 #include <cstdlib>
+#include <deque>
+#include <mutex>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,16 +53,42 @@ struct DeviceOnce {
   }
 };
 
+// The "done" bits of one kernel, found by its address (kernels of one
+// signature share the template instance, so a static per instance would not
+// tell them apart).
+inline DeviceOnce &carveout_once(const void *kern) {
+  static std::mutex mu;
+  static std::deque<std::pair<const void *, DeviceOnce>> done;  // appends keep references valid
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto &d : done)
+    if (d.first == kern) return d.second;
+  done.emplace_back(kern, DeviceOnce{});
+  return done.back().second;
+}
+
 template <class Kernel>
 inline cudaError_t prefer_shared_carveout(Kernel *kern) {
-  static DeviceOnce once;
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (once.done(dev)) return cudaSuccess;
+  {
+    DeviceOnce &once = carveout_once(reinterpret_cast<const void *>(kern));
+    if (once.done(dev)) return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess) once.set(dev);
+  if (e == cudaSuccess) carveout_once(reinterpret_cast<const void *>(kern)).set(dev);
+  return e;
+}
+
+// CTAs of `kern` (`threads` per CTA, `smem` bytes of dynamic shared memory)
+// that one SM holds at once; a grid-stride kernel launched with this many
+// per SM starts every CTA in one wave.
+template <class Kernel>
+inline cudaError_t resident_ctas_per_sm(Kernel *kern, int threads, size_t smem, int *n) {
+  *n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, kern, threads, smem);
+  if (e == cudaSuccess && *n < 1) *n = 1;
   return e;
 }
 

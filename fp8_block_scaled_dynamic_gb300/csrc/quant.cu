@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -227,21 +228,34 @@ struct RowDivisor {
     r = __fdiv_rn(1.0f, s_);
     fast = s_ >= 7.8886090522101181e-31f;  // 2^-100
   }
-  __device__ __forceinline__ float operator()(float x) const {
-    if (!fast) return __fdiv_rn(x, s);
+  // x / s on a fast row: one multiply, two fused multiply-adds
+  __device__ __forceinline__ float correct(float x) const {
     const float q = __fmul_rn(x, r);
     return __fmaf_rn(__fmaf_rn(-q, s, x), r, q);
   }
 };
 
 // 8 bf16 values -> 8 E4M3 bytes: q = E4M3_RNE_sat(x / s), the sign of x kept
-// on codes that round to zero.
+// on codes that round to zero.  kFast: the row's divisor is fast (the
+// choice is made once per row, outside the loops over its chunks, so that
+// the division's instructions stay out of the fast loop).
+template <bool kFast>
 __device__ __forceinline__ uint2 fp8_quant8(const uint4 &w, const RowDivisor &d) {
-  uint32_t lo = e4m3x2(d(bf16_lo(w.x)), d(bf16_hi(w.x))) | (e4m3x2(d(bf16_lo(w.y)), d(bf16_hi(w.y))) << 16);
-  uint32_t hi = e4m3x2(d(bf16_lo(w.z)), d(bf16_hi(w.z))) | (e4m3x2(d(bf16_lo(w.w)), d(bf16_hi(w.w))) << 16);
+  auto q = [&](float x) { return kFast ? d.correct(x) : __fdiv_rn(x, d.s); };
+  uint32_t lo = e4m3x2(q(bf16_lo(w.x)), q(bf16_hi(w.x))) | (e4m3x2(q(bf16_lo(w.y)), q(bf16_hi(w.y))) << 16);
+  uint32_t hi = e4m3x2(q(bf16_lo(w.z)), q(bf16_hi(w.z))) | (e4m3x2(q(bf16_lo(w.w)), q(bf16_hi(w.w))) << 16);
   lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
   hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
   return make_uint2(lo, hi);
+}
+
+// Runs f(std::true_type) on a fast row, f(std::false_type) otherwise.
+template <class F>
+__device__ __forceinline__ void by_divisor(const RowDivisor &d, F &&f) {
+  if (d.fast)
+    f(std::true_type{});
+  else
+    f(std::false_type{});
 }
 
 // Where row r of a per-row FP8 output of K bytes goes: 128-byte column c of
@@ -332,7 +346,10 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
     const RowDivisor dv(s);
-    for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = fp8_quant8(ld_keep_v4(xr + (size_t)c * 8), dv);
+    by_divisor(dv, [&](auto fast) {
+      for (int c = tid; c < cpr; c += kF8Threads)
+        *dst.chunk(q, c) = fp8_quant8<decltype(fast)::value>(ld_keep_v4(xr + (size_t)c * 8), dv);
+    });
   }
 }
 
@@ -354,21 +371,31 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
   if (early_trigger) pdl_trigger();
   pdl_wait();
   int parity = 0;
+  // a row's chunks (zeros past the row and on padding rows); the next row's
+  // loads go out before this row's reduction and codes
+  auto load_row = [&](int r, uint4 (&v)[kF8Hold]) {
+    const uint16_t *xr = x + (size_t)r * ldx;
+#pragma unroll
+    for (int i = 0; i < kF8Hold; ++i) {
+      const int c = tid + i * kF8Threads;
+      v[i] = (r < rows && c < cpr) ? ld_stream_v4(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  uint4 vn[kF8Hold];
+  if ((int)blockIdx.x < rows_iter) load_row(blockIdx.x, vn);
   for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
+    uint4 v[kF8Hold];
+#pragma unroll
+    for (int i = 0; i < kF8Hold; ++i) v[i] = vn[i];
+    if (r + (int)gridDim.x < rows_iter) load_row(r + gridDim.x, vn);
     const Fp8RowDest dst(r, K, tile_rows);
     if (r >= rows) {  // panel padding (uniform over the CTA)
       for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
       continue;
     }
-    const uint16_t *xr = x + (size_t)r * ldx;
-    uint4 v[kF8Hold];
     uint32_t amax = 0;
 #pragma unroll
-    for (int i = 0; i < kF8Hold; ++i) {
-      const int c = tid + i * kF8Threads;
-      v[i] = c < cpr ? ld_stream_v4(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
-      amax = max(amax, amax_bf16x8(v[i]));
-    }
+    for (int i = 0; i < kF8Hold; ++i) amax = max(amax, amax_bf16x8(v[i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     // two reduction buffers, alternating over the rows that reduce: one
@@ -388,11 +415,13 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
     const RowDivisor dv(s);
+    by_divisor(dv, [&](auto fast) {
 #pragma unroll
-    for (int i = 0; i < kF8Hold; ++i) {
-      const int c = tid + i * kF8Threads;
-      if (c < cpr) *dst.chunk(q, c) = fp8_quant8(v[i], dv);
-    }
+      for (int i = 0; i < kF8Hold; ++i) {
+        const int c = tid + i * kF8Threads;
+        if (c < cpr) *dst.chunk(q, c) = fp8_quant8<decltype(fast)::value>(v[i], dv);
+      }
+    });
   }
 }
 
@@ -435,28 +464,85 @@ __device__ __forceinline__ float cw_exp(float t) {
   return __fmul_rn(p, __uint_as_float((uint32_t)(n + 127) << 23));
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  const float d = __fadd_rn(1.0f, cw_exp(-g));
-  return __fmul_rn(__fdiv_rn(g, d), u);
+// silu(g) = g / (1 + e^-g) in binary32
+__device__ __forceinline__ float silu_f32(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, cw_exp(-g))); }
+
+// silu depends on the bf16 gate alone: a table of it over the gates with
+// 2^-25 <= |g| < 2^7 (biased exponents kSiluE0 .. kSiluE0 + 31, both signs;
+// what a bf16 gate_up output holds nearly always), index sign * 4096 +
+// (exponent - kSiluE0) * 128 + mantissa, each entry formed by silu_f32
+// itself.  Gates outside it (zeros, tiny, huge, non-finite) take silu_f32
+// directly, so the result is the same bit for bit either way.
+constexpr uint32_t kSiluE0 = 102;
+constexpr int kSiluEntries = 2 * 32 * 128;
+constexpr int kSiluTableBytes = kSiluEntries * 4;
+
+__device__ __forceinline__ float silu_of_bits(uint32_t gb, const float *tab) {
+  if (tab) {
+    const uint32_t rel = (gb & 0x7FFFu) - (kSiluE0 << 7);  // wraps above 4095 below the range
+    if (rel < (32u << 7)) return tab[((gb >> 15) << 12) | rel];
+  }
+  return silu_f32(__uint_as_float(gb << 16));
 }
 
-// two bf16 gate values and the matching up values -> two bf16 h values
-__device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
-  return pack_bf16x2(silu_mul(bf16_lo(g), bf16_lo(u)), silu_mul(bf16_hi(g), bf16_hi(u)));
+// two bf16 gate values and the matching up values -> two bf16 h values,
+// h = bf16(silu(g) * u)
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u, const float *tab) {
+  return pack_bf16x2(__fmul_rn(silu_of_bits(g & 0xFFFFu, tab), bf16_lo(u)),
+                     __fmul_rn(silu_of_bits(g >> 16, tab), bf16_hi(u)));
+}
+
+// A chunk of 8 gates with any of them outside the table: each value on its
+// own (not inlined, so that none of silu_f32 lands in the table path).
+__device__ __noinline__ uint4 swiglu8_any(uint4 g, uint4 u, const float *tab) {
+  return make_uint4(swiglu2(g.x, u.x, tab), swiglu2(g.y, u.y, tab), swiglu2(g.z, u.z, tab),
+                    swiglu2(g.w, u.w, tab));
+}
+
+// For the two bf16 gates of g: (|g| | 0x8000) - (kSiluE0 << 7) per half (no
+// borrow crosses the halves), which lies in [0x8000, 0x9000) -- its low 12
+// bits the table index without the sign -- exactly when the gate is inside
+// the table.
+__device__ __forceinline__ uint32_t table_rel2(uint32_t g) {
+  return ((g & 0x7FFF7FFFu) | 0x80008000u) - (kSiluE0 << 7) * 0x10001u;
+}
+
+// two gates known to be inside the table
+__device__ __forceinline__ uint32_t swiglu2_table(uint32_t g, uint32_t t, uint32_t u, const float *tab) {
+  const uint32_t i_lo = (t & 0xFFFu) | ((g >> 3) & 0x1000u);
+  const uint32_t i_hi = ((t >> 16) & 0xFFFu) | ((g >> 19) & 0x1000u);
+  return pack_bf16x2(__fmul_rn(tab[i_lo], bf16_lo(u)), __fmul_rn(tab[i_hi], bf16_hi(u)));
+}
+
+__device__ __forceinline__ uint4 swiglu8(const uint4 &g, const uint4 &u, const float *tab) {
+  if (tab) {
+    // each half of a t word lies in [0x4D00, 0xCCFF]: its top four bits are
+    // 8 inside the table and another nonzero value outside, so OR-ed over
+    // the chunk they are 8 only if every gate is inside
+    const uint4 t = make_uint4(table_rel2(g.x), table_rel2(g.y), table_rel2(g.z), table_rel2(g.w));
+    if (((t.x | t.y | t.z | t.w) & 0xF000F000u) == 0x80008000u)
+      return make_uint4(swiglu2_table(g.x, t.x, u.x, tab), swiglu2_table(g.y, t.y, u.y, tab),
+                        swiglu2_table(g.z, t.z, u.z, tab), swiglu2_table(g.w, t.w, u.w, tab));
+  }
+  return swiglu8_any(g, u, tab);
 }
 
 constexpr int kSwThreads = 256;
+constexpr int kSwUnroll = 3;  // chunk pairs (gate, up) whose loads are in flight together
 
 // One CTA per row (grid-stride over rows): pass 1 forms h for the row into
 // shared memory (I bf16) and takes its amax; pass 2 quantizes h from shared
 // memory into q (row-major or the down GEMM's token tiles) and writes the
-// row's scale.  h_out (optional) receives h itself.
+// row's scale.  h_out (optional) receives h itself.  kTable: the silu table
+// sits in shared memory after the row (filled before the dependency wait,
+// while the kernel ahead finishes).
+template <bool kTable>
 __global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *__restrict__ gu,
                                                                 long long ldgu, int rows, int I,
                                                                 int tile_rows, uint16_t *__restrict__ h_out,
                                                                 long long ldh, uint8_t *__restrict__ q,
                                                                 float *__restrict__ scale) {
-  extern __shared__ uint4 hrow[];  // I / 8 chunks of 8 bf16
+  extern __shared__ uint4 hrow[];  // I / 8 chunks of 8 bf16, then (kTable) the silu table
   __shared__ uint32_t red[kSwThreads / 32];
   const int tid = threadIdx.x;
   const int cpr = I >> 3;
@@ -466,18 +552,45 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *
     for (int c = 0; c < 2 * cpr; c += 1024)
       prefetch_l2_bulk(g + (size_t)c * 8, (uint32_t)min(1024, 2 * cpr - c) * 16u);
   }
+  float *tab = nullptr;
+  if (kTable) {
+    tab = reinterpret_cast<float *>(hrow + cpr);
+    for (int i = tid; i < kSiluEntries; i += kSwThreads) {
+      const uint32_t gb = ((uint32_t)(i >> 12) << 15) | ((kSiluE0 << 7) + (uint32_t)(i & 0xFFF));
+      tab[i] = silu_f32(__uint_as_float(gb << 16));
+    }
+    __syncthreads();
+  }
   pdl_wait();  // gu comes from the kernel ahead (the gate_up GEMM)
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint16_t *gr = gu + (size_t)r * ldgu;
     const uint16_t *ur = gr + I;
+    if (tid == 0 && r + (int)gridDim.x < rows) {  // warm L2 with this CTA's next row
+      const uint16_t *g = gu + (size_t)(r + gridDim.x) * ldgu;
+      for (int c = 0; c < 2 * cpr; c += 1024)
+        prefetch_l2_bulk(g + (size_t)c * 8, (uint32_t)min(1024, 2 * cpr - c) * 16u);
+    }
     uint32_t amax = 0;
-    for (int c = tid; c < cpr; c += kSwThreads) {
-      const uint4 g = ld_stream_v4(gr + (size_t)c * 8);
-      const uint4 u = ld_stream_v4(ur + (size_t)c * 8);
-      const uint4 h = make_uint4(swiglu2(g.x, u.x), swiglu2(g.y, u.y), swiglu2(g.z, u.z), swiglu2(g.w, u.w));
-      hrow[c] = h;
-      if (h_out) *reinterpret_cast<uint4 *>(h_out + (size_t)r * ldh + (size_t)c * 8) = h;
-      amax = max(amax, amax_bf16x8(h));
+    for (int c0 = tid; c0 < cpr; c0 += kSwUnroll * kSwThreads) {
+      uint4 g[kSwUnroll], u[kSwUnroll];
+#pragma unroll
+      for (int j = 0; j < kSwUnroll; ++j) {
+        const int c = c0 + j * kSwThreads;
+        if (c < cpr) {
+          g[j] = ld_stream_v4(gr + (size_t)c * 8);
+          u[j] = ld_stream_v4(ur + (size_t)c * 8);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kSwUnroll; ++j) {
+        const int c = c0 + j * kSwThreads;
+        if (c < cpr) {
+          const uint4 h = swiglu8(g[j], u[j], tab);
+          hrow[c] = h;
+          if (h_out) *reinterpret_cast<uint4 *>(h_out + (size_t)r * ldh + (size_t)c * 8) = h;
+          amax = max(amax, amax_bf16x8(h));
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -494,7 +607,10 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *
       const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
       if (tid == 0) scale[r] = s;
       const RowDivisor dv(s);
-      for (int c = tid; c < cpr; c += kSwThreads) *dst.chunk(q, c) = fp8_quant8(hrow[c], dv);
+      by_divisor(dv, [&](auto fast) {
+        for (int c = tid; c < cpr; c += kSwThreads)
+          *dst.chunk(q, c) = fp8_quant8<decltype(fast)::value>(hrow[c], dv);
+      });
     }
     __syncthreads();  // red[] and hrow are reused by the next row
   }
@@ -512,13 +628,20 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   const int rows_iter = tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows
                         : swizzled                   ? ((rows + 127) / 128) * 128
                                                      : rows;
-  // enough CTAs for ~8 resident per SM, rows beyond that are grid-strided;
-  // for a decode-sized activation (a few hundred rows at most) one CTA per
-  // SM: launched early beside the GEMMs of a layer chain, a second
-  // quantizer CTA on an SM would leave no registers for the next GEMM CTA
+  auto kern = swizzled ? (big ? mx_quant_kernel<true, 4> : mx_quant_kernel<true, 2>)
+                       : (big ? mx_quant_kernel<false, 4> : mx_quant_kernel<false, 2>);
+  cudaError_t e = prefer_shared_carveout(kern);
+  if (e != cudaSuccess) return e;
+  // as many CTAs as are resident at once (one wave), rows beyond that
+  // grid-strided; for a decode-sized activation (a few hundred rows at most)
+  // one CTA per SM: launched early beside the GEMMs of a layer chain, a
+  // second quantizer CTA on an SM would leave no registers for the next GEMM
+  // CTA
+  int per_sm = 1;
+  if (!(act && rows <= 512) && (e = resident_ctas_per_sm(kern, kMxThreads, 0, &per_sm)) != cudaSuccess) return e;
   int gy = rows_iter;
   const int sms = sm_count > 0 ? sm_count : 152;
-  const int cap = (act && rows <= 512) ? sms : sms * 8;
+  const int cap = sms * per_sm;
   if (gy * gx > cap) gy = (cap + gx - 1) / gx;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
@@ -526,10 +649,6 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
-  auto kern = swizzled ? (big ? mx_quant_kernel<true, 4> : mx_quant_kernel<true, 2>)
-                       : (big ? mx_quant_kernel<false, 4> : mx_quant_kernel<false, 2>);
-  cudaError_t e = prefer_shared_carveout(kern);
-  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, kern, xp, ldx, rows, rows_iter, K, tile_rows, act ? 1 : 0, codes, sf);
 }
 
@@ -538,16 +657,19 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
                              cudaStream_t stream) {
   const int rows_iter =
       tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows : rows;
-  int g = rows_iter;
-  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
-  if (g > cap) g = cap;
-  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
-  cudaLaunchAttribute attr[1];
-  attach_pdl(cfg, attr);
   // large inputs whose rows fit in the CTA's registers: one read of each row
   auto kern = (rows > 512 && K / 8 <= kF8Hold * kF8Threads) ? fp8_quant_hold_kernel : fp8_quant_kernel;
   cudaError_t e = prefer_shared_carveout(kern);
   if (e != cudaSuccess) return e;
+  // one CTA per row, at most as many as are resident at once (one wave)
+  int per_sm = 1;
+  if ((e = resident_ctas_per_sm(kern, kF8Threads, 0, &per_sm)) != cudaSuccess) return e;
+  int g = rows_iter;
+  const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
+  if (g > cap) g = cap;
+  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
+  cudaLaunchAttribute attr[1];
+  attach_pdl(cfg, attr);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, tile_rows,
                             act ? 1 : 0, q, scale);
 }
@@ -555,11 +677,13 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
 cudaError_t launch_mx_quant_grouped(const void *x, long long ldx, int M_total, int K, const int *row_off,
                                     int E, int *tile_off, uint8_t *codes, uint8_t *sf, int sm_count,
                                     cudaStream_t stream) {
-  int g = M_total < 1 ? 1 : M_total;
-  const int cap = (sm_count > 0 ? sm_count : 152) * 8;
-  if (g > cap) g = cap;
   cudaError_t e = prefer_shared_carveout(mx_quant_grouped_kernel);
   if (e != cudaSuccess) return e;
+  int per_sm = 1;  // one wave of CTAs, rows grid-strided
+  if ((e = resident_ctas_per_sm(mx_quant_grouped_kernel, kMxThreads, 0, &per_sm)) != cudaSuccess) return e;
+  int g = M_total < 1 ? 1 : M_total;
+  const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
+  if (g > cap) g = cap;
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kMxThreads), 0, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
@@ -569,27 +693,31 @@ cudaError_t launch_mx_quant_grouped(const void *x, long long ldx, int M_total, i
 
 cudaError_t launch_swiglu_fp8(const void *gu, long long ldgu, int rows, int I, int tile_rows, void *h_out,
                               long long ldh, uint8_t *q, float *scale, int sm_count, cudaStream_t stream) {
-  const size_t smem = (size_t)I * 2u;
-  int g = rows;
-  const int per_sm = (int)std::max<size_t>(1, std::min<size_t>(8, (200u * 1024u) / std::max<size_t>(smem, 1)));
-  const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
-  if (g > cap) g = cap;
-  static DeviceOnce once;
+  constexpr size_t kMaxSmem = 200u * 1024u;
+  const bool table = (size_t)I * 2u + kSiluTableBytes <= kMaxSmem;
+  const size_t smem = (size_t)I * 2u + (table ? kSiluTableBytes : 0);
+  auto kern = table ? swiglu_fp8_kernel<true> : swiglu_fp8_kernel<false>;
+  static DeviceOnce once[2];
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (!once.done(dev)) {
-    e = cudaFuncSetAttribute(swiglu_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (!once[table].done(dev)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(swiglu_fp8_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    once.set(dev);
+    once[table].set(dev);
   }
+  int per_sm = 1;  // one wave of CTAs, rows grid-strided
+  if ((e = resident_ctas_per_sm(kern, kSwThreads, smem, &per_sm)) != cudaSuccess) return e;
+  int g = rows;
+  const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
+  if (g > cap) g = cap;
   cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kSwThreads), smem, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
-  return cudaLaunchKernelEx(&cfg, swiglu_fp8_kernel, static_cast<const uint16_t *>(gu), ldgu, rows, I, tile_rows,
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t *>(gu), ldgu, rows, I, tile_rows,
                             static_cast<uint16_t *>(h_out), ldh, q, scale);
 }
 

@@ -76,6 +76,16 @@ def test_random_rows(M, I, T):
     run_and_check(gu, T)
 
 
+@pytest.mark.parametrize("I", [86016, 90112, 102400])
+def test_wide_rows(I):
+    """Rows at the widest I that keeps the 32 KiB silu table beside the row
+    in shared memory (86016), and wider ones formed without it, up to the
+    largest I the call takes: the same bits either way."""
+    gu = synth.bf16_randn(2, 2 * I, seed=I, sigma=4.0, outlier_frac=0.001)
+    run_and_check(gu)
+    run_and_check(gu, 16)
+
+
 def test_special_rows():
     """A zero row (s = 1, codes +-0), a row whose gates all saturate to -0
     (h = -0 everywhere), rows with an infinite or NaN up value, a row with
