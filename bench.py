@@ -1071,6 +1071,9 @@ def _code_only(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
+GEMM_SOURCES = ("api.cu", "gemm.cu", "kernels.h", "ptx.cuh")
+
+
 def kernel_sources_hash():
     """Hash of the GEMM kernel's code (gemm.cu, the headers it includes, and
     api.cu, whose plan sets the tile order and so the DRAM traffic), comments
@@ -1078,7 +1081,7 @@ def kernel_sources_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_dynamic_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cuh", ".h")) or f in ("gemm.cu", "api.cu"):
+        if f in GEMM_SOURCES:
             with open(os.path.join(csrc, f), encoding="utf-8") as fh:
                 h.update(_code_only(fh.read()).encode())
     return h.hexdigest()

@@ -37,7 +37,6 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
-#include "quant_math.cuh"
 
 namespace mxg {
 namespace {

@@ -67,66 +67,87 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   const bool panel = tile_rows == kPanelLayout;
   const int KC = K >> 8;  // 128-byte code columns per row
   const int t_shift = (tile_rows > 0) ? __ffs(tile_rows) - 1 : 0;  // tile_rows is a power of 2
-  int cc[CPT];
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) cc[i] = (blockIdx.x * CPT + i) * kMxThreads + threadIdx.x;
+  // where a row's codes go: 128-byte column c at row_base + c * col_stride,
+  // its 16-byte unit j at ((j ^ rsw) * 16) (row-major: rsw = 0)
+  const size_t col_stride = panel ? (size_t)kMxPanelBytes : tile_rows > 0 ? (size_t)tile_rows * 128u : 128u;
+  // this thread's chunks c0 + 256 i, i < CPT: in the row or past it (cpr %
+  // 16 == 0: a half-warp is wholly inside the row or wholly past it; past
+  // it, it reads the row's first chunk so that the shuffles have data, and
+  // stores nothing).  Within a row, chunk i's codes go at code_col0 + i *
+  // code_step (the same 16-byte unit of a column 8 columns on) and its scale
+  // word at sf_col0 + i * sf_step (4 blocks = 16 chunks further on).
+  const int c0 = blockIdx.x * CPT * kMxThreads + threadIdx.x;
+  const size_t code_col0 = (size_t)(c0 >> 5) * col_stride + (size_t)((c0 * 4) & 15);
+  const size_t code_step = 8 * col_stride;
+  const uint32_t unit = (uint32_t)(c0 >> 2) & 7u;  // 16-byte unit of the column (byte 4 c0 / 16)
+  const int g0 = c0 >> 2;                          // first of the 4 blocks of a scale word
+  const size_t sf_col0 = panel       ? (size_t)(g0 >> 3) * 34816u + (size_t)((g0 >> 2) & 1) * 512u
+                         : kSwizzled ? (size_t)(g0 >> 2) * 512u
+                                     : (size_t)g0;
+  const size_t sf_step = panel ? 8u * 34816u : kSwizzled ? 16u * 512u : 64u;
+  const bool sf_lane = (lane & 15) == 0;
+  auto in_row = [&](int i) { return c0 + i * kMxThreads < cpr; };
+  uint8_t *const sf_dst = panel ? codes : sf;
   auto load_row = [&](int r, uint4 (&v)[CPT]) {
+    if (r >= rows) return;  // padding: not read
+    const uint16_t *xr = x + (size_t)r * ldx;
 #pragma unroll
-    for (int i = 0; i < CPT; ++i) {
-      v[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (r < rows && cc[i] < cpr) v[i] = ld_stream_v4(x + (size_t)r * ldx + (size_t)cc[i] * 8);
-    }
+    for (int i = 0; i < CPT; ++i) v[i] = ld_stream_v4(xr + (in_row(i) ? (size_t)(c0 + i * kMxThreads) * 8 : 0));
   };
-  uint4 v[CPT];
-  int r = blockIdx.y;
-  if (r < rows_iter) load_row(r, v);
-  for (; r < rows_iter; r += gridDim.y) {
-    // the next row's loads go out before this row's arithmetic
-    uint4 vn[CPT] = {};
-    if (r + (int)gridDim.y < rows_iter) load_row(r + gridDim.y, vn);
-    const bool real_row = r < rows;
-    // where this row's codes go: column c of the row at row_base + c *
-    // col_stride, its 16-byte unit j at ((j ^ rsw) * 16) (row-major: rsw = 0)
-    size_t row_base, col_stride;
-    int rsw;
+  auto do_row = [&](int r, const uint4 (&v)[CPT]) {
+    size_t row_base, sf_row;
+    uint32_t rsw;
     if (panel) {
       row_base = (size_t)(r >> 8) * KC * kMxPanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
-      col_stride = kMxPanelBytes;
       rsw = r & 7;
-    } else if (tile_rows > 0) {
-      const int rr = r & (tile_rows - 1);
-      row_base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
-      col_stride = (size_t)tile_rows * 128u;
-      rsw = rr & 7;
+      sf_row = (size_t)(r >> 8) * KC * 34816u + 32768u + (size_t)((r >> 7) & 1) * 1024u + (size_t)(r & 31) * 16u +
+               (size_t)((r >> 5) & 3) * 4u;
     } else {
-      row_base = (size_t)r * (K >> 1);
-      col_stride = 128;
-      rsw = 0;
+      if (tile_rows > 0) {
+        const int rr = r & (tile_rows - 1);
+        row_base = ((size_t)(r >> t_shift) * KC << (t_shift + 7)) + (size_t)rr * 128u;
+        rsw = rr & 7;
+      } else {
+        row_base = (size_t)r * (K >> 1);
+        rsw = 0;
+      }
+      sf_row = kSwizzled ? (size_t)(r >> 7) * (size_t)(G >> 2) * 512u + (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u
+                         : (size_t)r * G;
+    }
+    uint8_t *const code_at = codes + row_base + code_col0 + ((unit ^ rsw) << 4);
+    uint8_t *const sf_at = sf_dst + sf_row + sf_col0;
+    if (r >= rows) {  // padding (uniform over the CTA): zero scales, and zero codes in a panel
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        if (panel) st_global_b32_if(code_at + i * code_step, 0u, in_row(i));
+        st_global_b32_if(sf_at + i * sf_step, 0u, in_row(i) && sf_lane);
+      }
+      return;
     }
 #pragma unroll
     for (int i = 0; i < CPT; ++i) {
-      // cpr % 16 == 0: a half-warp is wholly inside the row or wholly past
-      // it; past the row it runs on zeros (the shuffles need every lane)
-      // and stores nothing.
-      const bool in_row = cc[i] < cpr;
       uint32_t scode;
       const uint32_t packed = mx_encode_chunk(v[i], scode);
-      if ((real_row || panel) && in_row) {
-        const int b = cc[i] * 4;  // byte of the row's codes
-        const size_t off = row_base + (size_t)(b >> 7) * col_stride + (size_t)((((b >> 4) & 7) ^ rsw) << 4) + (b & 15);
-        *reinterpret_cast<uint32_t *>(codes + off) = packed;
-      }
+      st_global_b32_if(code_at + i * code_step, packed, in_row(i));
       const uint32_t word = mx_scale_word(scode);
-      if (in_row && (lane & 15) == 0) {
-        const int g = cc[i] >> 2;  // first of the 4 blocks, g % 4 == 0
-        const size_t off = panel       ? panel_sf_offset(r, g, KC)
-                           : kSwizzled ? sf_swizzled_offset(r, g, G)
-                                       : (size_t)r * G + g;
-        *reinterpret_cast<uint32_t *>((panel ? codes : sf) + off) = word;
-      }
+      st_global_b32_if(sf_at + i * sf_step, word, in_row(i) && sf_lane);
     }
-#pragma unroll
-    for (int i = 0; i < CPT; ++i) v[i] = vn[i];
+  };
+  // two row buffers in turn: the next row's loads go out before this row's
+  // arithmetic, with no copy between the buffers
+  uint4 va[CPT], vb[CPT];
+  const int step = gridDim.y;
+  int r = blockIdx.y;
+  load_row(r, va);
+  while (r < rows_iter) {
+    const int r1 = r + step;
+    if (r1 < rows_iter) load_row(r1, vb);
+    do_row(r, va);
+    if (r1 >= rows_iter) break;
+    const int r2 = r1 + step;
+    if (r2 < rows_iter) load_row(r2, va);
+    do_row(r1, vb);
+    r = r2;
   }
 }
 

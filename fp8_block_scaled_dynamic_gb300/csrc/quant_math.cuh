@@ -1,5 +1,5 @@
-// quant_math.cuh -- the per-value arithmetic of the quantizers, shared by
-// the standalone quantizer kernels and the GEMM's fused activation phase.
+// quant_math.cuh -- the per-value arithmetic and the output layouts of the
+// quantizer kernels.
 //
 // OCP-MX MXFP4 ("Kimi-K3 DSpark O-Proj-only MXFP4", "Exact quantization
 // coverage"): a 32-value block gets the E8M0 scale e = clamp(floor(log2 amax)
@@ -86,14 +86,13 @@ __device__ __forceinline__ uint32_t mx_encode_chunk(const uint4 &w, uint32_t &sc
   uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16);
   amax = max(amax, __shfl_xor_sync(kFull, amax, 1));
   amax = max(amax, __shfl_xor_sync(kFull, amax, 2));
-  if (amax >= 0x7F80u) {  // the block holds Inf or NaN
-    scode = 0xFFu;
-    return 0u;
-  }
   // floor(log2 amax) = ef - 127 for a normal amax; a zero or subnormal amax
-  // clamps to e = -127 like ef in {1, 2}: e = max(ef, 2) - 129.
+  // clamps to e = -127 like ef in {1, 2}: e = max(ef, 2) - 129.  A block
+  // holding Inf or NaN (amax >= 0x7F80) gets scale code 0xFF and zero codes;
+  // its conversions below run on a finite 2^-e (ef <= 255) and are dropped.
+  const bool bad = amax >= 0x7F80u;
   const int ef = max(static_cast<int>(amax >> 7), 2);
-  scode = static_cast<uint32_t>(ef - 2);
+  scode = bad ? 0xFFu : static_cast<uint32_t>(ef - 2);
   const float inv = __uint_as_float(static_cast<uint32_t>(256 - ef) << 23);  // 2^-e
   // four conversions of two values each, the four code bytes packed by one
   // vector move (value 2i in the low nibble of byte i); the conversion keeps
@@ -108,17 +107,27 @@ __device__ __forceinline__ uint32_t mx_encode_chunk(const uint4 &w, uint32_t &sc
       : "=r"(packed)
       : "f"(bf16_lo(w.x) * inv), "f"(bf16_hi(w.x) * inv), "f"(bf16_lo(w.y) * inv), "f"(bf16_hi(w.y) * inv),
         "f"(bf16_lo(w.z) * inv), "f"(bf16_hi(w.z) * inv), "f"(bf16_lo(w.w) * inv), "f"(bf16_hi(w.w) * inv));
-  return packed;
+  return bad ? 0u : packed;
 }
 
 // The scales of 4 consecutive blocks (lanes 0, 4, 8, 12 of a half-warp) as
-// one 32-bit word, valid in lanes 0 and 16.  Every lane must call it.
+// one 32-bit word, valid in lanes 0 and 16: two blocks per word in lanes 0,
+// 8, 16, 24 first, then the pairs joined.  Every lane must call it.
 __device__ __forceinline__ uint32_t mx_scale_word(uint32_t scode) {
   const unsigned kFull = 0xFFFFFFFFu;
-  const uint32_t s1 = __shfl_down_sync(kFull, scode, 4);
-  const uint32_t s2 = __shfl_down_sync(kFull, scode, 8);
-  const uint32_t s3 = __shfl_down_sync(kFull, scode, 12);
-  return scode | (s1 << 8) | (s2 << 16) | (s3 << 24);
+  const uint32_t two = scode | (__shfl_down_sync(kFull, scode, 4) << 8);
+  return two | (__shfl_down_sync(kFull, two, 8) << 16);
+}
+
+// A 32-bit global store that only the lanes with `pred` make (a predicated
+// store, no branch around it).
+__device__ __forceinline__ void st_global_b32_if(void *p, uint32_t v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "@p st.global.b32 [%0], %1;\n\t}" ::"l"(p),
+      "r"(v), "r"((uint32_t)pred)
+      : "memory");
 }
 
 // Byte offset of the scale of (row r, block g) -- g % 4 == 0 for a word -- in
