@@ -88,11 +88,22 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   const bool sf_lane = (lane & 15) == 0;
   auto in_row = [&](int i) { return c0 + i * kMxThreads < cpr; };
   uint8_t *const sf_dst = panel ? codes : sf;
+  // this CTA's part of a row: chunks cta_c0 .. cta_c0 + cta_nc - 1
+  const int cta_c0 = blockIdx.x * CPT * kMxThreads;
+  const int cta_nc = min(CPT * kMxThreads, cpr - cta_c0);
   auto load_row = [&](int r, uint4 (&v)[CPT]) {
     if (r >= rows) return;  // padding: not read
     const uint16_t *xr = x + (size_t)r * ldx;
 #pragma unroll
     for (int i = 0; i < CPT; ++i) v[i] = ld_stream_v4(xr + (in_row(i) ? (size_t)(c0 + i * kMxThreads) * 8 : 0));
+    // the row two steps on heads for L2 now, so that its register loads
+    // (issued one row later) wait for L2, not for HBM
+    const int rp = r + 2 * (int)gridDim.y;
+    if (threadIdx.x == 0 && rp < rows && cta_nc > 0) {
+      const uint16_t *xp = x + (size_t)rp * ldx + (size_t)cta_c0 * 8;
+      for (int c = 0; c < cta_nc; c += 1024)
+        prefetch_l2_bulk(xp + (size_t)c * 8, (uint32_t)min(1024, cta_nc - c) * 16u);
+    }
   };
   auto do_row = [&](int r, const uint4 (&v)[CPT]) {
     size_t row_base, sf_row;
@@ -257,17 +268,16 @@ struct RowDivisor {
 };
 
 // 8 bf16 values -> 8 E4M3 bytes: q = E4M3_RNE_sat(x / s), the sign of x kept
-// on codes that round to zero.  kFast: the row's divisor is fast (the
+// on codes that round to zero (the correction step turns x = -0 into +0, so
+// the sign bits are set from x).  kFast: the row's divisor is fast (the
 // choice is made once per row, outside the loops over its chunks, so that
 // the division's instructions stay out of the fast loop).
 template <bool kFast>
 __device__ __forceinline__ uint2 fp8_quant8(const uint4 &w, const RowDivisor &d) {
   auto q = [&](float x) { return kFast ? d.correct(x) : __fdiv_rn(x, d.s); };
-  uint32_t lo = e4m3x2(q(bf16_lo(w.x)), q(bf16_hi(w.x))) | (e4m3x2(q(bf16_lo(w.y)), q(bf16_hi(w.y))) << 16);
-  uint32_t hi = e4m3x2(q(bf16_lo(w.z)), q(bf16_hi(w.z))) | (e4m3x2(q(bf16_lo(w.w)), q(bf16_hi(w.w))) << 16);
-  lo |= byte_signs(w.x) | (byte_signs(w.y) << 16);
-  hi |= byte_signs(w.z) | (byte_signs(w.w) << 16);
-  return make_uint2(lo, hi);
+  const uint32_t lo = e4m3x2(q(bf16_lo(w.x)), q(bf16_hi(w.x))) | (e4m3x2(q(bf16_lo(w.y)), q(bf16_hi(w.y))) << 16);
+  const uint32_t hi = e4m3x2(q(bf16_lo(w.z)), q(bf16_hi(w.z))) | (e4m3x2(q(bf16_lo(w.w)), q(bf16_hi(w.w))) << 16);
+  return make_uint2(lo | e4m3_signs4(w.x, w.y), hi | e4m3_signs4(w.z, w.w));
 }
 
 // Runs f(std::true_type) on a fast row, f(std::false_type) otherwise.
@@ -390,29 +400,43 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
   const int cpr = K >> 3;  // <= kF8Hold * kF8Threads
   const int tid = threadIdx.x;
   if (early_trigger) pdl_trigger();
-  pdl_wait();
-  int parity = 0;
-  // a row's chunks (zeros past the row and on padding rows); the next row's
-  // loads go out before this row's reduction and codes
-  auto load_row = [&](int r, uint4 (&v)[kF8Hold]) {
-    const uint16_t *xr = x + (size_t)r * ldx;
-#pragma unroll
-    for (int i = 0; i < kF8Hold; ++i) {
-      const int c = tid + i * kF8Threads;
-      v[i] = (r < rows && c < cpr) ? ld_stream_v4(xr + (size_t)c * 8) : make_uint4(0u, 0u, 0u, 0u);
+  // warm L2 with the CTA's first two rows while the kernel ahead finishes
+  auto prefetch_row = [&](int r) {
+    if (tid == 0 && r < rows) {
+      const uint16_t *xr = x + (size_t)r * ldx;
+      for (int c = 0; c < cpr; c += 1024) prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
     }
   };
-  uint4 vn[kF8Hold];
-  if ((int)blockIdx.x < rows_iter) load_row(blockIdx.x, vn);
-  for (int r = blockIdx.x; r < rows_iter; r += gridDim.x) {
-    uint4 v[kF8Hold];
+  prefetch_row(blockIdx.x);
+  prefetch_row(blockIdx.x + gridDim.x);
+  pdl_wait();
+  // this thread's chunks tid + 256 i, i < kF8Hold: in the row or past it
+  // (past it, a thread reads the row's first chunk -- a repeat does not
+  // change the row's amax -- and stores nothing).  Within a row, chunk i's
+  // codes go at col0 + i * step (the same 16-byte unit of a column 16
+  // columns on).
+  const size_t col_stride = tile_rows == kPanelLayout ? (size_t)kF8PanelBytes
+                            : tile_rows > 0           ? (size_t)tile_rows * 128u
+                                                      : 128u;
+  const size_t col0 = (size_t)(tid >> 4) * col_stride + (size_t)((tid & 1) * 8);
+  const size_t step = 16 * col_stride;
+  const uint32_t unit = (uint32_t)(tid >> 1) & 7u;
+  auto in_row = [&](int i) { return tid + i * kF8Threads < cpr; };
+  auto load_row = [&](int r, uint4 (&v)[kF8Hold]) {
+    if (r >= rows) return;  // padding: not read
+    const uint16_t *xr = x + (size_t)r * ldx;
 #pragma unroll
-    for (int i = 0; i < kF8Hold; ++i) v[i] = vn[i];
-    if (r + (int)gridDim.x < rows_iter) load_row(r + gridDim.x, vn);
+    for (int i = 0; i < kF8Hold; ++i) v[i] = ld_stream_v4(xr + (in_row(i) ? (size_t)(tid + i * kF8Threads) * 8 : 0));
+    prefetch_row(r + 2 * (int)gridDim.x);  // two steps on: to L2 now, into registers one row later
+  };
+  int parity = 0;
+  auto do_row = [&](int r, const uint4 (&v)[kF8Hold]) {
     const Fp8RowDest dst(r, K, tile_rows);
-    if (r >= rows) {  // panel padding (uniform over the CTA)
-      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
-      continue;
+    uint8_t *const at = q + dst.base + col0 + ((unit ^ (uint32_t)dst.rsw) << 4);
+    if (r >= rows) {  // panel padding (uniform over the CTA): zero bytes, no scale
+#pragma unroll
+      for (int i = 0; i < kF8Hold; ++i) st_global_v2_if(at + i * step, make_uint2(0u, 0u), in_row(i));
+      return;
     }
     uint32_t amax = 0;
 #pragma unroll
@@ -430,19 +454,34 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
     parity ^= 1;
     if (amax >= 0x7F80u) {  // Inf or NaN in the row
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
-      for (int c = tid; c < cpr; c += kF8Threads) *dst.chunk(q, c) = make_uint2(0u, 0u);
-      continue;
+#pragma unroll
+      for (int i = 0; i < kF8Hold; ++i) st_global_v2_if(at + i * step, make_uint2(0u, 0u), in_row(i));
+      return;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
     const RowDivisor dv(s);
     by_divisor(dv, [&](auto fast) {
 #pragma unroll
-      for (int i = 0; i < kF8Hold; ++i) {
-        const int c = tid + i * kF8Threads;
-        if (c < cpr) *dst.chunk(q, c) = fp8_quant8<decltype(fast)::value>(v[i], dv);
-      }
+      for (int i = 0; i < kF8Hold; ++i)
+        st_global_v2_if(at + i * step, fp8_quant8<decltype(fast)::value>(v[i], dv), in_row(i));
     });
+  };
+  // two row buffers in turn: the next row's loads go out before this row's
+  // reduction and codes, with no copy between the buffers
+  uint4 va[kF8Hold], vb[kF8Hold];
+  const int stride = gridDim.x;
+  int r = blockIdx.x;
+  load_row(r, va);
+  while (r < rows_iter) {
+    const int r1 = r + stride;
+    if (r1 < rows_iter) load_row(r1, vb);
+    do_row(r, va);
+    if (r1 >= rows_iter) break;
+    const int r2 = r1 + stride;
+    if (r2 < rows_iter) load_row(r2, va);
+    do_row(r1, vb);
+    r = r2;
   }
 }
 

@@ -35,11 +35,17 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Sign bits of the two bf16 in `w`, moved to bits 7 and 15 (the sign bits
-// of the two E4M3 bytes).
-__device__ __forceinline__ uint32_t byte_signs(uint32_t w) {
-  return ((w >> 8) & 0x80u) | ((w >> 16) & 0x8000u);
+// The sign bits of the four bf16 values in (a, b) (a's low, a's high, b's
+// low, b's high) at bits 7, 15, 23 and 31: the sign bits of their four E4M3
+// bytes.  One byte permute whose selectors (source bytes 1, 3, 5, 7, the
+// high bytes of the four values) have the sign-replicate bit set, then the
+// byte sign bits kept.
+__device__ __forceinline__ uint32_t e4m3_signs4(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, 0xFDB9;" : "=r"(r) : "r"(a), "r"(b));
+  return r & 0x80808080u;
 }
+
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint16_t *p) {
   uint4 v;
@@ -117,6 +123,16 @@ __device__ __forceinline__ uint32_t mx_scale_word(uint32_t scode) {
   const unsigned kFull = 0xFFFFFFFFu;
   const uint32_t two = scode | (__shfl_down_sync(kFull, scode, 4) << 8);
   return two | (__shfl_down_sync(kFull, two, 8) << 16);
+}
+
+// A 64-bit global store that only the lanes with `pred` make.
+__device__ __forceinline__ void st_global_v2_if(void *p, uint2 v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "@p st.global.v2.b32 [%0], {%1, %2};\n\t}" ::"l"(p),
+      "r"(v.x), "r"(v.y), "r"((uint32_t)pred)
+      : "memory");
 }
 
 // A 32-bit global store that only the lanes with `pred` make (a predicated
