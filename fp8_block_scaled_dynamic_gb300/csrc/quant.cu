@@ -384,32 +384,62 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
   }
 }
 
-// The same per-row FP8 quantization for large inputs with K <= 8192: one
-// read of the row, held in registers (kF8Hold chunks of 8 values per thread)
-// between its amax and its codes.  (The two-pass kernel above, at 40
-// registers, is kept for decode-sized inputs, whose CTAs sit beside GEMM CTAs
-// of a layer chain.)
+// The same per-row FP8 quantization for large inputs with K <= 8192: the
+// CTA's rows stream into a ring of kF8Slots row buffers in shared memory by
+// bulk copies (one thread issues them; the bytes in flight are not bounded
+// by registers), each row read from shared memory once into registers
+// (kF8Hold chunks of 8 values per thread), reduced, and quantized.  (The
+// two-pass kernel above, at 40 registers and no shared memory, is kept for
+// decode-sized inputs, whose CTAs sit beside GEMM CTAs of a layer chain.)
 constexpr int kF8Hold = 4;
+constexpr int kF8Slots = 4;
+constexpr uint64_t kQuantWaitNs = 1000000000ull;  // a copy that has not landed in 1 s never will
 
-__global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16_t *__restrict__ x,
-                                                                    long long ldx, int rows, int rows_iter,
-                                                                    int K, int tile_rows, int early_trigger,
-                                                                    uint8_t *__restrict__ q,
-                                                                    float *__restrict__ scale) {
+// Bounded wait for a copy still in flight before the CTA exits (its shared
+// memory must not be reused while the copy can still write it).
+__device__ __forceinline__ void drain_copy(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kQuantWaitNs) return;
+}
+
+size_t fp8_staged_smem(int K) { return (size_t)kF8Slots * ((size_t)K * 2u) + 8u * kF8Slots; }
+
+__global__ void __launch_bounds__(kF8Threads) fp8_quant_staged_kernel(const uint16_t *__restrict__ x,
+                                                                      long long ldx, int rows, int rows_iter,
+                                                                      int K, int tile_rows, int early_trigger,
+                                                                      uint8_t *__restrict__ q,
+                                                                      float *__restrict__ scale) {
+  extern __shared__ __align__(128) uint8_t ring[];  // kF8Slots rows of K bf16, then one mbarrier a slot
   __shared__ uint32_t red[2][kF8Threads / 32];
+  __shared__ int abort_flag;
   const int cpr = K >> 3;  // <= kF8Hold * kF8Threads
   const int tid = threadIdx.x;
+  const uint32_t row_bytes = (uint32_t)K * 2u;  // a multiple of 256
+  const uint32_t slots = smem_addr(ring);
+  const uint32_t bars = slots + kF8Slots * row_bytes;
   if (early_trigger) pdl_trigger();
-  // warm L2 with the CTA's first two rows while the kernel ahead finishes
-  auto prefetch_row = [&](int r) {
-    if (tid == 0 && r < rows) {
-      const uint16_t *xr = x + (size_t)r * ldx;
-      for (int c = 0; c < cpr; c += 1024) prefetch_l2_bulk(xr + (size_t)c * 8, (uint32_t)min(1024, cpr - c) * 16u);
-    }
+  if (tid == 0) {
+    for (int i = 0; i < kF8Slots; ++i) mbar_init(bars + 8u * i, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();  // x may be the previous kernel's output
+  const WaitCtl ctl{&abort_flag, nullptr, kQuantWaitNs};
+  // row k of this CTA is blockIdx.x + k * gridDim.x; thread 0 copies it into
+  // slot k % kF8Slots (rows past the input -- panel padding -- are not read)
+  auto row_of = [&](int k) { return (int)blockIdx.x + k * (int)gridDim.x; };
+  auto issue = [&](int k) {
+    const int r = row_of(k);
+    if (r >= rows) return;
+    const uint32_t bar = bars + 8u * (uint32_t)(k % kF8Slots);
+    mbar_arrive_expect_tx(bar, row_bytes);
+    bulk_load(slots + (uint32_t)(k % kF8Slots) * row_bytes, x + (size_t)r * ldx, row_bytes, bar,
+              policy_evict_first());
   };
-  prefetch_row(blockIdx.x);
-  prefetch_row(blockIdx.x + gridDim.x);
-  pdl_wait();
+  if (tid == 0)
+    for (int k = 0; k < kF8Slots; ++k) issue(k);
   // this thread's chunks tid + 256 i, i < kF8Hold: in the row or past it
   // (past it, a thread reads the row's first chunk -- a repeat does not
   // change the row's amax -- and stores nothing).  Within a row, chunk i's
@@ -422,22 +452,30 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
   const size_t step = 16 * col_stride;
   const uint32_t unit = (uint32_t)(tid >> 1) & 7u;
   auto in_row = [&](int i) { return tid + i * kF8Threads < cpr; };
-  auto load_row = [&](int r, uint4 (&v)[kF8Hold]) {
-    if (r >= rows) return;  // padding: not read
-    const uint16_t *xr = x + (size_t)r * ldx;
-#pragma unroll
-    for (int i = 0; i < kF8Hold; ++i) v[i] = ld_stream_v4(xr + (in_row(i) ? (size_t)(tid + i * kF8Threads) * 8 : 0));
-    prefetch_row(r + 2 * (int)gridDim.x);  // two steps on: to L2 now, into registers one row later
-  };
   int parity = 0;
-  auto do_row = [&](int r, const uint4 (&v)[kF8Hold]) {
+  for (int k = 0; row_of(k) < rows_iter; ++k) {
+    const int r = row_of(k);
     const Fp8RowDest dst(r, K, tile_rows);
     uint8_t *const at = q + dst.base + col0 + ((unit ^ (uint32_t)dst.rsw) << 4);
-    if (r >= rows) {  // panel padding (uniform over the CTA): zero bytes, no scale
+    if (r >= rows) {  // panel padding (uniform over the CTA; after every real row): zero bytes, no scale
 #pragma unroll
       for (int i = 0; i < kF8Hold; ++i) st_global_v2_if(at + i * step, make_uint2(0u, 0u), in_row(i));
+      continue;
+    }
+    const uint32_t slot = slots + (uint32_t)(k % kF8Slots) * row_bytes;
+    const bool landed = mbar_wait(bars + 8u * (uint32_t)(k % kF8Slots), (uint32_t)(k / kF8Slots) & 1u, ctl);
+    if (__syncthreads_or(!landed)) {
+      // a copy did not land: let every copy still in flight finish (bounded),
+      // mark this CTA's rows from here on with NaN scales, and leave
+      if (tid == 0)
+        for (int j = k; j < k + kF8Slots; ++j)
+          if (row_of(j) < rows) drain_copy(bars + 8u * (uint32_t)(j % kF8Slots), (uint32_t)(j / kF8Slots) & 1u);
+      for (int j = k; tid == 0 && row_of(j) < rows; ++j) scale[row_of(j)] = __uint_as_float(0x7FC00000u);
       return;
     }
+    uint4 v[kF8Hold];
+#pragma unroll
+    for (int i = 0; i < kF8Hold; ++i) v[i] = ld_shared_v4(slot + (in_row(i) ? (uint32_t)(tid + i * kF8Threads) * 16u : 0u));
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < kF8Hold; ++i) amax = max(amax, amax_bf16x8(v[i]));
@@ -447,7 +485,11 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
     // barrier a row suffices (a buffer is rewritten only after the barrier
     // of the row between, which every reader of it has passed)
     if ((tid & 31) == 0) red[parity][tid >> 5] = amax;
-    __syncthreads();
+    __syncthreads();  // also: every thread has read its chunks of the slot
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      issue(k + kF8Slots);  // the slot's next row
+    }
     amax = red[parity][0];
 #pragma unroll
     for (int i = 1; i < kF8Threads / 32; ++i) amax = max(amax, red[parity][i]);
@@ -456,7 +498,7 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
       if (tid == 0) scale[r] = __uint_as_float(0x7FC00000u);
 #pragma unroll
       for (int i = 0; i < kF8Hold; ++i) st_global_v2_if(at + i * step, make_uint2(0u, 0u), in_row(i));
-      return;
+      continue;
     }
     const float s = (amax == 0u) ? 1.0f : __fdiv_rn(__uint_as_float(amax << 16), 448.0f);
     if (tid == 0) scale[r] = s;
@@ -466,22 +508,6 @@ __global__ void __launch_bounds__(kF8Threads) fp8_quant_hold_kernel(const uint16
       for (int i = 0; i < kF8Hold; ++i)
         st_global_v2_if(at + i * step, fp8_quant8<decltype(fast)::value>(v[i], dv), in_row(i));
     });
-  };
-  // two row buffers in turn: the next row's loads go out before this row's
-  // reduction and codes, with no copy between the buffers
-  uint4 va[kF8Hold], vb[kF8Hold];
-  const int stride = gridDim.x;
-  int r = blockIdx.x;
-  load_row(r, va);
-  while (r < rows_iter) {
-    const int r1 = r + stride;
-    if (r1 < rows_iter) load_row(r1, vb);
-    do_row(r, va);
-    if (r1 >= rows_iter) break;
-    const int r2 = r1 + stride;
-    if (r2 < rows_iter) load_row(r2, va);
-    do_row(r1, vb);
-    r = r2;
   }
 }
 
@@ -717,17 +743,31 @@ cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint
                              cudaStream_t stream) {
   const int rows_iter =
       tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows : rows;
-  // large inputs whose rows fit in the CTA's registers: one read of each row
-  auto kern = (rows > 512 && K / 8 <= kF8Hold * kF8Threads) ? fp8_quant_hold_kernel : fp8_quant_kernel;
+  // large inputs whose rows fit in the CTA's registers: rows staged in
+  // shared memory by bulk copies, one read of each
+  const bool staged = rows > 512 && K / 8 <= kF8Hold * kF8Threads;
+  auto kern = staged ? fp8_quant_staged_kernel : fp8_quant_kernel;
+  const size_t smem = staged ? fp8_staged_smem(K) : 0;
   cudaError_t e = prefer_shared_carveout(kern);
   if (e != cudaSuccess) return e;
+  if (staged) {
+    static DeviceOnce once;
+    int dev = -1;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (!once.done(dev)) {
+      e = cudaFuncSetAttribute(fp8_quant_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)fp8_staged_smem(8192));
+      if (e != cudaSuccess) return e;
+      once.set(dev);
+    }
+  }
   // one CTA per row, at most as many as are resident at once (one wave)
   int per_sm = 1;
-  if ((e = resident_ctas_per_sm(kern, kF8Threads, 0, &per_sm)) != cudaSuccess) return e;
+  if ((e = resident_ctas_per_sm(kern, kF8Threads, smem, &per_sm)) != cudaSuccess) return e;
   int g = rows_iter;
   const int cap = (sm_count > 0 ? sm_count : 152) * per_sm;
   if (g > cap) g = cap;
-  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), 0, stream);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(g), dim3(kF8Threads), smem, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t *>(x), ldx, rows, rows_iter, K, tile_rows,

@@ -12,7 +12,7 @@ import torch
 import fp8_block_scaled_dynamic_gb300 as mx
 import oracle
 import synth
-from gpu_util import assert_codes_equal, dev, np_u8
+from gpu_util import assert_codes_equal, dev, np_u8, untile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -160,6 +160,45 @@ def test_fp8_special_rows():
                                  (2, 24576), (2, 24704), (5, 30720)])
 def test_fp8_act_shapes(M, K):
     check_fp8(synth.activation(M, K, seed=M * 7 + K), f"act {M}x{K}")
+
+
+def staged_rows(M, K, seed):
+    """More than 512 rows of K <= 8192 values (the quantizer that streams
+    rows through shared memory): every finite bf16 value below 448 in rows
+    whose first value is 448 (s = 1), then a zero row, an all -0 row, a row
+    with a NaN and one with -Inf, then seeded activations."""
+    vals = np.arange(0, 0x43E0, dtype=np.uint16)
+    vals = np.concatenate([vals, vals | 0x8000])
+    per_row = K - 1
+    n = -(-len(vals) // per_row)
+    vals = np.concatenate([vals, np.zeros(n * per_row - len(vals), np.uint16)]).reshape(n, per_row)
+    ex = np.concatenate([np.full((n, 1), 0x43E0, np.uint16), vals], 1)
+    special = np.zeros((4, K), np.uint16)
+    special[1, :] = 0x8000
+    special[2, :] = 0x3F80
+    special[2, K // 3] = 0x7FC0
+    special[3, :] = 0xBF80
+    special[3, K - 1] = 0xFF80
+    rest = synth.activation(M - n - 4, K, seed=seed).view(torch.int16).numpy().view(np.uint16)
+    x = np.concatenate([ex, special, rest])
+    assert x.shape[0] == M > 512
+    return bits_to_bf16(x)
+
+
+@pytest.mark.parametrize("M,K", [(700, 256), (600, 7168)])
+def test_fp8_rows_through_shared_memory(M, K):
+    """Exhaustive values, special rows and ragged rows (K = 256: most of a
+    CTA's threads lie past the row) on the shared-memory-staged quantizer,
+    row-major and in token tiles."""
+    x = staged_rows(M, K, seed=M + K)
+    check_fp8(x, f"staged {M}x{K}")
+    q_ref, s_ref = oracle.fp8_quantize_rows(x)
+    for T in (64, 128):
+        q, s = mx.fp8_quantize_act_tiled(x.to(dev()), T)
+        rows = -(-M // T) * T
+        assert_codes_equal(untile_rows(np_u8(q), rows, K, T)[:M], q_ref, f"staged tiles {T} codes")
+        sc = s.cpu().numpy()
+        assert_codes_equal(sc.view(np.uint32), s_ref.view(np.uint32), f"staged tiles {T} scales")
 
 
 @pytest.mark.parametrize("K", [8320, 30720])
