@@ -36,11 +36,28 @@ constexpr int kMxThreads = 256;
 // tile_rows: 0 = row-major codes, kPanelLayout = weight panels (codes and
 // scales; padding rows get zero codes), else the tile layout with that tile
 // height.
-// CPT: 16-byte chunks per thread per row, independent loads in flight (4 for
-// large inputs: a CTA covers a whole 8192-value row and its per-row address
-// work is shared by more chunks; 2 for decode-sized inputs, whose latency
-// wants more, smaller CTAs).
-template <bool kSwizzled, int CPT>
+// CPT: 16-byte chunks per thread per row (4 for large inputs: a CTA covers a
+// whole 8192-value row and its per-row address work is shared by more
+// chunks; 2 for decode-sized inputs, whose latency wants more, smaller CTAs).
+// kStaged (large inputs): the CTA's parts of its rows stream into a ring of
+// kMxSlots buffers in shared memory by bulk copies that one thread issues,
+// so that the bytes in flight are not bounded by registers; otherwise two
+// row buffers in registers are used in turn.
+constexpr uint64_t kQuantWaitNs = 1000000000ull;  // a copy that has not landed in 1 s never will
+
+// Bounded wait for a copy still in flight before the CTA exits (its shared
+// memory must not be reused while the copy can still write it).
+__device__ __forceinline__ void drain_copy(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kQuantWaitNs) return;
+}
+
+constexpr int kMxSlots = 2;
+constexpr uint32_t kMxSlotBytes = 4 * kMxThreads * 16;  // a CTA's part of a row at CPT = 4
+constexpr size_t kMxStagedSmem = (size_t)kMxSlots * kMxSlotBytes + 8u * kMxSlots;
+
+template <bool kSwizzled, int CPT, bool kStaged>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
                                                               long long ldx, int rows,
                                                               int rows_iter, int K, int tile_rows,
@@ -105,9 +122,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
         prefetch_l2_bulk(xp + (size_t)c * 8, (uint32_t)min(1024, cta_nc - c) * 16u);
     }
   };
-  auto do_row = [&](int r, const uint4 (&v)[CPT]) {
-    size_t row_base, sf_row;
-    uint32_t rsw;
+  // where row r's codes and scale words go
+  auto row_dest = [&](int r, size_t &row_base, size_t &sf_row, uint32_t &rsw) {
     if (panel) {
       row_base = (size_t)(r >> 8) * KC * kMxPanelBytes + (size_t)((r >> 7) & 1) * 16384u + (size_t)(r & 127) * 128u;
       rsw = r & 7;
@@ -125,6 +141,11 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       sf_row = kSwizzled ? (size_t)(r >> 7) * (size_t)(G >> 2) * 512u + (size_t)(r & 31) * 16u + (size_t)((r >> 5) & 3) * 4u
                          : (size_t)r * G;
     }
+  };
+  auto do_row = [&](int r, const uint4 (&v)[CPT]) {
+    size_t row_base, sf_row;
+    uint32_t rsw;
+    row_dest(r, row_base, sf_row, rsw);
     uint8_t *const code_at = codes + row_base + code_col0 + ((unit ^ rsw) << 4);
     uint8_t *const sf_at = sf_dst + sf_row + sf_col0;
     if (r >= rows) {  // padding (uniform over the CTA): zero scales, and zero codes in a panel
@@ -144,21 +165,83 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
       st_global_b32_if(sf_at + i * sf_step, word, in_row(i) && sf_lane);
     }
   };
-  // two row buffers in turn: the next row's loads go out before this row's
-  // arithmetic, with no copy between the buffers
   uint4 va[CPT], vb[CPT];
-  const int step = gridDim.y;
-  int r = blockIdx.y;
-  load_row(r, va);
-  while (r < rows_iter) {
-    const int r1 = r + step;
-    if (r1 < rows_iter) load_row(r1, vb);
-    do_row(r, va);
-    if (r1 >= rows_iter) break;
-    const int r2 = r1 + step;
-    if (r2 < rows_iter) load_row(r2, va);
-    do_row(r1, vb);
-    r = r2;
+  if constexpr (kStaged) {
+    extern __shared__ __align__(128) uint8_t ring[];  // kMxSlots row parts, then one mbarrier a slot
+    __shared__ int abort_flag;
+    const uint32_t slots = smem_addr(ring);
+    const uint32_t bars = slots + kMxSlots * kMxSlotBytes;
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < kMxSlots; ++i) mbar_init(bars + 8u * i, 1);
+      abort_flag = 0;
+      fence_barrier_init();
+    }
+    __syncthreads();
+    const WaitCtl ctl{&abort_flag, nullptr, kQuantWaitNs};
+    const uint32_t part_bytes = (uint32_t)cta_nc * 16u;  // cta_nc % 16 == 0
+    // row k of this CTA is blockIdx.y + k * gridDim.y; thread 0 copies its
+    // part into slot k % kMxSlots (padding rows are not read)
+    auto row_of = [&](int k) { return (int)blockIdx.y + k * (int)gridDim.y; };
+    auto issue = [&](int k) {
+      const int r = row_of(k);
+      if (r >= rows || cta_nc <= 0) return;
+      const uint32_t bar = bars + 8u * (uint32_t)(k % kMxSlots);
+      mbar_arrive_expect_tx(bar, part_bytes);
+      bulk_load(slots + (uint32_t)(k % kMxSlots) * kMxSlotBytes, x + (size_t)r * ldx + (size_t)cta_c0 * 8, part_bytes,
+                bar, policy_evict_first());
+    };
+    if (threadIdx.x == 0)
+      for (int k = 0; k < kMxSlots; ++k) issue(k);
+    for (int k = 0; row_of(k) < rows_iter; ++k) {
+      const int r = row_of(k);
+      if (r >= rows) {  // padding (uniform over the CTA; after every real row)
+        do_row(r, va);
+        continue;
+      }
+      const bool landed = mbar_wait(bars + 8u * (uint32_t)(k % kMxSlots), (uint32_t)(k / kMxSlots) & 1u, ctl);
+      if (__syncthreads_or(!landed)) {
+        // a copy did not land: let every copy still in flight finish
+        // (bounded), give this CTA's remaining rows NaN scales (E8M0 0xFF),
+        // and leave
+        if (threadIdx.x == 0)
+          for (int j = k; j < k + kMxSlots; ++j)
+            if (row_of(j) < rows) drain_copy(bars + 8u * (uint32_t)(j % kMxSlots), (uint32_t)(j / kMxSlots) & 1u);
+        for (int j = k; row_of(j) < rows; ++j) {
+          size_t row_base, sf_row;
+          uint32_t rsw;
+          row_dest(row_of(j), row_base, sf_row, rsw);
+#pragma unroll
+          for (int i = 0; i < CPT; ++i) st_global_b32_if(sf_dst + sf_row + sf_col0 + i * sf_step, 0xFFFFFFFFu, in_row(i) && sf_lane);
+        }
+        return;
+      }
+      const uint32_t slot = slots + (uint32_t)(k % kMxSlots) * kMxSlotBytes;
+#pragma unroll
+      for (int i = 0; i < CPT; ++i)
+        va[i] = ld_shared_v4(slot + (in_row(i) ? (uint32_t)(threadIdx.x + i * kMxThreads) * 16u : 0u));
+      __syncthreads();  // every thread has read its chunks of the slot
+      if (threadIdx.x == 0) {
+        fence_proxy_async_smem();
+        issue(k + kMxSlots);  // the slot's next row
+      }
+      do_row(r, va);
+    }
+  } else {
+    // two row buffers in turn: the next row's loads go out before this row's
+    // arithmetic, with no copy between the buffers
+    const int step = gridDim.y;
+    int r = blockIdx.y;
+    load_row(r, va);
+    while (r < rows_iter) {
+      const int r1 = r + step;
+      if (r1 < rows_iter) load_row(r1, vb);
+      do_row(r, va);
+      if (r1 >= rows_iter) break;
+      const int r2 = r1 + step;
+      if (r2 < rows_iter) load_row(r2, va);
+      do_row(r1, vb);
+      r = r2;
+    }
   }
 }
 
@@ -392,17 +475,7 @@ __global__ void __maxnreg__(40) fp8_quant_kernel(const uint16_t *__restrict__ x,
 // two-pass kernel above, at 40 registers and no shared memory, is kept for
 // decode-sized inputs, whose CTAs sit beside GEMM CTAs of a layer chain.)
 constexpr int kF8Hold = 4;
-constexpr int kF8Slots = 4;
-constexpr uint64_t kQuantWaitNs = 1000000000ull;  // a copy that has not landed in 1 s never will
-
-// Bounded wait for a copy still in flight before the CTA exits (its shared
-// memory must not be reused while the copy can still write it).
-__device__ __forceinline__ void drain_copy(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_timer_ns() - t0 > kQuantWaitNs) return;
-}
-
+constexpr int kF8Slots = 3;
 size_t fp8_staged_smem(int K) { return (size_t)kF8Slots * ((size_t)K * 2u) + 8u * kF8Slots; }
 
 __global__ void __launch_bounds__(kF8Threads) fp8_quant_staged_kernel(const uint16_t *__restrict__ x,
@@ -714,24 +787,35 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   const int rows_iter = tile_rows == kPanelLayout ? ((rows + kPanelRows - 1) / kPanelRows) * kPanelRows
                         : swizzled                   ? ((rows + 127) / 128) * 128
                                                      : rows;
-  auto kern = swizzled ? (big ? mx_quant_kernel<true, 4> : mx_quant_kernel<true, 2>)
-                       : (big ? mx_quant_kernel<false, 4> : mx_quant_kernel<false, 2>);
+  auto kern = swizzled ? (big ? mx_quant_kernel<true, 4, true> : mx_quant_kernel<true, 2, false>)
+                       : (big ? mx_quant_kernel<false, 4, true> : mx_quant_kernel<false, 2, false>);
+  const size_t smem = big ? kMxStagedSmem : 0;
   cudaError_t e = prefer_shared_carveout(kern);
   if (e != cudaSuccess) return e;
+  if (big) {
+    static DeviceOnce once[2];
+    int dev = -1;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (!once[swizzled].done(dev)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxStagedSmem);
+      if (e != cudaSuccess) return e;
+      once[swizzled].set(dev);
+    }
+  }
   // as many CTAs as are resident at once (one wave), rows beyond that
   // grid-strided; for a decode-sized activation (a few hundred rows at most)
   // one CTA per SM: launched early beside the GEMMs of a layer chain, a
   // second quantizer CTA on an SM would leave no registers for the next GEMM
   // CTA
   int per_sm = 1;
-  if (!(act && rows <= 512) && (e = resident_ctas_per_sm(kern, kMxThreads, 0, &per_sm)) != cudaSuccess) return e;
+  if (!(act && rows <= 512) && (e = resident_ctas_per_sm(kern, kMxThreads, smem, &per_sm)) != cudaSuccess) return e;
   int gy = rows_iter;
   const int sms = sm_count > 0 ? sm_count : 152;
   const int cap = sms * per_sm;
   if (gy * gx > cap) gy = (cap + gx - 1) / gx;
   if (gy > 65535) gy = 65535;
   if (gy < 1) gy = 1;
-  cudaLaunchConfig_t cfg = pdl_config(dim3(gx, gy), dim3(kMxThreads), 0, stream);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(gx, gy), dim3(kMxThreads), smem, stream);
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
