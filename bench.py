@@ -1175,6 +1175,7 @@ def run_ours(args, rank, world, local_rank):
             r2 = measure(w2, stream, flush, steps, args.warmup, 0.2, local_rank, world, e2e=False)
             r2["ms"], r2["kernel_ms"] = max_over_ranks([r2["ms"], r2["kernel_ms"]], dev, world)
             e = workload_summary(w2, r2, hbm, bf16, peak_src, world)
+            e["roofline"]["traffic"] = traffic_record(key)
             e["steps"] = steps
             e["workload"] = w2.name
             extras[key] = e
