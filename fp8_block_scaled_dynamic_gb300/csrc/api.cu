@@ -103,6 +103,10 @@ size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 constexpr uint64_t kL2KeepBytes = 96ull << 20;
 constexpr uint64_t kL2ActBudget = 32ull << 20;
 
+// The split-K reduce kernel chained behind a GEMM, in K-stages of one CTA's
+// time (see plan_impl).
+constexpr long long kReduceStages = 7;
+
 // CTA that owns stream-K unit u (must equal the device-side owner_of).
 long long owner_of(long long u, long long U, long long G) { return ((u + 1) * G - 1) / U; }
 
@@ -164,12 +168,26 @@ mxg_status plan_impl(int kind, int M, int N, int K, int sm_count, const mxg_gemm
     const long long U = tiles * KB;
     if (U > (1LL << 40) / 4) return MXG_ERR_UNSUPPORTED_SHAPE;
     // persistent: at most one CTA per SM
-    long long G = (opts && opts->ctas > 0 && opts->ctas < sm_count) ? opts->ctas : sm_count;
+    const bool fixed = opts && opts->ctas > 0;
+    long long G = (fixed && opts->ctas < sm_count) ? opts->ctas : sm_count;
     if (G > U) G = U;
-    int seg_max = 1;
-    for (long long t = 0; t < tiles; ++t) {
-      const long long n = owner_of(t * KB + KB - 1, U, G) - owner_of(t * KB, U, G) + 1;
-      if (n > seg_max) seg_max = (int)n;
+    auto segments = [&](long long g) {  // most CTAs that share one tile
+      int sm_ = 1;
+      for (long long t = 0; t < tiles; ++t) {
+        const long long n = owner_of(t * KB + KB - 1, U, g) - owner_of(t * KB, U, g) + 1;
+        if (n > sm_) sm_ = (int)n;
+      }
+      return sm_;
+    };
+    int seg_max = segments(G);
+    // Without a CTA count from the caller: whole tiles (one CTA a tile, no
+    // partial sums, no reduce kernel) when they fit in one wave and cost no
+    // more than stream-K does.  Measured on GB300, a CTA's time grows by about
+    // one unit per K-stage it takes (~0.5 us) and the reduce kernel chained
+    // behind the GEMM costs about kReduceStages of them (~3.5 us).
+    if (!fixed && tiles <= sm_count && seg_max > 1 && KB <= (U + G - 1) / G + kReduceStages) {
+      G = tiles;
+      seg_max = 1;
     }
     // the kernel walks its stream-K range in 32-bit arithmetic
     if ((U + 1) * G >= (1LL << 32)) return MXG_ERR_UNSUPPORTED_SHAPE;

@@ -137,8 +137,14 @@ def owner_sim(U, G):
 
 @pytest.mark.parametrize("kind,M,N,K,sm", [(0, 8, 7168, 8192, 152), (0, 64, 7168, 8192, 152),
                                            (1, 64, 36864, 7168, 152), (1, 64, 7168, 18432, 152),
-                                           (0, 200, 1024, 2048, 7), (1, 1, 128, 128, 152)])
+                                           (0, 200, 1024, 2048, 7), (1, 1, 128, 128, 152),
+                                           (1, 64, 16384, 512, 152), (1, 64, 12288, 1536, 152),
+                                           (0, 64, 12288, 1536, 152), (1, 8, 4096, 2048, 152)])
 def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
+    """The stream-K cut over min(SMs, units) CTAs -- or, when the tiles fit
+    in one wave and their K takes no more stages than a stream-K CTA's share
+    plus the 7 stages a chained reduce kernel costs, one CTA per whole tile
+    (no partial sums)."""
     p = mx.mxg_plan_gemm(kind, M, N, K, sm, variant="splitk")
     assert p["variant"] == 2 and p["bm"] == 128
     assert p["bn"] >= M and p["bn"] in (16, 32, 64, 128, 256) and (p["bn"] // 2 < M or p["bn"] == 16)
@@ -149,9 +155,13 @@ def test_plan_splitk_matches_simulation(kind, M, N, K, sm):
     assert p["tiles"] == tiles
     U = tiles * KB
     G = min(sm, U)
-    assert p["ctas"] == G
     own = owner_sim(U, G)
     seg = max(len(set(own[t * KB:(t + 1) * KB])) for t in range(tiles))
+    if tiles <= sm and seg > 1 and KB <= -(-U // G) + 7:
+        G, seg = tiles, 1
+        own = owner_sim(U, G)
+        assert max(len(set(own[t * KB:(t + 1) * KB])) for t in range(tiles)) == 1
+    assert p["ctas"] == G
     assert p["seg_max"] == seg
     if seg > 1:
         assert p["ws_bytes"] >= tiles * seg * p["bn"] * 128 * 4

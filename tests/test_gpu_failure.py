@@ -23,10 +23,11 @@ def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
     w = synth.weight(N, K, seed=51)
     status = torch.zeros(1, dtype=torch.int32, device=d)
     ws = torch.zeros(1 << 22, dtype=torch.uint8, device=d)
+    ctas = 8 if variant == "splitk" else 0  # split-K: partial sums and the reduce kernel
     if kind == 0:
         wc, wsf = mx.mx_quantize_weight(w.to(d))
         run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, variant=variant, ws=ws,
-                                           splitk_reduce=reduce, **kw)
+                                           splitk_reduce=reduce, ctas=ctas, **kw)
         ac, asf = oracle.mx_quantize_rows(x)
         wr, wsr = oracle.mx_quantize_rows(w)
         ref, bound = oracle.gemm_a4w4(ac, asf, wr, wsr)
@@ -34,7 +35,7 @@ def test_stall_times_out_then_next_call_is_correct(kind, variant, reduce):
         qw, sw = mx.fp8_quantize_act(w.to(d))
         qa, sa = mx.fp8_quantize_act(x.to(d))
         run = lambda **kw: mx.fp8_gemm_ptpc(qa, sa, qw, sw, out_f32=True, variant=variant, ws=ws,
-                                            splitk_reduce=reduce, **kw)
+                                            splitk_reduce=reduce, ctas=ctas, **kw)
         qar, sar = oracle.fp8_quantize_rows(x)
         qwr, swr = oracle.fp8_quantize_rows(w)
         ref, bound = oracle.gemm_ptpc(qar, sar, qwr, swr)
