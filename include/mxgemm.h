@@ -33,7 +33,11 @@
  *     returned before anything is launched.  A failed launch returns
  *     MXG_ERR_CUDA.  Device-side waits are bounded; a wait that runs out
  *     ORs MXG_DEV_TIMEOUT into opts->dev_status (if given) and the kernel
- *     returns early, leaving the context usable.
+ *     returns early, leaving the context usable.  The quantizers have no
+ *     status word: large inputs (more than 512 rows) stream through shared
+ *     memory by bulk copies, and a copy wait that runs out (1 s) leaves the
+ *     rows not yet quantized with NaN scales (FP8 s = NaN, MX scale code
+ *     0xFF), which make every product with them NaN.
  *   - Requirements: compute capability 10.3 (GB300); K % 128 == 0; M, N >= 1
  *     (N % 128 == 0 for the GEMMs); every pointer 16-byte aligned; every
  *     leading dimension a multiple of 16 bytes.
