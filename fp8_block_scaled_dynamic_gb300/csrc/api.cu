@@ -300,7 +300,7 @@ mxg_status run_gemm(int kind, const GemmOperands &op, int M, int N, int K, void 
   p.status = opts ? opts->dev_status : nullptr;
   const uint32_t tmo = (opts && opts->timeout_ms) ? opts->timeout_ms : 1000u;
   p.timeout_ns = (unsigned long long)tmo * 1000000ull;
-  p.debug_stall = opts ? opts->debug_stall : 0;
+  p.debug_stall = (opts && opts->debug_stall == 1) ? 1 : 0;
   p.early_w = (opts && opts->weights_static) ? 1 : 0;
 
   p.trace = opts ? static_cast<unsigned long long *>(opts->trace) : nullptr;
@@ -565,7 +565,13 @@ mxg_status mx_gemm_a4w4(const uint8_t *a_codes, const uint8_t *a_sf, const void 
     a_codes = codes;
     a_sf = sf;
     part_off += need;
-    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s);
+    mxg::QuantWatch watch;
+    if (opts) {
+      watch.status = opts->dev_status;
+      watch.timeout_ns = (unsigned long long)(opts->timeout_ms ? opts->timeout_ms : 1000u) * 1000000ull;
+      watch.debug_stall = opts->debug_stall == 2 ? 1 : 0;
+    }
+    cudaError_t e = mxg::launch_mx_quant(x_bf16, ldx, M, K, codes, sf, true, act_tile_rows, true, sm, s, watch);
     if (e != cudaSuccess) return MXG_ERR_CUDA;
   }
   GemmOperands op{a_codes, a_sf, w_codes, w_sf, nullptr, nullptr};
@@ -657,7 +663,7 @@ mxg_status mx_gemm_a4w4_grouped(const void *x_bf16, int ldx, const int *row_off,
   p.status = opts->dev_status;
   const uint32_t tmo = opts->timeout_ms ? opts->timeout_ms : 1000u;
   p.timeout_ns = (unsigned long long)tmo * 1000000ull;
-  p.debug_stall = opts->debug_stall;
+  p.debug_stall = opts->debug_stall == 1 ? 1 : 0;
   p.early_w = opts->weights_static ? 1 : 0;
   p.trace = static_cast<unsigned long long *>(opts->trace);
   p.a_tiles = codes;

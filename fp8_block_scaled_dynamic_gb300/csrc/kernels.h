@@ -100,11 +100,21 @@ constexpr int kPanelLayout = -1;
 constexpr int kPanelRows = 256;
 constexpr int kMxPanelBytes = 256 * 128 + 2048;  // per 128-byte column
 constexpr int kF8PanelBytes = 256 * 128;
+// Bounded-wait controls of a quantizer that streams rows through shared
+// memory (more than 512 rows): the caller's status word (may be null), the
+// wait limit, and the test hook that makes its first wait one that nothing
+// satisfies.
+struct QuantWatch {
+  int *status = nullptr;
+  unsigned long long timeout_ns = 1000000000ull;
+  int debug_stall = 0;
+};
+
 // act: the input is an activation; the next kernel may launch at once.  For
 // weights (act = false) no later kernel starts before this one has finished.
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
                             uint8_t *sf, bool swizzled, int tile_rows, bool act, int sm_count,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const QuantWatch &watch = QuantWatch{});
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,
                              float *scale, int tile_rows, bool act, int sm_count,

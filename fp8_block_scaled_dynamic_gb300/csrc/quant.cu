@@ -55,7 +55,7 @@ __device__ __forceinline__ void drain_copy(uint32_t bar, uint32_t parity) {
 
 constexpr int kMxSlots = 2;
 constexpr uint32_t kMxSlotBytes = 4 * kMxThreads * 16;  // a CTA's part of a row at CPT = 4
-constexpr size_t kMxStagedSmem = (size_t)kMxSlots * kMxSlotBytes + 8u * kMxSlots;
+constexpr size_t kMxStagedSmem = (size_t)kMxSlots * kMxSlotBytes + 8u * (kMxSlots + 1);
 
 template <bool kSwizzled, int CPT, bool kStaged>
 __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__restrict__ x,
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
                                                               int rows_iter, int K, int tile_rows,
                                                               int early_trigger,
                                                               uint8_t *__restrict__ codes,
-                                                              uint8_t *__restrict__ sf) {
+                                                              uint8_t *__restrict__ sf, int *status,
+                                                              unsigned long long timeout_ns, int debug_stall) {
   const int cpr = K >> 3;  // 16-byte chunks per row; K % 128 == 0 => cpr % 16 == 0
   const int G = K >> 5;    // MX blocks per row
   const int lane = threadIdx.x & 31;
@@ -167,17 +168,20 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
   };
   uint4 va[CPT], vb[CPT];
   if constexpr (kStaged) {
-    extern __shared__ __align__(128) uint8_t ring[];  // kMxSlots row parts, then one mbarrier a slot
+    // kMxSlots row parts, then one mbarrier a slot and one that nothing
+    // arrives at (the debug_stall test hook waits on it)
+    extern __shared__ __align__(128) uint8_t ring[];
     __shared__ int abort_flag;
     const uint32_t slots = smem_addr(ring);
     const uint32_t bars = slots + kMxSlots * kMxSlotBytes;
+    const uint32_t never = bars + 8u * kMxSlots;
     if (threadIdx.x == 0) {
-      for (int i = 0; i < kMxSlots; ++i) mbar_init(bars + 8u * i, 1);
+      for (int i = 0; i <= kMxSlots; ++i) mbar_init(bars + 8u * i, 1);
       abort_flag = 0;
       fence_barrier_init();
     }
     __syncthreads();
-    const WaitCtl ctl{&abort_flag, nullptr, kQuantWaitNs};
+    const WaitCtl ctl{&abort_flag, status, timeout_ns};
     const uint32_t part_bytes = (uint32_t)cta_nc * 16u;  // cta_nc % 16 == 0
     // row k of this CTA is blockIdx.y + k * gridDim.y; thread 0 copies its
     // part into slot k % kMxSlots (padding rows are not read)
@@ -198,7 +202,9 @@ __global__ void __launch_bounds__(kMxThreads) mx_quant_kernel(const uint16_t *__
         do_row(r, va);
         continue;
       }
-      const bool landed = mbar_wait(bars + 8u * (uint32_t)(k % kMxSlots), (uint32_t)(k / kMxSlots) & 1u, ctl);
+      const bool landed = (debug_stall && k == 0)
+                              ? mbar_wait(never, 0u, ctl)
+                              : mbar_wait(bars + 8u * (uint32_t)(k % kMxSlots), (uint32_t)(k / kMxSlots) & 1u, ctl);
       if (__syncthreads_or(!landed)) {
         // a copy did not land: let every copy still in flight finish
         // (bounded), give this CTA's remaining rows NaN scales (E8M0 0xFF),
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(kSwThreads) swiglu_fp8_kernel(const uint16_t *
 
 cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8_t *codes,
                             uint8_t *sf, bool swizzled, int tile_rows, bool act, int sm_count,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const QuantWatch &watch) {
   const int cpr = K / 8;
   const bool big = rows > 512;
   const int per_block = kMxThreads * (big ? 4 : 2);
@@ -819,7 +825,8 @@ cudaError_t launch_mx_quant(const void *x, long long ldx, int rows, int K, uint8
   cudaLaunchAttribute attr[1];
   attach_pdl(cfg, attr);
   const uint16_t *xp = static_cast<const uint16_t *>(x);
-  return cudaLaunchKernelEx(&cfg, kern, xp, ldx, rows, rows_iter, K, tile_rows, act ? 1 : 0, codes, sf);
+  return cudaLaunchKernelEx(&cfg, kern, xp, ldx, rows, rows_iter, K, tile_rows, act ? 1 : 0, codes, sf,
+                            watch.status, watch.timeout_ns, watch.debug_stall);
 }
 
 cudaError_t launch_fp8_quant(const void *x, long long ldx, int rows, int K, uint8_t *q,

@@ -33,11 +33,13 @@
  *     returned before anything is launched.  A failed launch returns
  *     MXG_ERR_CUDA.  Device-side waits are bounded; a wait that runs out
  *     ORs MXG_DEV_TIMEOUT into opts->dev_status (if given) and the kernel
- *     returns early, leaving the context usable.  The quantizers have no
- *     status word: large inputs (more than 512 rows) stream through shared
- *     memory by bulk copies, and a copy wait that runs out (1 s) leaves the
- *     rows not yet quantized with NaN scales (FP8 s = NaN, MX scale code
- *     0xFF), which make every product with them NaN.
+ *     returns early, leaving the context usable.  Large inputs (more than
+ *     512 rows) of the quantizers stream through shared memory by bulk
+ *     copies; a copy wait that runs out leaves the rows not yet quantized
+ *     with NaN scales (FP8 s = NaN, MX scale code 0xFF), which make every
+ *     product with them NaN.  The quantizer entry points have no status word
+ *     (their limit is 1 s); the activation quantizer of a fused mx_gemm_a4w4
+ *     call uses opts->dev_status and opts->timeout_ms.
  *   - Requirements: compute capability 10.3 (GB300); K % 128 == 0; M, N >= 1
  *     (N % 128 == 0 for the GEMMs); every pointer 16-byte aligned; every
  *     leading dimension a multiple of 16 bytes.
@@ -141,7 +143,10 @@ typedef struct {
     int *dev_status;      /* optional device int; kernels OR MXG_DEV_* bits into it */
     uint32_t timeout_ms;  /* limit of every device-side wait; 0 = 1000 ms */
     int debug_stall;      /* test hook: 1 makes the epilogue wait on a barrier nothing
-                             arrives at, so the timeout path runs (no fault, no hang) */
+                             arrives at, so the timeout path runs (no fault, no hang);
+                             2 does the same in the activation quantizer of a fused
+                             mx_gemm_a4w4 call of more than 512 rows, which then
+                             leaves NaN scales (0xFF), so the GEMM writes NaN rows */
     int weights_static;   /* 1: no kernel that may still be running when the GEMM starts
                              writes the weight operands (w_codes/w_sf or qw/sw), so the
                              GEMM may stream them in before the kernels ahead of it on

@@ -76,3 +76,27 @@ def test_stall_on_cta_pairs_times_out_then_next_call_is_correct(kind):
     y = run(dev_status=status)
     assert mx.mxg_query_status(status) == 0
     assert_gemm_close(y.cpu().numpy(), ref, bound, "after timeout, pairs")
+
+
+def test_stall_in_fused_quantizer_times_out_then_next_call_is_correct():
+    """debug_stall = 2: the activation quantizer of a fused call with more
+    than 512 token rows (rows streamed through shared memory) waits on a
+    barrier that nothing arrives at.  Every CTA gives up, lets its copies in
+    flight land, records MXG_DEV_TIMEOUT and leaves NaN scales (E8M0 0xFF)
+    on its rows, so every output row is NaN; the next call is correct."""
+    d = dev()
+    M, N, K = 600, 512, 1024
+    x = synth.activation(M, K, seed=54)
+    w = synth.weight(N, K, seed=55)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    wc, wsf = mx.mx_quantize_weight(w.to(d))
+    run = lambda **kw: mx.mx_gemm_a4w4(wc, wsf, x=x.to(d), out_f32=True, **kw)
+    y = run(dev_status=status, timeout_ms=20, debug_stall=2)
+    assert mx.mxg_query_status(status) == 6  # MXG_ERR_TIMEOUT
+    assert np.isnan(y.cpu().numpy()).all()
+    y = run(dev_status=status)
+    assert mx.mxg_query_status(status) == 0
+    ac, asf = oracle.mx_quantize_rows(x)
+    wr, wsr = oracle.mx_quantize_rows(w)
+    ref, bound = oracle.gemm_a4w4(ac, asf, wr, wsr)
+    assert_gemm_close(y.cpu().numpy(), ref, bound, "after a quantizer timeout")
