@@ -108,6 +108,14 @@ def test_mx_oproj_weight_full_size():
     assert_codes_equal(np_u8(sfz), oracle.sf_swizzle(s_ref), "o_proj swizzled scales")
 
 
+@pytest.mark.parametrize("M,K", [(600, 10240), (520, 16384)])
+def test_mx_act_rows_in_parts(M, K):
+    """More than 512 rows of more than 8192 values: several CTAs stream
+    parts of each row through shared memory (K = 10240: a 1024-chunk part
+    and a 256-chunk one), padding rows of the swizzled scales included."""
+    check_mx(synth.activation(M, K, seed=M + K, row_scale=True), what=f"parts {M}x{K}")
+
+
 def test_mx_act_prefill_full_size():
     # 8 requests x 1024 tokens, per-row log-uniform scale in [0.1, 10], 0.1% x50 outliers
     x = synth.activation(8192, synth.OPROJ_K, seed=synth.act_seed(2, 0, 0), row_scale=True)
