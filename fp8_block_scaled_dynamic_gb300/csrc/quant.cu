@@ -5,16 +5,23 @@
 //    scale per 32 consecutive input channels).  One thread owns one 16-byte
 //    chunk (8 values = a quarter block); the block amax is a max over 4
 //    lanes by warp shuffles; codes leave as packed nibbles and scales go
-//    straight into the row-major or the 128x4-tile layout.
-//  * fp8_quant_kernel: per-row E4M3 quantization with an FP32 scale
-//    ("Kimi-K3-DSpark-FP8-PTPC", "Phase 1 FP8 PTPC Quantization": dynamic
-//    per-token activations; per-output-channel weights are per-row of W).
+//    straight into the row-major, 128x4-tile or panel layout.  Large inputs
+//    stream through shared memory by bulk copies.
+//  * mx_quant_grouped_kernel: the same for token rows grouped by expert.
+//  * fp8_quant_kernel / fp8_quant_staged_kernel: per-row E4M3 quantization
+//    with an FP32 scale ("Kimi-K3-DSpark-FP8-PTPC", "Phase 1 FP8 PTPC
+//    Quantization": dynamic per-token activations; per-output-channel
+//    weights are per-row of W), two passes over a row or (large inputs) one
+//    read of rows streamed through shared memory.
+//  * swiglu_fp8_kernel: SwiGLU of the packed gate_up output fused with the
+//    per-token FP8 quantization of its result.
 //
 // Numerics (shared readings, see the public header): MX scale e =
 // clamp(floor(log2 amax) - 2, -127, 127), code = E2M1_RNE_sat(x * 2^-e) with
 // the sign of x; FP8 s = amax / 448 (1 for an all-zero row), q =
 // E4M3_RNE_sat(x / s).  Built without fast-math: x * 2^-e is an exact fp32
-// product (subnormal inputs included) and x / s is IEEE division.
+// product (subnormal inputs included), and x / s is the IEEE division or,
+// where it decides the same code (RowDivisor), Markstein's correction step.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
