@@ -189,10 +189,15 @@ def act_tile_rows(plan: dict) -> int:
     return plan["bn"] if plan["variant"] == 2 else 128
 
 
+def split_desc(plan):
+    """A split-K plan in words: stream-K, or one CTA per whole tile."""
+    return "split-K (swapped, stream-K)" if plan["seg_max"] > 1 else "split-K (swapped, whole tiles)"
+
+
 def variant_desc(plan):
     """How the dispatcher runs a GEMM, for the bench line."""
     if plan["variant"] == 2:
-        return f"split-K (swapped, stream-K), {plan['ctas']} CTAs"
+        return f"{split_desc(plan)}, {plan['ctas']} CTAs"
     if plan["cta_pair"]:
         return f"full-tile, CTA pairs (2-SM MMA, 256 x 256 tiles), {plan['ctas']} CTAs"
     return f"full-tile, {plan['ctas']} CTAs"
@@ -622,7 +627,7 @@ class DraftLayers(Workload):
         self.flops_per_step = layers * (2 * M * H * KO + 2 * M * 2 * I * H + 2 * M * H * I)
         self.dtype = "e2m1 x e2m1 (o_proj), e4m3 x e4m3 (MLP) -> f32 (bf16 out)"
         self.bound = "hbm" if M <= 256 else "tensor"
-        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[self.plan_g["variant"]]
+        v = "full-tile" if self.plan_g["variant"] == 1 else split_desc(self.plan_g)
         self.kernel_desc = f"gemm_kernel<PTPC, BN={self.plan_g['bn']}> {v}, {self.plan_g['ctas']} CTAs (gate_up)"
         self.h2d = layers * 2 * M * KO
         self.d2h = layers * M * H * ydt.itemsize
@@ -703,7 +708,7 @@ class MlaFp8(Workload):
         self.flops_per_step = sum(2 * M * g["N"] * g["K"] for g in self.g)
         self.dtype = "e4m3 x e4m3 -> f32 (bf16 out)"
         self.bound = "hbm" if M <= 256 else "tensor"
-        v = {1: "full-tile", 2: "split-K (swapped, stream-K)"}[g1["plan"]["variant"]]
+        v = "full-tile" if g1["plan"]["variant"] == 1 else split_desc(g1["plan"])
         self.kernel_desc = f"gemm_kernel<PTPC, BN={g1['plan']['bn']}> {v}, {g1['plan']['ctas']} CTAs (kv_b)"
         self.h2d = sum(2 * M * g["K"] for g in self.g)
         self.d2h = sum(M * g["N"] * ydt.itemsize for g in self.g)
