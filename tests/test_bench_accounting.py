@@ -50,6 +50,18 @@ def test_act_tile_rows_follow_the_plan():
     assert full["variant"] == 1 and bench.act_tile_rows(full) == 128
 
 
+@pytest.mark.parametrize("kind,M,N,K,kernels", [(0, 64, 7168, 8192, 2), (1, 64, 16384, 512, 1),
+                                                 (1, 64, 12288, 1536, 1), (1, 64, 36864, 7168, 1),
+                                                 (1, 64, 7168, 18432, 2)])
+def test_launch_count_follows_the_plan(kind, M, N, K, kernels):
+    """The bench's launch count: a GEMM call launches its kernel, plus the
+    split-K reduce only when a tile's K is spread over several CTAs (not for
+    whole-tile or full-tile plans)."""
+    plan = mx.mxg_plan_gemm(kind, M, N, K, 152)
+    assert bench.gemm_kernels(plan) == kernels
+    assert ("stream-K" in bench.variant_desc(plan)) == (plan["variant"] == 2 and plan["seg_max"] > 1)
+
+
 def test_bench_interval_check_catches_a_wrong_value():
     """The bf16 check the bench applies to its timed outputs rejects a value
     one bf16 step off when the tolerance is far below a step."""
