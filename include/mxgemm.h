@@ -132,8 +132,12 @@ typedef enum {
 
 typedef struct {
     int variant;          /* mxg_variant */
-    int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over; 0 or more
-                             than the SM count = the SM count (one persistent CTA per SM) */
+    int ctas;             /* SPLITK: number of CTAs to spread the K-blocks over (stream-K);
+                             more than the SM count = the SM count (one persistent CTA per
+                             SM).  0 = the dispatcher's choice: the SM count, or one CTA per
+                             whole tile (no partial sums, no reduce kernel) when the tiles
+                             fit on the SMs and a tile's K-stages are at most a stream-K
+                             CTA's share plus 7 (the measured cost of the reduce kernel) */
     void *workspace;      /* device scratch of >= mxg_gemm_workspace_bytes() bytes,
                              256-byte aligned: the fused path's quantized activations, then
                              the split-K partial tiles.  Its contents on entry do not
