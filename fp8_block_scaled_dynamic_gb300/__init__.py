@@ -348,7 +348,10 @@ def mx_gemm_a4w4(w_codes: torch.Tensor, w_sf, *, a_codes=None, a_sf=None, x=None
     (or True); with weights_tiled=W_PANEL w_codes is flat in 256-row panels
     (scales inside, w_sf None) and n, k give N, K.  With act_tile_rows,
     a_codes is flat in the activation tile layout and m gives M.  cta_pair:
-    run a full-tile GEMM of M > 128 on CTA pairs (2-SM MMAs)."""
+    run a full-tile GEMM of M > 128 on CTA pairs (2-SM MMAs).  dev_status,
+    timeout_ms: the bounded-wait controls; debug_stall (test hook): 1 stalls
+    the GEMM's epilogue, 2 the activation quantizer of a fused call of more
+    than 512 rows, until the limit runs out."""
     if w_codes.dim() == 1:
         _need(n > 0 and k > 0, "flat weight codes need n and k")
         N, K = n, k
